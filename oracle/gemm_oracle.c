@@ -1,0 +1,280 @@
+/*
+ * Fused-epilogue GEMM oracle.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+ * load this library.  It shares no source, header, table or helper with the
+ * CUDA path: every decode, index computation and rounding below is written
+ * out here from the definitions.
+ *
+ * What it computes, one output row at a time, in fp64:
+ *
+ *   acc(l,m,n) = sum_k a(l,m,k) * b(l,k,n)          a = op(A), b = op(B)
+ *   t          = alpha*scale_a*scale_b*acc + beta*c(l,m,n) + bias
+ *   t          = max(t, 0)                          if the activation is ReLU
+ *   D(l,m,n)   = round-to-nearest-even(t) in D's type
+ *
+ * Sources (page title, section):
+ *  - "CUTLASS" (knowledge-base page), opening section: the operation is
+ *    C = alpha * op(A) * op(B) + beta * C, op in {N, T}, column-major BLAS
+ *    convention; D may be the same buffer as C ("Technical Documentation:
+ *    NVIDIA/cutlass", "Launching a GEMM kernel in CUDA").
+ *  - "CUTLASS" (knowledge-base page), "Epilogues": bias, activation and
+ *    scaling are applied to the accumulated tile before it is written.
+ *  - "Utilities for SM100", "Background - SM100 epilogue flow": accumulator,
+ *    then the optional source C, then the fusion (bias, activation), then the
+ *    store of D.
+ *  - "Technical Documentation: NVIDIA/cutlass", "Blackwell Narrow Precision
+ *    Data Types" table: e4m3 has 4 exponent and 3 mantissa bits, signed.
+ *    The encoding details (bias 7, no infinities, S.1111.111 is NaN, largest
+ *    finite 448) are the OCP 8-bit float E4M3 definition the table points to.
+ *  - Per-tensor dequantisation scales scale_a, scale_b multiply the
+ *    accumulator (the block-scaled form D = C + (A x SFA)(B x SFB) of
+ *    "Blackwell SM100 GEMMs", "Block Scaled GEMMs", with one scale per
+ *    tensor).
+ *
+ * Every product of two operands (<= 11 significant bits each) is exact in
+ * fp64, and the fp64 sum over K carries a relative error of order K * 2^-53,
+ * far below any output type's half-ulp, so the single final rounding is the
+ * only rounding that matters.
+ *
+ * Readings where the pages leave a step open:
+ *  - bias is added after alpha scaling and is not scaled itself;
+ *  - beta == 0 means C is not read at all (a NaN in C does not propagate);
+ *  - ReLU(t) = t > 0 ? t : 0 (so NaN maps to 0, like fmaxf);
+ *  - a batch index l adds l * stride_x elements to operand x's base.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Element type codes of this oracle's own interface. */
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3 };
+
+typedef struct {
+    int64_t M, N, K, L;
+    int32_t op_a, op_b;                          /* 0 = N (as stored), 1 = T */
+    int32_t order_a, order_b, order_c, order_d;  /* 0 = column-major, 1 = row-major */
+    int64_t lda, ldb, ldc, ldd;                  /* leading dimensions, elements */
+    int64_t stride_a, stride_b, stride_c, stride_d, stride_bias; /* batch strides, elements */
+    int32_t dtype_a, dtype_b, dtype_c, dtype_d;
+    double alpha, beta, scale_a, scale_b;
+    int32_t has_bias;      /* bias is fp32 */
+    int32_t bias_per_row;  /* 0: bias[n] broadcast down the columns; 1: bias[m] */
+    int32_t act;           /* 0 = identity, 1 = ReLU */
+} oracle_problem_t;
+
+/* ---------------------------------------------------------------------------
+ * Bit-level codecs.  A binary float with `eb` exponent bits and `mb` stored
+ * mantissa bits has bias 2^(eb-1)-1; a zero exponent field means subnormal
+ * (value = mant * 2^(1-bias-mb)).  IEEE formats reserve the all-ones exponent
+ * for inf/NaN; e4m3 uses it for normal numbers except mantissa 111 (NaN).
+ * ------------------------------------------------------------------------- */
+static int type_bits(int dt, int* eb, int* mb, int* ieee) {
+    switch (dt) {
+        case OR_F32:  *eb = 8; *mb = 23; *ieee = 1; return 32;
+        case OR_F16:  *eb = 5; *mb = 10; *ieee = 1; return 16;
+        case OR_BF16: *eb = 8; *mb = 7;  *ieee = 1; return 16;
+        case OR_E4M3: *eb = 4; *mb = 3;  *ieee = 0; return 8;
+        default: return 0;
+    }
+}
+
+double oracle_decode(int dt, uint32_t bits) {
+    int eb, mb, ieee;
+    if (!type_bits(dt, &eb, &mb, &ieee)) return NAN;
+    const uint32_t mant = bits & ((1u << mb) - 1u);
+    const uint32_t expf = (bits >> mb) & ((1u << eb) - 1u);
+    const int neg = (bits >> (mb + eb)) & 1u;
+    const int bias = (1 << (eb - 1)) - 1;
+    const uint32_t all_ones = (1u << eb) - 1u;
+    double v;
+    if (expf == all_ones && ieee) {
+        v = mant ? NAN : INFINITY;
+    } else if (expf == all_ones && !ieee && mant == (1u << mb) - 1u) {
+        v = NAN;
+    } else if (expf == 0) {
+        v = ldexp((double)mant, 1 - bias - mb);
+    } else {
+        v = ldexp((double)(mant | (1u << mb)), (int)expf - bias - mb);
+    }
+    return neg ? -v : v;
+}
+
+/* Round-to-nearest, ties-to-even, from fp64 into an IEEE type (f32/f16/bf16).
+ * Overflow goes to infinity as IEEE 754 prescribes for this rounding mode. */
+uint32_t oracle_encode(int dt, double v) {
+    int eb, mb, ieee;
+    if (!type_bits(dt, &eb, &mb, &ieee) || !ieee) return 0xFFFFFFFFu;
+    const int bias = (1 << (eb - 1)) - 1;
+    const uint32_t sign = signbit(v) ? (1u << (eb + mb)) : 0u;
+    const uint32_t inf_bits = sign | (((1u << eb) - 1u) << mb);
+    if (isnan(v)) return inf_bits | (1u << (mb - 1));   /* quiet NaN */
+    const double a = fabs(v);
+    if (isinf(a)) return inf_bits;
+    if (a == 0.0) return sign;
+    const int emin = 1 - bias;
+    const int emax = bias;
+    const double max_finite = ldexp(2.0 - ldexp(1.0, -mb), emax);
+    int e2;
+    frexp(a, &e2);               /* a = f * 2^e2, f in [0.5, 1) */
+    int E = e2 - 1;              /* a in [2^E, 2^(E+1)) */
+    if (E < emin) E = emin;      /* subnormal range shares emin's quantum */
+    /* a / 2^(E-mb) is exact in fp64 (power-of-two scaling); nearbyint rounds it
+     * to an integer with ties to even under the default rounding mode. */
+    const double r = nearbyint(ldexp(a, mb - E));
+    const double res = ldexp(r, E - mb);
+    if (res > max_finite) return inf_bits;
+    if (r == 0.0) return sign;
+    frexp(res, &e2);
+    E = e2 - 1;
+    if (E < emin) {
+        return sign | (uint32_t)ldexp(res, mb - emin);
+    }
+    const uint32_t mant = (uint32_t)(ldexp(res, mb - E) - ldexp(1.0, mb));
+    return sign | ((uint32_t)(E + bias) << mb) | mant;
+}
+
+static uint32_t load_bits(const void* base, int dt, int64_t idx) {
+    switch (dt) {
+        case OR_F32: { uint32_t x; memcpy(&x, (const char*)base + 4 * idx, 4); return x; }
+        case OR_F16:
+        case OR_BF16: { uint16_t x; memcpy(&x, (const char*)base + 2 * idx, 2); return x; }
+        case OR_E4M3: return ((const uint8_t*)base)[idx];
+        default: return 0;
+    }
+}
+
+static void store_bits(void* base, int dt, int64_t idx, uint32_t bits) {
+    switch (dt) {
+        case OR_F32: memcpy((char*)base + 4 * idx, &bits, 4); break;
+        case OR_F16:
+        case OR_BF16: { uint16_t x = (uint16_t)bits; memcpy((char*)base + 2 * idx, &x, 2); break; }
+        default: break;
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Addressing, BLAS convention.  op(A) is M x K: with op N the stored matrix is
+ * M x K, with op T it is K x M.  A stored R x S matrix is read at
+ * r * ld + s (row-major) or r + s * ld (column-major).
+ * ------------------------------------------------------------------------- */
+static int64_t stored_index(int order, int64_t r, int64_t s, int64_t ld) {
+    return order == 1 ? r * ld + s : r + s * ld;
+}
+
+static int64_t a_index(const oracle_problem_t* p, int64_t l, int64_t m, int64_t k) {
+    const int64_t off = p->op_a == 0 ? stored_index(p->order_a, m, k, p->lda)
+                                     : stored_index(p->order_a, k, m, p->lda);
+    return l * p->stride_a + off;
+}
+
+static int64_t b_index(const oracle_problem_t* p, int64_t l, int64_t k, int64_t n) {
+    const int64_t off = p->op_b == 0 ? stored_index(p->order_b, k, n, p->ldb)
+                                     : stored_index(p->order_b, n, k, p->ldb);
+    return l * p->stride_b + off;
+}
+
+static int64_t cd_index(int order, int64_t ld, int64_t stride, int64_t l, int64_t m, int64_t n) {
+    return l * stride + stored_index(order, m, n, ld);
+}
+
+static int nthreads_or_default(int nthreads) {
+#ifdef _OPENMP
+    return nthreads > 0 ? nthreads : omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
+int oracle_max_threads(void) { return nthreads_or_default(0); }
+
+/*
+ * Computes the full output rows listed in `rows` (each entry is l*M + m).
+ * Row i of the result goes to Dout[i*N .. i*N+N-1], packed in D's type, and,
+ * when Tout is not NULL, the fp64 value before rounding to Tout[i*N + n].
+ * The full GEMM is the call with every row listed.
+ * Returns 0 on success, a negative code on bad arguments or allocation failure.
+ */
+int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, const void* C,
+                     const float* bias, int64_t nrows, const int64_t* rows, void* Dout,
+                     double* Tout, int nthreads) {
+    int eb, mb, ieee;
+    if (!p || p->M < 0 || p->N < 0 || p->K < 0 || p->L < 1) return -1;
+    if (!type_bits(p->dtype_a, &eb, &mb, &ieee) || !type_bits(p->dtype_b, &eb, &mb, &ieee)) return -2;
+    if (!type_bits(p->dtype_d, &eb, &mb, &ieee) || !ieee) return -3;
+    const int use_c = p->beta != 0.0;
+    if (use_c && (!C || !type_bits(p->dtype_c, &eb, &mb, &ieee))) return -4;
+    if (p->has_bias && !bias) return -5;
+    const int64_t M = p->M, N = p->N, K = p->K;
+    const double scale = p->alpha * p->scale_a * p->scale_b;
+    const int nt = nthreads_or_default(nthreads);
+    if (nrows == 0 || N == 0) return 0;
+
+    /* b(l, k, n) decoded once per batch into a k-major fp64 panel. */
+    double* Bd = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)N);
+    if (!Bd) return -6;
+    int status = 0;
+    for (int64_t l = 0; l < p->L; ++l) {
+        int64_t in_batch = 0;
+        for (int64_t i = 0; i < nrows; ++i) in_batch += (rows[i] / M) == l;
+        if (!in_batch) continue;
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t n = 0; n < N; ++n)
+                Bd[k * N + n] = oracle_decode(p->dtype_b, load_bits(B, p->dtype_b, b_index(p, l, k, n)));
+
+#pragma omp parallel num_threads(nt)
+        {
+            double* acc = (double*)malloc(sizeof(double) * (size_t)N);
+            if (!acc) {
+#pragma omp atomic write
+                status = -6;
+            }
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t i = 0; i < nrows; ++i) {
+                if (!acc || rows[i] / M != l) continue;
+                const int64_t m = rows[i] % M;
+                for (int64_t n = 0; n < N; ++n) acc[n] = 0.0;
+                /* i-k-j order: one a(m,k) times the k-th row of b, summed. */
+                for (int64_t k = 0; k < K; ++k) {
+                    const double a = oracle_decode(p->dtype_a, load_bits(A, p->dtype_a, a_index(p, l, m, k)));
+                    const double* brow = Bd + k * N;
+                    for (int64_t n = 0; n < N; ++n) acc[n] += a * brow[n];
+                }
+                for (int64_t n = 0; n < N; ++n) {
+                    double t = scale * acc[n];
+                    if (use_c)
+                        t += p->beta * oracle_decode(p->dtype_c,
+                                 load_bits(C, p->dtype_c, cd_index(p->order_c, p->ldc, p->stride_c, l, m, n)));
+                    if (p->has_bias)
+                        t += (double)bias[l * p->stride_bias + (p->bias_per_row ? m : n)];
+                    if (p->act == 1) t = t > 0.0 ? t : 0.0;
+                    if (Tout) Tout[i * N + n] = t;
+                    store_bits(Dout, p->dtype_d, i * N + n, oracle_encode(p->dtype_d, t));
+                }
+            }
+            free(acc);
+        }
+    }
+    free(Bd);
+    return status;
+}
+
+/* Scatters packed rows (as produced by oracle_gemm_rows for every row, in
+ * order) into D's own storage layout: D(l,m,n) at l*stride_d + (m,n) by
+ * order_d and ldd.  Lets a test build a full D buffer the way a caller lays
+ * it out. */
+int oracle_scatter_d(const oracle_problem_t* p, const void* packed, void* Dstore) {
+    int eb, mb, ieee;
+    if (!type_bits(p->dtype_d, &eb, &mb, &ieee)) return -1;
+    for (int64_t l = 0; l < p->L; ++l)
+        for (int64_t m = 0; m < p->M; ++m)
+            for (int64_t n = 0; n < p->N; ++n)
+                store_bits(Dstore, p->dtype_d, cd_index(p->order_d, p->ldd, p->stride_d, l, m, n),
+                           load_bits(packed, p->dtype_d, (l * p->M + m) * p->N + n));
+    return 0;
+}

@@ -1,0 +1,154 @@
+"""Python face of the C GEMM oracle.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg import this module.  It marshals numpy/torch CPU buffers into the oracle's
+own ``oracle_problem_t`` and calls ``oracle_gemm_rows``; all arithmetic lives in
+``gemm_oracle.c``.  See that file's header for what is computed and where the
+pages define it.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+# The oracle's own element-type codes.
+F32, F16, BF16, E4M3 = 0, 1, 2, 3
+_NAMES = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3}
+_BYTES = {F32: 4, F16: 2, BF16: 2, E4M3: 1}
+_BITS_NP = {F32: np.uint32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8}
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [
+        ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("L", ctypes.c_int64),
+        ("op_a", ctypes.c_int32), ("op_b", ctypes.c_int32),
+        ("order_a", ctypes.c_int32), ("order_b", ctypes.c_int32),
+        ("order_c", ctypes.c_int32), ("order_d", ctypes.c_int32),
+        ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64), ("ldd", ctypes.c_int64),
+        ("stride_a", ctypes.c_int64), ("stride_b", ctypes.c_int64), ("stride_c", ctypes.c_int64),
+        ("stride_d", ctypes.c_int64), ("stride_bias", ctypes.c_int64),
+        ("dtype_a", ctypes.c_int32), ("dtype_b", ctypes.c_int32),
+        ("dtype_c", ctypes.c_int32), ("dtype_d", ctypes.c_int32),
+        ("alpha", ctypes.c_double), ("beta", ctypes.c_double),
+        ("scale_a", ctypes.c_double), ("scale_b", ctypes.c_double),
+        ("has_bias", ctypes.c_int32), ("bias_per_row", ctypes.c_int32), ("act", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        l = ctypes.CDLL(path)
+        l.oracle_gemm_rows.restype = ctypes.c_int
+        l.oracle_gemm_rows.argtypes = [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        l.oracle_decode.restype = ctypes.c_double
+        l.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_uint32]
+        l.oracle_encode.restype = ctypes.c_uint32
+        l.oracle_encode.argtypes = [ctypes.c_int, ctypes.c_double]
+        l.oracle_max_threads.restype = ctypes.c_int
+        l.oracle_scatter_d.restype = ctypes.c_int
+        l.oracle_scatter_d.argtypes = [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_void_p]
+        _lib = l
+    return _lib
+
+
+def dtype_code(name: str) -> int:
+    return _NAMES[name]
+
+
+def decode(dtype: str, bits: int) -> float:
+    return lib().oracle_decode(_NAMES[dtype], bits)
+
+
+def encode(dtype: str, value: float) -> int:
+    return lib().oracle_encode(_NAMES[dtype], value)
+
+
+def max_threads() -> int:
+    return lib().oracle_max_threads()
+
+
+def _addr(buf):
+    """Address of a CPU buffer: a numpy array or a contiguous CPU torch tensor."""
+    if buf is None:
+        return None
+    if isinstance(buf, np.ndarray):
+        assert buf.flags["C_CONTIGUOUS"]
+        return buf.ctypes.data
+    assert buf.device.type == "cpu" and buf.is_contiguous()
+    return buf.data_ptr()
+
+
+def make_problem(M, N, K, L=1, op_a="N", op_b="N", order_a="row", order_b="col",
+                 order_c="row", order_d="row", lda=None, ldb=None, ldc=None, ldd=None,
+                 stride_a=0, stride_b=0, stride_c=0, stride_d=0, stride_bias=0,
+                 dtype_a="bf16", dtype_b="bf16", dtype_c="bf16", dtype_d="bf16",
+                 alpha=1.0, beta=0.0, scale_a=1.0, scale_b=1.0, has_bias=False,
+                 bias_per_row=False, act="none"):
+    """Builds an oracle problem; leading dimensions default to the tight ones."""
+
+    def tight(order, rows, cols):
+        return cols if order == "row" else rows
+
+    a_rows, a_cols = (M, K) if op_a == "N" else (K, M)
+    b_rows, b_cols = (K, N) if op_b == "N" else (N, K)
+    p = Problem()
+    p.M, p.N, p.K, p.L = M, N, K, L
+    p.op_a, p.op_b = int(op_a == "T"), int(op_b == "T")
+    p.order_a, p.order_b = int(order_a == "row"), int(order_b == "row")
+    p.order_c, p.order_d = int(order_c == "row"), int(order_d == "row")
+    p.lda = lda if lda is not None else max(1, tight(order_a, a_rows, a_cols))
+    p.ldb = ldb if ldb is not None else max(1, tight(order_b, b_rows, b_cols))
+    p.ldc = ldc if ldc is not None else max(1, tight(order_c, M, N))
+    p.ldd = ldd if ldd is not None else max(1, tight(order_d, M, N))
+    p.stride_a, p.stride_b, p.stride_c, p.stride_d, p.stride_bias = (
+        stride_a, stride_b, stride_c, stride_d, stride_bias)
+    p.dtype_a, p.dtype_b = _NAMES[dtype_a], _NAMES[dtype_b]
+    p.dtype_c, p.dtype_d = _NAMES[dtype_c], _NAMES[dtype_d]
+    p.alpha, p.beta, p.scale_a, p.scale_b = alpha, beta, scale_a, scale_b
+    p.has_bias, p.bias_per_row = int(bool(has_bias)), int(bool(bias_per_row))
+    p.act = {"none": 0, "relu": 1}[act]
+    return p
+
+
+def gemm_rows(p: Problem, A, B, C=None, bias=None, rows=None, nthreads=0, want_t=False):
+    """Runs the oracle on the listed rows (l*M + m; default: all rows).
+
+    Returns (bits, t): ``bits`` is a (len(rows), N) array of D's raw bit
+    patterns (uint16 for 16-bit types, uint32 for fp32); ``t`` the fp64
+    values before rounding when ``want_t`` is set, else None.
+    """
+    if rows is None:
+        rows = np.arange(p.L * p.M, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.zeros((len(rows), p.N), dtype=_BITS_NP[p.dtype_d])
+    t = np.zeros((len(rows), p.N), dtype=np.float64) if want_t else None
+    rc = lib().oracle_gemm_rows(ctypes.byref(p), _addr(A), _addr(B), _addr(C), _addr(bias),
+                                len(rows), rows.ctypes.data, out.ctypes.data,
+                                None if t is None else t.ctypes.data, nthreads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_rows failed with code {rc}")
+    return out, t
+
+
+def bits_to_float64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact fp64 values of raw bit patterns, via the oracle's own decoder."""
+    code = _NAMES[dtype]
+    flat = bits.reshape(-1)
+    if dtype == "f32":
+        return flat.view(np.float32).astype(np.float64).reshape(bits.shape)
+    if dtype == "f16":
+        return flat.view(np.float16).astype(np.float64).reshape(bits.shape)
+    if dtype == "bf16":
+        widened = (flat.astype(np.uint32) << 16).view(np.float32)
+        return widened.astype(np.float64).reshape(bits.shape)
+    dec = lib().oracle_decode
+    return np.array([dec(code, int(x)) for x in flat], dtype=np.float64).reshape(bits.shape)
