@@ -1,0 +1,375 @@
+"""Benchmark: fused-epilogue GEMM TFLOP/s on one GB300 (or N replicas).
+
+A step is one launch of the whole path (the fused GEMM) over the workload's
+inputs, already resident in HBM.  Default workload: bf16 8192^3 with
+D = ReLU(0.5*A*B + 1.0*C + bias[n]) (inputs 384 MiB + 128 MiB output, far
+larger than the 129 MB L2, so no flush is needed between steps).
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle as
+the reference arm on a bounded row sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "fused_bf16_8192"
+METRIC = "GEMM TFLOP/s (2MNK/s) bf16 8192^3 and % of GB300 dense tensor peak"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = ["dense_gemm_epilogue_sm_gb300/csrc/gemm_sm103.cu", "dense_gemm_epilogue_sm_gb300/csrc/ptx.cuh",
+                  "dense_gemm_epilogue_sm_gb300/csrc/gemm_internal.h"]
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        entries = json.load(f)
+    kh = kernel_hash()
+    for e in entries:
+        if e.get("kernel_hash") == kh and e.get("workload") == workload:
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:
+            inside = [p for _, p in self.samples]
+            window = "whole run (no sample fell inside the timed region)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max((num(p[3]) or 0.0) for p in inside)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(spec, inputs, rows_target_s=12.0, min_rows=2):
+    """Times the oracle on a bounded row sample; returns (tflops, rows, secs, threads)."""
+    import numpy as np
+
+    from oracle import gemm_ref
+
+    threads = gemm_ref.max_threads()
+    rng = np.random.default_rng(0)
+    total_rows = spec.batch * spec.M
+    probe = np.sort(rng.choice(total_rows, size=min(total_rows, max(min_rows, threads)), replace=False))
+    t0 = time.perf_counter()
+    gemm_ref.run_spec_rows(spec, inputs, rows=probe)
+    dt = time.perf_counter() - t0
+    per_row = dt / len(probe)
+    n = int(min(total_rows, max(len(probe), rows_target_s / max(per_row, 1e-9))))
+    rows = np.sort(rng.choice(total_rows, size=n, replace=False))
+    t0 = time.perf_counter()
+    gemm_ref.run_spec_rows(spec, inputs, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * len(rows) * spec.N * spec.K
+    return flops / dt / 1e12, len(rows), dt, threads
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, as it stands, on bounded row samples."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    from dense_gemm_epilogue_sm_gb300 import workloads as wl
+    from oracle import gemm_ref
+    import numpy as np
+
+    spec = wl.get(args.workload)
+    inputs = wl.make_inputs(spec)
+    threads = gemm_ref.max_threads()
+    rng = np.random.default_rng(1)
+    total_rows = spec.batch * spec.M
+    # size each step so the whole --steps/--warmup run stays within about two minutes
+    probe = np.sort(rng.choice(total_rows, size=min(total_rows, threads), replace=False))
+    t0 = time.perf_counter()
+    gemm_ref.run_spec_rows(spec, inputs, rows=probe)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    budget = 100.0 / max(1, args.steps + args.warmup)
+    nrows = int(min(total_rows, max(len(probe), budget / max(per_row, 1e-9))))
+    samples = [np.sort(rng.choice(total_rows, size=nrows, replace=False)) for _ in range(args.steps + args.warmup)]
+    for s in samples[: args.warmup]:
+        gemm_ref.run_spec_rows(spec, inputs, rows=s)
+    t0 = time.perf_counter()
+    for s in samples[args.warmup:]:
+        gemm_ref.run_spec_rows(spec, inputs, rows=s)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * nrows * spec.N * spec.K * args.steps
+    value = flops / dt / 1e12
+    sample = f"{nrows} random full rows of the {spec.M}x{spec.N}x{spec.K} workload per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": spec.name, "M": spec.M, "N": spec.N, "K": spec.K},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import dense_gemm_epilogue_sm_gb300 as g
+    from dense_gemm_epilogue_sm_gb300 import workloads as wl
+    from dense_gemm_epilogue_sm_gb300.torch_ops import GemmOp, desc_from_spec
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = wl.get(args.workload)
+    inputs = wl.make_inputs(spec)
+
+    # oracle sample first (on the host cores, before the GPU is busy)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tflops, nrows, secs, threads = oracle_sample(spec, inputs, rows_target_s=args.cpu_seconds)
+        cpu = {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nrows} random full rows of {spec.M}x{spec.N}x{spec.K} ({secs:.1f} s, fp64 C loop)"}
+
+    A = inputs.A.to(dev)
+    B = inputs.B.to(dev)
+    C = inputs.C.to(dev) if inputs.C is not None else None
+    bias = inputs.bias.to(dev) if inputs.bias is not None else None
+    D = torch.empty(spec.batch * spec.matrix_elems("d"), dtype=wl.DT[spec.dtype_d], device=dev)
+    desc = desc_from_spec(spec, inputs.scale_a, inputs.scale_b)
+    info = g.gemm_plan(desc)
+    op = GemmOp(desc)
+    stream = torch.cuda.current_stream(dev)
+    flops = spec.flops()
+    in_bytes = spec.algorithmic_bytes()
+    l2_bytes = 129e6
+    flush = None
+    if in_bytes < 2 * l2_bytes:
+        flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        op(A, B, C, D, bias, stream)
+    op.check()
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local)))
+    sampler.start()
+    time.sleep(0.3)
+
+    launches0 = op.launches
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    total0 = torch.cuda.Event(enable_timing=True)
+    total1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    total0.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        op(A, B, C, D, bias, stream)
+        ends[i].record(stream)
+    total1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall1 = time.time()
+    op.check()
+    launches = op.launches - launches0
+    total_ms = total0.elapsed_time(total1)
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(wall0, wall1)
+
+    # timed region includes the flush writes when a flush is needed; the
+    # per-launch kernel time excludes them
+    step_ms = total_ms / args.steps if flush is None else statistics.mean(kernel_ms)
+    value = flops * world / (step_ms * 1e-3) / 1e12
+    avg_kernel_ms = statistics.mean(kernel_ms)
+
+    # end to end through the public API with host buffers: H2D of the inputs,
+    # the GEMM, D2H of the result, every step
+    e2e = None
+    if not args.no_e2e:
+        hA, hB = inputs.A.pin_memory(), inputs.B.pin_memory()
+        hC = inputs.C.pin_memory() if inputs.C is not None else None
+        hbias = inputs.bias.pin_memory() if inputs.bias is not None else None
+        hD = torch.empty(D.shape, dtype=D.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hA, hB, hC, hbias) if t is not None)
+        d2h = hD.numel() * hD.element_size()
+        e_steps = max(1, min(args.steps, args.e2e_steps))
+        for it in range(e_steps + 1):
+            if it == 1:
+                torch.cuda.synchronize()
+                e0 = time.perf_counter()
+            A.copy_(hA, non_blocking=True)
+            B.copy_(hB, non_blocking=True)
+            if hC is not None:
+                C.copy_(hC, non_blocking=True)
+            if hbias is not None:
+                bias.copy_(hbias, non_blocking=True)
+            op(A, B, C, D, bias, stream)
+            hD.copy_(D, non_blocking=True)
+            torch.cuda.synchronize()
+        e_dt = (time.perf_counter() - e0) / e_steps
+        e2e = {"value": flops / e_dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_dt * 1e3, "steps": e_steps}
+        op.check()
+
+    peaks, peak_src = load_peaks()
+    long_region = total_ms > 1000.0
+    pkey = "bf16_tflops_sustained" if long_region else "bf16_tflops"
+    peak = float(peaks.get(pkey, FALLBACK_PEAKS[pkey]))
+    if spec.dtype_in == "e4m3":
+        peak *= 2.0       # nominal fp8:bf16 dense ratio 4.5 : 2.25
+    achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
+    traffic = load_traffic(spec.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} {pkey}" + (" x2 (fp8 nominal ratio)" if spec.dtype_in == "e4m3" else ""),
+                "algorithmic_bytes": in_bytes,
+                "hbm_frac": (in_bytes / (avg_kernel_ms * 1e-3)) / (float(peaks.get("hbm_gbs", 6800)) * 1e9)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": spec.dtype_in if spec.dtype_in != "e4m3" else "e4m3",
+        "data": "synthetic (seeded torch CPU generator; N(0,1) operands, bias N(0,0.1))",
+        "config": {"workload": spec.name, "M": spec.M, "N": spec.N, "K": spec.K, "batch": spec.batch,
+                   "alpha": spec.alpha, "beta": spec.beta, "act": spec.act, "bias": spec.bias,
+                   "out": spec.dtype_d, "l2": "inputs larger than L2" if flush is None else "L2 flushed between steps",
+                   "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "stages": info.stages,
+                   "cta_group": info.cta_group, "tiles": info.tiles, "kernel_hash": kernel_hash()},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    op.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,499 @@
+// api.cpp - the C ABI of gemm.h: descriptor validation, planning (operand
+// orientation, tile shape, raster order), TMA descriptor encoding and launch.
+//
+// Planning follows the pages' host-side steps: the BLAS argument set and
+// "first kernel whose types, layouts and alignment fit" selection of
+// "Technical Documentation: NVIDIA/cutlass" ("Launching a GEMM kernel in
+// CUDA", "CUTLASS Library"); the alignment table of "Layouts, Tensor
+// Alignment Requirements to Target tcgen05.mma Instructions"; and tile
+// addressing and TMA metadata derived from shape:stride layouts ("CUTLASS"
+// knowledge-base page, "CuTe and layouts").
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+
+#include "../../include/gemm.h"
+#include "gemm_internal.h"
+
+using namespace gemm_sm103;
+
+namespace {
+
+int dtype_bytes(int dt) {
+    switch (dt) {
+        case GEMM_F32: return 4;
+        case GEMM_F16: return 2;
+        case GEMM_BF16: return 2;
+        case GEMM_E4M3: return 1;
+        default: return 0;
+    }
+}
+
+// Layout of a stored matrix as seen through op(): logical (r, c) of the
+// rows x cols operand.  op N: stored rows x cols; op T: stored cols x rows.
+// Row-major storage puts (i, j) at i*ld + j, column-major at i + j*ld.
+gl::Layout logical_layout(int op, int order, int64_t rows, int64_t cols, int64_t ld, int64_t batch,
+                          int64_t bstride) {
+    int64_t sr, sc;                              // strides of logical row / column index
+    const bool row_major = order == GEMM_ROW_MAJOR;
+    if (op == GEMM_OP_N) {
+        sr = row_major ? ld : 1;
+        sc = row_major ? 1 : ld;
+    } else {
+        sr = row_major ? 1 : ld;
+        sc = row_major ? ld : 1;
+    }
+    gl::Layout parts[3] = {gl::leaf(rows > 0 ? rows : 1, sr), gl::leaf(cols > 0 ? cols : 1, sc),
+                           gl::leaf(batch, bstride)};
+    gl::Layout out;
+    gl::concat(parts, 3, &out);
+    return out;
+}
+
+// Stride of mode i of a rank-3 layout built by logical_layout.
+int64_t mode_stride(const gl::Layout& l, int i) { return gl::mode(l, i).stride[0]; }
+int64_t mode_extent(const gl::Layout& l, int i) { return gl::mode(l, i).shape[0]; }
+
+// Swap the first two modes (a transpose view): composition with (c,r):(r,1)
+// would do the same; swapping the leaves is the direct form.
+gl::Layout transpose2(const gl::Layout& l) {
+    gl::Layout parts[3] = {gl::mode(l, 1), gl::mode(l, 0), gl::mode(l, 2)};
+    gl::Layout out;
+    gl::concat(parts, 3, &out);
+    return out;
+}
+
+struct Plan {
+    gemm_desc_t d;
+    gemm_plan_info_t info;
+    // kernel orientation
+    gl::Layout a, b, cd;     // a: (M', K, L), b: (N', K, L), cd: (M', N', L)
+    int64_t Mk, Nk;
+    int a_bytes, out_bytes;
+    int tile_n;
+    bool has_c;
+    int bias_mode;           // 0 none, 1 per kernel column, 2 per kernel row
+    uint32_t idesc;
+    KernelParams kp;
+};
+
+bool aligned16(int64_t elems, int bytes) { return ((elems * bytes) % 16) == 0; }
+
+gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
+    if (!desc || !out) return GEMM_ERR_INVALID_ARG;
+    const gemm_desc_t& d = *desc;
+    if (d.M < 0 || d.N < 0 || d.K < 0 || d.batch < 1) return GEMM_ERR_INVALID_ARG;
+    if (d.M > INT32_MAX || d.N > INT32_MAX || d.K > INT32_MAX || d.batch > 65535) return GEMM_ERR_UNSUPPORTED;
+    if ((d.op_a != GEMM_OP_N && d.op_a != GEMM_OP_T) || (d.op_b != GEMM_OP_N && d.op_b != GEMM_OP_T))
+        return GEMM_ERR_INVALID_ARG;
+    for (int o : {d.order_a, d.order_b, d.order_c, d.order_d})
+        if (o != GEMM_ROW_MAJOR && o != GEMM_COL_MAJOR) return GEMM_ERR_INVALID_ARG;
+    if (d.act != GEMM_ACT_NONE && d.act != GEMM_ACT_RELU) return GEMM_ERR_INVALID_ARG;
+    if (d.bias != GEMM_BIAS_NONE && d.bias != GEMM_BIAS_COL && d.bias != GEMM_BIAS_ROW) return GEMM_ERR_INVALID_ARG;
+    for (int t : {d.dtype_a, d.dtype_b, d.dtype_d})
+        if (!dtype_bytes(t)) return GEMM_ERR_INVALID_ARG;
+    const bool has_c = d.beta != 0.0f;
+    if (has_c && !dtype_bytes(d.dtype_c)) return GEMM_ERR_INVALID_ARG;
+
+    // One operand type per MMA: both f16, both bf16 or both e4m3.
+    if (d.dtype_a != d.dtype_b) return GEMM_ERR_UNSUPPORTED;
+    if (d.dtype_a == GEMM_F32) return GEMM_ERR_UNSUPPORTED;
+    if (d.dtype_d == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
+    if (has_c && (d.dtype_c != d.dtype_d || d.order_c != d.order_d)) return GEMM_ERR_UNSUPPORTED;
+
+    const int ab = dtype_bytes(d.dtype_a), ob = dtype_bytes(d.dtype_d);
+
+    // Leading dimensions must cover the stored rows (BLAS rule).
+    auto ld_ok = [](int order, int64_t srows, int64_t scols, int64_t ld) {
+        const int64_t need = order == GEMM_ROW_MAJOR ? scols : srows;
+        return ld >= (need > 1 ? need : 1);
+    };
+    const int64_t a_sr = d.op_a == GEMM_OP_N ? d.M : d.K, a_sc = d.op_a == GEMM_OP_N ? d.K : d.M;
+    const int64_t b_sr = d.op_b == GEMM_OP_N ? d.K : d.N, b_sc = d.op_b == GEMM_OP_N ? d.N : d.K;
+    if (!ld_ok(d.order_a, a_sr, a_sc, d.lda) || !ld_ok(d.order_b, b_sr, b_sc, d.ldb) ||
+        !ld_ok(d.order_d, d.M, d.N, d.ldd) || (has_c && !ld_ok(d.order_c, d.M, d.N, d.ldc)))
+        return GEMM_ERR_INVALID_ARG;
+    if (d.stride_a < 0 || d.stride_b < 0 || d.stride_c < 0 || d.stride_d < 0 || d.stride_bias < 0)
+        return GEMM_ERR_INVALID_ARG;
+    // Batches of D must not overlap.
+    if (d.batch > 1) {
+        const int64_t outer = d.order_d == GEMM_ROW_MAJOR ? d.M : d.N;
+        if (d.stride_d < outer * d.ldd) return GEMM_ERR_INVALID_ARG;
+    }
+    // TMA needs 16-byte strides: 8 elements for 16-bit, 16 for 8-bit types.
+    if (!aligned16(d.lda, ab) || !aligned16(d.ldb, ab) || !aligned16(d.ldd, ob) || (has_c && !aligned16(d.ldc, ob)))
+        return GEMM_ERR_MISALIGNED;
+    if (d.batch > 1 && (!aligned16(d.stride_a, ab) || !aligned16(d.stride_b, ab) || !aligned16(d.stride_d, ob) ||
+                        (has_c && !aligned16(d.stride_c, ob))))
+        return GEMM_ERR_MISALIGNED;
+
+    Plan& P = *out;
+    memset(&P.info, 0, sizeof(P.info));
+    P.d = d;
+    P.has_c = has_c;
+    P.a_bytes = ab;
+    P.out_bytes = ob;
+
+    const int64_t L = d.batch;
+    gl::Layout la = logical_layout(d.op_a, d.order_a, d.M, d.K, d.lda, L, L > 1 ? d.stride_a : 0);  // (M,K,L)
+    gl::Layout lbt = transpose2(logical_layout(d.op_b, d.order_b, d.K, d.N, d.ldb, L, L > 1 ? d.stride_b : 0));  // (N,K,L)
+    gl::Layout ld_ = logical_layout(GEMM_OP_N, d.order_d, d.M, d.N, d.ldd, L, d.stride_d);   // (M,N,L)
+
+    // The kernel writes D with N contiguous.  A column-major D is the
+    // row-major D^T = op(B)^T op(A)^T: swap the operands.
+    const bool swap = mode_stride(ld_, 1) != 1;
+    P.info.swapped = swap;
+    if (!swap) {
+        P.a = la;
+        P.b = lbt;
+        P.cd = ld_;
+        P.Mk = d.M;
+        P.Nk = d.N;
+    } else {
+        P.a = lbt;
+        P.b = la;
+        P.cd = transpose2(ld_);
+        P.Mk = d.N;
+        P.Nk = d.M;
+    }
+    // An operand is K-major when its K mode has unit stride.  Leading
+    // dimensions are at least 16 bytes, so exactly one mode has unit stride.
+    const bool a_kmaj = mode_stride(P.a, 1) == 1;
+    const bool b_kmaj = mode_stride(P.b, 1) == 1;
+    P.info.a_k_major = a_kmaj;
+    P.info.b_k_major = b_kmaj;
+    P.bias_mode = d.bias == GEMM_BIAS_NONE ? 0 : ((d.bias == GEMM_BIAS_COL) != swap ? 1 : 2);
+
+    // Tile shape.  1-SM MMA 128 x BN; BN = 256 reads 96 B/clk of shared
+    // memory per SM at full MMA rate (128 x 128 would need the whole 128 B/clk),
+    // so 256 is the default; 128 when N fits in it or when 256-wide tiles
+    // would leave most SMs idle.
+    const int64_t tiles_m = (P.Mk + kTileM - 1) / kTileM;
+    const int64_t tn256 = (P.Nk + 255) / 256;
+    int tile_n = 256;
+    if (P.Nk <= 128 || tiles_m * tn256 * L < 76) tile_n = 128;
+    P.tile_n = tile_n;
+    const int64_t tiles_n = (P.Nk + tile_n - 1) / tile_n;
+
+    P.info.tile_m = kTileM;
+    P.info.tile_n = tile_n;
+    P.info.tile_k = kStageKBytes / ab;
+    P.info.cta_group = 1;
+    P.info.stages = stages_for(tile_n);
+    P.info.epi_cols = 128 / ob;
+    P.info.tiles_m = tiles_m;
+    P.info.tiles_n = tiles_n;
+    P.info.tiles = tiles_m * tiles_n * L;
+    P.info.kernel_m = P.Mk;
+    P.info.kernel_n = P.Nk;
+    if (P.info.tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+
+    // Grouped raster: walk `G` M tiles, then the next N tile, so CTAs that
+    // run together share A and B panels in L2.  As layouts from the tile
+    // counter t to the linear tile index m_blk + tiles_m * n_blk.
+    const int64_t G = tiles_m < 1 ? 1 : (tiles_m < 16 ? tiles_m : 16);
+    const int64_t full_groups = tiles_m / G;
+    const int64_t tail = tiles_m - full_groups * G;
+    P.info.raster_group = (int32_t)G;
+
+    KernelParams& k = P.kp;
+    memset(&k, 0, sizeof(k));
+    k.M = (int32_t)P.Mk;
+    k.N = (int32_t)P.Nk;
+    k.K = (int32_t)d.K;
+    k.L = (int32_t)L;
+    k.tiles_m = (int32_t)tiles_m;
+    k.tiles_n = (int32_t)tiles_n;
+    k.tiles_per_batch = (int32_t)(tiles_m * tiles_n);
+    k.num_tiles = (int32_t)(tiles_m * tiles_n * L);
+    const int kel = kStageKBytes / ab;
+    k.num_kb = (int32_t)((d.K + kel - 1) / kel);
+    {
+        gl::Layout parts[3] = {gl::leaf(G, 1), gl::leaf(tiles_n, tiles_m), gl::leaf(full_groups > 0 ? full_groups : 1, G)};
+        gl::Layout full;
+        gl::concat(parts, 3, &full);
+        gl::flatten(full, &k.raster_full);
+        k.raster_full_count = (int32_t)(G * tiles_n * full_groups);
+        gl::Layout tparts[2] = {gl::leaf(tail > 0 ? tail : 1, 1), gl::leaf(tiles_n, tiles_m)};
+        gl::Layout tl;
+        gl::concat(tparts, 2, &tl);
+        gl::flatten(tl, &k.raster_tail);
+        k.raster_tail_offset = (int32_t)(full_groups * G);
+    }
+    k.a_kmajor = a_kmaj;
+    k.b_kmajor = b_kmaj;
+    k.elem_bytes = ab;
+    k.kind_f8 = d.dtype_a == GEMM_E4M3;
+    {
+        uint32_t fmt = 0;                                   // kind::f16: 0 f16, 1 bf16; kind::f8f6f4: 0 e4m3
+        if (d.dtype_a == GEMM_BF16) fmt = 1;
+        uint32_t id = 0;
+        id |= 1u << 4;                                      // accumulator fp32
+        id |= fmt << 7;                                     // A type
+        id |= fmt << 10;                                    // B type
+        id |= (a_kmaj ? 0u : 1u) << 15;                     // A MN-major
+        id |= (b_kmaj ? 0u : 1u) << 16;                     // B MN-major
+        id |= (uint32_t)(tile_n >> 3) << 17;                // N / 8
+        id |= (uint32_t)(kTileM >> 4) << 24;                // M / 16
+        P.idesc = id;
+        k.idesc = id;
+    }
+    k.a_batched = L > 1 && mode_stride(P.a, 2) != 0;
+    k.b_batched = L > 1 && mode_stride(P.b, 2) != 0;
+    k.c_batched = L > 1 && d.stride_c != 0;
+    k.alpha = d.alpha * d.scale_a * d.scale_b;            // per-tensor dequantisation folded into alpha
+    k.beta = d.beta;
+    k.has_c = has_c;
+    k.bias_mode = P.bias_mode;
+    k.bias_stride = d.stride_bias;
+    k.act = d.act;
+    k.out_f16 = d.dtype_d == GEMM_F16;
+    k.timeout_ns = kDefaultTimeoutNs;
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------------ TMA maps ----
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+CUtensorMapDataType tma_type(int dt) {
+    switch (dt) {
+        case GEMM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    }
+}
+
+// 3-D map over a kernel-orientation operand layout (rows, cols, batch): the
+// unit-stride mode becomes TMA dimension 0 (as the layout's strides dictate),
+// the other matrix mode dimension 1, the batch dimension 2.
+bool encode_map(CUtensorMap* map, const gl::Layout& lay, int dt, const void* base, uint32_t box0, uint32_t box1,
+                bool batched) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int es = dtype_bytes(dt);
+    const int inner = mode_stride(lay, 0) == 1 ? 0 : 1;
+    const int outer = 1 - inner;
+    const int64_t e_in = mode_extent(lay, inner), e_out = mode_extent(lay, outer);
+    const int64_t s_out = mode_stride(lay, outer);
+    cuuint64_t dims[3] = {(cuuint64_t)e_in, (cuuint64_t)e_out, (cuuint64_t)(batched ? mode_extent(lay, 2) : 1)};
+    const cuuint64_t row_bytes = (cuuint64_t)s_out * es;
+    const cuuint64_t bs = batched ? (cuuint64_t)mode_stride(lay, 2) * es : row_bytes * dims[1];
+    cuuint64_t strides[2] = {row_bytes, bs < row_bytes ? row_bytes : bs};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, tma_type(dt), 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+struct gemm_handle_s {
+    Plan plan;
+    int device = -1;
+    int sm_count = 0;
+    uint32_t* status = nullptr;
+    cudaStream_t last_stream = nullptr;
+    bool launched = false;
+    uint64_t launches = 0;
+    // map cache, keyed by the pointers of the last run
+    const void* cached[4] = {nullptr, nullptr, nullptr, nullptr};
+    bool cache_valid = false;
+    CUtensorMap maps[4];
+};
+
+extern "C" {
+
+gemm_status_t gemm_plan(const gemm_desc_t* desc, gemm_plan_info_t* info) {
+    if (!info) return GEMM_ERR_INVALID_ARG;
+    Plan* p = new (std::nothrow) Plan;
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    const gemm_status_t s = validate_and_plan(desc, p);
+    if (s == GEMM_OK) *info = p->info;
+    delete p;
+    return s;
+}
+
+gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    gemm_handle_s* h = new (std::nothrow) gemm_handle_s;
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t s = validate_and_plan(desc, &h->plan);
+    if (s != GEMM_OK) {
+        delete h;
+        return s;
+    }
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+        cudaGetLastError();
+        delete h;
+        return GEMM_ERR_NO_DEVICE;
+    }
+    int major = 0, minor = 0;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, h->device) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return GEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) {      // built for sm_103a only
+        delete h;
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (prepare_kernel(h->plan.tile_n, h->plan.out_bytes) != cudaSuccess ||
+        cudaMalloc(&h->status, sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        if (h->status) cudaFree(h->status);
+        delete h;
+        return GEMM_ERR_CUDA;
+    }
+    h->plan.kp.status = h->status;
+    *out = h;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D, const float* bias,
+                       void* stream) {
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    Plan& P = h->plan;
+    const gemm_desc_t& d = P.d;
+    if (d.M == 0 || d.N == 0) return GEMM_OK;
+    if (!D || (d.K > 0 && (!A || !B)) || (P.has_c && !C) || (d.bias != GEMM_BIAS_NONE && !bias))
+        return GEMM_ERR_INVALID_ARG;
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al16(D) || (A && !al16(A)) || (B && !al16(B)) || (P.has_c && !al16(C))) return GEMM_ERR_MISALIGNED;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return GEMM_ERR_MISALIGNED;
+
+    // With K == 0 nothing is loaded; give the maps a valid placeholder base.
+    const void* a_ptr = A ? A : D;
+    const void* b_ptr = B ? B : D;
+    const void* c_ptr = P.has_c ? C : D;
+    const bool swap = P.info.swapped;
+    const void* ka = swap ? b_ptr : a_ptr;
+    const void* kb = swap ? a_ptr : b_ptr;
+    const int ab = P.a_bytes;
+    const uint32_t kel = kStageKBytes / ab;
+    if (!h->cache_valid || h->cached[0] != ka || h->cached[1] != kb || h->cached[2] != c_ptr || h->cached[3] != D) {
+        const int tn = P.tile_n;
+        const uint32_t epi_cols = 128u / P.out_bytes;
+        const int adt = d.dtype_a;
+        bool ok = true;
+        // A: box {K: kel, M: 128} (K-major) or {M: kel, K: kel} (MN-major)
+        ok = ok && encode_map(&h->maps[0], P.a, adt, ka, kel, P.kp.a_kmajor ? kTileM : kel, P.kp.a_batched);
+        ok = ok && encode_map(&h->maps[1], P.b, adt, kb, kel, P.kp.b_kmajor ? (uint32_t)tn : kel, P.kp.b_batched);
+        ok = ok && encode_map(&h->maps[3], P.cd, d.dtype_d, D, epi_cols, kEpiRows, d.batch > 1);
+        if (P.has_c) {
+            gl::Layout lc = logical_layout(GEMM_OP_N, d.order_c, d.M, d.N, d.ldc, d.batch, d.stride_c);
+            if (swap) lc = transpose2(lc);
+            ok = ok && encode_map(&h->maps[2], lc, d.dtype_c, C, epi_cols, kEpiRows, P.kp.c_batched);
+        } else {
+            h->maps[2] = h->maps[3];
+        }
+        if (!ok) {
+            h->cache_valid = false;
+            return GEMM_ERR_CUDA;
+        }
+        h->cached[0] = ka;
+        h->cached[1] = kb;
+        h->cached[2] = c_ptr;
+        h->cached[3] = D;
+        h->cache_valid = true;
+    }
+    LaunchArgs la;
+    la.tmA = h->maps[0];
+    la.tmB = h->maps[1];
+    la.tmC = h->maps[2];
+    la.tmD = h->maps[3];
+    la.p = P.kp;
+    la.p.bias = bias;
+    la.tile_n = P.tile_n;
+    la.out_bytes = P.out_bytes;
+    const int64_t tiles = P.info.tiles;
+    la.grid = (int)(tiles < h->sm_count ? tiles : h->sm_count);
+    la.stream = static_cast<cudaStream_t>(stream);
+    if (la.grid < 1) return GEMM_OK;
+    const cudaError_t e = launch(la);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    h->last_stream = la.stream;
+    h->launched = true;
+    ++h->launches;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_check(gemm_handle_t h) {
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    if (h->launched && cudaStreamSynchronize(h->last_stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, h->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (word) {
+        cudaMemset(h->status, 0, sizeof(uint32_t));
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_destroy(gemm_handle_t h) {
+    if (!h) return GEMM_OK;
+    if (h->launched) cudaStreamSynchronize(h->last_stream);
+    if (h->status) cudaFree(h->status);
+    cudaGetLastError();
+    delete h;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_set_debug(gemm_handle_t h, int32_t inject_fault, uint32_t timeout_ms) {
+    if (!h || (inject_fault != 0 && inject_fault != 1)) return GEMM_ERR_INVALID_ARG;
+    h->plan.kp.inject = inject_fault;
+    if (timeout_ms) h->plan.kp.timeout_ns = (uint64_t)timeout_ms * 1000000ull;
+    return GEMM_OK;
+}
+
+uint64_t gemm_launch_count(gemm_handle_t h) { return h ? h->launches : 0; }
+
+const char* gemm_status_str(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "ok";
+        case GEMM_ERR_INVALID_ARG: return "invalid argument";
+        case GEMM_ERR_UNSUPPORTED: return "unsupported combination";
+        case GEMM_ERR_MISALIGNED: return "misaligned pointer, leading dimension or batch stride";
+        case GEMM_ERR_CUDA: return "CUDA error";
+        case GEMM_ERR_TIMEOUT: return "an in-kernel wait ran out of time";
+        case GEMM_ERR_NO_DEVICE: return "no sm_103 GPU available";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

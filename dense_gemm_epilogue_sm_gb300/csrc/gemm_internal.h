@@ -1,0 +1,74 @@
+// gemm_internal.h - what the host planner (api.cpp) hands the sm_103a kernel
+// (gemm_sm103.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "layout.hpp"
+
+namespace gemm_sm103 {
+
+// Fixed tile geometry.  A stage holds 128 bytes of K per operand row
+// (64 16-bit or 128 8-bit elements), i.e. one 128-byte swizzle row, and the
+// MMA consumes it in four 32-byte K steps (16 elements for kind::f16, 32 for
+// kind::f8f6f4).
+constexpr int kTileM = 128;
+constexpr int kStageKBytes = 128;
+constexpr int kKStepBytes = 32;
+constexpr int kThreads = 192;          // warp 0 loads, warp 1 issues MMAs, warps 2-5 run the epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kEpiRows = 32;           // rows per epilogue warp (one TMEM lane quadrant)
+constexpr int kEpiBufBytes = kEpiRows * 128;
+constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;
+
+// Status-word bits written by the kernel.
+constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusRoleLoad = 1u << 8;
+constexpr uint32_t kStatusRoleMma = 1u << 9;
+constexpr uint32_t kStatusRoleEpi = 1u << 10;
+constexpr uint32_t kStatusRoleDrain = 1u << 11;
+
+struct KernelParams {
+    int32_t M, N, K, L;           // kernel orientation: D is M x N row-major
+    int32_t tiles_m, tiles_n;
+    int32_t tiles_per_batch, num_tiles;
+    int32_t num_kb;               // K blocks of kStageKBytes
+    // Persistent tile order: tile t of a batch -> linear index m_blk + tiles_m * n_blk.
+    gl::FlatLayout raster_full;   // the groups of `raster_group` M tiles
+    gl::FlatLayout raster_tail;   // the last, shorter group
+    int32_t raster_full_count;    // tiles covered by raster_full
+    int32_t raster_tail_offset;   // first M tile of the tail group
+    int32_t a_kmajor, b_kmajor;
+    int32_t elem_bytes;           // operand element size, 1 or 2
+    int32_t kind_f8;              // 1: kind::f8f6f4, 0: kind::f16
+    uint32_t idesc;               // tcgen05 instruction descriptor
+    int32_t a_batched, b_batched, c_batched;   // 0: operand shared by all batches
+    float alpha, beta;
+    int32_t has_c;
+    int32_t bias_mode;            // 0 none, 1 per kernel column, 2 per kernel row
+    const float* bias;
+    int64_t bias_stride;
+    int32_t act;                  // 0 none, 1 ReLU
+    int32_t out_f16;              // 2-byte outputs: 1 fp16, 0 bf16
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int32_t inject;               // 1: skip the first load (bounded-wait test)
+};
+
+struct LaunchArgs {
+    CUtensorMap tmA, tmB, tmC, tmD;
+    KernelParams p;
+    int tile_n;                   // 128 or 256
+    int out_bytes;                // 2 or 4
+    int grid;
+    cudaStream_t stream;
+};
+
+int stages_for(int tile_n);
+size_t smem_bytes_for(int tile_n, int out_bytes);
+cudaError_t prepare_kernel(int tile_n, int out_bytes);
+cudaError_t launch(const LaunchArgs& a);
+
+}  // namespace gemm_sm103

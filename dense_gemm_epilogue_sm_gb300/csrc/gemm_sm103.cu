@@ -1,0 +1,461 @@
+// gemm_sm103.cu - persistent, warp-specialised fused-epilogue GEMM for
+// sm_103a (GB300): TMA -> shared-memory ring -> tcgen05.mma (fp32
+// accumulator in TMEM) -> TMEM loads -> fused alpha/beta/bias/ReLU -> TMA
+// store.
+//
+// Structure (the roles of "Technical Documentation: NVIDIA/cutlass",
+// "Blackwell Warp-specialized Persistent Kernel", re-split for this kernel):
+//   warp 0      one lane issues TMA loads of A and B tiles into a STAGES-deep
+//               ring; full[s] counts the bytes, empty[s] is released by the
+//               MMA's commit;
+//   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma into
+//               one of two TMEM accumulators (double buffering lets the
+//               epilogue of tile i overlap the main loop of tile i+1);
+//   warps 2..5  the epilogue: each warp owns one 32-lane TMEM quadrant
+//               (rows 32q..32q+31 of the 128-row tile), loads the source C
+//               subtile by TMA, applies the fusion in registers, stages D in
+//               swizzled shared memory and stores it by TMA.
+// The persistent loop is the static scheduler of "Blackwell Cluster Launch
+// Control", "Static Persistent Kernel": CTA b takes tiles b, b+grid, ...,
+// in a grouped raster order given as a layout (raster_full / raster_tail).
+//
+// Every mbarrier wait is bounded: on expiry the waiting thread sets the
+// kernel's status word and a shared abort flag, all roles leave their loops,
+// outstanding TMA loads are awaited (bounded), the MMA pipe is drained, and
+// TMEM is freed before the CTA exits.  Nothing traps.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemm_internal.h"
+#include "ptx.cuh"
+
+namespace gemm_sm103 {
+
+int stages_for(int tile_n) { return tile_n == 256 ? 4 : 6; }
+
+template <int BN, int OB>
+struct Cfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kABytes = kTileM * kStageKBytes;           // 16 KiB
+    static constexpr int kBBytes = BN * kStageKBytes;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kEpiCols = 128 / OB;                       // 64 (16-bit D) or 32 (fp32 D)
+    static constexpr int kSubtiles = BN / kEpiCols;
+    static constexpr int kTmemCols = 2 * BN;                        // two accumulators
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+    static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps + 1;
+    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kNumBars * 8 + 16;
+};
+
+size_t smem_bytes_for(int tile_n, int out_bytes) {
+    if (tile_n == 256) return out_bytes == 2 ? Cfg<256, 2>::kSmemBytes : Cfg<256, 4>::kSmemBytes;
+    return out_bytes == 2 ? Cfg<128, 2>::kSmemBytes : Cfg<128, 4>::kSmemBytes;
+}
+
+// ------------------------------------------------------------------------
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand tile
+// (tcgen05 "matrix descriptor": start address, leading- and stride-dimension
+// byte offsets, all >> 4; version 1 at bit 46; swizzle mode 2 = 128B at bits
+// 61-63).  K-major: rows of 128 bytes, 8-row groups 1024 bytes apart (SBO);
+// LBO unused.  MN-major: 128-byte rows along M/N, one row per K index;
+// 8-row K groups 1024 bytes apart (SBO), 128-byte-wide M/N chunks LBO apart.
+// ------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Bounded wait on phase `parity` of `bar`.  Gives up when another role has
+// aborted or after p.timeout_ns; on timeout records `role` in the status word
+// and raises the abort flag.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const KernelParams& p,
+                                      volatile uint32_t* abort_flag, uint32_t role) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((n & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                *abort_flag = 1u;
+                atomicOr(p.status, kStatusTimeout | role);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight copies
+// and MMAs before the CTA releases its resources).
+__device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, const KernelParams& p) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t n = 0;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((n & 31u) == 31u && ptx::globaltimer() - t0 > p.timeout_ns) {
+            atomicOr(p.status, kStatusTimeout | kStatusRoleDrain);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int& mb, int& nb, int& l) {
+    l = tile / p.tiles_per_batch;
+    const int t = tile - l * p.tiles_per_batch;
+    const int64_t idx = t < p.raster_full_count ? p.raster_full(t)
+                                                : p.raster_tail(t - p.raster_full_count) + p.raster_tail_offset;
+    mb = (int)(idx % p.tiles_m);
+    nb = (int)(idx / p.tiles_m);
+}
+
+__device__ __forceinline__ void unpack2(uint32_t w, bool f16, float& lo, float& hi) {
+    if (f16) {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w);
+        const float2 f = __half22float2(h);
+        lo = f.x;
+        hi = f.y;
+    } else {
+        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w);
+        const float2 f = __bfloat1622float2(h);
+        lo = f.x;
+        hi = f.y;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
+    uint32_t w;
+    if (f16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        w = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        w = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return w;
+}
+
+template <int BN, int OB>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                const __grid_constant__ KernelParams p) {
+    using C = Cfg<BN, OB>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = smem;
+    uint8_t* epi = ring + C::kRingBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::kEpiBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+    auto cfull_bar = [&](int i) { return bar0 + 8u * (2 * S + 4 + i); };
+    const uint32_t drain = bar0 + 8u * (2 * S + 4 + 2 * kEpiWarps);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(accf_bar(b), 1);
+            ptx::mbar_init(acce_bar(b), kEpiWarps);
+        }
+        for (int i = 0; i < 2 * kEpiWarps; ++i) ptx::mbar_init(cfull_bar(i), 1);
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmD);
+        if (p.has_c) ptx::prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<1>(ptx::smem_addr(tmem_slot), C::kTmemCols);
+        ptx::tmem_relinquish<1>();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA loads --
+        if (lane == 0) {
+            const int eb = p.elem_bytes;
+            const int kel = kStageKBytes / eb;          // K elements per stage
+            const int mn_box = kStageKBytes / eb;       // M/N elements per 128-byte row (MN-major)
+            uint32_t pend_parity[S];
+            bool pend[S];
+            for (int s = 0; s < S; ++s) pend[s] = false;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool skip_first = p.inject != 0;
+            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+                int mb, nb, l;
+                tile_coords(p, tile, mb, nb, l);
+                const int la = p.a_batched ? l : 0, lb = p.b_batched ? l : 0;
+                const int m0 = mb * kTileM, n0 = nb * BN;
+                bool stop = false;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(empty_bar(stage), phase ^ 1u, p, abort_flag, kStatusRoleLoad)) {
+                        stop = true;
+                        break;
+                    }
+                    if (skip_first) {
+                        skip_first = false;       // test hook: this stage is never filled
+                    } else {
+                        const uint32_t fb = full_bar(stage);
+                        ptx::mbar_arrive_expect_tx(fb, C::kStageBytes);
+                        const uint32_t sa = ptx::smem_addr(ring + stage * C::kStageBytes);
+                        const uint32_t sb = sa + C::kABytes;
+                        const int k0 = kb * kel;
+                        if (p.a_kmajor) {
+                            ptx::tma_load_3d(sa, &tmA, k0, m0, la, fb);
+                        } else {
+                            for (int c = 0; c < kTileM / mn_box; ++c)
+                                ptx::tma_load_3d(sa + c * (kel * 128), &tmA, m0 + c * mn_box, k0, la, fb);
+                        }
+                        if (p.b_kmajor) {
+                            ptx::tma_load_3d(sb, &tmB, k0, n0, lb, fb);
+                        } else {
+                            for (int c = 0; c < BN / mn_box; ++c)
+                                ptx::tma_load_3d(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb, fb);
+                        }
+                        pend[stage] = true;
+                        pend_parity[stage] = phase;
+                    }
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (stop) break;
+            }
+            // Every issued copy must land before the CTA may exit.
+            for (int s = 0; s < S; ++s)
+                if (pend[s]) drain_bar(full_bar(s), pend_parity[s], p);
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA -----
+        if (lane == 0) {
+            const int eb = p.elem_bytes;
+            const int kel = kStageKBytes / eb;
+            // per-K-step advance of the descriptors' start address
+            const uint32_t a_step = p.a_kmajor ? kKStepBytes : (kKStepBytes / eb) * 128u;
+            const uint32_t b_step = p.b_kmajor ? kKStepBytes : (kKStepBytes / eb) * 128u;
+            const uint32_t a_lbo = p.a_kmajor ? 16u : (uint32_t)(kel * 128);
+            const uint32_t b_lbo = p.b_kmajor ? 16u : (uint32_t)(kel * 128);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+                const int buf = it & 1;
+                const uint32_t acc_par = (uint32_t)(it >> 1) & 1u;
+                if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, abort_flag, kStatusRoleMma)) break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                bool stop = false;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(full_bar(stage), phase, p, abort_flag, kStatusRoleMma)) {
+                        stop = true;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_addr(ring + stage * C::kStageBytes);
+                    const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+                    for (int j = 0; j < kStageKBytes / kKStepBytes; ++j) {
+                        const uint64_t ad = smem_desc(sa + j * a_step, a_lbo, 1024u);
+                        const uint64_t bd = smem_desc(sb + j * b_step, b_lbo, 1024u);
+                        const uint32_t acc = (kb | j) != 0;
+                        if (p.kind_f8)
+                            ptx::mma_f8<1>(d_tmem, ad, bd, p.idesc, acc);
+                        else
+                            ptx::mma_f16<1>(d_tmem, ad, bd, p.idesc, acc);
+                    }
+                    ptx::mma_commit(empty_bar(stage));   // frees the stage once these MMAs have read it
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (stop) break;
+                if (p.num_kb > 0)
+                    ptx::mma_commit(accf_bar(buf));      // accumulator complete
+                else
+                    ptx::mbar_arrive(accf_bar(buf));     // K == 0: nothing accumulated
+            }
+            // Drain: every MMA issued above must finish before TMEM is freed.
+            ptx::mma_commit(drain);
+            drain_bar(drain, 0, p);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue -----
+        constexpr int VPC = 16 / OB;                    // output values per 16-byte chunk
+        const int ew = warp - 2;                        // staging-buffer owner
+        const int q = warp & 3;                         // TMEM lane quadrant this warp may read
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const bool f16_out = p.out_f16 != 0;
+        uint32_t c_phase[2] = {0u, 0u};
+        int sub_count = 0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+            const int buf = it & 1;
+            const uint32_t acc_par = (uint32_t)(it >> 1) & 1u;
+            int mb, nb, l;
+            tile_coords(p, tile, mb, nb, l);
+            ok = __all_sync(0xffffffffu, wait_bar(accf_bar(buf), acc_par, p, abort_flag, kStatusRoleEpi));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const int row0 = mb * kTileM + q * kEpiRows;
+            const int row = row0 + lane;
+            float row_bias = 0.f;
+            if (p.bias_mode == 2 && row < p.M) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
+            const float* bias_l = p.bias + (int64_t)l * p.bias_stride;
+            const int lc = p.c_batched ? l : 0;
+#pragma unroll 1
+            for (int sub = 0; sub < C::kSubtiles; ++sub) {
+                const int col0 = nb * BN + sub * C::kEpiCols;
+                if (row0 >= p.M || col0 >= p.N) continue;     // nothing of this subtile is in range
+                const int sbi = sub_count & 1;
+                ++sub_count;
+                uint8_t* sbuf = epi + (ew * 2 + sbi) * kEpiBufBytes;
+                const uint32_t sbuf_a = ptx::smem_addr(sbuf);
+                if (lane == 0) ptx::bulk_wait_read<1>();       // the store that last used sbuf has read it
+                __syncwarp();
+                if (p.has_c) {
+                    const uint32_t cb = cfull_bar(ew * 2 + sbi);
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(cb, kEpiBufBytes);
+                        ptx::tma_load_3d(sbuf_a, &tmC, col0, row0, lc, cb);
+                    }
+                    ok = __all_sync(0xffffffffu, wait_bar(cb, c_phase[sbi], p, abort_flag, kStatusRoleEpi));
+                    c_phase[sbi] ^= 1u;
+                    if (!ok) break;
+                }
+                uint32_t acc[C::kEpiCols];
+                if (p.num_kb > 0) {
+                    const uint32_t taddr = tmem_base + lane_off + (uint32_t)(buf * BN + sub * C::kEpiCols);
+                    ptx::tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
+                    if constexpr (C::kEpiCols == 64)
+                        ptx::tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
+                    ptx::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
+                }
+                // Row `lane` of the 32-row slab; 128-byte rows, 16-byte chunk c
+                // stored at chunk c ^ (row % 8) (the TMA 128B swizzle).
+                uint8_t* row_base = sbuf + lane * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4* slot = reinterpret_cast<uint4*>(row_base + ((ch ^ (lane & 7)) << 4));
+                    float v[VPC];
+#pragma unroll
+                    for (int i = 0; i < VPC; ++i) v[i] = p.alpha * __uint_as_float(acc[ch * VPC + i]);
+                    if (p.has_c) {
+                        const uint4 craw = *slot;
+                        const uint32_t w[4] = {craw.x, craw.y, craw.z, craw.w};
+                        if constexpr (OB == 4) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) v[i] = fmaf(p.beta, __uint_as_float(w[i]), v[i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                float lo, hi;
+                                unpack2(w[i], f16_out, lo, hi);
+                                v[2 * i] = fmaf(p.beta, lo, v[2 * i]);
+                                v[2 * i + 1] = fmaf(p.beta, hi, v[2 * i + 1]);
+                            }
+                        }
+                    }
+                    if (p.bias_mode == 1) {
+                        const int cb0 = col0 + ch * VPC;
+#pragma unroll
+                        for (int i = 0; i < VPC; ++i) v[i] += (cb0 + i < p.N) ? __ldg(bias_l + cb0 + i) : 0.f;
+                    } else if (p.bias_mode == 2) {
+#pragma unroll
+                        for (int i = 0; i < VPC; ++i) v[i] += row_bias;
+                    }
+                    if (p.act == 1) {
+#pragma unroll
+                        for (int i = 0; i < VPC; ++i) v[i] = fmaxf(v[i], 0.f);
+                    }
+                    uint4 out;
+                    if constexpr (OB == 4) {
+                        out = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                                         __float_as_uint(v[3]));
+                    } else {
+                        out = make_uint4(pack2(v[0], v[1], f16_out), pack2(v[2], v[3], f16_out),
+                                         pack2(v[4], v[5], f16_out), pack2(v[6], v[7], f16_out));
+                    }
+                    *slot = out;
+                }
+                ptx::fence_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, l);
+                    ptx::bulk_commit();
+                }
+            }
+            // This warp is done reading accumulator `buf`.
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && ok) ptx::mbar_arrive(acce_bar(buf));
+        }
+        if (lane == 0) ptx::bulk_wait<0>();
+        ptx::tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<1>(tmem_base, C::kTmemCols);
+    }
+}
+
+template <int BN, int OB>
+static cudaError_t set_attrs() {
+    return cudaFuncSetAttribute(gemm_kernel<BN, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<BN, OB>::kSmemBytes);
+}
+
+cudaError_t prepare_kernel(int tile_n, int out_bytes) {
+    if (tile_n == 256) return out_bytes == 2 ? set_attrs<256, 2>() : set_attrs<256, 4>();
+    return out_bytes == 2 ? set_attrs<128, 2>() : set_attrs<128, 4>();
+}
+
+template <int BN, int OB>
+static cudaError_t launch_t(const LaunchArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<BN, OB>::kSmemBytes;
+    cfg.stream = a.stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, OB>, a.tmA, a.tmB, a.tmC, a.tmD, a.p);
+}
+
+cudaError_t launch(const LaunchArgs& a) {
+    if (a.tile_n == 256) return a.out_bytes == 2 ? launch_t<256, 2>(a) : launch_t<256, 4>(a);
+    return a.out_bytes == 2 ? launch_t<128, 2>(a) : launch_t<128, 4>(a);
+}
+
+}  // namespace gemm_sm103

@@ -1,0 +1,61 @@
+"""Torch-facing helpers over the C ABI: descriptor construction from a
+workload spec and a handle wrapper that passes tensor pointers and the
+current CUDA stream.  Argument marshalling only; the GEMM runs in
+``libgemm_sm103.so``."""
+import torch
+
+from . import (ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E4M3, F16, F32, OP_N, OP_T,
+               ROW_MAJOR, gemm_check, gemm_create, gemm_destroy, gemm_launch_count, gemm_run, make_desc)
+
+DTYPE_CODE = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3}
+ORDER_CODE = {"row": ROW_MAJOR, "col": COL_MAJOR}
+OP_CODE = {"N": OP_N, "T": OP_T}
+ACT_CODE = {"none": ACT_NONE, "relu": ACT_RELU}
+BIAS_CODE = {"none": BIAS_NONE, "col": BIAS_COL, "row": BIAS_ROW}
+
+
+def desc_from_spec(spec, scale_a=1.0, scale_b=1.0):
+    L = spec.batch
+    stride = lambda w: spec.matrix_elems(w) if L > 1 else 0
+    bias_len = 0 if spec.bias == "none" else (spec.N if spec.bias == "col" else spec.M)
+    return make_desc(
+        spec.M, spec.N, spec.K, L, OP_CODE[spec.op_a], OP_CODE[spec.op_b], ORDER_CODE[spec.order_a],
+        ORDER_CODE[spec.order_b], ORDER_CODE[spec.order_c], ORDER_CODE[spec.order_d],
+        spec.ld("a"), spec.ld("b"), spec.ld("c"), spec.ld("d"),
+        stride("a"), stride("b"), stride("c"), stride("d"), bias_len if L > 1 else 0,
+        DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_d], DTYPE_CODE[spec.dtype_d],
+        spec.alpha, spec.beta, scale_a, scale_b, ACT_CODE[spec.act], BIAS_CODE[spec.bias])
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+class GemmOp:
+    """One planned GEMM (a handle) bound to a device; call with device tensors."""
+
+    def __init__(self, desc):
+        self.desc = desc
+        self.handle = gemm_create(desc)
+
+    def __call__(self, A, B, C, D, bias=None, stream=None):
+        s = stream if stream is not None else torch.cuda.current_stream()
+        gemm_run(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(bias), s.cuda_stream)
+
+    def check(self):
+        gemm_check(self.handle)
+
+    @property
+    def launches(self):
+        return gemm_launch_count(self.handle)
+
+    def close(self):
+        if self.handle is not None:
+            gemm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

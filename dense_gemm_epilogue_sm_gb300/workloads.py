@@ -1,0 +1,191 @@
+"""Seeded synthetic GEMM workloads: problem specs and input tensors.
+
+Input generation only; no GEMM arithmetic lives here.  Both the CUDA path
+(tests, benchmark) and the oracle read the tensors built here, so parity does
+not depend on how they are drawn.
+
+Recipe: a ``torch.Generator('cpu')`` seeded per workload draws, in this
+order, A, B, C, bias as fp32 in storage order; 16-bit operands are the fp32
+draws rounded to nearest-even.  8-bit (e4m3) operands are quantised with a
+per-tensor scale s = 448 / max|x| (q = e4m3(clamp(x*s, +-448)), rounded to
+nearest-even by torch) and the dequantisation factors 1/s are handed to the
+GEMM as scale_a / scale_b.
+
+The named workloads are the five configurations the method is measured on:
+a tiny exact fp16 GEMM, plain bf16 4096^3, the fused-epilogue bf16 8192^3
+ReLU(0.5*A*B + C + bias), e4m3 8192^3, and odd/skinny/batched bf16 shapes.
+"""
+from dataclasses import dataclass, field, replace
+
+import torch
+
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
+ESIZE = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
+
+
+@dataclass
+class Spec:
+    name: str
+    M: int
+    N: int
+    K: int
+    batch: int = 1
+    op_a: str = "N"
+    op_b: str = "N"
+    order_a: str = "row"
+    order_b: str = "col"
+    order_c: str = "row"
+    order_d: str = "row"
+    dtype_in: str = "bf16"
+    dtype_d: str = "bf16"
+    alpha: float = 1.0
+    beta: float = 0.0
+    act: str = "none"
+    bias: str = "none"          # none | col | row
+    dist: str = "normal"        # normal | int4 | uniform1
+    bias_sigma: float = 0.1
+    seed: int = 0
+    pad: int = 0                # extra elements added to every leading dimension
+    lda: int = 0                # 0: tight (+pad)
+    ldb: int = 0
+    ldc: int = 0
+    ldd: int = 0
+    notes: str = ""
+
+    # ----------------------------------------------------------- geometry --
+    def stored(self, which):
+        """(rows, cols) of the stored matrix."""
+        if which == "a":
+            return (self.M, self.K) if self.op_a == "N" else (self.K, self.M)
+        if which == "b":
+            return (self.K, self.N) if self.op_b == "N" else (self.N, self.K)
+        return (self.M, self.N)
+
+    def order(self, which):
+        return {"a": self.order_a, "b": self.order_b, "c": self.order_c, "d": self.order_d}[which]
+
+    def ld(self, which):
+        given = {"a": self.lda, "b": self.ldb, "c": self.ldc, "d": self.ldd}[which]
+        if given:
+            return given
+        r, c = self.stored(which)
+        tight = c if self.order(which) == "row" else r
+        esz = ESIZE[self.dtype_in if which in "ab" else self.dtype_d]
+        align = 16 // esz
+        return max(align, -(-(tight + self.pad) // align) * align)
+
+    def outer(self, which):
+        r, c = self.stored(which)
+        return r if self.order(which) == "row" else c
+
+    def matrix_elems(self, which):
+        return self.outer(which) * self.ld(which)
+
+    def flops(self):
+        return 2.0 * self.M * self.N * self.K * self.batch
+
+    def algorithmic_bytes(self):
+        """Each operand read once, D written once (bias and C included)."""
+        e_in, e_d = ESIZE[self.dtype_in], ESIZE[self.dtype_d]
+        b = self.batch * (self.M * self.K * e_in + self.K * self.N * e_in + self.M * self.N * e_d)
+        if self.beta != 0:
+            b += self.batch * self.M * self.N * e_d
+        if self.bias != "none":
+            b += 4 * (self.N if self.bias == "col" else self.M)
+        return b
+
+
+WORKLOADS = {
+    "tiny_exact_fp16_256": Spec(
+        "tiny_exact_fp16_256", 256, 256, 256, op_a="N", op_b="N", order_a="col", order_b="col",
+        order_c="col", order_d="col", dtype_in="f16", dtype_d="f32", dist="int4", seed=0,
+        notes="integer entries in [-4,4]; every sum exact in fp32"),
+    "bf16_4096": Spec("bf16_4096", 4096, 4096, 4096, order_a="row", order_b="col", seed=1),
+    "fused_bf16_8192": Spec(
+        "fused_bf16_8192", 8192, 8192, 8192, order_a="row", order_b="col", alpha=0.5, beta=1.0,
+        act="relu", bias="col", seed=2, notes="D = ReLU(0.5*A*B + 1.0*C + bias[n])"),
+    "fp8_e4m3_8192": Spec(
+        "fp8_e4m3_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e4m3",
+        dist="uniform1", seed=3, notes="per-tensor scales folded into alpha"),
+    "odd_1000_at": Spec(
+        "odd_1000_at", 1000, 1000, 1000, op_a="T", order_a="col", order_b="col", seed=4,
+        notes="A transposed: stored K x M column-major, lda = K"),
+    "skinny_65536x256x4096": Spec(
+        "skinny_65536x256x4096", 65536, 256, 4096, order_a="row", order_b="col", beta=1.0, seed=5,
+        notes="memory-bound: A dominates the bytes"),
+    "batched_32x512": Spec("batched_32x512", 512, 512, 512, batch=32, order_a="row", order_b="col", seed=6),
+}
+
+
+def get(name, **overrides):
+    return replace(WORKLOADS[name], **overrides)
+
+
+def _draw(gen, n, dist):
+    if dist == "normal":
+        return torch.randn(n, generator=gen, dtype=torch.float32)
+    if dist == "int4":
+        return torch.randint(-4, 5, (n,), generator=gen).to(torch.float32)
+    if dist == "uniform1":
+        return torch.rand(n, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    raise ValueError(dist)
+
+
+def _quantise_e4m3(x):
+    """Per-tensor e4m3 quantisation: returns (codes, dequantisation factor)."""
+    amax = float(x.abs().max())
+    s = 448.0 / amax if amax > 0 else 1.0
+    s = float(torch.tensor(s, dtype=torch.float32))
+    q = (x * s).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q, float(torch.tensor(1.0 / s, dtype=torch.float32))
+
+
+@dataclass
+class Inputs:
+    spec: Spec
+    A: torch.Tensor                  # flat storage, operand dtype
+    B: torch.Tensor
+    C: torch.Tensor = None           # flat storage, D's dtype (None when beta == 0)
+    bias: torch.Tensor = None        # fp32, (batch * len) when present
+    scale_a: float = 1.0
+    scale_b: float = 1.0
+    extras: dict = field(default_factory=dict)
+
+    def stride(self, which):
+        return self.spec.matrix_elems(which) if self.spec.batch > 1 else 0
+
+    def bias_len(self):
+        s = self.spec
+        return 0 if s.bias == "none" else (s.N if s.bias == "col" else s.M)
+
+
+def make_inputs(spec: Spec) -> Inputs:
+    """Builds the storage buffers of one workload (CPU tensors).  Padding
+    elements beyond each leading extent are drawn too (they are never read)."""
+    gen = torch.Generator(device="cpu").manual_seed(spec.seed)
+    L = spec.batch
+    out = {}
+    scales = {}
+    for which in ("a", "b"):
+        n = L * spec.matrix_elems(which)
+        x = _draw(gen, n, spec.dist)
+        if spec.dtype_in == "e4m3":
+            q, d = _quantise_e4m3(x)
+            out[which] = q
+            scales[which] = d
+        else:
+            out[which] = x.to(DT[spec.dtype_in])
+            scales[which] = 1.0
+    C = None
+    if spec.beta != 0:
+        C = _draw(gen, L * spec.matrix_elems("c"), "normal" if spec.dist != "int4" else "int4").to(DT[spec.dtype_d])
+    bias = None
+    if spec.bias != "none":
+        n = spec.N if spec.bias == "col" else spec.M
+        bias = (torch.randn(L * n, generator=gen, dtype=torch.float32) * spec.bias_sigma)
+    return Inputs(spec, out["a"], out["b"], C, bias, scales["a"], scales["b"])
+
+
+def empty_output(spec: Spec, device="cpu", fill=float("nan")):
+    n = spec.batch * spec.matrix_elems("d")
+    return torch.full((n,), fill, dtype=DT[spec.dtype_d], device=device)

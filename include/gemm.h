@@ -1,0 +1,152 @@
+/*
+ * gemm.h - C ABI of the GB300 (sm_103a) fused-epilogue dense GEMM.
+ *
+ * Operation (one call, all batches l < batch):
+ *
+ *   D(l) = act( alpha * scale_a * scale_b * op(A(l)) * op(B(l))
+ *               + beta * C(l) + bias(l) )
+ *
+ * with fp32 accumulation, op in {N, T}, and D rounded to its type with
+ * round-to-nearest-even.  This is the BLAS-style operation
+ * "C = alpha * op(A) * op(B) + beta * C" of the page "CUTLASS" (knowledge
+ * base, opening section) with a separate output D that may alias C
+ * ("Technical Documentation: NVIDIA/cutlass", "Launching a GEMM kernel in
+ * CUDA"), and the fused epilogue of the same page's "Epilogues" section and of
+ * "Utilities for SM100", "Background - SM100 epilogue flow": accumulator, then
+ * source C, then bias and activation, then the store.  scale_a / scale_b are
+ * per-tensor dequantisation factors for 8-bit operands (the block-scaled form
+ * of "Blackwell SM100 GEMMs", "Block Scaled GEMMs", with one factor per
+ * tensor); pass 1.0 otherwise.
+ *
+ * Storage follows the BLAS convention: op(A) is M x K, stored as M x K (op N)
+ * or K x M (op T) in row- or column-major order with leading dimension lda;
+ * likewise op(B) is K x N; C and D are M x N.  All counts are in elements.
+ * Batch l starts at base + l * stride_x.  bias is fp32: bias[n] (per column,
+ * broadcast down M) or bias[m] (per row), batch stride stride_bias (0 shares
+ * one vector across batches).
+ *
+ * Supported (anything else returns GEMM_ERR_UNSUPPORTED; there is no
+ * fallback path):
+ *   A, B: both F16, both BF16, or both E4M3 (a single tensor-core operand
+ *         type per MMA); any op/order combination.
+ *   C, D: F32, F16 or BF16, same type for C and D, same order for C and D.
+ * Alignment (the tensor-alignment tables of "Technical Documentation:
+ * NVIDIA/cutlass", "Layouts, Tensor Alignment Requirements to Target
+ * tcgen05.mma Instructions": 8 elements for 16-bit, 16 for 8-bit operands):
+ * every leading dimension and batch stride must be a multiple of 16 bytes and
+ * every base pointer 16-byte aligned; otherwise GEMM_ERR_MISALIGNED.
+ *
+ * Ownership: the caller owns every device buffer.  A handle owns host state
+ * and one 4-byte device status word allocated by gemm_create and freed by
+ * gemm_destroy.  gemm_run never allocates or frees memory.
+ *
+ * Errors: argument errors are returned synchronously.  gemm_run is
+ * asynchronous on the given stream; a failed launch returns GEMM_ERR_CUDA.
+ * Every wait inside the kernel is bounded: if one runs out (default 2 s, see
+ * gemm_set_debug) the kernel stops, records the fact in the status word and
+ * returns without faulting, and the next gemm_check reports
+ * GEMM_ERR_TIMEOUT.  The CUDA context stays usable.
+ */
+#ifndef GEMM_SM103_H
+#define GEMM_SM103_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifndef GEMM_API
+#define GEMM_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,
+    GEMM_ERR_UNSUPPORTED = 2,
+    GEMM_ERR_MISALIGNED = 3,
+    GEMM_ERR_CUDA = 4,
+    GEMM_ERR_TIMEOUT = 5,
+    GEMM_ERR_NO_DEVICE = 6
+} gemm_status_t;
+
+typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3 } gemm_dtype_t;
+typedef enum { GEMM_COL_MAJOR = 0, GEMM_ROW_MAJOR = 1 } gemm_order_t;
+typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1 } gemm_act_t;
+typedef enum { GEMM_BIAS_NONE = 0, GEMM_BIAS_COL = 1, GEMM_BIAS_ROW = 2 } gemm_bias_t;
+
+/* Problem descriptor.  Enumerations are carried as int32_t. */
+typedef struct {
+    int64_t M, N, K, batch;                        /* batch >= 1; M, N, K >= 0 */
+    int32_t op_a, op_b;                            /* gemm_op_t */
+    int32_t order_a, order_b, order_c, order_d;    /* gemm_order_t */
+    int64_t lda, ldb, ldc, ldd;                    /* leading dimensions, elements */
+    int64_t stride_a, stride_b, stride_c, stride_d, stride_bias; /* batch strides, elements */
+    int32_t dtype_a, dtype_b, dtype_c, dtype_d;    /* gemm_dtype_t */
+    float alpha, beta;
+    float scale_a, scale_b;                        /* 1.0 unless 8-bit operands */
+    int32_t act;                                   /* gemm_act_t */
+    int32_t bias;                                  /* gemm_bias_t; bias is fp32 */
+} gemm_desc_t;
+
+/* How a descriptor is executed; filled by gemm_plan (host only, no GPU). */
+typedef struct {
+    int32_t swapped;          /* 1: computed as D^T = op(B)^T op(A)^T because D is column-major */
+    int32_t a_k_major;        /* kernel operand A (after any swap) is K-contiguous */
+    int32_t b_k_major;        /* kernel operand B (after any swap) is K-contiguous */
+    int32_t tile_m, tile_n;   /* output tile per CTA (per CTA pair when cta_group == 2) */
+    int32_t tile_k;           /* K elements per pipeline stage */
+    int32_t cta_group;        /* SMs sharing one MMA: 1 or 2 */
+    int32_t stages;           /* shared-memory pipeline depth */
+    int32_t raster_group;     /* M tiles walked together by the persistent scheduler */
+    int32_t epi_cols;         /* epilogue subtile width, columns */
+    int64_t tiles_m, tiles_n, tiles;   /* tiles along M and N (kernel orientation), total incl. batch */
+    int64_t kernel_m, kernel_n;        /* problem extents in kernel orientation */
+} gemm_plan_info_t;
+
+typedef struct gemm_handle_s* gemm_handle_t;
+
+/* Validates `desc` and reports how it would run.  Host only: makes no CUDA
+ * call and works without a GPU.  Returns GEMM_OK, GEMM_ERR_INVALID_ARG,
+ * GEMM_ERR_UNSUPPORTED or GEMM_ERR_MISALIGNED (strides). */
+GEMM_API gemm_status_t gemm_plan(const gemm_desc_t* desc, gemm_plan_info_t* info);
+
+/* Validates `desc`, plans it and allocates the handle (host state plus a
+ * 4-byte device status word on the current device).  Returns
+ * GEMM_ERR_NO_DEVICE when no usable GPU is present.  *out is NULL on error. */
+GEMM_API gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc);
+
+/* Launches the GEMM on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) with device pointers.  C may be NULL iff beta == 0; bias may be
+ * NULL iff the descriptor has no bias.  D may equal C (same layout).
+ * Asynchronous; never allocates.  M == 0 or N == 0 launches nothing. */
+GEMM_API gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
+                       const float* bias, void* stream);
+
+/* Waits for the handle's last launch and reads its device status word:
+ * GEMM_ERR_TIMEOUT if any bounded wait ran out (the word is then cleared),
+ * GEMM_ERR_CUDA on a CUDA error, else GEMM_OK. */
+GEMM_API gemm_status_t gemm_check(gemm_handle_t h);
+
+/* Frees the handle (synchronises with its last launch first). NULL is a no-op. */
+GEMM_API gemm_status_t gemm_destroy(gemm_handle_t h);
+
+/* Test hooks.  inject_fault = 1 makes the load warp skip the very first
+ * tile load of the next launches (the consumer then waits until its bound
+ * runs out); 0 restores normal operation.  timeout_ms bounds every
+ * in-kernel wait (0 keeps the current bound; default 2000 ms). */
+GEMM_API gemm_status_t gemm_set_debug(gemm_handle_t h, int32_t inject_fault, uint32_t timeout_ms);
+
+/* Kernel launches issued through this handle so far. */
+GEMM_API uint64_t gemm_launch_count(gemm_handle_t h);
+
+/* Static string for a status code. */
+GEMM_API const char* gemm_status_str(gemm_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_SM103_H */

@@ -152,3 +152,24 @@ def bits_to_float64(bits: np.ndarray, dtype: str) -> np.ndarray:
         return widened.astype(np.float64).reshape(bits.shape)
     dec = lib().oracle_decode
     return np.array([dec(code, int(x)) for x in flat], dtype=np.float64).reshape(bits.shape)
+
+
+def problem_from_spec(spec, inputs):
+    """Oracle problem for a workload spec and its generated inputs (duck-typed:
+    any object with the workload's attribute names)."""
+    L = spec.batch
+    stride = lambda w: spec.matrix_elems(w) if L > 1 else 0
+    bias_len = 0 if spec.bias == "none" else (spec.N if spec.bias == "col" else spec.M)
+    return make_problem(
+        spec.M, spec.N, spec.K, L, spec.op_a, spec.op_b, spec.order_a, spec.order_b, spec.order_c, spec.order_d,
+        spec.ld("a"), spec.ld("b"), spec.ld("c"), spec.ld("d"),
+        stride("a"), stride("b"), stride("c"), stride("d"), bias_len if L > 1 else 0,
+        spec.dtype_in, spec.dtype_in, spec.dtype_d, spec.dtype_d,
+        spec.alpha, spec.beta, inputs.scale_a, inputs.scale_b,
+        spec.bias != "none", spec.bias == "row", spec.act)
+
+
+def run_spec_rows(spec, inputs, rows=None, nthreads=0, want_t=False):
+    """Oracle rows (l*M + m) of a workload; returns (bits, t) as gemm_rows."""
+    p = problem_from_spec(spec, inputs)
+    return gemm_rows(p, inputs.A, inputs.B, inputs.C, inputs.bias, rows=rows, nthreads=nthreads, want_t=want_t)

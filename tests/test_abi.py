@@ -1,0 +1,160 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+public headers declare, validates descriptors and plans them (host only)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import dense_gemm_epilogue_sm_gb300 as g
+from dense_gemm_epilogue_sm_gb300 import workloads as wl
+from dense_gemm_epilogue_sm_gb300.torch_ops import desc_from_spec
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names.update(re.findall(r"^GEMM_API\s+[\w\s\*]+?\b(gemm_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_headers_declare_something():
+    names = _declared_symbols()
+    assert {"gemm_create", "gemm_run", "gemm_destroy", "gemm_plan", "gemm_layout_eval"} <= names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(g.LIBRARY_PATH)
+    missing = [n for n in sorted(_declared_symbols()) if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    assert set(g.EXPORTED) == _declared_symbols()
+
+
+def test_status_strings():
+    for s in range(7):
+        assert g.gemm_status_str(s)
+    assert "unknown" in g.gemm_status_str(99)
+
+
+def _desc(**kw):
+    base = dict(M=256, N=512, K=128)
+    base.update(kw)
+    M, N, K = base.pop("M"), base.pop("N"), base.pop("K")
+    return g.make_desc(M, N, K, **base)
+
+
+def _status(desc):
+    info = g.GemmPlanInfo()
+    return g.lib.gemm_plan(ctypes.byref(desc), ctypes.byref(info)), info
+
+
+@pytest.mark.parametrize("field,value,want", [
+    ("M", -1, g.ERR_INVALID_ARG), ("K", -5, g.ERR_INVALID_ARG), ("batch", 0, g.ERR_INVALID_ARG),
+    ("op_a", 2, g.ERR_INVALID_ARG), ("order_d", 7, g.ERR_INVALID_ARG), ("act", 3, g.ERR_INVALID_ARG),
+    ("bias", 9, g.ERR_INVALID_ARG), ("dtype_a", 11, g.ERR_INVALID_ARG),
+    ("lda", 64, g.ERR_INVALID_ARG),           # row-major A needs lda >= K = 128
+    ("lda", 132, g.ERR_MISALIGNED),           # 264 bytes: not a multiple of 16
+    ("ldd", 516, g.ERR_MISALIGNED),
+])
+def test_rejects_bad_descriptors(field, value, want):
+    d = _desc()
+    setattr(d, field, value)
+    assert _status(d)[0] == want
+
+
+def test_rejects_unsupported_combinations():
+    d = _desc(dtype_a=g.F16, dtype_b=g.BF16)          # one operand type per MMA
+    assert _status(d)[0] == g.ERR_UNSUPPORTED
+    d = _desc(dtype_a=g.F32, dtype_b=g.F32)
+    assert _status(d)[0] == g.ERR_UNSUPPORTED
+    d = _desc(beta=1.0, dtype_c=g.F32, dtype_d=g.BF16)
+    assert _status(d)[0] == g.ERR_UNSUPPORTED
+    d = _desc(beta=1.0, order_c=g.COL_MAJOR, order_d=g.ROW_MAJOR)
+    assert _status(d)[0] == g.ERR_UNSUPPORTED
+    d = _desc(dtype_d=g.E4M3)
+    assert _status(d)[0] == g.ERR_UNSUPPORTED
+
+
+def test_e4m3_needs_16_element_alignment():
+    d = _desc(dtype_a=g.E4M3, dtype_b=g.E4M3, K=136)   # lda = 136 bytes
+    assert _status(d)[0] == g.ERR_MISALIGNED
+    d = _desc(dtype_a=g.E4M3, dtype_b=g.E4M3, K=144)
+    assert _status(d)[0] == g.OK
+
+
+def test_batch_d_must_not_overlap():
+    d = _desc(batch=2)
+    d.stride_d = 10
+    assert _status(d)[0] == g.ERR_INVALID_ARG
+
+
+def test_plan_orientation_and_majorness():
+    # row-major D: no swap; A row-major op N is K-major; B column-major op N is K-major
+    s, info = _status(_desc(order_a=g.ROW_MAJOR, order_b=g.COL_MAJOR, order_d=g.ROW_MAJOR))
+    assert s == g.OK and not info.swapped and info.a_k_major and info.b_k_major
+    assert (info.kernel_m, info.kernel_n) == (256, 512)
+    # column-major D: computed as D^T; the kernel's A is op(B)^T, its B is op(A)
+    s, info = _status(_desc(order_a=g.COL_MAJOR, order_b=g.COL_MAJOR, order_c=g.COL_MAJOR, order_d=g.COL_MAJOR))
+    assert s == g.OK and info.swapped
+    assert (info.kernel_m, info.kernel_n) == (512, 256)
+    assert info.a_k_major and not info.b_k_major       # B col-major is K-contiguous; A col-major is M-contiguous
+    # transposes flip majorness
+    s, info = _status(_desc(op_a=g.OP_T, order_a=g.ROW_MAJOR, lda=256))
+    assert s == g.OK and not info.a_k_major
+
+
+def test_plan_tiles_for_the_named_workloads():
+    want = {
+        "bf16_4096": (256, 32, 16, 512),
+        "fused_bf16_8192": (256, 64, 32, 2048),
+        "fp8_e4m3_8192": (256, 64, 32, 2048),
+        "skinny_65536x256x4096": (256, 512, 1, 512),
+        "batched_32x512": (256, 4, 2, 256),
+    }
+    for name, (tn, tm, tnn, tiles) in want.items():
+        spec = wl.get(name)
+        info = g.gemm_plan(desc_from_spec(spec))
+        assert (info.tile_n, info.tiles_m, info.tiles_n, info.tiles) == (tn, tm, tnn, tiles), name
+        assert info.tile_k == (128 if spec.dtype_in == "e4m3" else 64)
+    info = g.gemm_plan(desc_from_spec(wl.get("tiny_exact_fp16_256")))
+    assert info.swapped and info.tile_n == 128 and info.epi_cols == 32
+    info = g.gemm_plan(desc_from_spec(wl.get("odd_1000_at")))
+    assert info.a_k_major and info.b_k_major and info.tile_n == 128
+
+
+def test_raster_order_is_a_bijection():
+    # The persistent scheduler's tile order, built from the plan exactly as
+    # the planner does, must visit every tile once.
+    for tm, tn in [(64, 32), (20, 3), (16, 16), (1, 7), (37, 5)]:
+        G = min(tm, 16)
+        full = tm // G
+        tail = tm - full * G
+        order = []
+        lay_full = f"({G},{tn},{max(full, 1)}):(1,{tm},{G})"
+        for t in range(G * tn * full):
+            order.append(g.gemm_layout_eval(lay_full, t))
+        lay_tail = f"({max(tail, 1)},{tn}):(1,{tm})"
+        for t in range(tm * tn - G * tn * full):
+            order.append(g.gemm_layout_eval(lay_tail, t) + full * G)
+        assert sorted(order) == list(range(tm * tn))
+        # consecutive tiles walk G rows of M before the next column of N
+        assert [o % tm for o in order[:G]] == list(range(G))
+
+
+def test_create_without_gpu_reports_no_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_create(_desc())
+    assert e.value.status == g.ERR_NO_DEVICE
+    # argument errors are still reported first
+    d = _desc()
+    d.M = -3
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_create(d)
+    assert e.value.status == g.ERR_INVALID_ARG
