@@ -250,6 +250,9 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     k.bias_stride = d.stride_bias;
     k.act = d.act;
     k.out_f16 = d.dtype_d == GEMM_F16;
+    k.d_ragged = ((P.Nk * ob) % 16) != 0;
+    k.ldd = mode_stride(P.cd, 0);
+    k.d_bstride = mode_stride(P.cd, 2);
     k.timeout_ns = kDefaultTimeoutNs;
     return GEMM_OK;
 }
@@ -430,6 +433,7 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void
     la.tmD = h->maps[3];
     la.p = P.kp;
     la.p.bias = bias;
+    la.p.d_ptr = D;
     la.tile_n = P.tile_n;
     la.out_bytes = P.out_bytes;
     const int64_t tiles = P.info.tiles;

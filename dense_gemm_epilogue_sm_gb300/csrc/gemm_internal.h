@@ -52,6 +52,13 @@ struct KernelParams {
     int64_t bias_stride;
     int32_t act;                  // 0 none, 1 ReLU
     int32_t out_f16;              // 2-byte outputs: 1 fp16, 0 bf16
+    // A TMA store clips the inner dimension only at 16-byte granules, so when
+    // a D row does not end on a 16-byte boundary the subtile holding its last
+    // columns is written with plain stores instead.
+    int32_t d_ragged;
+    void* d_ptr;
+    int64_t ldd;                  // kernel orientation: row stride of D, elements
+    int64_t d_bstride;            // batch stride of D, elements
     uint32_t* status;
     uint64_t timeout_ns;
     int32_t inject;               // 1: skip the first load (bounded-wait test)

@@ -333,6 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int sub = 0; sub < C::kSubtiles; ++sub) {
                 const int col0 = nb * BN + sub * C::kEpiCols;
                 if (row0 >= p.M || col0 >= p.N) continue;     // nothing of this subtile is in range
+                // the subtile holding a ragged row end is stored element by element
+                const bool direct = p.d_ragged && col0 + C::kEpiCols > p.N;
                 const int sbi = sub_count & 1;
                 ++sub_count;
                 uint8_t* sbuf = epi + (ew * 2 + sbi) * kEpiBufBytes;
@@ -405,13 +407,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         out = make_uint4(pack2(v[0], v[1], f16_out), pack2(v[2], v[3], f16_out),
                                          pack2(v[4], v[5], f16_out), pack2(v[6], v[7], f16_out));
                     }
-                    *slot = out;
+                    if (!direct) {
+                        *slot = out;
+                    } else if (row < p.M) {
+                        const int c0 = col0 + ch * VPC;
+                        const uint32_t w[4] = {out.x, out.y, out.z, out.w};
+                        uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
+                                        ((int64_t)l * p.d_bstride + (int64_t)row * p.ldd) * OB;
+#pragma unroll
+                        for (int i = 0; i < VPC; ++i) {
+                            if (c0 + i >= p.N) break;
+                            if constexpr (OB == 4)
+                                *reinterpret_cast<uint32_t*>(drow + (int64_t)(c0 + i) * 4) = w[i];
+                            else
+                                *reinterpret_cast<uint16_t*>(drow + (int64_t)(c0 + i) * 2) =
+                                    (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
+                        }
+                    }
                 }
-                ptx::fence_async_shared();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, l);
-                    ptx::bulk_commit();
+                if (!direct) {
+                    ptx::fence_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, l);
+                        ptx::bulk_commit();
+                    }
                 }
             }
             // This warp is done reading accumulator `buf`.

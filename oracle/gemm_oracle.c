@@ -194,6 +194,72 @@ static int nthreads_or_default(int nthreads) {
 int oracle_max_threads(void) { return nthreads_or_default(0); }
 
 /*
+ * b(l, k, n) decoded into a k-major fp64 panel (K x N).  The last panel is
+ * kept and reused when the next call names the same storage with the same
+ * bytes (an FNV-1a hash of the operand's storage span is part of the key), so
+ * repeated calls on one operand decode it once.  Not thread-safe: calls into
+ * the oracle are sequential.
+ */
+static double* g_panel = NULL;
+static size_t g_panel_cap = 0;
+static struct {
+    const void* base;
+    int64_t K, N, l, ldb, stride_b;
+    int32_t op_b, order_b, dtype_b;
+    uint64_t hash;
+    int valid;
+} g_key;
+
+static uint64_t fnv1a(const uint8_t* p, size_t n) {
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < n; ++i) {
+        h ^= p[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+static const double* b_panel(const oracle_problem_t* p, const void* B, int64_t l) {
+    const int64_t K = p->K, N = p->N;
+    int eb, mb, ieee;
+    const int bytes = type_bits(p->dtype_b, &eb, &mb, &ieee) / 8;
+    /* the storage span this batch of B occupies */
+    const int64_t srows = p->op_b == 0 ? K : N, scols = p->op_b == 0 ? N : K;
+    const int64_t outer = p->order_b == 1 ? srows : scols;
+    const int64_t inner = p->order_b == 1 ? scols : srows;
+    const int64_t span = outer > 0 && inner > 0 ? (outer - 1) * p->ldb + inner : 0;
+    const uint8_t* first = (const uint8_t*)B + (size_t)(l * p->stride_b) * bytes;
+    const uint64_t h = fnv1a(first, (size_t)span * bytes);
+    if (g_key.valid && g_key.base == B && g_key.K == K && g_key.N == N && g_key.l == l && g_key.ldb == p->ldb &&
+        g_key.stride_b == p->stride_b && g_key.op_b == p->op_b && g_key.order_b == p->order_b &&
+        g_key.dtype_b == p->dtype_b && g_key.hash == h)
+        return g_panel;
+    const size_t need = (size_t)(K > 0 ? K : 1) * (size_t)N;
+    if (need > g_panel_cap) {
+        free(g_panel);
+        g_panel = (double*)malloc(sizeof(double) * need);
+        g_panel_cap = g_panel ? need : 0;
+        g_key.valid = 0;
+        if (!g_panel) return NULL;
+    }
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n)
+            g_panel[k * N + n] = oracle_decode(p->dtype_b, load_bits(B, p->dtype_b, b_index(p, l, k, n)));
+    g_key.base = B;
+    g_key.K = K;
+    g_key.N = N;
+    g_key.l = l;
+    g_key.ldb = p->ldb;
+    g_key.stride_b = p->stride_b;
+    g_key.op_b = p->op_b;
+    g_key.order_b = p->order_b;
+    g_key.dtype_b = p->dtype_b;
+    g_key.hash = h;
+    g_key.valid = 1;
+    return g_panel;
+}
+
+/*
  * Computes the full output rows listed in `rows` (each entry is l*M + m).
  * Row i of the result goes to Dout[i*N .. i*N+N-1], packed in D's type, and,
  * when Tout is not NULL, the fp64 value before rounding to Tout[i*N + n].
@@ -215,17 +281,13 @@ int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, co
     const int nt = nthreads_or_default(nthreads);
     if (nrows == 0 || N == 0) return 0;
 
-    /* b(l, k, n) decoded once per batch into a k-major fp64 panel. */
-    double* Bd = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)N);
-    if (!Bd) return -6;
     int status = 0;
     for (int64_t l = 0; l < p->L; ++l) {
         int64_t in_batch = 0;
         for (int64_t i = 0; i < nrows; ++i) in_batch += (rows[i] / M) == l;
         if (!in_batch) continue;
-        for (int64_t k = 0; k < K; ++k)
-            for (int64_t n = 0; n < N; ++n)
-                Bd[k * N + n] = oracle_decode(p->dtype_b, load_bits(B, p->dtype_b, b_index(p, l, k, n)));
+        const double* Bd = b_panel(p, B, l);
+        if (!Bd) return -6;
 
 #pragma omp parallel num_threads(nt)
         {
@@ -260,7 +322,6 @@ int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, co
             free(acc);
         }
     }
-    free(Bd);
     return status;
 }
 

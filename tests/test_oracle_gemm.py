@@ -316,3 +316,20 @@ def test_sampled_rows_equal_full_rows():
     rows = np.array([0, 7, M - 1, M + 3, 2 * M - 1])
     part, _ = g.gemm_rows(p, abuf, bbuf, rows=rows)
     assert np.array_equal(part, full.reshape(L * M, N)[rows])
+
+
+def test_panel_reuse_sees_changed_operand_bytes():
+    # The oracle keeps its last decoded B panel; a B rewritten in place (same
+    # address, new bytes) must not be served from it.
+    rng = np.random.default_rng(14)
+    M, N, K = 4, 6, 5
+    a, b = _normal_bf16(rng, (1, M, K)), _normal_bf16(rng, (1, K, N))
+    abuf, lda, _ = to_storage(to_bits(a, "bf16").reshape(a.shape), "N", "row")
+    bbuf, ldb, _ = to_storage(to_bits(b, "bf16").reshape(b.shape), "N", "row")
+    p = g.make_problem(M, N, K, 1, "N", "N", "row", "row", "row", "row", lda, ldb, dtype_d="f32")
+    first, _ = g.gemm_rows(p, abuf, bbuf)
+    again, _ = g.gemm_rows(p, abuf, bbuf)
+    assert np.array_equal(first, again)
+    bbuf[:] = to_bits(2.0 * b, "bf16").reshape(-1)          # exact doubling, same buffer
+    doubled, _ = g.gemm_rows(p, abuf, bbuf)
+    assert np.array_equal(from_bits(doubled, "f32"), 2.0 * from_bits(first, "f32"))
