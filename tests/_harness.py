@@ -51,7 +51,8 @@ def canary_buffer(spec, extra=4096, device="cuda"):
 
 def run_gpu(spec, inputs, *, alias_c=False, op=None, repeat=1, stream=None):
     """Runs the workload on cuda:0 through the C ABI.  Returns (D storage
-    incl. guard band as raw bits, the op)."""
+    incl. guard band as raw bits, the op).  With alias_c, D is C's own buffer
+    (followed by a canary guard band)."""
     dev = torch.device("cuda", 0)
     A = inputs.A.to(dev)
     B = inputs.B.to(dev)
@@ -79,11 +80,14 @@ def logical_d(spec, bits):
                         spec.matrix_elems("d"))
 
 
-def untouched_outside(spec, bits):
+def untouched_outside(spec, bits, before=None):
     """True when every element outside the logical D (padding, guard band)
-    still holds the canary pattern."""
+    still holds what it held before the run: the canary pattern, or the
+    matching elements of `before` (raw bits) where given."""
     n = spec.batch * spec.matrix_elems("d")
     canary = CANARY[spec.dtype_d]
+    if before is not None:
+        canary = np.asarray(before).astype(np.uint64)
     mask = np.ones(bits.shape[0], dtype=bool)
     idx = np.arange(n)
     L, per, ld = spec.batch, spec.matrix_elems("d"), spec.ld("d")
@@ -93,7 +97,8 @@ def untouched_outside(spec, bits):
     rows, cols = (spec.M, spec.N) if spec.order_d == "row" else (spec.N, spec.M)
     inside = (inner < cols) & (outer < rows)
     mask[:n] = ~inside
-    return bool(np.all(bits[mask].astype(np.uint64) == canary))
+    want = canary[mask] if isinstance(canary, np.ndarray) else canary
+    return bool(np.all(bits[mask].astype(np.uint64) == want))
 
 
 def oracle_rows(spec, inputs, rows=None):
