@@ -95,6 +95,7 @@ def _load():
         "gemm_set_debug": (i32, [vp, i32, u32]),
         "gemm_launch_count": (ctypes.c_uint64, [vp]),
         "gemm_status_str": (ctypes.c_char_p, [i32]),
+        "gemm_run_noalloc": (i32, [ctypes.POINTER(GemmDesc), vp, vp, vp, vp, vp, vp, i32]),
         "gemm_layout_query": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_char_p, ctypes.POINTER(i64)]),
         "gemm_layout_eval": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(i64), i32, ctypes.POINTER(i64)]),
         "gemm_layout_op": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_char_p, ctypes.c_char_p, i64,
@@ -110,7 +111,7 @@ def _load():
 
 lib = _load()
 EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_check", "gemm_destroy", "gemm_set_debug",
-            "gemm_launch_count", "gemm_status_str", "gemm_layout_query", "gemm_layout_eval",
+            "gemm_launch_count", "gemm_status_str", "gemm_run_noalloc", "gemm_layout_query", "gemm_layout_eval",
             "gemm_layout_op", "gemm_layout_gather_f32")
 
 
@@ -196,6 +197,14 @@ def gemm_set_debug(handle, inject_fault, timeout_ms):
 
 def gemm_launch_count(handle):
     return int(lib.gemm_launch_count(handle))
+
+
+def gemm_run_noalloc(desc, A, B, C, D, bias, stream, wait=True):
+    """Allocation-free launch (see gemm.h): no handle, scratch in a fixed
+    device array; with wait=True it synchronises and reports timeouts."""
+    s = lib.gemm_run_noalloc(ctypes.byref(desc), A, B, C, D, bias, stream, 1 if wait else 0)
+    if s != OK:
+        raise GemmError(s, "gemm_run_noalloc")
 
 
 class LayoutError(ValueError):

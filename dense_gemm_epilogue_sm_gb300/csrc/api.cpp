@@ -501,3 +501,66 @@ const char* gemm_status_str(gemm_status_t s) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// One-shot plan-and-launch into a caller-provided status word, with every
+// host object on the stack: used by the allocation-free entry point
+// (noalloc.cu).  Nothing here allocates host or device memory.
+// ---------------------------------------------------------------------------
+namespace gemm_sm103 {
+
+gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void* B, const void* C, void* D,
+                              const float* bias, uint32_t* status, int sm_count, cudaStream_t stream) {
+    Plan P;
+    const gemm_status_t s = validate_and_plan(desc, &P);
+    if (s != GEMM_OK) return s;
+    const gemm_desc_t& d = P.d;
+    if (d.M == 0 || d.N == 0) return GEMM_OK;
+    if (!D || (d.K > 0 && (!A || !B)) || (P.has_c && !C) || (d.bias != GEMM_BIAS_NONE && !bias))
+        return GEMM_ERR_INVALID_ARG;
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al16(D) || (A && !al16(A)) || (B && !al16(B)) || (P.has_c && !al16(C))) return GEMM_ERR_MISALIGNED;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return GEMM_ERR_MISALIGNED;
+
+    const void* a_ptr = A ? A : D;
+    const void* b_ptr = B ? B : D;
+    const bool swap = P.info.swapped;
+    const void* ka = swap ? b_ptr : a_ptr;
+    const void* kb = swap ? a_ptr : b_ptr;
+    const uint32_t kel = kStageKBytes / P.a_bytes;
+    const uint32_t epi_cols = 128u / P.out_bytes;
+    LaunchArgs la;
+    bool ok = encode_map(&la.tmA, P.a, d.dtype_a, ka, kel, P.kp.a_kmajor ? kTileM : kel, P.kp.a_batched);
+    ok = ok && encode_map(&la.tmB, P.b, d.dtype_a, kb, kel, P.kp.b_kmajor ? (uint32_t)P.tile_n : kel,
+                          P.kp.b_batched);
+    ok = ok && encode_map(&la.tmD, P.cd, d.dtype_d, D, epi_cols, kEpiRows, d.batch > 1);
+    if (P.has_c) {
+        gl::Layout lc = logical_layout(GEMM_OP_N, d.order_c, d.M, d.N, d.ldc, d.batch, d.stride_c);
+        if (swap) lc = transpose2(lc);
+        ok = ok && encode_map(&la.tmC, lc, d.dtype_c, C, epi_cols, kEpiRows, P.kp.c_batched);
+    } else {
+        la.tmC = la.tmD;
+    }
+    if (!ok) return GEMM_ERR_CUDA;
+    if (prepare_kernel(P.tile_n, P.out_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    la.p = P.kp;
+    la.p.bias = bias;
+    la.p.d_ptr = D;
+    la.p.status = status;
+    la.tile_n = P.tile_n;
+    la.out_bytes = P.out_bytes;
+    const int64_t tiles = P.info.tiles;
+    la.grid = (int)(tiles < sm_count ? tiles : sm_count);
+    la.stream = stream;
+    if (la.grid < 1) return GEMM_OK;
+    if (launch(la) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace gemm_sm103

@@ -142,6 +142,34 @@ GEMM_API gemm_status_t gemm_set_debug(gemm_handle_t h, int32_t inject_fault, uin
 /* Kernel launches issued through this handle so far. */
 GEMM_API uint64_t gemm_launch_count(gemm_handle_t h);
 
+/* Allocation-free variant of gemm_run.  The pages have no counterpart; this
+ * entry point exists for callers that must not call cudaMalloc: code running
+ * inside a framework whose memory pool owns the whole device (a raw
+ * allocation there can fail or fragment the pool) and latency-critical paths
+ * where cudaMalloc/cudaFree may synchronise the device.
+ *
+ * It plans `desc` and launches the same kernel as gemm_run on `stream`, with
+ * all host state on the stack and no handle.  The kernel's only scratch
+ * memory, its 4-byte status word, lives in a fixed file-scope device array of
+ * 64 words (256 bytes) that every GPU loading this library keeps until the
+ * process exits; a call needs 1 word, and a call needing more than the array
+ * holds is refused with GEMM_ERR_UNSUPPORTED.  No cudaMalloc, cudaFree or
+ * other allocating routine is called.
+ *
+ * The first call on a device looks up that array's device address
+ * (cudaGetSymbolAddress, once per device, with the device current); make
+ * that first call before any stream capture.  Each call clears the status
+ * word on `stream` before launching.  All calls on a device share the array,
+ * so calls whose kernels overlap on the GPU race on the status word: issue
+ * them on one stream, or wait between them.
+ *
+ * wait = 0: asynchronous; argument and launch errors are returned, an
+ * in-kernel timeout is not reported.  wait = 1: the call synchronises
+ * `stream` and returns GEMM_ERR_TIMEOUT if a bounded wait ran out.
+ * Pointers, alignment and errors are as for gemm_run. */
+GEMM_API gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const void* B, const void* C,
+                                        void* D, const float* bias, void* stream, int32_t wait);
+
 /* Static string for a status code. */
 GEMM_API const char* gemm_status_str(gemm_status_t s);
 
