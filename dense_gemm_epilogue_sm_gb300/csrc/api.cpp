@@ -72,6 +72,7 @@ struct Plan {
     gl::Layout a, b, cd;     // a: (M', K, L), b: (N', K, L), cd: (M', N', L)
     int64_t Mk, Nk;
     int a_bytes, out_bytes;
+    int cta_group;
     int tile_n;
     bool has_c;
     int bias_mode;           // 0 none, 1 per kernel column, 2 per kernel row
@@ -166,22 +167,27 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     P.info.b_k_major = b_kmaj;
     P.bias_mode = d.bias == GEMM_BIAS_NONE ? 0 : ((d.bias == GEMM_BIAS_COL) != swap ? 1 : 2);
 
-    // Tile shape.  1-SM MMA 128 x BN; BN = 256 reads 96 B/clk of shared
-    // memory per SM at full MMA rate (128 x 128 would need the whole 128 B/clk),
-    // so 256 is the default; 128 when N fits in it or when 256-wide tiles
-    // would leave most SMs idle.
-    const int64_t tiles_m = (P.Mk + kTileM - 1) / kTileM;
-    const int64_t tn256 = (P.Nk + 255) / 256;
+    // Tile shape.  Default: a CTA pair (cta_group::2) computes 256 x 256, each
+    // SM loading 128 rows of A and 128 of B per K block: 64 B/clk/SM of
+    // L2->SM traffic at full MMA rate.  A single CTA's 128 x 256 tile needs
+    // 96 B/clk/SM and 128 x 128 the whole 128 B/clk of shared-memory reads,
+    // so one CTA is used only where pairs would leave most SMs idle (small
+    // problems) or N fits in 128.
+    const int64_t tiles2 = ((P.Mk + 255) / 256) * ((P.Nk + 255) / 256) * L;
+    int cg = (P.Mk > 128 && P.Nk > 128 && tiles2 >= 64) ? 2 : 1;
     int tile_n = 256;
-    if (P.Nk <= 128 || tiles_m * tn256 * L < 76) tile_n = 128;
+    if (cg == 1 && (P.Nk <= 128 || ((P.Mk + kTileM - 1) / kTileM) * ((P.Nk + 255) / 256) * L < 76)) tile_n = 128;
+    const int tile_m = kTileM * cg;
+    P.cta_group = cg;
     P.tile_n = tile_n;
+    const int64_t tiles_m = (P.Mk + tile_m - 1) / tile_m;
     const int64_t tiles_n = (P.Nk + tile_n - 1) / tile_n;
 
-    P.info.tile_m = kTileM;
+    P.info.tile_m = tile_m;
     P.info.tile_n = tile_n;
     P.info.tile_k = kStageKBytes / ab;
-    P.info.cta_group = 1;
-    P.info.stages = stages_for(tile_n);
+    P.info.cta_group = cg;
+    P.info.stages = stages_for(cg, tile_n);
     P.info.epi_cols = 128 / ob;
     P.info.tiles_m = tiles_m;
     P.info.tiles_n = tiles_n;
@@ -193,7 +199,8 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     // Grouped raster: walk `G` M tiles, then the next N tile, so CTAs that
     // run together share A and B panels in L2.  As layouts from the tile
     // counter t to the linear tile index m_blk + tiles_m * n_blk.
-    const int64_t G = tiles_m < 1 ? 1 : (tiles_m < 16 ? tiles_m : 16);
+    const int64_t gmax = cg == 2 ? 8 : 16;
+    const int64_t G = tiles_m < 1 ? 1 : (tiles_m < gmax ? tiles_m : gmax);
     const int64_t full_groups = tiles_m / G;
     const int64_t tail = tiles_m - full_groups * G;
     P.info.raster_group = (int32_t)G;
@@ -236,7 +243,7 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
         id |= (a_kmaj ? 0u : 1u) << 15;                     // A MN-major
         id |= (b_kmaj ? 0u : 1u) << 16;                     // B MN-major
         id |= (uint32_t)(tile_n >> 3) << 17;                // N / 8
-        id |= (uint32_t)(kTileM >> 4) << 24;                // M / 16
+        id |= (uint32_t)(tile_m >> 4) << 24;                // M / 16 (256 for a CTA pair)
         P.idesc = id;
         k.idesc = id;
     }
@@ -309,12 +316,24 @@ bool encode_map(CUtensorMap* map, const gl::Layout& lay, int dt, const void* bas
     return r == CUDA_SUCCESS;
 }
 
+// Persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more
+// than there are tiles.
+int grid_for(const Plan& P, int sm_count, int max_clusters) {
+    const int64_t tiles = P.info.tiles;
+    const int cg = P.cta_group;
+    int64_t slots = sm_count / cg;
+    if (max_clusters > 0 && max_clusters < slots) slots = max_clusters;
+    if (slots < 1) slots = 1;
+    return (int)((tiles < slots ? tiles : slots) * cg);
+}
+
 }  // namespace
 
 struct gemm_handle_s {
     Plan plan;
     int device = -1;
     int sm_count = 0;
+    int max_clusters = 0;     // co-resident clusters of the planned kernel (0: unknown)
     uint32_t* status = nullptr;
     cudaStream_t last_stream = nullptr;
     bool launched = false;
@@ -366,7 +385,7 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
         delete h;
         return GEMM_ERR_NO_DEVICE;
     }
-    if (prepare_kernel(h->plan.tile_n, h->plan.out_bytes) != cudaSuccess ||
+    if (prepare_kernel(h->plan.cta_group, h->plan.tile_n, h->plan.out_bytes) != cudaSuccess ||
         cudaMalloc(&h->status, sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) {
         cudaGetLastError();
@@ -375,6 +394,7 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
         return GEMM_ERR_CUDA;
     }
     h->plan.kp.status = h->status;
+    h->max_clusters = max_active_clusters(h->plan.cta_group, h->plan.tile_n, h->plan.out_bytes);
     *out = h;
     return GEMM_OK;
 }
@@ -407,7 +427,8 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void
         bool ok = true;
         // A: box {K: kel, M: 128} (K-major) or {M: kel, K: kel} (MN-major)
         ok = ok && encode_map(&h->maps[0], P.a, adt, ka, kel, P.kp.a_kmajor ? kTileM : kel, P.kp.a_batched);
-        ok = ok && encode_map(&h->maps[1], P.b, adt, kb, kel, P.kp.b_kmajor ? (uint32_t)tn : kel, P.kp.b_batched);
+        ok = ok && encode_map(&h->maps[1], P.b, adt, kb, kel, P.kp.b_kmajor ? (uint32_t)(tn / P.cta_group) : kel,
+                              P.kp.b_batched);
         ok = ok && encode_map(&h->maps[3], P.cd, d.dtype_d, D, epi_cols, kEpiRows, d.batch > 1);
         if (P.has_c) {
             gl::Layout lc = logical_layout(GEMM_OP_N, d.order_c, d.M, d.N, d.ldc, d.batch, d.stride_c);
@@ -434,10 +455,10 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void
     la.p = P.kp;
     la.p.bias = bias;
     la.p.d_ptr = D;
+    la.cta_group = P.cta_group;
     la.tile_n = P.tile_n;
     la.out_bytes = P.out_bytes;
-    const int64_t tiles = P.info.tiles;
-    la.grid = (int)(tiles < h->sm_count ? tiles : h->sm_count);
+    la.grid = grid_for(P, h->sm_count, h->max_clusters);
     la.stream = static_cast<cudaStream_t>(stream);
     if (la.grid < 1) return GEMM_OK;
     const cudaError_t e = launch(la);
@@ -531,8 +552,8 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
     const uint32_t epi_cols = 128u / P.out_bytes;
     LaunchArgs la;
     bool ok = encode_map(&la.tmA, P.a, d.dtype_a, ka, kel, P.kp.a_kmajor ? kTileM : kel, P.kp.a_batched);
-    ok = ok && encode_map(&la.tmB, P.b, d.dtype_a, kb, kel, P.kp.b_kmajor ? (uint32_t)P.tile_n : kel,
-                          P.kp.b_batched);
+    ok = ok && encode_map(&la.tmB, P.b, d.dtype_a, kb, kel,
+                          P.kp.b_kmajor ? (uint32_t)(P.tile_n / P.cta_group) : kel, P.kp.b_batched);
     ok = ok && encode_map(&la.tmD, P.cd, d.dtype_d, D, epi_cols, kEpiRows, d.batch > 1);
     if (P.has_c) {
         gl::Layout lc = logical_layout(GEMM_OP_N, d.order_c, d.M, d.N, d.ldc, d.batch, d.stride_c);
@@ -542,7 +563,7 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
         la.tmC = la.tmD;
     }
     if (!ok) return GEMM_ERR_CUDA;
-    if (prepare_kernel(P.tile_n, P.out_bytes) != cudaSuccess) {
+    if (prepare_kernel(P.cta_group, P.tile_n, P.out_bytes) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -550,10 +571,10 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
     la.p.bias = bias;
     la.p.d_ptr = D;
     la.p.status = status;
+    la.cta_group = P.cta_group;
     la.tile_n = P.tile_n;
     la.out_bytes = P.out_bytes;
-    const int64_t tiles = P.info.tiles;
-    la.grid = (int)(tiles < sm_count ? tiles : sm_count);
+    la.grid = grid_for(P, sm_count, max_active_clusters(P.cta_group, P.tile_n, P.out_bytes));
     la.stream = stream;
     if (la.grid < 1) return GEMM_OK;
     if (launch(la) != cudaSuccess) {

@@ -67,15 +67,17 @@ struct KernelParams {
 struct LaunchArgs {
     CUtensorMap tmA, tmB, tmC, tmD;
     KernelParams p;
+    int cta_group;                // 1 or 2 (CTA pair, cluster of 2)
     int tile_n;                   // 128 or 256
     int out_bytes;                // 2 or 4
-    int grid;
+    int grid;                     // CTAs (a multiple of cta_group)
     cudaStream_t stream;
 };
 
-int stages_for(int tile_n);
-size_t smem_bytes_for(int tile_n, int out_bytes);
-cudaError_t prepare_kernel(int tile_n, int out_bytes);
+int stages_for(int cta_group, int tile_n);
+size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes);
+cudaError_t prepare_kernel(int cta_group, int tile_n, int out_bytes);
+int max_active_clusters(int cta_group, int tile_n, int out_bytes);   // 0 if unknown
 cudaError_t launch(const LaunchArgs& a);
 
 }  // namespace gemm_sm103

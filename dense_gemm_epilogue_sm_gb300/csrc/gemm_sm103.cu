@@ -3,6 +3,14 @@
 // accumulator in TMEM) -> TMEM loads -> fused alpha/beta/bias/ReLU -> TMA
 // store.
 //
+// Two variants share this source.  CG = 1: one CTA computes a 128 x BN tile
+// with tcgen05 cta_group::1.  CG = 2: a cluster of two CTAs computes a
+// 256 x BN tile with cta_group::2 MMAs issued by the even CTA (the leader);
+// each CTA loads its own 128 rows of A and BN/2 rows of B, the leader's
+// full[s] barrier counts both CTAs' bytes, commits are multicast to both
+// CTAs, and each CTA's epilogue reads the 128 accumulator rows in its own
+// TMEM and signals the leader's acc_empty barrier.
+//
 // Structure (the roles of "Technical Documentation: NVIDIA/cutlass",
 // "Blackwell Warp-specialized Persistent Kernel", re-split for this kernel):
 //   warp 0      one lane issues TMA loads of A and B tiles into a STAGES-deep
@@ -31,26 +39,33 @@
 
 namespace gemm_sm103 {
 
-int stages_for(int tile_n) { return tile_n == 256 ? 4 : 6; }
+int stages_for(int cta_group, int tile_n) { return (cta_group == 1 && tile_n == 256) ? 4 : 6; }
 
-template <int BN, int OB>
+// TMEM accumulators per CTA: two, so the epilogue of one tile overlaps the
+// main loop of the next (512 columns for BN = 256).
+constexpr int kPairAccBufs = 2;
+
+template <int CG, int BN, int OB>
 struct Cfg {
-    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
+    static constexpr int kBRows = BN / CG;                          // rows of B this CTA loads
+    static constexpr int kStages = (CG == 1 && BN == 256) ? 4 : 6;
     static constexpr int kABytes = kTileM * kStageKBytes;           // 16 KiB
-    static constexpr int kBBytes = BN * kStageKBytes;
-    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBBytes = kBRows * kStageKBytes;
+    static constexpr int kStageBytes = kABytes + kBBytes;           // this CTA's share of a stage
     static constexpr int kEpiCols = 128 / OB;                       // 64 (16-bit D) or 32 (fp32 D)
     static constexpr int kSubtiles = BN / kEpiCols;
-    static constexpr int kTmemCols = 2 * BN;                        // two accumulators
+    static constexpr int kTmemCols = kAccBufs * BN;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
     static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps + 1;
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kNumBars * 8 + 16;
 };
 
-size_t smem_bytes_for(int tile_n, int out_bytes) {
-    if (tile_n == 256) return out_bytes == 2 ? Cfg<256, 2>::kSmemBytes : Cfg<256, 4>::kSmemBytes;
-    return out_bytes == 2 ? Cfg<128, 2>::kSmemBytes : Cfg<128, 4>::kSmemBytes;
+size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes) {
+    if (cta_group == 2) return out_bytes == 2 ? Cfg<2, 256, 2>::kSmemBytes : Cfg<2, 256, 4>::kSmemBytes;
+    if (tile_n == 256) return out_bytes == 2 ? Cfg<1, 256, 2>::kSmemBytes : Cfg<1, 256, 4>::kSmemBytes;
+    return out_bytes == 2 ? Cfg<1, 128, 2>::kSmemBytes : Cfg<1, 128, 4>::kSmemBytes;
 }
 
 // ------------------------------------------------------------------------
@@ -73,8 +88,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 // Bounded wait on phase `parity` of `bar`.  Gives up when another role has
 // aborted or after p.timeout_ns; on timeout records `role` in the status word
 // and raises the abort flag.
+// `peer_abort` (0 outside a CTA pair) is the peer CTA's abort flag as a
+// shared::cluster address: a timeout raises it too, so the peer stops
+// waiting for work that will not come.
 __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const KernelParams& p,
-                                      volatile uint32_t* abort_flag, uint32_t role) {
+                                      volatile uint32_t* abort_flag, uint32_t role, uint32_t peer_abort) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t n = 1;; ++n) {
@@ -83,6 +101,7 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Kerne
             if (*abort_flag) return false;
             if (ptx::globaltimer() - t0 > p.timeout_ns) {
                 *abort_flag = 1u;
+                if (peer_abort) ptx::st_cluster_u32(peer_abort, 1u);
                 atomicOr(p.status, kStatusTimeout | role);
                 return false;
             }
@@ -138,13 +157,14 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
     return w;
 }
 
-template <int BN, int OB>
+template <int CG, int BN, int OB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                 const __grid_constant__ KernelParams p) {
-    using C = Cfg<BN, OB>;
+    using C = Cfg<CG, BN, OB>;
     constexpr int S = C::kStages;
+    constexpr int kTileRows = kTileM * CG;               // output rows per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
@@ -163,6 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // CTA pair bookkeeping (CG == 2): rank 0 is the leader that issues MMAs.
+    const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;
+    const int first_tile = CG == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int tile_step = CG == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const uint32_t peer_abort = CG == 2 ? ptx::mapa(ptx::smem_addr(tmem_slot + 1), rank ^ 1u) : 0u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -171,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf_bar(b), 1);
-            ptx::mbar_init(acce_bar(b), kEpiWarps);
+            ptx::mbar_init(acce_bar(b), kEpiWarps * CG);   // every epilogue warp of the pair
         }
         for (int i = 0; i < 2 * kEpiWarps; ++i) ptx::mbar_init(cfull_bar(i), 1);
         ptx::mbar_init(drain, 1);
@@ -185,11 +210,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.has_c) ptx::prefetch_tensormap(&tmC);
     }
     if (warp == 1) {
-        ptx::tmem_alloc<1>(ptx::smem_addr(tmem_slot), C::kTmemCols);
-        ptx::tmem_relinquish<1>();
+        ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), C::kTmemCols);
+        ptx::tmem_relinquish<CG>();
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) ptx::cluster_sync();   // the peer's barriers exist before anyone signals them
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -204,37 +230,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < S; ++s) pend[s] = false;
             int stage = 0;
             uint32_t phase = 0;
-            bool skip_first = p.inject != 0;
-            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+            bool skip_first = p.inject != 0 && rank == 0;
+            for (int tile = first_tile; tile < p.num_tiles; tile += tile_step) {
                 int mb, nb, l;
                 tile_coords(p, tile, mb, nb, l);
                 const int la = p.a_batched ? l : 0, lb = p.b_batched ? l : 0;
-                const int m0 = mb * kTileM, n0 = nb * BN;
+                const int m0 = mb * kTileRows + (int)rank * kTileM;
+                const int n0 = nb * BN + (int)rank * C::kBRows;
                 bool stop = false;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(empty_bar(stage), phase ^ 1u, p, abort_flag, kStatusRoleLoad)) {
+                    if (!wait_bar(empty_bar(stage), phase ^ 1u, p, abort_flag, kStatusRoleLoad, peer_abort)) {
                         stop = true;
                         break;
                     }
                     if (skip_first) {
                         skip_first = false;       // test hook: this stage is never filled
                     } else {
-                        const uint32_t fb = full_bar(stage);
-                        ptx::mbar_arrive_expect_tx(fb, C::kStageBytes);
+                        // the pair's leader counts both CTAs' bytes
+                        const uint32_t fb = CG == 2 ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes * CG);
                         const uint32_t sa = ptx::smem_addr(ring + stage * C::kStageBytes);
                         const uint32_t sb = sa + C::kABytes;
                         const int k0 = kb * kel;
+                        auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
+                            if constexpr (CG == 2)
+                                ptx::tma_load_3d_cg2(dst, map, c0, c1, c2, fb);
+                            else
+                                ptx::tma_load_3d(dst, map, c0, c1, c2, fb);
+                        };
                         if (p.a_kmajor) {
-                            ptx::tma_load_3d(sa, &tmA, k0, m0, la, fb);
+                            load(sa, &tmA, k0, m0, la);
                         } else {
-                            for (int c = 0; c < kTileM / mn_box; ++c)
-                                ptx::tma_load_3d(sa + c * (kel * 128), &tmA, m0 + c * mn_box, k0, la, fb);
+                            for (int c = 0; c < kTileM / mn_box; ++c) load(sa + c * (kel * 128), &tmA, m0 + c * mn_box, k0, la);
                         }
                         if (p.b_kmajor) {
-                            ptx::tma_load_3d(sb, &tmB, k0, n0, lb, fb);
+                            load(sb, &tmB, k0, n0, lb);
                         } else {
-                            for (int c = 0; c < BN / mn_box; ++c)
-                                ptx::tma_load_3d(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb, fb);
+                            for (int c = 0; c < C::kBRows / mn_box; ++c)
+                                load(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb);
                         }
                         pend[stage] = true;
                         pend_parity[stage] = phase;
@@ -246,13 +279,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (stop) break;
             }
-            // Every issued copy must land before the CTA may exit.
+            // Every issued copy must land before the CTA may exit.  In a pair
+            // the copies complete on the leader's barrier, so each CTA waits
+            // for the MMA to have consumed its stages instead.
             for (int s = 0; s < S; ++s)
-                if (pend[s]) drain_bar(full_bar(s), pend_parity[s], p);
+                if (pend[s]) {
+                    if constexpr (CG == 2)
+                        drain_bar(empty_bar(s), pend_parity[s], p);
+                    else
+                        drain_bar(full_bar(s), pend_parity[s], p);
+                }
         }
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA -----
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             const int eb = p.elem_bytes;
             const int kel = kStageKBytes / eb;
             // per-K-step advance of the descriptors' start address
@@ -263,15 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
-            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-                const int buf = it & 1;
-                const uint32_t acc_par = (uint32_t)(it >> 1) & 1u;
-                if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, abort_flag, kStatusRoleMma)) break;
+            bool issued = false;
+            for (int tile = first_tile; tile < p.num_tiles; tile += tile_step, ++it) {
+                const int buf = it % C::kAccBufs;
+                const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
+                if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, abort_flag, kStatusRoleMma, peer_abort)) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
                 bool stop = false;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(full_bar(stage), phase, p, abort_flag, kStatusRoleMma)) {
+                    if (!wait_bar(full_bar(stage), phase, p, abort_flag, kStatusRoleMma, peer_abort)) {
                         stop = true;
                         break;
                     }
@@ -284,25 +325,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bd = smem_desc(sb + j * b_step, b_lbo, 1024u);
                         const uint32_t acc = (kb | j) != 0;
                         if (p.kind_f8)
-                            ptx::mma_f8<1>(d_tmem, ad, bd, p.idesc, acc);
+                            ptx::mma_f8<CG>(d_tmem, ad, bd, p.idesc, acc);
                         else
-                            ptx::mma_f16<1>(d_tmem, ad, bd, p.idesc, acc);
+                            ptx::mma_f16<CG>(d_tmem, ad, bd, p.idesc, acc);
                     }
-                    ptx::mma_commit(empty_bar(stage));   // frees the stage once these MMAs have read it
+                    issued = true;
+                    // frees the stage (in both CTAs of a pair) once these MMAs have read it
+                    if constexpr (CG == 2)
+                        ptx::mma_commit_mc(empty_bar(stage), 0x3);
+                    else
+                        ptx::mma_commit(empty_bar(stage));
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (stop) break;
-                if (p.num_kb > 0)
-                    ptx::mma_commit(accf_bar(buf));      // accumulator complete
-                else
-                    ptx::mbar_arrive(accf_bar(buf));     // K == 0: nothing accumulated
+                if (p.num_kb > 0) {                      // accumulator complete
+                    if constexpr (CG == 2)
+                        ptx::mma_commit_mc(accf_bar(buf), 0x3);
+                    else
+                        ptx::mma_commit(accf_bar(buf));
+                } else {                                  // K == 0: nothing accumulated
+                    ptx::mbar_arrive(accf_bar(buf));
+                    if constexpr (CG == 2) ptx::mbar_arrive_cluster(accf_bar(buf), 1);
+                }
             }
             // Drain: every MMA issued above must finish before TMEM is freed.
-            ptx::mma_commit(drain);
-            drain_bar(drain, 0, p);
+            if (issued) {
+                if constexpr (CG == 2)
+                    ptx::mma_commit_cg2(drain);
+                else
+                    ptx::mma_commit(drain);
+                drain_bar(drain, 0, p);
+            }
         }
     } else {
         // ---------------------------------------------------- epilogue -----
@@ -315,19 +371,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         int sub_count = 0;
         int it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
-            const int buf = it & 1;
-            const uint32_t acc_par = (uint32_t)(it >> 1) & 1u;
+        for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step, ++it) {
+            const int buf = it % C::kAccBufs;
+            const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
             int mb, nb, l;
             tile_coords(p, tile, mb, nb, l);
-            ok = __all_sync(0xffffffffu, wait_bar(accf_bar(buf), acc_par, p, abort_flag, kStatusRoleEpi));
+            ok = __all_sync(0xffffffffu, wait_bar(accf_bar(buf), acc_par, p, abort_flag, kStatusRoleEpi, peer_abort));
             if (!ok) break;
             ptx::tc_fence_after();
-            const int row0 = mb * kTileM + q * kEpiRows;
+            const int row0 = mb * kTileRows + (int)rank * kTileM + q * kEpiRows;
             const int row = row0 + lane;
             float row_bias = 0.f;
             if (p.bias_mode == 2 && row < p.M) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
-            const float* bias_l = p.bias + (int64_t)l * p.bias_stride;
+            const float* bias_l = p.bias_mode == 1 ? p.bias + (int64_t)l * p.bias_stride : nullptr;
             const int lc = p.c_batched ? l : 0;
 #pragma unroll 1
             for (int sub = 0; sub < C::kSubtiles; ++sub) {
@@ -347,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mbar_arrive_expect_tx(cb, kEpiBufBytes);
                         ptx::tma_load_3d(sbuf_a, &tmC, col0, row0, lc, cb);
                     }
-                    ok = __all_sync(0xffffffffu, wait_bar(cb, c_phase[sbi], p, abort_flag, kStatusRoleEpi));
+                    ok = __all_sync(0xffffffffu, wait_bar(cb, c_phase[sbi], p, abort_flag, kStatusRoleEpi, peer_abort));
                     c_phase[sbi] ^= 1u;
                     if (!ok) break;
                 }
@@ -434,48 +490,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // This warp is done reading accumulator `buf`.
+            // This warp is done reading accumulator `buf`: tell the MMA issuer.
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0 && ok) ptx::mbar_arrive(acce_bar(buf));
+            if (lane == 0 && ok) {
+                if constexpr (CG == 2) {
+                    if (rank == 0)
+                        ptx::mbar_arrive(acce_bar(buf));
+                    else
+                        ptx::mbar_arrive_cluster(acce_bar(buf), 0);
+                } else {
+                    ptx::mbar_arrive(acce_bar(buf));
+                }
+            }
         }
         if (lane == 0) ptx::bulk_wait<0>();
         ptx::tc_fence_before();
     }
 
     __syncthreads();
+    if constexpr (CG == 2) ptx::cluster_sync();   // no CTA leaves while its peer may still touch its memory
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc<1>(tmem_base, C::kTmemCols);
+        ptx::tmem_dealloc<CG>(tmem_base, C::kTmemCols);
     }
 }
 
-template <int BN, int OB>
+template <int CG, int BN, int OB>
 static cudaError_t set_attrs() {
-    return cudaFuncSetAttribute(gemm_kernel<BN, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg<BN, OB>::kSmemBytes);
+    return cudaFuncSetAttribute(gemm_kernel<CG, BN, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<CG, BN, OB>::kSmemBytes);
 }
 
-cudaError_t prepare_kernel(int tile_n, int out_bytes) {
-    if (tile_n == 256) return out_bytes == 2 ? set_attrs<256, 2>() : set_attrs<256, 4>();
-    return out_bytes == 2 ? set_attrs<128, 2>() : set_attrs<128, 4>();
+cudaError_t prepare_kernel(int cta_group, int tile_n, int out_bytes) {
+    if (cta_group == 2) return out_bytes == 2 ? set_attrs<2, 256, 2>() : set_attrs<2, 256, 4>();
+    if (tile_n == 256) return out_bytes == 2 ? set_attrs<1, 256, 2>() : set_attrs<1, 256, 4>();
+    return out_bytes == 2 ? set_attrs<1, 128, 2>() : set_attrs<1, 128, 4>();
 }
 
-template <int BN, int OB>
-static cudaError_t launch_t(const LaunchArgs& a) {
+template <int CG, int BN, int OB>
+static cudaLaunchConfig_t make_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<BN, OB>::kSmemBytes;
-    cfg.stream = a.stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, OB>, a.tmA, a.tmB, a.tmC, a.tmD, a.p);
+    cfg.dynamicSmemBytes = Cfg<CG, BN, OB>::kSmemBytes;
+    cfg.stream = stream;
+    attr->id = cudaLaunchAttributeClusterDimension;
+    attr->val.clusterDim.x = CG;
+    attr->val.clusterDim.y = 1;
+    attr->val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CG == 2 ? 1 : 0;      // CTA pairs are launched as clusters of two
+    return cfg;
+}
+
+template <int CG, int BN, int OB>
+static cudaError_t launch_t(const LaunchArgs& a) {
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = make_config<CG, BN, OB>(a.grid, a.stream, &attr);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<CG, BN, OB>, a.tmA, a.tmB, a.tmC, a.tmD, a.p);
+}
+
+template <int CG, int BN, int OB>
+static int max_clusters_t() {
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = make_config<CG, BN, OB>(CG * 64, nullptr, &attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<CG, BN, OB>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int max_active_clusters(int cta_group, int tile_n, int out_bytes) {
+    if (cta_group == 2) return out_bytes == 2 ? max_clusters_t<2, 256, 2>() : max_clusters_t<2, 256, 4>();
+    if (tile_n == 256) return out_bytes == 2 ? max_clusters_t<1, 256, 2>() : max_clusters_t<1, 256, 4>();
+    return out_bytes == 2 ? max_clusters_t<1, 128, 2>() : max_clusters_t<1, 128, 4>();
 }
 
 cudaError_t launch(const LaunchArgs& a) {
-    if (a.tile_n == 256) return a.out_bytes == 2 ? launch_t<256, 2>(a) : launch_t<256, 4>(a);
-    return a.out_bytes == 2 ? launch_t<128, 2>(a) : launch_t<128, 4>(a);
+    if (a.cta_group == 2) return a.out_bytes == 2 ? launch_t<2, 256, 2>(a) : launch_t<2, 256, 4>(a);
+    if (a.tile_n == 256) return a.out_bytes == 2 ? launch_t<1, 256, 2>(a) : launch_t<1, 256, 4>(a);
+    return a.out_bytes == 2 ? launch_t<1, 128, 2>(a) : launch_t<1, 128, 4>(a);
 }
 
 }  // namespace gemm_sm103

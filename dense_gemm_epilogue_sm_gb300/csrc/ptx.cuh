@@ -77,6 +77,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int32
         : "memory");
 }
 
+// 2-SM form: the copy lands in this CTA's shared memory and completes its
+// bytes on `bar_cluster`, a shared::cluster address that may name the peer
+// CTA's barrier (the pair's leader).
+__device__ __forceinline__ void tma_load_3d_cg2(uint32_t dst, const void* map, int32_t c0, int32_t c1, int32_t c2,
+                                                uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
+        : "memory");
+}
+
 // Same, with an L2 eviction-priority hint (a createpolicy value).
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* map, int32_t c0, int32_t c1,
                                                  int32_t c2, uint32_t bar, uint64_t policy) {
@@ -209,6 +221,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
+// 2-SM form, this CTA's barrier only.
+__device__ __forceinline__ void mma_commit_cg2(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
 // 2-SM form: arrive on the barrier at offset `bar` in every CTA of `mask`.
 __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
     asm volatile(
@@ -240,6 +258,18 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
+}
+
+// Address of this CTA's shared-memory location `addr` as seen in CTA `cta`
+// of the cluster (a shared::cluster address).
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t cta) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(cta));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr_cluster, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {

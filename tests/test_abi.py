@@ -108,22 +108,26 @@ def test_plan_orientation_and_majorness():
 
 
 def test_plan_tiles_for_the_named_workloads():
+    # (cta_group, tile_m, tile_n, tiles_m, tiles_n, tiles)
     want = {
-        "bf16_4096": (256, 32, 16, 512),
-        "fused_bf16_8192": (256, 64, 32, 2048),
-        "fp8_e4m3_8192": (256, 64, 32, 2048),
-        "skinny_65536x256x4096": (256, 512, 1, 512),
-        "batched_32x512": (256, 4, 2, 256),
+        "bf16_4096": (2, 256, 256, 16, 16, 256),
+        "fused_bf16_8192": (2, 256, 256, 32, 32, 1024),
+        "fp8_e4m3_8192": (2, 256, 256, 32, 32, 1024),
+        "skinny_65536x256x4096": (2, 256, 256, 256, 1, 256),
+        "batched_32x512": (2, 256, 256, 2, 2, 128),
+        "tiny_exact_fp16_256": (1, 128, 128, 2, 2, 4),
+        "odd_1000_at": (1, 128, 128, 8, 8, 64),
     }
-    for name, (tn, tm, tnn, tiles) in want.items():
+    for name, w in want.items():
         spec = wl.get(name)
         info = g.gemm_plan(desc_from_spec(spec))
-        assert (info.tile_n, info.tiles_m, info.tiles_n, info.tiles) == (tn, tm, tnn, tiles), name
+        got = (info.cta_group, info.tile_m, info.tile_n, info.tiles_m, info.tiles_n, info.tiles)
+        assert got == w, (name, got)
         assert info.tile_k == (128 if spec.dtype_in == "e4m3" else 64)
     info = g.gemm_plan(desc_from_spec(wl.get("tiny_exact_fp16_256")))
-    assert info.swapped and info.tile_n == 128 and info.epi_cols == 32
+    assert info.swapped and info.epi_cols == 32
     info = g.gemm_plan(desc_from_spec(wl.get("odd_1000_at")))
-    assert info.a_k_major and info.b_k_major and info.tile_n == 128
+    assert info.a_k_major and info.b_k_major
 
 
 def test_raster_order_is_a_bijection():

@@ -129,6 +129,28 @@ def test_deterministic_run_to_run():
     assert np.array_equal(a, b)
 
 
+# ------------------------------------------------------ CTA pairs ---------
+PAIR_SPECS = [
+    wl.Spec("pair_fused", 2100, 2100, 200, alpha=0.5, beta=1.0, act="relu", bias="col", seed=41, pad=3),
+    wl.Spec("pair_colmajor_d", 2050, 2300, 136, op_a="T", order_a="col", order_b="row", order_c="col",
+            order_d="col", beta=1.0, bias="row", seed=42),
+    wl.Spec("pair_mn_major", 2304, 2048, 128, order_a="col", order_b="row", dtype_in="f16", dtype_d="f32",
+            seed=43),
+    wl.Spec("pair_e4m3", 2100, 2060, 256, dtype_in="e4m3", dist="uniform1", bias="col", seed=44),
+    wl.Spec("pair_batched", 256, 256, 96, batch=64, beta=1.0, seed=45),
+    wl.Spec("pair_exact", 2048, 2048, 264, order_a="col", order_b="col", order_c="col", order_d="col",
+            dtype_in="f16", dtype_d="f32", dist="int4", seed=46),
+]
+
+
+@pytest.mark.parametrize("spec", PAIR_SPECS, ids=lambda s: s.name)
+def test_cta_pair_kernel(spec):
+    from dense_gemm_epilogue_sm_gb300 import gemm_plan
+    from dense_gemm_epilogue_sm_gb300.torch_ops import desc_from_spec
+    assert gemm_plan(desc_from_spec(spec)).cta_group == 2
+    _full_check(spec, exact=spec.dist == "int4")
+
+
 # ---------------------------------------------------- full workloads ------
 @pytest.mark.parametrize("name", ["odd_1000_at", "batched_32x512"])
 def test_workload_full_parity(name):
