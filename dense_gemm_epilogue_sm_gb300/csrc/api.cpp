@@ -76,7 +76,6 @@ struct Plan {
     int tile_n;
     bool has_c;
     int bias_mode;           // 0 none, 1 per kernel column, 2 per kernel row
-    uint32_t idesc;
     KernelParams kp;
 };
 
@@ -233,20 +232,8 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     k.b_kmajor = b_kmaj;
     k.elem_bytes = ab;
     k.kind_f8 = d.dtype_a == GEMM_E4M3;
-    {
-        uint32_t fmt = 0;                                   // kind::f16: 0 f16, 1 bf16; kind::f8f6f4: 0 e4m3
-        if (d.dtype_a == GEMM_BF16) fmt = 1;
-        uint32_t id = 0;
-        id |= 1u << 4;                                      // accumulator fp32
-        id |= fmt << 7;                                     // A type
-        id |= fmt << 10;                                    // B type
-        id |= (a_kmaj ? 0u : 1u) << 15;                     // A MN-major
-        id |= (b_kmaj ? 0u : 1u) << 16;                     // B MN-major
-        id |= (uint32_t)(tile_n >> 3) << 17;                // N / 8
-        id |= (uint32_t)(tile_m >> 4) << 24;                // M / 16 (256 for a CTA pair)
-        P.idesc = id;
-        k.idesc = id;
-    }
+    k.mma_variant = (d.dtype_a == GEMM_E4M3 ? 8 : 0) + (d.dtype_a == GEMM_BF16 ? 4 : 0) + (a_kmaj ? 0 : 2) +
+                    (b_kmaj ? 0 : 1);
     k.a_batched = L > 1 && mode_stride(P.a, 2) != 0;
     k.b_batched = L > 1 && mode_stride(P.b, 2) != 0;
     k.c_batched = L > 1 && d.stride_c != 0;

@@ -43,7 +43,9 @@ struct KernelParams {
     int32_t a_kmajor, b_kmajor;
     int32_t elem_bytes;           // operand element size, 1 or 2
     int32_t kind_f8;              // 1: kind::f8f6f4, 0: kind::f16
-    uint32_t idesc;               // tcgen05 instruction descriptor
+    // MMA loop variant, one per instruction descriptor:
+    // 8*kind_f8 + 4*(operands bf16) + 2*(A MN-major) + (B MN-major)
+    int32_t mma_variant;
     int32_t a_batched, b_batched, c_batched;   // 0: operand shared by all batches
     float alpha, beta;
     int32_t has_c;

@@ -157,6 +157,112 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
     return w;
 }
 
+// tcgen05 instruction descriptor (kind::f16 / kind::f8f6f4, dense): D fp32
+// (bits 4-5 = 1), A and B type (bits 7-9, 10-12: f16 0 / bf16 1 for kind::f16,
+// e4m3 0 for kind::f8f6f4), A / B MN-major (bits 15, 16), N >> 3 (bits
+// 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_for(int cg, int bn, bool f8, uint32_t bf16, uint32_t a_mn,
+                                                 uint32_t b_mn) {
+    return (1u << 4) | ((f8 ? 0u : bf16) << 7) | ((f8 ? 0u : bf16) << 10) | (a_mn << 15) | (b_mn << 16) |
+           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)((128 * cg) >> 4) << 24);
+}
+
+// What the MMA issuer needs from the kernel.
+template <int CG, int BN, int S>
+struct MmaCtx {
+    const KernelParams& p;
+    uint32_t ring;          // shared address of stage 0
+    uint32_t a_bytes;       // A tile bytes at the front of a stage
+    uint32_t stage_bytes;
+    uint32_t bar0;          // barrier block
+    uint32_t tmem_base;
+    int first_tile, tile_step;
+    volatile uint32_t* abort_flag;
+    uint32_t peer_abort;
+};
+
+// The MMA issuer (one thread of the pair leader).  A tcgen05.mma blocks its
+// issuing thread until the tensor core takes it (the queue is about one
+// instruction deep), so any work between two MMAs is tensor-pipe idle time:
+// the loop asks for the next stage's barrier while the current stage's MMAs
+// issue, builds descriptors by adding offsets to a precomputed base, and
+// carries the instruction descriptor as an immediate.
+template <int CG, int BN, int S, bool F8, uint32_t IDESC>
+__device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
+    const KernelParams& p = m.p;
+    constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
+    auto full_bar = [&](int s) { return m.bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return m.bar0 + 8u * (S + s); };
+    auto accf_bar = [&](int b) { return m.bar0 + 8u * (2 * S + b); };
+    auto acce_bar = [&](int b) { return m.bar0 + 8u * (2 * S + 2 + b); };
+    const uint32_t drain = m.bar0 + 8u * (2 * S + 4 + 2 * kEpiWarps);
+    constexpr bool a_mn = (IDESC >> 15) & 1u, b_mn = (IDESC >> 16) & 1u;
+    constexpr int eb = F8 ? 1 : 2;
+    constexpr int kel = kStageKBytes / eb;
+    // per-K-step advance of the descriptors' start address, in 16-byte units
+    constexpr uint32_t a_step = (a_mn ? (kKStepBytes / eb) * 128u : kKStepBytes) >> 4;
+    constexpr uint32_t b_step = (b_mn ? (kKStepBytes / eb) * 128u : kKStepBytes) >> 4;
+    // shared addresses stay below 2^18, so offsets added to the 14-bit
+    // start-address field never carry into the other fields
+    const uint64_t a_base = smem_desc(m.ring, a_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
+    const uint64_t b_base = smem_desc(m.ring + m.a_bytes, b_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool issued = false;
+    bool ready = ptx::mbar_test_wait(full_bar(0), 0);
+    for (int tile = m.first_tile; tile < p.num_tiles; tile += m.tile_step, ++it) {
+        const int buf = it % kAccBufs;
+        const uint32_t acc_par = (uint32_t)(it / kAccBufs) & 1u;
+        if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, m.abort_flag, kStatusRoleMma, m.peer_abort)) break;
+        ptx::tc_fence_after();   // the epilogue's reads of this accumulator come first
+        const uint32_t d_tmem = m.tmem_base + (uint32_t)(buf * BN);
+        bool stop = false;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!ready && !wait_bar(full_bar(stage), phase, p, m.abort_flag, kStatusRoleMma, m.peer_abort)) {
+                stop = true;
+                break;
+            }
+            const int next = stage + 1 == S ? 0 : stage + 1;
+            const uint32_t next_phase = stage + 1 == S ? phase ^ 1u : phase;
+            const uint64_t soff = (uint64_t)((stage * m.stage_bytes) >> 4);
+            const uint64_t ad = a_base + soff, bd = b_base + soff;
+            const uint32_t first = kb != 0;
+#pragma unroll
+            for (int j = 0; j < kStageKBytes / kKStepBytes; ++j) {
+                ptx::mma_imm<CG, F8, IDESC>(d_tmem, ad + j * a_step, bd + j * b_step, j ? 1u : first);
+                if (j == 0) ready = ptx::mbar_test_wait(full_bar(next), next_phase);
+            }
+            issued = true;
+            // frees the stage (in both CTAs of a pair) once these MMAs have read it
+            if constexpr (CG == 2)
+                ptx::mma_commit_mc(empty_bar(stage), 0x3);
+            else
+                ptx::mma_commit(empty_bar(stage));
+            stage = next;
+            phase = next_phase;
+        }
+        if (stop) break;
+        if (p.num_kb > 0) {                      // accumulator complete
+            if constexpr (CG == 2)
+                ptx::mma_commit_mc(accf_bar(buf), 0x3);
+            else
+                ptx::mma_commit(accf_bar(buf));
+        } else {                                  // K == 0: nothing accumulated
+            ptx::mbar_arrive(accf_bar(buf));
+            if constexpr (CG == 2) ptx::mbar_arrive_cluster(accf_bar(buf), 1);
+        }
+    }
+    // Drain: every MMA issued above must finish before TMEM is freed.
+    if (issued) {
+        if constexpr (CG == 2)
+            ptx::mma_commit_cg2(drain);
+        else
+            ptx::mma_commit(drain);
+        drain_bar(drain, 0, p);
+    }
+}
+
 template <int CG, int BN, int OB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -293,71 +399,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA -----
         if (lane == 0 && rank == 0) {
-            const int eb = p.elem_bytes;
-            const int kel = kStageKBytes / eb;
-            // per-K-step advance of the descriptors' start address
-            const uint32_t a_step = p.a_kmajor ? kKStepBytes : (kKStepBytes / eb) * 128u;
-            const uint32_t b_step = p.b_kmajor ? kKStepBytes : (kKStepBytes / eb) * 128u;
-            const uint32_t a_lbo = p.a_kmajor ? 16u : (uint32_t)(kel * 128);
-            const uint32_t b_lbo = p.b_kmajor ? 16u : (uint32_t)(kel * 128);
-            int stage = 0;
-            uint32_t phase = 0;
-            int it = 0;
-            bool issued = false;
-            for (int tile = first_tile; tile < p.num_tiles; tile += tile_step, ++it) {
-                const int buf = it % C::kAccBufs;
-                const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
-                if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, abort_flag, kStatusRoleMma, peer_abort)) break;
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-                bool stop = false;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(full_bar(stage), phase, p, abort_flag, kStatusRoleMma, peer_abort)) {
-                        stop = true;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint32_t sa = ptx::smem_addr(ring + stage * C::kStageBytes);
-                    const uint32_t sb = sa + C::kABytes;
-#pragma unroll
-                    for (int j = 0; j < kStageKBytes / kKStepBytes; ++j) {
-                        const uint64_t ad = smem_desc(sa + j * a_step, a_lbo, 1024u);
-                        const uint64_t bd = smem_desc(sb + j * b_step, b_lbo, 1024u);
-                        const uint32_t acc = (kb | j) != 0;
-                        if (p.kind_f8)
-                            ptx::mma_f8<CG>(d_tmem, ad, bd, p.idesc, acc);
-                        else
-                            ptx::mma_f16<CG>(d_tmem, ad, bd, p.idesc, acc);
-                    }
-                    issued = true;
-                    // frees the stage (in both CTAs of a pair) once these MMAs have read it
-                    if constexpr (CG == 2)
-                        ptx::mma_commit_mc(empty_bar(stage), 0x3);
-                    else
-                        ptx::mma_commit(empty_bar(stage));
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (stop) break;
-                if (p.num_kb > 0) {                      // accumulator complete
-                    if constexpr (CG == 2)
-                        ptx::mma_commit_mc(accf_bar(buf), 0x3);
-                    else
-                        ptx::mma_commit(accf_bar(buf));
-                } else {                                  // K == 0: nothing accumulated
-                    ptx::mbar_arrive(accf_bar(buf));
-                    if constexpr (CG == 2) ptx::mbar_arrive_cluster(accf_bar(buf), 1);
-                }
-            }
-            // Drain: every MMA issued above must finish before TMEM is freed.
-            if (issued) {
-                if constexpr (CG == 2)
-                    ptx::mma_commit_cg2(drain);
-                else
-                    ptx::mma_commit(drain);
-                drain_bar(drain, 0, p);
+            MmaCtx<CG, BN, S> m{p,         ptx::smem_addr(ring), C::kABytes, C::kStageBytes, bar0, tmem_base,
+                                first_tile, tile_step, abort_flag, peer_abort};
+            switch (p.mma_variant) {     // one loop per tcgen05 instruction descriptor
+#define GEMM_MMA_CASE(v)                                                         \
+    case v:                                                                      \
+        mma_role<CG, BN, S, (v) >= 8, idesc_for(CG, BN, (v) >= 8, ((v) >> 2) & 1, \
+                                               ((v) >> 1) & 1, (v) & 1)>(m);     \
+        break;
+                GEMM_MMA_CASE(0) GEMM_MMA_CASE(1) GEMM_MMA_CASE(2) GEMM_MMA_CASE(3)
+                GEMM_MMA_CASE(4) GEMM_MMA_CASE(5) GEMM_MMA_CASE(6) GEMM_MMA_CASE(7)
+                GEMM_MMA_CASE(8) GEMM_MMA_CASE(9) GEMM_MMA_CASE(10) GEMM_MMA_CASE(11)
+#undef GEMM_MMA_CASE
+                default: break;
             }
         }
     } else {
