@@ -58,6 +58,11 @@ struct Cfg {
     static constexpr int kTmemCols = kAccBufs * BN;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+    // Stages are released to the producer in groups: every tcgen05.commit
+    // costs the tensor front end cycles that MMAs cannot use, so one commit
+    // frees kGroup stages.
+    static constexpr int kGroup = (kStages % 2 == 0 && kStages >= 6) ? 2 : 1;
+    static constexpr int kGroups = kStages / kGroup;
     static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps + 1;
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kNumBars * 8 + 16;
 };
@@ -187,7 +192,7 @@ struct MmaCtx {
 // the loop asks for the next stage's barrier while the current stage's MMAs
 // issue, builds descriptors by adding offsets to a precomputed base, and
 // carries the instruction descriptor as an immediate.
-template <int CG, int BN, int S, bool F8, uint32_t IDESC>
+template <int CG, int BN, int S, int G, bool F8, uint32_t IDESC>
 __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     const KernelParams& p = m.p;
     constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
@@ -206,6 +211,14 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     // start-address field never carry into the other fields
     const uint64_t a_base = smem_desc(m.ring, a_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
     const uint64_t b_base = smem_desc(m.ring + m.a_bytes, b_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
+    // One commit releases a whole group of G stages (empty[] is indexed by
+    // group); the commit covers every earlier MMA of this thread.
+    auto release = [&](int g) {
+        if constexpr (CG == 2)
+            ptx::mma_commit_mc(empty_bar(g), 0x3);
+        else
+            ptx::mma_commit(empty_bar(g));
+    };
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
@@ -234,11 +247,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
                 if (j == 0) ready = ptx::mbar_test_wait(full_bar(next), next_phase);
             }
             issued = true;
-            // frees the stage (in both CTAs of a pair) once these MMAs have read it
-            if constexpr (CG == 2)
-                ptx::mma_commit_mc(empty_bar(stage), 0x3);
-            else
-                ptx::mma_commit(empty_bar(stage));
+            if (stage % G == G - 1) release(stage / G);   // the group's last stage
             stage = next;
             phase = next_phase;
         }
@@ -253,6 +262,9 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
             if constexpr (CG == 2) ptx::mbar_arrive_cluster(accf_bar(buf), 1);
         }
     }
+    // A group left partly issued is released too, so a producer waiting to
+    // drain its copies is not left waiting.
+    if (issued && stage % G != 0) release(stage / G);
     // Drain: every MMA issued above must finish before TMEM is freed.
     if (issued) {
         if constexpr (CG == 2)
@@ -345,7 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n0 = nb * BN + (int)rank * C::kBRows;
                 bool stop = false;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(empty_bar(stage), phase ^ 1u, p, abort_flag, kStatusRoleLoad, peer_abort)) {
+                    // a group of stages is released together: wait at its first stage
+                    if (stage % C::kGroup == 0 &&
+                        !wait_bar(empty_bar(stage / C::kGroup), phase ^ 1u, p, abort_flag, kStatusRoleLoad, peer_abort)) {
                         stop = true;
                         break;
                     }
@@ -390,10 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // for the MMA to have consumed its stages instead.
             for (int s = 0; s < S; ++s)
                 if (pend[s]) {
+                    bool ok_drain;
                     if constexpr (CG == 2)
-                        drain_bar(empty_bar(s), pend_parity[s], p);
+                        ok_drain = drain_bar(empty_bar(s / C::kGroup), pend_parity[s], p);
                     else
-                        drain_bar(full_bar(s), pend_parity[s], p);
+                        ok_drain = drain_bar(full_bar(s), pend_parity[s], p);
+                    if (!ok_drain) break;   // already past the time bound: stop waiting
                 }
         }
     } else if (warp == 1) {
@@ -404,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             switch (p.mma_variant) {     // one loop per tcgen05 instruction descriptor
 #define GEMM_MMA_CASE(v)                                                         \
     case v:                                                                      \
-        mma_role<CG, BN, S, (v) >= 8, idesc_for(CG, BN, (v) >= 8, ((v) >> 2) & 1, \
+        mma_role<CG, BN, S, C::kGroup, (v) >= 8, idesc_for(CG, BN, (v) >= 8, ((v) >> 2) & 1, \
                                                ((v) >> 1) & 1, (v) & 1)>(m);     \
         break;
                 GEMM_MMA_CASE(0) GEMM_MMA_CASE(1) GEMM_MMA_CASE(2) GEMM_MMA_CASE(3)
