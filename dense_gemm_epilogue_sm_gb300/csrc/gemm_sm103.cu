@@ -343,9 +343,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int eb = p.elem_bytes;
             const int kel = kStageKBytes / eb;          // K elements per stage
             const int mn_box = kStageKBytes / eb;       // M/N elements per 128-byte row (MN-major)
+            // Latest fill of each stage (single CTA: drained on full[s]) or of
+            // each release group (pair: drained on empty[g], which a later
+            // fill of any stage of the group moves on).
             uint32_t pend_parity[S];
             bool pend[S];
             for (int s = 0; s < S; ++s) pend[s] = false;
+            auto pend_slot = [&](int st) { return CG == 2 ? st / C::kGroup : st; };
             int stage = 0;
             uint32_t phase = 0;
             bool skip_first = p.inject != 0 && rank == 0;
@@ -389,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < C::kBRows / mn_box; ++c)
                                 load(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb);
                         }
-                        pend[stage] = true;
-                        pend_parity[stage] = phase;
+                        pend[pend_slot(stage)] = true;
+                        pend_parity[pend_slot(stage)] = phase;
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (pend[s]) {
                     bool ok_drain;
                     if constexpr (CG == 2)
-                        ok_drain = drain_bar(empty_bar(s / C::kGroup), pend_parity[s], p);
+                        ok_drain = drain_bar(empty_bar(s), pend_parity[s], p);   // s indexes a group here
                     else
                         ok_drain = drain_bar(full_bar(s), pend_parity[s], p);
                     if (!ok_drain) break;   // already past the time bound: stop waiting

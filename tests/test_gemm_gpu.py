@@ -151,6 +151,22 @@ def test_cta_pair_kernel(spec):
     _full_check(spec, exact=spec.dist == "int4")
 
 
+def test_cta_pair_odd_stage_count_wraps_the_ring():
+    # K = 136 bf16 is 3 K blocks per tile; 256 pair tiles over the pairs give
+    # 3 or 4 tiles each, so a pair issues 9 or 12 stages: the ring (6 stages,
+    # released in groups) wraps and the last group is only partly refilled.
+    # The run must finish without any bounded wait running out.
+    from dense_gemm_epilogue_sm_gb300 import gemm_plan
+    from dense_gemm_epilogue_sm_gb300.torch_ops import desc_from_spec
+    spec = wl.Spec("pair_odd_stages", 4096, 4096, 136, beta=1.0, seed=47)
+    assert gemm_plan(desc_from_spec(spec)).cta_group == 2
+    inputs = wl.make_inputs(spec)
+    bits, op = H.run_gpu(spec, inputs)          # raises on a timeout status
+    d = H.logical_d(spec, bits)
+    rows = H.sample_rows(spec, per_tile=2)
+    H.compare(spec, inputs, d, H.oracle_rows(spec, inputs, rows), rows=rows)
+
+
 # ---------------------------------------------------- full workloads ------
 @pytest.mark.parametrize("name", ["odd_1000_at", "batched_32x512"])
 def test_workload_full_parity(name):
