@@ -92,24 +92,25 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 // Bounded wait on phase `parity` of `bar`.  Gives up when another role has
 // aborted or after p.timeout_ns; on timeout records `role` in the status word
-// and raises the abort flag.
+// and raises the abort flag.  Waiting threads sleep in try_wait (suspend
+// hint) rather than re-polling: polling threads slow the barrier and tensor
+// front end that the MMA issuer depends on.
 // `peer_abort` (0 outside a CTA pair) is the peer CTA's abort flag as a
 // shared::cluster address: a timeout raises it too, so the peer stops
 // waiting for work that will not come.
+constexpr uint32_t kSleepHintNs = 200000;
 __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const KernelParams& p,
                                       volatile uint32_t* abort_flag, uint32_t role, uint32_t peer_abort) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t n = 1;; ++n) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((n & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (ptx::globaltimer() - t0 > p.timeout_ns) {
-                *abort_flag = 1u;
-                if (peer_abort) ptx::st_cluster_u32(peer_abort, 1u);
-                atomicOr(p.status, kStatusTimeout | role);
-                return false;
-            }
+    for (;;) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1u;
+            if (peer_abort) ptx::st_cluster_u32(peer_abort, 1u);
+            atomicOr(p.status, kStatusTimeout | role);
+            return false;
         }
     }
 }
@@ -118,9 +119,9 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Kerne
 // and MMAs before the CTA releases its resources).
 __device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, const KernelParams& p) {
     const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t n = 0;; ++n) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((n & 31u) == 31u && ptx::globaltimer() - t0 > p.timeout_ns) {
+    for (;;) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
             atomicOr(p.status, kStatusTimeout | kStatusRoleDrain);
             return false;
         }

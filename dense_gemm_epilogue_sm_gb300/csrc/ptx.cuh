@@ -62,6 +62,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Probe with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` pass, instead of re-polling the barrier.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Non-blocking test of phase `parity` (never suspends the thread); lets a
 // thread ask early and use the answer later.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
