@@ -129,8 +129,9 @@ def dist_setup():
     return world, rank, local
 
 
-def oracle_sample(spec, inputs, rows_target_s=12.0, min_rows=2):
-    """Times the oracle on a bounded row sample; returns (tflops, rows, secs, threads)."""
+def oracle_sample(spec, inputs, rows_target_s=12.0):
+    """Times the oracle on a bounded random row sample sized for about
+    `rows_target_s` seconds; returns (tflops, rows, secs, threads)."""
     import numpy as np
 
     from oracle import gemm_ref
@@ -138,13 +139,12 @@ def oracle_sample(spec, inputs, rows_target_s=12.0, min_rows=2):
     threads = gemm_ref.max_threads()
     rng = np.random.default_rng(0)
     total_rows = spec.batch * spec.M
-    probe = np.sort(rng.choice(total_rows, size=min(total_rows, max(min_rows, threads)), replace=False))
-    gemm_ref.run_spec_rows(spec, inputs, rows=probe[:1])     # decodes B once (kept by the oracle)
+    gemm_ref.run_spec_rows(spec, inputs, rows=np.array([0]))       # decodes B once (kept by the oracle)
+    probe = np.sort(rng.choice(total_rows, size=min(total_rows, 2 * threads), replace=False))
     t0 = time.perf_counter()
     gemm_ref.run_spec_rows(spec, inputs, rows=probe)
-    dt = time.perf_counter() - t0
-    per_row = dt / len(probe)
-    n = int(min(total_rows, max(len(probe), rows_target_s / max(per_row, 1e-9))))
+    rows_per_s = len(probe) / (time.perf_counter() - t0)
+    n = int(min(total_rows, max(len(probe), rows_target_s * rows_per_s)))
     rows = np.sort(rng.choice(total_rows, size=n, replace=False))
     t0 = time.perf_counter()
     gemm_ref.run_spec_rows(spec, inputs, rows=rows)
