@@ -193,15 +193,25 @@ struct MmaCtx {
 // the loop asks for the next stage's barrier while the current stage's MMAs
 // issue, builds descriptors by adding offsets to a precomputed base, and
 // carries the instruction descriptor as an immediate.
+//
+// Every scalar the loop reads is copied into a register first.  The tcgen05
+// and mbarrier wrappers clobber "memory", so a value read through `m` or `p`
+// (local and kernel-parameter memory behind a reference) would be re-loaded
+// after every MMA, a chain of dependent loads between two MMAs.
 template <int CG, int BN, int S, int G, bool F8, uint32_t IDESC>
 __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
-    const KernelParams& p = m.p;
+    const KernelParams& p = m.p;                 // slow paths (wait_bar) only
+    const int num_kb = p.num_kb, num_tiles = p.num_tiles;
+    const int first_tile = m.first_tile, tile_step = m.tile_step;
+    const uint32_t bar0 = m.bar0, ring = m.ring, a_bytes = m.a_bytes, stage_bytes = m.stage_bytes;
+    const uint32_t tmem_base = m.tmem_base, peer_abort = m.peer_abort;
+    volatile uint32_t* const abort_flag = m.abort_flag;
     constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
-    auto full_bar = [&](int s) { return m.bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return m.bar0 + 8u * (S + s); };
-    auto accf_bar = [&](int b) { return m.bar0 + 8u * (2 * S + b); };
-    auto acce_bar = [&](int b) { return m.bar0 + 8u * (2 * S + 2 + b); };
-    const uint32_t drain = m.bar0 + 8u * (2 * S + 4 + 2 * kEpiWarps);
+    auto full_bar = [=](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [=](int s) { return bar0 + 8u * (S + s); };
+    auto accf_bar = [=](int b) { return bar0 + 8u * (2 * S + b); };
+    auto acce_bar = [=](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+    const uint32_t drain = bar0 + 8u * (2 * S + 4 + 2 * kEpiWarps);
     constexpr bool a_mn = (IDESC >> 15) & 1u, b_mn = (IDESC >> 16) & 1u;
     constexpr int eb = F8 ? 1 : 2;
     constexpr int kel = kStageKBytes / eb;
@@ -210,11 +220,11 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     constexpr uint32_t b_step = (b_mn ? (kKStepBytes / eb) * 128u : kKStepBytes) >> 4;
     // shared addresses stay below 2^18, so offsets added to the 14-bit
     // start-address field never carry into the other fields
-    const uint64_t a_base = smem_desc(m.ring, a_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
-    const uint64_t b_base = smem_desc(m.ring + m.a_bytes, b_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
+    const uint64_t a_base = smem_desc(ring, a_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
+    const uint64_t b_base = smem_desc(ring + a_bytes, b_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
     // One commit releases a whole group of G stages (empty[] is indexed by
     // group); the commit covers every earlier MMA of this thread.
-    auto release = [&](int g) {
+    auto release = [=](int g) {
         if constexpr (CG == 2)
             ptx::mma_commit_mc(empty_bar(g), 0x3);
         else
@@ -225,21 +235,21 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     int it = 0;
     bool issued = false;
     bool ready = ptx::mbar_test_wait(full_bar(0), 0);
-    for (int tile = m.first_tile; tile < p.num_tiles; tile += m.tile_step, ++it) {
+    for (int tile = first_tile; tile < num_tiles; tile += tile_step, ++it) {
         const int buf = it % kAccBufs;
         const uint32_t acc_par = (uint32_t)(it / kAccBufs) & 1u;
-        if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, m.abort_flag, kStatusRoleMma, m.peer_abort)) break;
+        if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, abort_flag, kStatusRoleMma, peer_abort)) break;
         ptx::tc_fence_after();   // the epilogue's reads of this accumulator come first
-        const uint32_t d_tmem = m.tmem_base + (uint32_t)(buf * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
         bool stop = false;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!ready && !wait_bar(full_bar(stage), phase, p, m.abort_flag, kStatusRoleMma, m.peer_abort)) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+            if (!ready && !wait_bar(full_bar(stage), phase, p, abort_flag, kStatusRoleMma, peer_abort)) {
                 stop = true;
                 break;
             }
             const int next = stage + 1 == S ? 0 : stage + 1;
             const uint32_t next_phase = stage + 1 == S ? phase ^ 1u : phase;
-            const uint64_t soff = (uint64_t)((stage * m.stage_bytes) >> 4);
+            const uint64_t soff = (uint64_t)((stage * stage_bytes) >> 4);
             const uint64_t ad = a_base + soff, bd = b_base + soff;
             const uint32_t first = kb != 0;
 #pragma unroll
@@ -253,7 +263,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
             phase = next_phase;
         }
         if (stop) break;
-        if (p.num_kb > 0) {                      // accumulator complete
+        if (num_kb > 0) {                      // accumulator complete
             if constexpr (CG == 2)
                 ptx::mma_commit_mc(accf_bar(buf), 0x3);
             else
@@ -347,9 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Latest fill of each stage (single CTA: drained on full[s]) or of
             // each release group (pair: drained on empty[g], which a later
             // fill of any stage of the group moves on).
-            uint32_t pend_parity[S];
-            bool pend[S];
-            for (int s = 0; s < S; ++s) pend[s] = false;
+            // (bit masks, so they stay in registers)
+            uint32_t pend = 0u, pend_parity = 0u;
             auto pend_slot = [&](int st) { return CG == 2 ? st / C::kGroup : st; };
             int stage = 0;
             uint32_t phase = 0;
@@ -394,8 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < C::kBRows / mn_box; ++c)
                                 load(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb);
                         }
-                        pend[pend_slot(stage)] = true;
-                        pend_parity[pend_slot(stage)] = phase;
+                        const uint32_t bit = 1u << pend_slot(stage);
+                        pend |= bit;
+                        pend_parity = phase ? (pend_parity | bit) : (pend_parity & ~bit);
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -408,12 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the copies complete on the leader's barrier, so each CTA waits
             // for the MMA to have consumed its stages instead.
             for (int s = 0; s < S; ++s)
-                if (pend[s]) {
+                if ((pend >> s) & 1u) {
+                    const uint32_t par = (pend_parity >> s) & 1u;
                     bool ok_drain;
                     if constexpr (CG == 2)
-                        ok_drain = drain_bar(empty_bar(s), pend_parity[s], p);   // s indexes a group here
+                        ok_drain = drain_bar(empty_bar(s), par, p);   // s indexes a group here
                     else
-                        ok_drain = drain_bar(full_bar(s), pend_parity[s], p);
+                        ok_drain = drain_bar(full_bar(s), par, p);
                     if (!ok_drain) break;   // already past the time bound: stop waiting
                 }
         }
