@@ -257,6 +257,30 @@ def run_e2e(op, spec, inputs, dev, steps, flops):
             "how": "pinned host buffers; upload, GEMM and download on three streams over two device buffer sets"}
 
 
+def run_plain(wl, g, GemmOp, desc_from_spec, A, B, dev, stream, launches=300):
+    """Plain bf16 8192^3 (no C, no bias, no activation) on the fused workload's A and B."""
+    import torch
+    pspec = wl.get("plain_bf16_8192")
+    op = GemmOp(desc_from_spec(pspec))
+    D = torch.empty(pspec.matrix_elems("d"), dtype=wl.DT[pspec.dtype_d], device=dev)
+    for _ in range(5):
+        op(A, B, None, D, None, stream)
+    op.check()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(launches):
+        op(A, B, None, D, None, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    op.check()
+    ms = e0.elapsed_time(e1) / launches
+    op.close()
+    return {"workload": pspec.name, "value": pspec.flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_launch": ms, "launches": launches,
+            "note": "same A and B, beta = 0, no bias, no activation; back-to-back launches after the headline run"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -356,6 +380,12 @@ def run_ours(args):
         e2e = run_e2e(op, spec, inputs, dev, max(1, min(args.steps, args.e2e_steps)), flops)
         op.check()
 
+    # The bare GEMM of the same size (beta = 0, no bias, no activation) on the
+    # same operands, timed separately and reported beside the headline.
+    plain = None
+    if spec.name == "fused_bf16_8192" and world == 1:
+        plain = run_plain(wl, g, GemmOp, desc_from_spec, A, B, dev, stream)
+
     peaks, peak_src = load_peaks()
     long_region = total_ms > 1000.0
     pkey = "bf16_tflops_sustained" if long_region else "bf16_tflops"
@@ -386,6 +416,9 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if plain is not None:
+        plain["frac_of_burst_peak"] = plain["value"] / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        line["plain_gemm"] = plain
     if rank == 0:
         print(json.dumps(line), flush=True)
     op.close()

@@ -104,6 +104,9 @@ WORKLOADS = {
     "fused_bf16_8192": Spec(
         "fused_bf16_8192", 8192, 8192, 8192, order_a="row", order_b="col", alpha=0.5, beta=1.0,
         act="relu", bias="col", seed=2, notes="D = ReLU(0.5*A*B + 1.0*C + bias[n])"),
+    "plain_bf16_8192": Spec(
+        "plain_bf16_8192", 8192, 8192, 8192, order_a="row", order_b="col", seed=2,
+        notes="the fused workload's GEMM alone: beta = 0, no bias, no activation"),
     "fp8_e4m3_8192": Spec(
         "fp8_e4m3_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e4m3",
         dist="uniform1", seed=3, notes="per-tensor scales folded into alpha"),

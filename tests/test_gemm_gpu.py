@@ -173,7 +173,8 @@ def test_workload_full_parity(name):
     _full_check(wl.get(name))
 
 
-@pytest.mark.parametrize("name", ["bf16_4096", "fused_bf16_8192", "fp8_e4m3_8192", "skinny_65536x256x4096"])
+@pytest.mark.parametrize("name", ["bf16_4096", "fused_bf16_8192", "plain_bf16_8192", "fp8_e4m3_8192",
+                                  "skinny_65536x256x4096"])
 def test_workload_sampled_rows(name):
     spec = wl.get(name)
     inputs = wl.make_inputs(spec)
