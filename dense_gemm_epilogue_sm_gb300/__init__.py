@@ -38,6 +38,8 @@ OP_N, OP_T = 0, 1
 ACT_NONE, ACT_RELU = 0, 1
 # gemm_bias_t
 BIAS_NONE, BIAS_COL, BIAS_ROW = 0, 1, 2
+# gemm_sched_t
+SCHED_AUTO, SCHED_DATA_PARALLEL, SCHED_STREAM_K, SCHED_SPLIT_TAIL = 0, 1, 2, 3
 
 DTYPE_BYTES = {F32: 4, F16: 2, BF16: 2, E4M3: 1}
 
@@ -94,6 +96,9 @@ def _load():
         "gemm_destroy": (i32, [vp]),
         "gemm_set_debug": (i32, [vp, i32, u32]),
         "gemm_launch_count": (ctypes.c_uint64, [vp]),
+        "gemm_set_schedule": (i32, [vp, i32]),
+        "gemm_get_schedule": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                    ctypes.POINTER(i32)]),
         "gemm_status_str": (ctypes.c_char_p, [i32]),
         "gemm_run_noalloc": (i32, [ctypes.POINTER(GemmDesc), vp, vp, vp, vp, vp, vp, i32]),
         "gemm_layout_query": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_char_p, ctypes.POINTER(i64)]),
@@ -111,8 +116,8 @@ def _load():
 
 lib = _load()
 EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_check", "gemm_destroy", "gemm_set_debug",
-            "gemm_launch_count", "gemm_status_str", "gemm_run_noalloc", "gemm_layout_query", "gemm_layout_eval",
-            "gemm_layout_op", "gemm_layout_gather_f32")
+            "gemm_set_schedule", "gemm_get_schedule", "gemm_launch_count", "gemm_status_str", "gemm_run_noalloc",
+            "gemm_layout_query", "gemm_layout_eval", "gemm_layout_op", "gemm_layout_gather_f32")
 
 
 def make_desc(M, N, K, batch=1, op_a=OP_N, op_b=OP_N, order_a=ROW_MAJOR, order_b=COL_MAJOR,
@@ -193,6 +198,22 @@ def gemm_set_debug(handle, inject_fault, timeout_ms):
     s = lib.gemm_set_debug(handle, inject_fault, timeout_ms)
     if s != OK:
         raise GemmError(s, "gemm_set_debug")
+
+
+def gemm_set_schedule(handle, mode):
+    s = lib.gemm_set_schedule(handle, mode)
+    if s != OK:
+        raise GemmError(s, "gemm_set_schedule")
+
+
+def gemm_get_schedule(handle):
+    """(workers, tiles computed whole, K-block iterations of the cut tiles,
+    ranges they are cut into)."""
+    w, dp, sk, nr = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    s = lib.gemm_get_schedule(handle, ctypes.byref(w), ctypes.byref(dp), ctypes.byref(sk), ctypes.byref(nr))
+    if s != OK:
+        raise GemmError(s, "gemm_get_schedule")
+    return w.value, dp.value, sk.value, nr.value
 
 
 def gemm_launch_count(handle):

@@ -216,6 +216,7 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     k.num_tiles = (int32_t)(tiles_m * tiles_n * L);
     const int kel = kStageKBytes / ab;
     k.num_kb = (int32_t)((d.K + kel - 1) / kel);
+    k.dp_tiles = k.num_tiles;                 // data parallel until a schedule says otherwise
     {
         gl::Layout parts[3] = {gl::leaf(G, 1), gl::leaf(tiles_n, tiles_m), gl::leaf(full_groups > 0 ? full_groups : 1, G)};
         gl::Layout full;
@@ -322,6 +323,9 @@ struct gemm_handle_s {
     int sm_count = 0;
     int max_clusters = 0;     // co-resident clusters of the planned kernel (0: unknown)
     uint32_t* status = nullptr;
+    int workers = 0;          // persistent CTAs (or CTA pairs) of a launch
+    void* ws = nullptr;       // stream-K partial sums, then the flag words
+    bool ws_dirty = false;    // a launch failed: flags may be left set
     cudaStream_t last_stream = nullptr;
     bool launched = false;
     uint64_t launches = 0;
@@ -330,6 +334,69 @@ struct gemm_handle_s {
     bool cache_valid = false;
     CUtensorMap maps[4];
 };
+
+namespace {
+
+// Work split for `mode` (gemm_sched_t) on the handle's device; allocates the
+// stream-K workspace when the split cuts tiles.
+gemm_status_t apply_schedule(gemm_handle_s* h, int mode) {
+    Plan& P = h->plan;
+    KernelParams& k = P.kp;
+    if (h->ws) {
+        cudaFree(h->ws);
+        h->ws = nullptr;
+    }
+    k.dp_tiles = k.num_tiles;
+    k.sk_iters = 0;
+    k.sk_ranges = 0;
+    k.sk_part = nullptr;
+    k.sk_flags = nullptr;
+    h->ws_dirty = false;
+    const int64_t workers = grid_for(P, h->sm_count, h->max_clusters) / P.cta_group;
+    h->workers = (int)workers;
+    const int64_t T = k.num_tiles, kb = k.num_kb;
+    if (mode == GEMM_SCHED_DATA_PARALLEL || workers < 1 || kb < 1) return GEMM_OK;
+    const int64_t waves = T / workers, rest = T % workers;
+    int64_t dp, sk, ranges;
+    if (mode == GEMM_SCHED_STREAM_K) {
+        // the last full wave and the ragged one, one equal range per worker
+        dp = waves >= 1 ? (waves - 1) * workers : 0;
+        sk = (T - dp) * kb;
+        ranges = workers;
+    } else {
+        // the ragged last wave only: each of its tiles cut into `pieces`
+        // equal K ranges, so that pieces * rest <= workers
+        if (rest == 0) return GEMM_OK;
+        int64_t pieces = workers / rest;
+        if (pieces > kb) pieces = kb;
+        if (mode == GEMM_SCHED_AUTO && (waves < 1 || pieces < 2 || kb / pieces < 4)) return GEMM_OK;
+        if (pieces < 1) pieces = 1;
+        dp = waves * workers;
+        sk = rest * kb;
+        ranges = rest * pieces;
+    }
+    const size_t part_bytes = (size_t)workers * P.cta_group * kTileM * P.tile_n * sizeof(float);
+    const size_t flag_bytes = (size_t)workers * P.cta_group * kEpiWarps * sizeof(uint32_t);
+    if (cudaMalloc(&h->ws, part_bytes + flag_bytes) != cudaSuccess ||
+        cudaMemset(static_cast<char*>(h->ws) + part_bytes, 0, flag_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        if (h->ws) cudaFree(h->ws);
+        h->ws = nullptr;
+        return GEMM_ERR_CUDA;
+    }
+    k.dp_tiles = (int32_t)dp;
+    k.sk_iters = sk;
+    k.sk_ranges = (int32_t)ranges;
+    k.sk_part = static_cast<float*>(h->ws);
+    k.sk_flags = reinterpret_cast<uint32_t*>(static_cast<char*>(h->ws) + part_bytes);
+    return GEMM_OK;
+}
+
+size_t flag_bytes_of(const gemm_handle_s* h) {
+    return (size_t)h->workers * h->plan.cta_group * kEpiWarps * sizeof(uint32_t);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -382,6 +449,12 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     }
     h->plan.kp.status = h->status;
     h->max_clusters = max_active_clusters(h->plan.cta_group, h->plan.tile_n, h->plan.out_bytes);
+    s = apply_schedule(h, GEMM_SCHED_AUTO);
+    if (s != GEMM_OK) {
+        cudaFree(h->status);
+        delete h;
+        return s;
+    }
     *out = h;
     return GEMM_OK;
 }
@@ -448,6 +521,13 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void
     la.grid = grid_for(P, h->sm_count, h->max_clusters);
     la.stream = static_cast<cudaStream_t>(stream);
     if (la.grid < 1) return GEMM_OK;
+    if (h->ws_dirty) {      // a failed launch may have left partial-sum flags set
+        if (cudaMemsetAsync(P.kp.sk_flags, 0, flag_bytes_of(h), la.stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        h->ws_dirty = false;
+    }
     const cudaError_t e = launch(la);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -472,8 +552,28 @@ gemm_status_t gemm_check(gemm_handle_t h) {
     }
     if (word) {
         cudaMemset(h->status, 0, sizeof(uint32_t));
+        if (h->ws) h->ws_dirty = true;
         return GEMM_ERR_TIMEOUT;
     }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_set_schedule(gemm_handle_t h, int32_t mode) {
+    if (!h || mode < GEMM_SCHED_AUTO || mode > GEMM_SCHED_SPLIT_TAIL) return GEMM_ERR_INVALID_ARG;
+    if (h->launched && cudaStreamSynchronize(h->last_stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return apply_schedule(h, mode);
+}
+
+gemm_status_t gemm_get_schedule(gemm_handle_t h, int32_t* workers, int64_t* dp_tiles, int64_t* sk_iters,
+                                int32_t* sk_ranges) {
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    if (workers) *workers = h->workers;
+    if (dp_tiles) *dp_tiles = h->plan.kp.dp_tiles;
+    if (sk_iters) *sk_iters = h->plan.kp.sk_iters;
+    if (sk_ranges) *sk_ranges = h->plan.kp.sk_ranges;
     return GEMM_OK;
 }
 
@@ -481,6 +581,7 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
     if (!h) return GEMM_OK;
     if (h->launched) cudaStreamSynchronize(h->last_stream);
     if (h->status) cudaFree(h->status);
+    if (h->ws) cudaFree(h->ws);
     cudaGetLastError();
     delete h;
     return GEMM_OK;

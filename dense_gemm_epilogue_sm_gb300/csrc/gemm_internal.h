@@ -29,6 +29,7 @@ constexpr uint32_t kStatusRoleLoad = 1u << 8;
 constexpr uint32_t kStatusRoleMma = 1u << 9;
 constexpr uint32_t kStatusRoleEpi = 1u << 10;
 constexpr uint32_t kStatusRoleDrain = 1u << 11;
+constexpr uint32_t kStatusRoleFixup = 1u << 12;   // a stream-K owner waiting for a partial sum
 
 struct KernelParams {
     int32_t M, N, K, L;           // kernel orientation: D is M x N row-major
@@ -63,6 +64,19 @@ struct KernelParams {
     int64_t d_bstride;            // batch stride of D, elements
     uint32_t* status;
     uint64_t timeout_ns;
+    // Work split (stream-K hybrid).  Tiles [0, dp_tiles) of the raster are
+    // computed whole, worker w taking tiles w, w + workers, ...; the K-block
+    // iterations of the remaining tiles, sk_iters in all, are cut into one
+    // contiguous range per worker.  A tile cut between workers is finished
+    // by the worker that ran its first K block (its owner), which adds the
+    // other workers' fp32 partial sums before the epilogue.  Without a split,
+    // dp_tiles = num_tiles and sk_iters = 0.
+    int32_t dp_tiles;
+    int64_t sk_iters;
+    int32_t sk_ranges;            // ranges the iterations are cut into (<= workers); range r
+                                  // is [sk_iters*r/sk_ranges, sk_iters*(r+1)/sk_ranges)
+    float* sk_part;               // per worker: one tile of fp32 partial sums
+    uint32_t* sk_flags;           // per worker, CTA and epilogue warp: 1 = partial written
     int32_t inject;               // 1: skip the first load (bounded-wait test)
 };
 

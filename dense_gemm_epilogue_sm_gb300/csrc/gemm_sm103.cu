@@ -137,6 +137,99 @@ __device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int
     nb = (int)(idx / p.tiles_m);
 }
 
+// ---------------------------------------------------------------- work ---
+// The sequence of work units (tile, K blocks [kb0, kb1)) of one worker (a CTA,
+// or a CTA pair).  Every role of the worker walks the same sequence.  First
+// the whole tiles w, w + workers, ... below dp_tiles; then the worker's range
+// of the split iterations (K blocks of the tiles from dp_tiles on, tile by
+// tile), cut at tile boundaries.  Range r goes to worker workers - 1 - r, so
+// the owner of a cut tile (the worker that ran its first K block) waits only
+// for workers of lower index, which were launched no later than itself.
+struct Sched {
+    int tile, step, dp_end, num_kb;
+    int64_t it, it_end;
+};
+
+__device__ __forceinline__ int64_t sk_range_start(int64_t sk_iters, int64_t r, int ranges) {
+    return sk_iters * r / ranges;
+}
+
+__device__ __forceinline__ Sched sched_make(const KernelParams& p, int worker, int workers) {
+    Sched s;
+    s.tile = worker;
+    s.step = workers;
+    s.dp_end = p.dp_tiles;
+    s.num_kb = p.num_kb;
+    const int64_t r = workers - 1 - worker;
+    if (r < p.sk_ranges) {
+        s.it = sk_range_start(p.sk_iters, r, p.sk_ranges);
+        s.it_end = sk_range_start(p.sk_iters, r + 1, p.sk_ranges);
+    } else {
+        s.it = s.it_end = 0;
+    }
+    return s;
+}
+
+__device__ __forceinline__ bool sched_next(Sched& s, int& tile, int& kb0, int& kb1) {
+    if (s.tile < s.dp_end) {
+        tile = s.tile;
+        kb0 = 0;
+        kb1 = s.num_kb;
+        s.tile += s.step;
+        return true;
+    }
+    if (s.it < s.it_end) {
+        const int64_t t = s.it / s.num_kb;
+        kb0 = (int)(s.it - t * s.num_kb);
+        const int64_t left = s.it_end - s.it;
+        kb1 = left < (int64_t)(s.num_kb - kb0) ? kb0 + (int)left : s.num_kb;
+        tile = s.dp_end + (int)t;
+        s.it += kb1 - kb0;
+        return true;
+    }
+    return false;
+}
+
+// Partial-sum slot of `worker`, CTA `rank`, epilogue warp `q`: the warp's 32
+// accumulator rows, stored so that each warp-wide 16-byte access is one
+// contiguous 512-byte run: [subtile][4-column group][lane] float4.
+template <int BN>
+__device__ __forceinline__ float4* part_slot(const KernelParams& p, int worker, int cg, uint32_t rank, int q) {
+    return reinterpret_cast<float4*>(p.sk_part) + ((size_t)(worker * cg + (int)rank) * kEpiWarps + q) * (kEpiRows * BN / 4);
+}
+
+__device__ __forceinline__ uint32_t* part_flag(const KernelParams& p, int worker, int cg, uint32_t rank, int q) {
+    return p.sk_flags + ((size_t)(worker * cg + (int)rank) * kEpiWarps + q);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* a) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(uint32_t* a, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// Bounded wait (all lanes of a warp) for another worker's partial sum.
+__device__ __noinline__ bool wait_part(const uint32_t* flag, const KernelParams& p, volatile uint32_t* abort_flag,
+                                       uint32_t peer_abort) {
+    if (ld_acquire(flag)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        __nanosleep(256);
+        if (ld_acquire(flag)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1u;
+            if (peer_abort) ptx::st_cluster_u32(peer_abort, 1u);
+            atomicOr(p.status, kStatusTimeout | kStatusRoleFixup);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ void unpack2(uint32_t w, bool f16, float& lo, float& hi) {
     if (f16) {
         const __half2 h = *reinterpret_cast<const __half2*>(&w);
@@ -201,7 +294,6 @@ struct MmaCtx {
 template <int CG, int BN, int S, int G, bool F8, uint32_t IDESC>
 __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     const KernelParams& p = m.p;                 // slow paths (wait_bar) only
-    const int num_kb = p.num_kb, num_tiles = p.num_tiles;
     const int first_tile = m.first_tile, tile_step = m.tile_step;
     const uint32_t bar0 = m.bar0, ring = m.ring, a_bytes = m.a_bytes, stage_bytes = m.stage_bytes;
     const uint32_t tmem_base = m.tmem_base, peer_abort = m.peer_abort;
@@ -235,14 +327,16 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     int it = 0;
     bool issued = false;
     bool ready = ptx::mbar_test_wait(full_bar(0), 0);
-    for (int tile = first_tile; tile < num_tiles; tile += tile_step, ++it) {
+    Sched sc = sched_make(p, first_tile, tile_step);
+    int tile, kb0, kb1;
+    for (; sched_next(sc, tile, kb0, kb1); ++it) {
         const int buf = it % kAccBufs;
         const uint32_t acc_par = (uint32_t)(it / kAccBufs) & 1u;
         if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, abort_flag, kStatusRoleMma, peer_abort)) break;
         ptx::tc_fence_after();   // the epilogue's reads of this accumulator come first
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
         bool stop = false;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
             if (!ready && !wait_bar(full_bar(stage), phase, p, abort_flag, kStatusRoleMma, peer_abort)) {
                 stop = true;
                 break;
@@ -251,7 +345,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
             const uint32_t next_phase = stage + 1 == S ? phase ^ 1u : phase;
             const uint64_t soff = (uint64_t)((stage * stage_bytes) >> 4);
             const uint64_t ad = a_base + soff, bd = b_base + soff;
-            const uint32_t first = kb != 0;
+            const uint32_t first = kb != kb0;
 #pragma unroll
             for (int j = 0; j < kStageKBytes / kKStepBytes; ++j) {
                 ptx::mma_imm<CG, F8, IDESC>(d_tmem, ad + j * a_step, bd + j * b_step, j ? 1u : first);
@@ -263,7 +357,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
             phase = next_phase;
         }
         if (stop) break;
-        if (num_kb > 0) {                      // accumulator complete
+        if (kb1 > kb0) {                         // accumulator complete
             if constexpr (CG == 2)
                 ptx::mma_commit_mc(accf_bar(buf), 0x3);
             else
@@ -363,14 +457,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool skip_first = p.inject != 0 && rank == 0;
-            for (int tile = first_tile; tile < p.num_tiles; tile += tile_step) {
+            Sched sc = sched_make(p, first_tile, tile_step);
+            int tile, kb0, kb1;
+            while (sched_next(sc, tile, kb0, kb1)) {
                 int mb, nb, l;
                 tile_coords(p, tile, mb, nb, l);
                 const int la = p.a_batched ? l : 0, lb = p.b_batched ? l : 0;
                 const int m0 = mb * kTileRows + (int)rank * kTileM;
                 const int n0 = nb * BN + (int)rank * C::kBRows;
                 bool stop = false;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     // a group of stages is released together: wait at its first stage
                     if (stage % C::kGroup == 0 &&
                         !wait_bar(empty_bar(stage / C::kGroup), phase ^ 1u, p, abort_flag, kStatusRoleLoad, peer_abort)) {
@@ -457,7 +553,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         int sub_count = 0;
         int it = 0;
         bool ok = true;
-        for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step, ++it) {
+        const int workers = tile_step;
+        // this warp's 32 rows of accumulator `b`, columns [32*..)
+        auto load_acc = [&](int b, int sub, uint32_t (&acc)[C::kEpiCols]) {
+            const uint32_t taddr = tmem_base + lane_off + (uint32_t)(b * BN + sub * C::kEpiCols);
+            ptx::tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
+            if constexpr (C::kEpiCols == 64)
+                ptx::tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
+            ptx::tmem_ld_wait();
+        };
+        // This warp is done reading accumulator `b`: tell the MMA issuer.
+        auto release_acc = [&](int b) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 2) {
+                    if (rank == 0)
+                        ptx::mbar_arrive(acce_bar(b));
+                    else
+                        ptx::mbar_arrive_cluster(acce_bar(b), 0);
+                } else {
+                    ptx::mbar_arrive(acce_bar(b));
+                }
+            }
+        };
+        // The workers whose stream-K ranges hold the later K blocks of a cut
+        // tile: ranges r_next, r_next + 1, ... that start before t_end.
+        auto for_each_part = [&](int64_t r_next, int64_t t_end, auto&& fn) {
+            for (int64_t j = r_next; j < p.sk_ranges; ++j) {
+                const int64_t js = sk_range_start(p.sk_iters, j, p.sk_ranges);
+                if (js >= t_end) break;
+                if (sk_range_start(p.sk_iters, j + 1, p.sk_ranges) == js) continue;     // empty range
+                if (!fn(workers - 1 - (int)j)) return false;
+            }
+            return true;
+        };
+        Sched sc = sched_make(p, first_tile, tile_step);
+        int tile, kb0, kb1;
+        for (; ok && sched_next(sc, tile, kb0, kb1); ++it) {
             const int buf = it % C::kAccBufs;
             const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
             int mb, nb, l;
@@ -465,6 +598,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, wait_bar(accf_bar(buf), acc_par, p, abort_flag, kStatusRoleEpi, peer_abort));
             if (!ok) break;
             ptx::tc_fence_after();
+            if (kb0 > 0) {
+                // Stream-K: this tile's first K blocks belong to another worker,
+                // its owner, which finishes the tile; hand it the raw sums.
+                float4* slot = part_slot<BN>(p, first_tile, CG, rank, q) + lane;
+#pragma unroll 1
+                for (int sub = 0; sub < C::kSubtiles; ++sub) {
+                    uint32_t acc[C::kEpiCols];
+                    load_acc(buf, sub, acc);
+#pragma unroll
+                    for (int c = 0; c < C::kEpiCols / 4; ++c)
+                        __stcg(slot + (sub * (C::kEpiCols / 4) + c) * 32,
+                               make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
+                                           __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3])));
+                }
+                release_acc(buf);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release(part_flag(p, first_tile, CG, rank, q), 1u);
+                continue;
+            }
+            // A tile cut short (kb1 < num_kb, stream-K region only): its later
+            // K blocks come from the next workers' partial sums.
+            const bool cut = kb1 < p.num_kb;
+            const int64_t t_end = cut ? (int64_t)(tile - p.dp_tiles + 1) * p.num_kb : 0;
+            const int64_t r_next = workers - first_tile;        // this worker's range index + 1
+            if (cut) {
+                ok = for_each_part(r_next, t_end, [&](int w) {
+                    return wait_part(part_flag(p, w, CG, rank, q), p, abort_flag, peer_abort);
+                });
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
             const int row0 = mb * kTileRows + (int)rank * kTileM + q * kEpiRows;
             const int row = row0 + lane;
             float row_bias = 0.f;
@@ -495,14 +660,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint32_t acc[C::kEpiCols];
                 if (p.num_kb > 0) {
-                    const uint32_t taddr = tmem_base + lane_off + (uint32_t)(buf * BN + sub * C::kEpiCols);
-                    ptx::tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
-                    if constexpr (C::kEpiCols == 64)
-                        ptx::tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
-                    ptx::tmem_ld_wait();
+                    load_acc(buf, sub, acc);
                 } else {
 #pragma unroll
                     for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
+                }
+                if (cut) {
+                    for_each_part(r_next, t_end, [&](int w) {
+                        const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
+#pragma unroll
+                        for (int c = 0; c < C::kEpiCols / 4; ++c) {
+                            const float4 v4 = __ldcg(ps + c * 32);
+                            acc[4 * c] = __float_as_uint(__uint_as_float(acc[4 * c]) + v4.x);
+                            acc[4 * c + 1] = __float_as_uint(__uint_as_float(acc[4 * c + 1]) + v4.y);
+                            acc[4 * c + 2] = __float_as_uint(__uint_as_float(acc[4 * c + 2]) + v4.z);
+                            acc[4 * c + 3] = __float_as_uint(__uint_as_float(acc[4 * c + 3]) + v4.w);
+                        }
+                        return true;
+                    });
                 }
                 // Row `lane` of the 32-row slab; 128-byte rows, 16-byte chunk c
                 // stored at chunk c ^ (row % 8) (the TMA 128B swizzle).
@@ -576,19 +751,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // This warp is done reading accumulator `buf`: tell the MMA issuer.
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && ok) {
-                if constexpr (CG == 2) {
-                    if (rank == 0)
-                        ptx::mbar_arrive(acce_bar(buf));
-                    else
-                        ptx::mbar_arrive_cluster(acce_bar(buf), 0);
-                } else {
-                    ptx::mbar_arrive(acce_bar(buf));
-                }
-            }
+            if (!ok) break;
+            release_acc(buf);
+            // the partial sums are consumed: clear their flags for the next launch
+            if (cut && lane == 0)
+                for_each_part(r_next, t_end, [&](int w) {
+                    *part_flag(p, w, CG, rank, q) = 0u;
+                    return true;
+                });
         }
         if (lane == 0) ptx::bulk_wait<0>();
         ptx::tc_fence_before();

@@ -5,7 +5,8 @@ current CUDA stream.  Argument marshalling only; the GEMM runs in
 import torch
 
 from . import (ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E4M3, F16, F32, OP_N, OP_T,
-               ROW_MAJOR, gemm_check, gemm_create, gemm_destroy, gemm_launch_count, gemm_run, make_desc)
+               ROW_MAJOR, gemm_check, gemm_create, gemm_destroy, gemm_get_schedule, gemm_launch_count, gemm_run,
+               gemm_set_schedule, make_desc)
 
 DTYPE_CODE = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3}
 ORDER_CODE = {"row": ROW_MAJOR, "col": COL_MAJOR}
@@ -44,6 +45,15 @@ class GemmOp:
 
     def check(self):
         gemm_check(self.handle)
+
+    def set_schedule(self, mode):
+        gemm_set_schedule(self.handle, mode)
+
+    @property
+    def schedule(self):
+        """(workers, tiles computed whole, K-block iterations of the cut tiles,
+        ranges they are cut into)."""
+        return gemm_get_schedule(self.handle)
 
     @property
     def launches(self):

@@ -36,9 +36,14 @@
  * every leading dimension and batch stride must be a multiple of 16 bytes and
  * every base pointer 16-byte aligned; otherwise GEMM_ERR_MISALIGNED.
  *
- * Ownership: the caller owns every device buffer.  A handle owns host state
- * and one 4-byte device status word allocated by gemm_create and freed by
- * gemm_destroy.  gemm_run never allocates or frees memory.
+ * Ownership: the caller owns every device buffer.  A handle owns host state,
+ * one 4-byte device status word and, when its schedule splits tiles between
+ * workers (stream-K, see gemm_set_schedule), a workspace of fp32 partial sums
+ * (one output tile per worker: 256 KiB per CTA pair, 128 KiB per CTA) plus one
+ * flag word per worker epilogue warp; gemm_create / gemm_set_schedule
+ * allocate them and gemm_destroy frees them.  gemm_run never allocates or
+ * frees memory.  Launches through one handle share its status word and
+ * workspace: issue them on one stream, or wait between them.
  *
  * Errors: argument errors are returned synchronously.  gemm_run is
  * asynchronous on the given stream; a failed launch returns GEMM_ERR_CUDA.
@@ -76,6 +81,12 @@ typedef enum { GEMM_COL_MAJOR = 0, GEMM_ROW_MAJOR = 1 } gemm_order_t;
 typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
 typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1 } gemm_act_t;
 typedef enum { GEMM_BIAS_NONE = 0, GEMM_BIAS_COL = 1, GEMM_BIAS_ROW = 2 } gemm_bias_t;
+typedef enum {
+    GEMM_SCHED_AUTO = 0,
+    GEMM_SCHED_DATA_PARALLEL = 1,
+    GEMM_SCHED_STREAM_K = 2,
+    GEMM_SCHED_SPLIT_TAIL = 3
+} gemm_sched_t;
 
 /* Problem descriptor.  Enumerations are carried as int32_t. */
 typedef struct {
@@ -138,6 +149,45 @@ GEMM_API gemm_status_t gemm_destroy(gemm_handle_t h);
  * runs out); 0 restores normal operation.  timeout_ms bounds every
  * in-kernel wait (0 keeps the current bound; default 2000 ms). */
 GEMM_API gemm_status_t gemm_set_debug(gemm_handle_t h, int32_t inject_fault, uint32_t timeout_ms);
+
+/* Work split of the persistent kernel.  The pages name split-K only as a
+ * profiler option ("Technical Documentation: NVIDIA/cutlass", "Performance
+ * Profiling": --split_k_mode=serial --split_k_slices=N); this library splits K
+ * to even out the last, ragged wave of tiles, in two forms:
+ *
+ *   GEMM_SCHED_DATA_PARALLEL  every tile is computed whole by one worker (a
+ *                             CTA, or a CTA pair), tile w, w + workers, ...
+ *   GEMM_SCHED_SPLIT_TAIL     the full waves are computed whole; each of the
+ *                             R tiles of the ragged last wave is cut into
+ *                             floor(workers / R) equal K ranges (at most one
+ *                             per K block), one range per worker.
+ *   GEMM_SCHED_STREAM_K       all full waves but the last are computed whole;
+ *                             the K blocks of the remaining tiles are cut
+ *                             into one equal contiguous range per worker.
+ *   GEMM_SCHED_AUTO (default) SPLIT_TAIL when there is at least one full
+ *                             wave, a ragged last wave, and it cuts each of
+ *                             its tiles into two or more ranges of at least
+ *                             4 K blocks; else data parallel.
+ *
+ * A tile cut between workers is finished by the worker that ran its first K
+ * block, after adding the other workers' fp32 partial sums, which they leave
+ * in the handle's workspace.  Under SPLIT_TAIL the workers of one cut index
+ * walk K together, as whole tiles of a wave do; under STREAM_K the ranges
+ * start at unrelated K offsets.
+ *
+ * Results of the two schedules can differ in the last bits of non-integer
+ * sums (fp32 summation order); each is deterministic from run to run.
+ * Allocates or frees the workspace as needed (synchronising with the
+ * handle's last launch first), so call it at set-up time, not between
+ * launches that are being captured.  Returns GEMM_ERR_INVALID_ARG for an
+ * unknown mode, GEMM_ERR_CUDA if the workspace cannot be allocated. */
+GEMM_API gemm_status_t gemm_set_schedule(gemm_handle_t h, int32_t mode);
+
+/* The handle's work split: workers (persistent CTAs, or CTA pairs), tiles
+ * computed whole, K-block iterations of the cut tiles (0: data parallel) and
+ * the number of ranges they are cut into.  Any output pointer may be NULL. */
+GEMM_API gemm_status_t gemm_get_schedule(gemm_handle_t h, int32_t* workers, int64_t* dp_tiles, int64_t* sk_iters,
+                                         int32_t* sk_ranges);
 
 /* Kernel launches issued through this handle so far. */
 GEMM_API uint64_t gemm_launch_count(gemm_handle_t h);
