@@ -11,6 +11,7 @@
  *   acc(l,m,n) = sum_k a(l,m,k) * b(l,k,n)          a = op(A), b = op(B)
  *   t          = alpha*scale_a*scale_b*acc + beta*c(l,m,n) + bias
  *   t          = max(t, 0)                          if the activation is ReLU
+ *   t          = t * Phi(t) = t/2 * (1 + erf(t/sqrt2))   if it is GELU
  *   D(l,m,n)   = round-to-nearest-even(t) in D's type
  *
  * Sources (page title, section):
@@ -41,6 +42,8 @@
  *  - bias is added after alpha scaling and is not scaled itself;
  *  - beta == 0 means C is not read at all (a NaN in C does not propagate);
  *  - ReLU(t) = t > 0 ? t : 0 (so NaN maps to 0, like fmaxf);
+ *  - GELU is the exact Gaussian-CDF form x * Phi(x) (the pages name no
+ *    GELU; the tanh approximation is not used);
  *  - a batch index l adds l * stride_x elements to operand x's base.
  */
 #include <math.h>
@@ -64,7 +67,7 @@ typedef struct {
     double alpha, beta, scale_a, scale_b;
     int32_t has_bias;      /* bias is fp32 */
     int32_t bias_per_row;  /* 0: bias[n] broadcast down the columns; 1: bias[m] */
-    int32_t act;           /* 0 = identity, 1 = ReLU */
+    int32_t act;           /* 0 = identity, 1 = ReLU, 2 = GELU */
 } oracle_problem_t;
 
 /* ---------------------------------------------------------------------------
@@ -315,6 +318,7 @@ int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, co
                     if (p->has_bias)
                         t += (double)bias[l * p->stride_bias + (p->bias_per_row ? m : n)];
                     if (p->act == 1) t = t > 0.0 ? t : 0.0;
+                    if (p->act == 2) t = 0.5 * t * (1.0 + erf(t * 0.70710678118654752440));
                     if (Tout) Tout[i * N + n] = t;
                     store_bits(Dout, p->dtype_d, i * N + n, oracle_encode(p->dtype_d, t));
                 }

@@ -115,7 +115,7 @@ def make_problem(M, N, K, L=1, op_a="N", op_b="N", order_a="row", order_b="col",
     p.dtype_c, p.dtype_d = _NAMES[dtype_c], _NAMES[dtype_d]
     p.alpha, p.beta, p.scale_a, p.scale_b = alpha, beta, scale_a, scale_b
     p.has_bias, p.bias_per_row = int(bool(has_bias)), int(bool(bias_per_row))
-    p.act = {"none": 0, "relu": 1}[act]
+    p.act = {"none": 0, "relu": 1, "gelu": 2}[act]
     return p
 
 
@@ -173,3 +173,27 @@ def run_spec_rows(spec, inputs, rows=None, nthreads=0, want_t=False):
     """Oracle rows (l*M + m) of a workload; returns (bits, t) as gemm_rows."""
     p = problem_from_spec(spec, inputs)
     return gemm_rows(p, inputs.A, inputs.B, inputs.C, inputs.bias, rows=rows, nthreads=nthreads, want_t=want_t)
+
+
+# ------------------------------------------------------------ reductions --
+# Per-row and per-column reductions of the epilogue's output ("Technical
+# Documentation: NVIDIA/cutlass", "What's New in CUTLASS 4.8": custom
+# epilogue fusions support per-row or per-column reductions).  Reading: the
+# reduced value is t, the epilogue result before it is rounded to D's type,
+# reduced over the whole (l, m, :) row or (l, :, n) column; the abs-max is
+# max |t| over each batch.  ``t`` is the (L, M, N) fp64 array of gemm_rows /
+# run_spec_rows with want_t, every row present.
+
+def row_sums(t):
+    """(L, M): sum over n of t(l, m, n)."""
+    return np.sum(t, axis=2)
+
+
+def col_sums(t):
+    """(L, N): sum over m of t(l, m, n)."""
+    return np.sum(t, axis=1)
+
+
+def abs_max(t):
+    """(L,): max over m, n of |t(l, m, n)| (NaN if any t is NaN)."""
+    return np.max(np.abs(t), axis=(1, 2))

@@ -333,3 +333,79 @@ def test_panel_reuse_sees_changed_operand_bytes():
     bbuf[:] = to_bits(2.0 * b, "bf16").reshape(-1)          # exact doubling, same buffer
     doubled, _ = g.gemm_rows(p, abuf, bbuf)
     assert np.array_equal(from_bits(doubled, "f32"), 2.0 * from_bits(first, "f32"))
+
+
+# ------------------------------------------------------------------ GELU ----
+def _t_of(values, act, dt_out="f32"):
+    """Oracle t for a K = 1 problem whose products are exactly `values`."""
+    x = np.asarray(values, dtype=np.float64)
+    n = x.size
+    a = x.reshape(1, 1, n).transpose(0, 2, 1)          # (L=1, M=n, K=1)
+    b = np.ones((1, 1, 1))
+    _, t = _run_oracle(a, b, None, None, op_a="N", op_b="N", order_a="row", order_b="row", order_cd="row",
+                       dt_in="bf16", dt_out=dt_out, act=act)
+    return t.reshape(-1)
+
+
+# Standard normal CDF values as printed in statistical tables (to 16 digits).
+PHI = {0.5: 0.6914624612740131, 1.0: 0.8413447460685429, 2.0: 0.9772498680518208,
+       3.0: 0.9986501019683699}
+
+
+def test_gelu_equals_x_times_the_normal_cdf_table():
+    xs = sorted(PHI) + [-x for x in sorted(PHI)] + [0.0]
+    got = _t_of(xs, "gelu")
+    for x, gx in zip(xs, got):
+        want = x * PHI[x] if x > 0 else (x * (1.0 - PHI[-x]) if x < 0 else 0.0)
+        assert abs(gx - want) <= 2e-15 * max(1.0, abs(x)), (x, gx, want)
+
+
+def test_gelu_odd_part_and_limits():
+    rng = np.random.default_rng(21)
+    x = from_bits(to_bits(rng.uniform(0.0, 6.0, 64), "bf16"), "bf16")
+    gp, gm = _t_of(x, "gelu"), _t_of(-x, "gelu")
+    # x*Phi(x) - (-x)*Phi(-x) = x, since Phi(-x) = 1 - Phi(x)
+    assert np.allclose(gp - gm, x, rtol=0, atol=1e-14)
+    big = _t_of([8.0, -8.0, 16.0, -16.0], "gelu")
+    assert abs(big[0] - 8.0) < 1e-13 and abs(big[1]) < 1e-13
+    assert big[2] == 16.0 and abs(big[3]) < 1e-50
+
+
+def test_gelu_rounds_once_to_the_output_type():
+    rng = np.random.default_rng(22)
+    x = from_bits(to_bits(rng.standard_normal(40), "bf16"), "bf16")
+    a = x.reshape(1, 40, 1)
+    bits, t = _run_oracle(a, np.ones((1, 1, 1)), None, None, op_a="N", op_b="N", order_a="row",
+                          order_b="row", order_cd="row", dt_in="bf16", dt_out="bf16", act="gelu")
+    assert np.array_equal(bits.reshape(-1), to_bits(t.reshape(-1), "bf16"))
+
+
+# ------------------------------------------------------------ reductions --
+def test_reductions_exact_on_integers():
+    rng = np.random.default_rng(23)
+    L, M, N, K = 2, 5, 7, 6
+    a = rng.integers(-4, 5, (L, M, K)).astype(np.float64)
+    b = rng.integers(-4, 5, (L, K, N)).astype(np.float64)
+    c = rng.integers(-4, 5, (L, M, N)).astype(np.float64)
+    bias = rng.integers(-3, 4, (L, N)).astype(np.float32)
+    for act in ("none", "relu"):
+        _, t = _run_oracle(a, b, c, bias, op_a="N", op_b="T", order_a="col", order_b="row", order_cd="row",
+                           dt_in="f16", dt_out="f32", alpha=1.0, beta=1.0, act=act)
+        exact = _exact_expected(a, b, c, bias, 1.0, 1.0, 1.0, 1.0, act, False)
+        rows = [[sum(exact[l, m, n] for n in range(N)) for m in range(M)] for l in range(L)]
+        cols = [[sum(exact[l, m, n] for m in range(M)) for n in range(N)] for l in range(L)]
+        amax = [max(abs(exact[l, m, n]) for m in range(M) for n in range(N)) for l in range(L)]
+        assert np.array_equal(g.row_sums(t), np.array(rows, dtype=np.float64))
+        assert np.array_equal(g.col_sums(t), np.array(cols, dtype=np.float64))
+        assert np.array_equal(g.abs_max(t), np.array(amax, dtype=np.float64))
+
+
+def test_row_and_column_sums_share_the_total():
+    rng = np.random.default_rng(24)
+    L, M, N, K = 3, 11, 13, 17
+    a, b = _normal_bf16(rng, (L, M, K)), _normal_bf16(rng, (L, K, N))
+    _, t = _run_oracle(a, b, None, None, op_a="N", op_b="N", order_a="row", order_b="col", order_cd="row",
+                       dt_in="bf16", dt_out="f32", act="gelu")
+    assert g.row_sums(t).shape == (L, M) and g.col_sums(t).shape == (L, N)
+    assert np.allclose(g.row_sums(t).sum(axis=1), g.col_sums(t).sum(axis=1), rtol=1e-13, atol=1e-12)
+    assert np.all(g.abs_max(t) >= np.abs(t).reshape(L, -1).max(axis=1))
