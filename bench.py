@@ -383,7 +383,7 @@ def run_ours(args):
     # The bare GEMM of the same size (beta = 0, no bias, no activation) on the
     # same operands, timed separately and reported beside the headline.
     plain = None
-    if spec.name == "fused_bf16_8192" and world == 1:
+    if spec.name == "fused_bf16_8192" and world == 1 and not args.no_plain:
         plain = run_plain(wl, g, GemmOp, desc_from_spec, A, B, dev, stream)
 
     peaks, peak_src = load_peaks()
@@ -437,6 +437,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-plain", action="store_true", help="skip the plain-GEMM line beside the fused headline")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
     if args.impl == "reference":

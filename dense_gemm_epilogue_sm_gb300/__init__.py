@@ -35,7 +35,9 @@ COL_MAJOR, ROW_MAJOR = 0, 1
 # gemm_op_t
 OP_N, OP_T = 0, 1
 # gemm_act_t
-ACT_NONE, ACT_RELU = 0, 1
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+# gemm_reduce_t (flags)
+REDUCE_NONE, REDUCE_ROW_SUM, REDUCE_COL_SUM, REDUCE_ABS_MAX = 0, 1, 2, 4
 # gemm_bias_t
 BIAS_NONE, BIAS_COL, BIAS_ROW = 0, 1, 2
 # gemm_sched_t
@@ -57,7 +59,7 @@ class GemmDesc(ctypes.Structure):
         ("dtype_c", ctypes.c_int32), ("dtype_d", ctypes.c_int32),
         ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
         ("scale_a", ctypes.c_float), ("scale_b", ctypes.c_float),
-        ("act", ctypes.c_int32), ("bias", ctypes.c_int32),
+        ("act", ctypes.c_int32), ("bias", ctypes.c_int32), ("reduce", ctypes.c_int32),
     ]
 
 
@@ -92,6 +94,7 @@ def _load():
         "gemm_plan": (i32, [ctypes.POINTER(GemmDesc), ctypes.POINTER(GemmPlanInfo)]),
         "gemm_create": (i32, [ctypes.POINTER(vp), ctypes.POINTER(GemmDesc)]),
         "gemm_run": (i32, [vp, vp, vp, vp, vp, vp, vp]),
+        "gemm_run_ex": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "gemm_check": (i32, [vp]),
         "gemm_destroy": (i32, [vp]),
         "gemm_set_debug": (i32, [vp, i32, u32]),
@@ -115,7 +118,7 @@ def _load():
 
 
 lib = _load()
-EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_check", "gemm_destroy", "gemm_set_debug",
+EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_run_ex", "gemm_check", "gemm_destroy", "gemm_set_debug",
             "gemm_set_schedule", "gemm_get_schedule", "gemm_launch_count", "gemm_status_str", "gemm_run_noalloc",
             "gemm_layout_query", "gemm_layout_eval", "gemm_layout_op", "gemm_layout_gather_f32")
 
@@ -124,7 +127,7 @@ def make_desc(M, N, K, batch=1, op_a=OP_N, op_b=OP_N, order_a=ROW_MAJOR, order_b
               order_c=ROW_MAJOR, order_d=ROW_MAJOR, lda=None, ldb=None, ldc=None, ldd=None,
               stride_a=0, stride_b=0, stride_c=0, stride_d=0, stride_bias=0,
               dtype_a=BF16, dtype_b=BF16, dtype_c=None, dtype_d=BF16, alpha=1.0, beta=0.0,
-              scale_a=1.0, scale_b=1.0, act=ACT_NONE, bias=BIAS_NONE):
+              scale_a=1.0, scale_b=1.0, act=ACT_NONE, bias=BIAS_NONE, reduce=REDUCE_NONE):
     """Fills a GemmDesc; leading dimensions default to the tight ones and the
     batch strides of A, B, C, D to the tight matrix sizes when batch > 1."""
 
@@ -152,7 +155,7 @@ def make_desc(M, N, K, batch=1, op_a=OP_N, op_b=OP_N, order_a=ROW_MAJOR, order_b
     d.dtype_d = dtype_d
     d.dtype_c = dtype_d if dtype_c is None else dtype_c
     d.alpha, d.beta, d.scale_a, d.scale_b = alpha, beta, scale_a, scale_b
-    d.act, d.bias = act, bias
+    d.act, d.bias, d.reduce = act, bias, reduce
     return d
 
 
@@ -182,6 +185,14 @@ def gemm_run(handle, A, B, C, D, bias, stream):
     s = lib.gemm_run(handle, A, B, C, D, bias, stream)
     if s != OK:
         raise GemmError(s, "gemm_run")
+
+
+def gemm_run_ex(handle, A, B, C, D, bias, row_sum, col_sum, abs_max, stream):
+    """gemm_run plus the descriptor's reductions into fp32 device arrays
+    (pointers as integers; None where not asked for)."""
+    s = lib.gemm_run_ex(handle, A, B, C, D, bias, row_sum, col_sum, abs_max, stream)
+    if s != OK:
+        raise GemmError(s, "gemm_run_ex")
 
 
 def gemm_check(handle):

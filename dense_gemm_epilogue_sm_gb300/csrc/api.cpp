@@ -90,7 +90,8 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
         return GEMM_ERR_INVALID_ARG;
     for (int o : {d.order_a, d.order_b, d.order_c, d.order_d})
         if (o != GEMM_ROW_MAJOR && o != GEMM_COL_MAJOR) return GEMM_ERR_INVALID_ARG;
-    if (d.act != GEMM_ACT_NONE && d.act != GEMM_ACT_RELU) return GEMM_ERR_INVALID_ARG;
+    if (d.act != GEMM_ACT_NONE && d.act != GEMM_ACT_RELU && d.act != GEMM_ACT_GELU) return GEMM_ERR_INVALID_ARG;
+    if (d.reduce & ~(GEMM_REDUCE_ROW_SUM | GEMM_REDUCE_COL_SUM | GEMM_REDUCE_ABS_MAX)) return GEMM_ERR_INVALID_ARG;
     if (d.bias != GEMM_BIAS_NONE && d.bias != GEMM_BIAS_COL && d.bias != GEMM_BIAS_ROW) return GEMM_ERR_INVALID_ARG;
     for (int t : {d.dtype_a, d.dtype_b, d.dtype_d})
         if (!dtype_bytes(t)) return GEMM_ERR_INVALID_ARG;
@@ -244,6 +245,12 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     k.bias_mode = P.bias_mode;
     k.bias_stride = d.stride_bias;
     k.act = d.act;
+    // reductions in kernel orientation: with D computed transposed, the
+    // caller's rows are the kernel's columns
+    const bool user_rows = (d.reduce & GEMM_REDUCE_ROW_SUM) != 0, user_cols = (d.reduce & GEMM_REDUCE_COL_SUM) != 0;
+    k.red_rows = P.info.swapped ? user_cols : user_rows;
+    k.red_cols = P.info.swapped ? user_rows : user_cols;
+    k.red_amax = (d.reduce & GEMM_REDUCE_ABS_MAX) != 0;
     k.out_f16 = d.dtype_d == GEMM_F16;
     k.d_ragged = ((P.Nk * ob) % 16) != 0;
     k.ldd = mode_stride(P.cd, 0);
@@ -325,7 +332,9 @@ struct gemm_handle_s {
     uint32_t* status = nullptr;
     int workers = 0;          // persistent CTAs (or CTA pairs) of a launch
     void* ws = nullptr;       // stream-K partial sums, then the flag words
-    bool ws_dirty = false;    // a launch failed: flags may be left set
+    bool ws_dirty = false;    // a launch failed: flags / abs-max words may be left set
+    void* red_ws = nullptr;   // reduction partials: rows, columns, abs-max words
+    size_t red_amax_off = 0;  // byte offset of the abs-max words in red_ws
     cudaStream_t last_stream = nullptr;
     bool launched = false;
     uint64_t launches = 0;
@@ -392,6 +401,32 @@ gemm_status_t apply_schedule(gemm_handle_s* h, int mode) {
     return GEMM_OK;
 }
 
+// Reduction partials (kernel orientation): rows [L][tiles_n][M], columns
+// [L][ceil(M/32)][N], abs-max words [L] (zeroed here; the finishing pass
+// zeroes them after each launch).
+gemm_status_t alloc_reductions(gemm_handle_s* h) {
+    KernelParams& k = h->plan.kp;
+    if (!k.red_rows && !k.red_cols && !k.red_amax) return GEMM_OK;
+    const int64_t L = k.L, M = k.M, N = k.N;
+    const size_t row_b = k.red_rows ? (size_t)(L * k.tiles_n * M) * sizeof(float) : 0;
+    const size_t col_b = k.red_cols ? (size_t)(L * ((M + 31) / 32) * N) * sizeof(float) : 0;
+    const size_t amax_off = (row_b + col_b + 255) & ~(size_t)255;
+    const size_t bytes = amax_off + (size_t)L * sizeof(uint32_t);
+    if (cudaMalloc(&h->red_ws, bytes) != cudaSuccess ||
+        cudaMemset(static_cast<char*>(h->red_ws) + amax_off, 0, (size_t)L * sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        if (h->red_ws) cudaFree(h->red_ws);
+        h->red_ws = nullptr;
+        return GEMM_ERR_CUDA;
+    }
+    char* base = static_cast<char*>(h->red_ws);
+    k.red_row_ws = k.red_rows ? reinterpret_cast<float*>(base) : nullptr;
+    k.red_col_ws = k.red_cols ? reinterpret_cast<float*>(base + row_b) : nullptr;
+    k.red_amax_ws = k.red_amax ? reinterpret_cast<uint32_t*>(base + amax_off) : nullptr;
+    h->red_amax_off = amax_off;
+    return GEMM_OK;
+}
+
 size_t flag_bytes_of(const gemm_handle_s* h) {
     return (size_t)h->workers * h->plan.cta_group * kEpiWarps * sizeof(uint32_t);
 }
@@ -450,7 +485,9 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     h->plan.kp.status = h->status;
     h->max_clusters = max_active_clusters(h->plan.cta_group, h->plan.tile_n, h->plan.out_bytes);
     s = apply_schedule(h, GEMM_SCHED_AUTO);
+    if (s == GEMM_OK) s = alloc_reductions(h);
     if (s != GEMM_OK) {
+        if (h->ws) cudaFree(h->ws);
         cudaFree(h->status);
         delete h;
         return s;
@@ -459,11 +496,14 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     return GEMM_OK;
 }
 
-gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D, const float* bias,
-                       void* stream) {
+static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
+                              const float* bias, float* row_sum, float* col_sum, float* abs_max, void* stream) {
     if (!h) return GEMM_ERR_INVALID_ARG;
     Plan& P = h->plan;
     const gemm_desc_t& d = P.d;
+    if (((d.reduce & GEMM_REDUCE_ROW_SUM) && !row_sum) || ((d.reduce & GEMM_REDUCE_COL_SUM) && !col_sum) ||
+        ((d.reduce & GEMM_REDUCE_ABS_MAX) && !abs_max))
+        return GEMM_ERR_INVALID_ARG;
     if (d.M == 0 || d.N == 0) return GEMM_OK;
     if (!D || (d.K > 0 && (!A || !B)) || (P.has_c && !C) || (d.bias != GEMM_BIAS_NONE && !bias))
         return GEMM_ERR_INVALID_ARG;
@@ -521,14 +561,32 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void
     la.grid = grid_for(P, h->sm_count, h->max_clusters);
     la.stream = static_cast<cudaStream_t>(stream);
     if (la.grid < 1) return GEMM_OK;
-    if (h->ws_dirty) {      // a failed launch may have left partial-sum flags set
-        if (cudaMemsetAsync(P.kp.sk_flags, 0, flag_bytes_of(h), la.stream) != cudaSuccess) {
+    if (h->ws_dirty) {      // a failed launch may have left flags or abs-max words set
+        if ((h->ws && cudaMemsetAsync(P.kp.sk_flags, 0, flag_bytes_of(h), la.stream) != cudaSuccess) ||
+            (P.kp.red_amax_ws &&
+             cudaMemsetAsync(P.kp.red_amax_ws, 0, (size_t)P.kp.L * sizeof(uint32_t), la.stream) != cudaSuccess)) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
         h->ws_dirty = false;
     }
-    const cudaError_t e = launch(la);
+    cudaError_t e = launch(la);
+    if (e == cudaSuccess && h->red_ws) {
+        FinishParams f;
+        f.L = P.kp.L;
+        f.M = P.kp.M;
+        f.N = P.kp.N;
+        f.tiles_n = P.kp.tiles_n;
+        f.slabs = (P.kp.M + 31) / 32;
+        f.row_ws = P.kp.red_row_ws;
+        f.col_ws = P.kp.red_col_ws;
+        f.amax_ws = P.kp.red_amax_ws;
+        // kernel rows are the caller's columns when D is computed transposed
+        f.out_rows = P.info.swapped ? col_sum : row_sum;
+        f.out_cols = P.info.swapped ? row_sum : col_sum;
+        f.out_amax = abs_max;
+        e = launch_finish(f, la.stream);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
@@ -537,6 +595,16 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void
     h->launched = true;
     ++h->launches;
     return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D, const float* bias,
+                       void* stream) {
+    return run_impl(h, A, B, C, D, bias, nullptr, nullptr, nullptr, stream);
+}
+
+gemm_status_t gemm_run_ex(gemm_handle_t h, const void* A, const void* B, const void* C, void* D, const float* bias,
+                          float* row_sum, float* col_sum, float* abs_max, void* stream) {
+    return run_impl(h, A, B, C, D, bias, row_sum, col_sum, abs_max, stream);
 }
 
 gemm_status_t gemm_check(gemm_handle_t h) {
@@ -552,7 +620,7 @@ gemm_status_t gemm_check(gemm_handle_t h) {
     }
     if (word) {
         cudaMemset(h->status, 0, sizeof(uint32_t));
-        if (h->ws) h->ws_dirty = true;
+        if (h->ws || h->red_ws) h->ws_dirty = true;
         return GEMM_ERR_TIMEOUT;
     }
     return GEMM_OK;
@@ -582,6 +650,7 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
     if (h->launched) cudaStreamSynchronize(h->last_stream);
     if (h->status) cudaFree(h->status);
     if (h->ws) cudaFree(h->ws);
+    if (h->red_ws) cudaFree(h->red_ws);
     cudaGetLastError();
     delete h;
     return GEMM_OK;
@@ -623,6 +692,7 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
     Plan P;
     const gemm_status_t s = validate_and_plan(desc, &P);
     if (s != GEMM_OK) return s;
+    if (P.d.reduce) return GEMM_ERR_UNSUPPORTED;     // reductions need a handle's workspace
     const gemm_desc_t& d = P.d;
     if (d.M == 0 || d.N == 0) return GEMM_OK;
     if (!D || (d.K > 0 && (!A || !B)) || (P.has_c && !C) || (d.bias != GEMM_BIAS_NONE && !bias))

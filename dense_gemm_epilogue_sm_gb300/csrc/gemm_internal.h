@@ -53,7 +53,7 @@ struct KernelParams {
     int32_t bias_mode;            // 0 none, 1 per kernel column, 2 per kernel row
     const float* bias;
     int64_t bias_stride;
-    int32_t act;                  // 0 none, 1 ReLU
+    int32_t act;                  // 0 none, 1 ReLU, 2 GELU (x * Phi(x))
     int32_t out_f16;              // 2-byte outputs: 1 fp16, 0 bf16
     // A TMA store clips the inner dimension only at 16-byte granules, so when
     // a D row does not end on a 16-byte boundary the subtile holding its last
@@ -77,6 +77,15 @@ struct KernelParams {
                                   // is [sk_iters*r/sk_ranges, sk_iters*(r+1)/sk_ranges)
     float* sk_part;               // per worker: one tile of fp32 partial sums
     uint32_t* sk_flags;           // per worker, CTA and epilogue warp: 1 = partial written
+    // Reductions of the epilogue value t (fp32, before rounding to D's type),
+    // kernel orientation.  Partials, each written once per launch:
+    //   red_row_ws[(l * tiles_n + n_tile) * M + m]   sum of t over one tile's columns
+    //   red_col_ws[(l * slabs + m / 32) * N + n]     sum of t over one 32-row slab
+    //   red_amax_ws[l]                               max |t| as fp32 bits (atomicMax)
+    int32_t red_rows, red_cols, red_amax;
+    float* red_row_ws;
+    float* red_col_ws;
+    uint32_t* red_amax_ws;
     int32_t inject;               // 1: skip the first load (bounded-wait test)
 };
 
@@ -89,6 +98,19 @@ struct LaunchArgs {
     int grid;                     // CTAs (a multiple of cta_group)
     cudaStream_t stream;
 };
+
+// Second pass of the reductions: sums the partials in a fixed order into the
+// caller's outputs (kernel orientation) and resets the abs-max words.
+struct FinishParams {
+    int32_t L, M, N, tiles_n, slabs;
+    const float* row_ws;          // null: no row sums
+    const float* col_ws;          // null: no column sums
+    uint32_t* amax_ws;            // null: no abs-max
+    float* out_rows;              // [L][M]
+    float* out_cols;              // [L][N]
+    float* out_amax;              // [L]
+};
+cudaError_t launch_finish(const FinishParams& f, cudaStream_t stream);
 
 int stages_for(int cta_group, int tile_n);
 size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes);

@@ -137,6 +137,11 @@ __device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int
     nb = (int)(idx / p.tiles_m);
 }
 
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
 // ---------------------------------------------------------------- work ---
 // The sequence of work units (tile, K blocks [kb0, kb1)) of one worker (a CTA,
 // or a CTA pair).  Every role of the worker walks the same sequence.  First
@@ -228,6 +233,32 @@ __device__ __noinline__ bool wait_part(const uint32_t* flag, const KernelParams&
             return false;
         }
     }
+}
+
+// Column sums of one 16-byte chunk over the warp's 32 rows: lane i holds
+// row i's V values.  Halving exchanges (lanes 16, 8, ... apart) leave each
+// lane the sum of one column over the lanes that share its high bits; the
+// remaining steps sum across the rest.  Returns that column sum; `j` is its
+// column within the chunk.  Lanes whose low log2(32/V) bits are zero hold
+// distinct columns.  Fixed order: the sums are the same on every run.
+template <int V>
+__device__ __forceinline__ float chunk_col_sum(float (&r)[V], int lane, int& j) {
+    j = 0;
+    int off = 16;
+#pragma unroll
+    for (int width = V; width > 1; width >>= 1, off >>= 1) {
+        const bool hi = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < width / 2; ++i) {
+            const float send = hi ? r[i] : r[width / 2 + i];
+            const float keep = hi ? r[width / 2 + i] : r[i];
+            r[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+        if (hi) j += width / 2;
+    }
+#pragma unroll
+    for (; off >= 1; off >>= 1) r[0] += __shfl_xor_sync(0xffffffffu, r[0], off);
+    return r[0];
 }
 
 __device__ __forceinline__ void unpack2(uint32_t w, bool f16, float& lo, float& hi) {
@@ -549,217 +580,260 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                         // TMEM lane quadrant this warp may read
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const bool f16_out = p.out_f16 != 0;
-        uint32_t c_phase[2] = {0u, 0u};
-        int sub_count = 0;
-        int it = 0;
-        bool ok = true;
-        const int workers = tile_step;
-        // this warp's 32 rows of accumulator `b`, columns [32*..)
-        auto load_acc = [&](int b, int sub, uint32_t (&acc)[C::kEpiCols]) {
-            const uint32_t taddr = tmem_base + lane_off + (uint32_t)(b * BN + sub * C::kEpiCols);
-            ptx::tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
-            if constexpr (C::kEpiCols == 64)
-                ptx::tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
-            ptx::tmem_ld_wait();
-        };
-        // This warp is done reading accumulator `b`: tell the MMA issuer.
-        auto release_acc = [&](int b) {
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (CG == 2) {
-                    if (rank == 0)
+        // Compiled twice: EXT adds GELU and the reductions, so the plain
+        // epilogue carries none of their code.
+        auto epilogue = [&](auto ext_tag) {
+            constexpr bool EXT = decltype(ext_tag)::value;
+            uint32_t c_phase[2] = {0u, 0u};
+            int sub_count = 0;
+            int it = 0;
+            bool ok = true;
+            const int workers = tile_step;
+            // this warp's 32 rows of accumulator `b`, columns [32*..)
+            auto load_acc = [&](int b, int sub, uint32_t (&acc)[C::kEpiCols]) {
+                const uint32_t taddr = tmem_base + lane_off + (uint32_t)(b * BN + sub * C::kEpiCols);
+                ptx::tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
+                if constexpr (C::kEpiCols == 64)
+                    ptx::tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
+                ptx::tmem_ld_wait();
+            };
+            // This warp is done reading accumulator `b`: tell the MMA issuer.
+            auto release_acc = [&](int b) {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CG == 2) {
+                        if (rank == 0)
+                            ptx::mbar_arrive(acce_bar(b));
+                        else
+                            ptx::mbar_arrive_cluster(acce_bar(b), 0);
+                    } else {
                         ptx::mbar_arrive(acce_bar(b));
-                    else
-                        ptx::mbar_arrive_cluster(acce_bar(b), 0);
-                } else {
-                    ptx::mbar_arrive(acce_bar(b));
-                }
-            }
-        };
-        // The workers whose stream-K ranges hold the later K blocks of a cut
-        // tile: ranges r_next, r_next + 1, ... that start before t_end.
-        auto for_each_part = [&](int64_t r_next, int64_t t_end, auto&& fn) {
-            for (int64_t j = r_next; j < p.sk_ranges; ++j) {
-                const int64_t js = sk_range_start(p.sk_iters, j, p.sk_ranges);
-                if (js >= t_end) break;
-                if (sk_range_start(p.sk_iters, j + 1, p.sk_ranges) == js) continue;     // empty range
-                if (!fn(workers - 1 - (int)j)) return false;
-            }
-            return true;
-        };
-        Sched sc = sched_make(p, first_tile, tile_step);
-        int tile, kb0, kb1;
-        for (; ok && sched_next(sc, tile, kb0, kb1); ++it) {
-            const int buf = it % C::kAccBufs;
-            const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
-            int mb, nb, l;
-            tile_coords(p, tile, mb, nb, l);
-            ok = __all_sync(0xffffffffu, wait_bar(accf_bar(buf), acc_par, p, abort_flag, kStatusRoleEpi, peer_abort));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            if (kb0 > 0) {
-                // Stream-K: this tile's first K blocks belong to another worker,
-                // its owner, which finishes the tile; hand it the raw sums.
-                float4* slot = part_slot<BN>(p, first_tile, CG, rank, q) + lane;
-#pragma unroll 1
-                for (int sub = 0; sub < C::kSubtiles; ++sub) {
-                    uint32_t acc[C::kEpiCols];
-                    load_acc(buf, sub, acc);
-#pragma unroll
-                    for (int c = 0; c < C::kEpiCols / 4; ++c)
-                        __stcg(slot + (sub * (C::kEpiCols / 4) + c) * 32,
-                               make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
-                                           __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3])));
-                }
-                release_acc(buf);
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) st_release(part_flag(p, first_tile, CG, rank, q), 1u);
-                continue;
-            }
-            // A tile cut short (kb1 < num_kb, stream-K region only): its later
-            // K blocks come from the next workers' partial sums.
-            const bool cut = kb1 < p.num_kb;
-            const int64_t t_end = cut ? (int64_t)(tile - p.dp_tiles + 1) * p.num_kb : 0;
-            const int64_t r_next = workers - first_tile;        // this worker's range index + 1
-            if (cut) {
-                ok = for_each_part(r_next, t_end, [&](int w) {
-                    return wait_part(part_flag(p, w, CG, rank, q), p, abort_flag, peer_abort);
-                });
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-            }
-            const int row0 = mb * kTileRows + (int)rank * kTileM + q * kEpiRows;
-            const int row = row0 + lane;
-            float row_bias = 0.f;
-            if (p.bias_mode == 2 && row < p.M) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
-            const float* bias_l = p.bias_mode == 1 ? p.bias + (int64_t)l * p.bias_stride : nullptr;
-            const int lc = p.c_batched ? l : 0;
-#pragma unroll 1
-            for (int sub = 0; sub < C::kSubtiles; ++sub) {
-                const int col0 = nb * BN + sub * C::kEpiCols;
-                if (row0 >= p.M || col0 >= p.N) continue;     // nothing of this subtile is in range
-                // the subtile holding a ragged row end is stored element by element
-                const bool direct = p.d_ragged && col0 + C::kEpiCols > p.N;
-                const int sbi = sub_count & 1;
-                ++sub_count;
-                uint8_t* sbuf = epi + (ew * 2 + sbi) * kEpiBufBytes;
-                const uint32_t sbuf_a = ptx::smem_addr(sbuf);
-                if (lane == 0) ptx::bulk_wait_read<1>();       // the store that last used sbuf has read it
-                __syncwarp();
-                if (p.has_c) {
-                    const uint32_t cb = cfull_bar(ew * 2 + sbi);
-                    if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(cb, kEpiBufBytes);
-                        ptx::tma_load_3d(sbuf_a, &tmC, col0, row0, lc, cb);
                     }
-                    ok = __all_sync(0xffffffffu, wait_bar(cb, c_phase[sbi], p, abort_flag, kStatusRoleEpi, peer_abort));
-                    c_phase[sbi] ^= 1u;
+                }
+            };
+            // The workers whose stream-K ranges hold the later K blocks of a cut
+            // tile: ranges r_next, r_next + 1, ... that start before t_end.
+            auto for_each_part = [&](int64_t r_next, int64_t t_end, auto&& fn) {
+                for (int64_t j = r_next; j < p.sk_ranges; ++j) {
+                    const int64_t js = sk_range_start(p.sk_iters, j, p.sk_ranges);
+                    if (js >= t_end) break;
+                    if (sk_range_start(p.sk_iters, j + 1, p.sk_ranges) == js) continue;     // empty range
+                    if (!fn(workers - 1 - (int)j)) return false;
+                }
+                return true;
+            };
+            Sched sc = sched_make(p, first_tile, tile_step);
+            int tile, kb0, kb1;
+            for (; ok && sched_next(sc, tile, kb0, kb1); ++it) {
+                const int buf = it % C::kAccBufs;
+                const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
+                int mb, nb, l;
+                tile_coords(p, tile, mb, nb, l);
+                ok = __all_sync(0xffffffffu, wait_bar(accf_bar(buf), acc_par, p, abort_flag, kStatusRoleEpi, peer_abort));
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if (kb0 > 0) {
+                    // Stream-K: this tile's first K blocks belong to another worker,
+                    // its owner, which finishes the tile; hand it the raw sums.
+                    float4* slot = part_slot<BN>(p, first_tile, CG, rank, q) + lane;
+    #pragma unroll 1
+                    for (int sub = 0; sub < C::kSubtiles; ++sub) {
+                        uint32_t acc[C::kEpiCols];
+                        load_acc(buf, sub, acc);
+    #pragma unroll
+                        for (int c = 0; c < C::kEpiCols / 4; ++c)
+                            __stcg(slot + (sub * (C::kEpiCols / 4) + c) * 32,
+                                   make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
+                                               __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3])));
+                    }
+                    release_acc(buf);
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) st_release(part_flag(p, first_tile, CG, rank, q), 1u);
+                    continue;
+                }
+                // A tile cut short (kb1 < num_kb, stream-K region only): its later
+                // K blocks come from the next workers' partial sums.
+                const bool cut = kb1 < p.num_kb;
+                const int64_t t_end = cut ? (int64_t)(tile - p.dp_tiles + 1) * p.num_kb : 0;
+                const int64_t r_next = workers - first_tile;        // this worker's range index + 1
+                if (cut) {
+                    ok = for_each_part(r_next, t_end, [&](int w) {
+                        return wait_part(part_flag(p, w, CG, rank, q), p, abort_flag, peer_abort);
+                    });
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
-                uint32_t acc[C::kEpiCols];
-                if (p.num_kb > 0) {
-                    load_acc(buf, sub, acc);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
-                }
-                if (cut) {
-                    for_each_part(r_next, t_end, [&](int w) {
-                        const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
-#pragma unroll
-                        for (int c = 0; c < C::kEpiCols / 4; ++c) {
-                            const float4 v4 = __ldcg(ps + c * 32);
-                            acc[4 * c] = __float_as_uint(__uint_as_float(acc[4 * c]) + v4.x);
-                            acc[4 * c + 1] = __float_as_uint(__uint_as_float(acc[4 * c + 1]) + v4.y);
-                            acc[4 * c + 2] = __float_as_uint(__uint_as_float(acc[4 * c + 2]) + v4.z);
-                            acc[4 * c + 3] = __float_as_uint(__uint_as_float(acc[4 * c + 3]) + v4.w);
-                        }
-                        return true;
-                    });
-                }
-                // Row `lane` of the 32-row slab; 128-byte rows, 16-byte chunk c
-                // stored at chunk c ^ (row % 8) (the TMA 128B swizzle).
-                uint8_t* row_base = sbuf + lane * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4* slot = reinterpret_cast<uint4*>(row_base + ((ch ^ (lane & 7)) << 4));
-                    float v[VPC];
-#pragma unroll
-                    for (int i = 0; i < VPC; ++i) v[i] = p.alpha * __uint_as_float(acc[ch * VPC + i]);
+                const bool reducing = EXT && (p.red_rows | p.red_cols | p.red_amax) != 0;
+                float row_acc = 0.f;          // sum of t over this tile's columns of row `row`
+                uint32_t amax_bits = 0u;      // max |t| as fp32 bits (NaN sorts above inf)
+                const int row0 = mb * kTileRows + (int)rank * kTileM + q * kEpiRows;
+                const int row = row0 + lane;
+                float row_bias = 0.f;
+                if (p.bias_mode == 2 && row < p.M) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
+                const float* bias_l = p.bias_mode == 1 ? p.bias + (int64_t)l * p.bias_stride : nullptr;
+                const int lc = p.c_batched ? l : 0;
+    #pragma unroll 1
+                for (int sub = 0; sub < C::kSubtiles; ++sub) {
+                    const int col0 = nb * BN + sub * C::kEpiCols;
+                    if (row0 >= p.M || col0 >= p.N) continue;     // nothing of this subtile is in range
+                    // the subtile holding a ragged row end is stored element by element
+                    const bool direct = p.d_ragged && col0 + C::kEpiCols > p.N;
+                    const int sbi = sub_count & 1;
+                    ++sub_count;
+                    uint8_t* sbuf = epi + (ew * 2 + sbi) * kEpiBufBytes;
+                    const uint32_t sbuf_a = ptx::smem_addr(sbuf);
+                    if (lane == 0) ptx::bulk_wait_read<1>();       // the store that last used sbuf has read it
+                    __syncwarp();
                     if (p.has_c) {
-                        const uint4 craw = *slot;
-                        const uint32_t w[4] = {craw.x, craw.y, craw.z, craw.w};
+                        const uint32_t cb = cfull_bar(ew * 2 + sbi);
+                        if (lane == 0) {
+                            ptx::mbar_arrive_expect_tx(cb, kEpiBufBytes);
+                            ptx::tma_load_3d(sbuf_a, &tmC, col0, row0, lc, cb);
+                        }
+                        ok = __all_sync(0xffffffffu, wait_bar(cb, c_phase[sbi], p, abort_flag, kStatusRoleEpi, peer_abort));
+                        c_phase[sbi] ^= 1u;
+                        if (!ok) break;
+                    }
+                    uint32_t acc[C::kEpiCols];
+                    if (p.num_kb > 0) {
+                        load_acc(buf, sub, acc);
+                    } else {
+    #pragma unroll
+                        for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
+                    }
+                    if (cut) {
+                        for_each_part(r_next, t_end, [&](int w) {
+                            const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
+    #pragma unroll
+                            for (int c = 0; c < C::kEpiCols / 4; ++c) {
+                                const float4 v4 = __ldcg(ps + c * 32);
+                                acc[4 * c] = __float_as_uint(__uint_as_float(acc[4 * c]) + v4.x);
+                                acc[4 * c + 1] = __float_as_uint(__uint_as_float(acc[4 * c + 1]) + v4.y);
+                                acc[4 * c + 2] = __float_as_uint(__uint_as_float(acc[4 * c + 2]) + v4.z);
+                                acc[4 * c + 3] = __float_as_uint(__uint_as_float(acc[4 * c + 3]) + v4.w);
+                            }
+                            return true;
+                        });
+                    }
+                    // Row `lane` of the 32-row slab; 128-byte rows, 16-byte chunk c
+                    // stored at chunk c ^ (row % 8) (the TMA 128B swizzle).
+                    uint8_t* row_base = sbuf + lane * 128;
+    #pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint4* slot = reinterpret_cast<uint4*>(row_base + ((ch ^ (lane & 7)) << 4));
+                        float v[VPC];
+    #pragma unroll
+                        for (int i = 0; i < VPC; ++i) v[i] = p.alpha * __uint_as_float(acc[ch * VPC + i]);
+                        if (p.has_c) {
+                            const uint4 craw = *slot;
+                            const uint32_t w[4] = {craw.x, craw.y, craw.z, craw.w};
+                            if constexpr (OB == 4) {
+    #pragma unroll
+                                for (int i = 0; i < 4; ++i) v[i] = fmaf(p.beta, __uint_as_float(w[i]), v[i]);
+                            } else {
+    #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    float lo, hi;
+                                    unpack2(w[i], f16_out, lo, hi);
+                                    v[2 * i] = fmaf(p.beta, lo, v[2 * i]);
+                                    v[2 * i + 1] = fmaf(p.beta, hi, v[2 * i + 1]);
+                                }
+                            }
+                        }
+                        if (p.bias_mode == 1) {
+                            const int cb0 = col0 + ch * VPC;
+    #pragma unroll
+                            for (int i = 0; i < VPC; ++i) v[i] += (cb0 + i < p.N) ? __ldg(bias_l + cb0 + i) : 0.f;
+                        } else if (p.bias_mode == 2) {
+    #pragma unroll
+                            for (int i = 0; i < VPC; ++i) v[i] += row_bias;
+                        }
+                        if (p.act == 1) {
+    #pragma unroll
+                            for (int i = 0; i < VPC; ++i) v[i] = fmaxf(v[i], 0.f);
+                        } else if (EXT && p.act == 2) {
+    #pragma unroll
+                            for (int i = 0; i < VPC; ++i) v[i] = 0.5f * v[i] * (1.f + erff(v[i] * 0.70710678118654752f));
+                        }
+                        if (reducing) {
+                            // elements outside D count as 0
+                            const int c0 = col0 + ch * VPC;
+                            float r[VPC];
+    #pragma unroll
+                            for (int i = 0; i < VPC; ++i) r[i] = (row < p.M && c0 + i < p.N) ? v[i] : 0.f;
+                            if (p.red_rows) {
+    #pragma unroll
+                                for (int i = 0; i < VPC; ++i) row_acc += r[i];
+                            }
+                            if (p.red_amax) {
+    #pragma unroll
+                                for (int i = 0; i < VPC; ++i) amax_bits = max(amax_bits, __float_as_uint(fabsf(r[i])));
+                            }
+                            if (p.red_cols) {
+                                int j;
+                                const float cs = chunk_col_sum<VPC>(r, lane, j);
+                                if ((lane & (32 / VPC - 1)) == 0 && c0 + j < p.N)
+                                    p.red_col_ws[((int64_t)l * ((p.M + 31) / 32) + row0 / 32) * p.N + c0 + j] = cs;
+                            }
+                        }
+                        uint4 out;
                         if constexpr (OB == 4) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) v[i] = fmaf(p.beta, __uint_as_float(w[i]), v[i]);
+                            out = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                                             __float_as_uint(v[3]));
                         } else {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                float lo, hi;
-                                unpack2(w[i], f16_out, lo, hi);
-                                v[2 * i] = fmaf(p.beta, lo, v[2 * i]);
-                                v[2 * i + 1] = fmaf(p.beta, hi, v[2 * i + 1]);
+                            out = make_uint4(pack2(v[0], v[1], f16_out), pack2(v[2], v[3], f16_out),
+                                             pack2(v[4], v[5], f16_out), pack2(v[6], v[7], f16_out));
+                        }
+                        if (!direct) {
+                            *slot = out;
+                        } else if (row < p.M) {
+                            const int c0 = col0 + ch * VPC;
+                            const uint32_t w[4] = {out.x, out.y, out.z, out.w};
+                            uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
+                                            ((int64_t)l * p.d_bstride + (int64_t)row * p.ldd) * OB;
+    #pragma unroll
+                            for (int i = 0; i < VPC; ++i) {
+                                if (c0 + i >= p.N) break;
+                                if constexpr (OB == 4)
+                                    *reinterpret_cast<uint32_t*>(drow + (int64_t)(c0 + i) * 4) = w[i];
+                                else
+                                    *reinterpret_cast<uint16_t*>(drow + (int64_t)(c0 + i) * 2) =
+                                        (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
                             }
                         }
                     }
-                    if (p.bias_mode == 1) {
-                        const int cb0 = col0 + ch * VPC;
-#pragma unroll
-                        for (int i = 0; i < VPC; ++i) v[i] += (cb0 + i < p.N) ? __ldg(bias_l + cb0 + i) : 0.f;
-                    } else if (p.bias_mode == 2) {
-#pragma unroll
-                        for (int i = 0; i < VPC; ++i) v[i] += row_bias;
-                    }
-                    if (p.act == 1) {
-#pragma unroll
-                        for (int i = 0; i < VPC; ++i) v[i] = fmaxf(v[i], 0.f);
-                    }
-                    uint4 out;
-                    if constexpr (OB == 4) {
-                        out = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
-                                         __float_as_uint(v[3]));
-                    } else {
-                        out = make_uint4(pack2(v[0], v[1], f16_out), pack2(v[2], v[3], f16_out),
-                                         pack2(v[4], v[5], f16_out), pack2(v[6], v[7], f16_out));
-                    }
                     if (!direct) {
-                        *slot = out;
-                    } else if (row < p.M) {
-                        const int c0 = col0 + ch * VPC;
-                        const uint32_t w[4] = {out.x, out.y, out.z, out.w};
-                        uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
-                                        ((int64_t)l * p.d_bstride + (int64_t)row * p.ldd) * OB;
-#pragma unroll
-                        for (int i = 0; i < VPC; ++i) {
-                            if (c0 + i >= p.N) break;
-                            if constexpr (OB == 4)
-                                *reinterpret_cast<uint32_t*>(drow + (int64_t)(c0 + i) * 4) = w[i];
-                            else
-                                *reinterpret_cast<uint16_t*>(drow + (int64_t)(c0 + i) * 2) =
-                                    (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
+                        ptx::fence_async_shared();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, l);
+                            ptx::bulk_commit();
                         }
                     }
                 }
-                if (!direct) {
-                    ptx::fence_async_shared();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, l);
-                        ptx::bulk_commit();
-                    }
+                if (!ok) break;
+                release_acc(buf);
+                if (EXT && p.red_rows && row < p.M) p.red_row_ws[((int64_t)l * p.tiles_n + nb) * p.M + row] = row_acc;
+                if (EXT && p.red_amax) {
+    #pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1)
+                        amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, off));
+                    if (lane == 0 && amax_bits) atomicMax(p.red_amax_ws + l, amax_bits);
                 }
+                // the partial sums are consumed: clear their flags for the next launch
+                if (cut && lane == 0)
+                    for_each_part(r_next, t_end, [&](int w) {
+                        *part_flag(p, w, CG, rank, q) = 0u;
+                        return true;
+                    });
             }
-            if (!ok) break;
-            release_acc(buf);
-            // the partial sums are consumed: clear their flags for the next launch
-            if (cut && lane == 0)
-                for_each_part(r_next, t_end, [&](int w) {
-                    *part_flag(p, w, CG, rank, q) = 0u;
-                    return true;
-                });
-        }
+        };
+        if (p.act == 2 || p.red_rows || p.red_cols || p.red_amax)
+            epilogue(BoolTag<true>{});
+        else
+            epilogue(BoolTag<false>{});
         if (lane == 0) ptx::bulk_wait<0>();
         ptx::tc_fence_before();
     }

@@ -4,14 +4,26 @@ current CUDA stream.  Argument marshalling only; the GEMM runs in
 ``libgemm_sm103.so``."""
 import torch
 
-from . import (ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E4M3, F16, F32, OP_N, OP_T,
-               ROW_MAJOR, gemm_check, gemm_create, gemm_destroy, gemm_get_schedule, gemm_launch_count, gemm_run,
-               gemm_set_schedule, make_desc)
+from . import (ACT_GELU, ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E4M3, F16, F32, OP_N,
+               OP_T, REDUCE_ABS_MAX, REDUCE_COL_SUM, REDUCE_ROW_SUM, ROW_MAJOR, gemm_check, gemm_create,
+               gemm_destroy, gemm_get_schedule, gemm_launch_count, gemm_run, gemm_run_ex, gemm_set_schedule,
+               make_desc)
 
 DTYPE_CODE = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3}
 ORDER_CODE = {"row": ROW_MAJOR, "col": COL_MAJOR}
 OP_CODE = {"N": OP_N, "T": OP_T}
-ACT_CODE = {"none": ACT_NONE, "relu": ACT_RELU}
+ACT_CODE = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU}
+REDUCE_CODE = {"row": REDUCE_ROW_SUM, "col": REDUCE_COL_SUM, "amax": REDUCE_ABS_MAX}
+
+
+def reduce_code(names):
+    """'none' or a '+'-joined subset of row, col, amax -> gemm_reduce_t flags."""
+    if names in ("", "none"):
+        return 0
+    code = 0
+    for n in names.split("+"):
+        code |= REDUCE_CODE[n]
+    return code
 BIAS_CODE = {"none": BIAS_NONE, "col": BIAS_COL, "row": BIAS_ROW}
 
 
@@ -25,7 +37,8 @@ def desc_from_spec(spec, scale_a=1.0, scale_b=1.0):
         spec.ld("a"), spec.ld("b"), spec.ld("c"), spec.ld("d"),
         stride("a"), stride("b"), stride("c"), stride("d"), bias_len if L > 1 else 0,
         DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_d], DTYPE_CODE[spec.dtype_d],
-        spec.alpha, spec.beta, scale_a, scale_b, ACT_CODE[spec.act], BIAS_CODE[spec.bias])
+        spec.alpha, spec.beta, scale_a, scale_b, ACT_CODE[spec.act], BIAS_CODE[spec.bias],
+        reduce_code(getattr(spec, "reduce", "none")))
 
 
 def _ptr(t):
@@ -42,6 +55,12 @@ class GemmOp:
     def __call__(self, A, B, C, D, bias=None, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream()
         gemm_run(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(bias), s.cuda_stream)
+
+    def run_ex(self, A, B, C, D, bias=None, row_sum=None, col_sum=None, abs_max=None, stream=None):
+        """With the descriptor's reductions (fp32 device tensors)."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        gemm_run_ex(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(bias), _ptr(row_sum), _ptr(col_sum),
+                    _ptr(abs_max), s.cuda_stream)
 
     def check(self):
         gemm_check(self.handle)

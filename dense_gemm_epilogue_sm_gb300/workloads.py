@@ -40,7 +40,7 @@ class Spec:
     dtype_d: str = "bf16"
     alpha: float = 1.0
     beta: float = 0.0
-    act: str = "none"
+    act: str = "none"          # none | relu | gelu
     bias: str = "none"          # none | col | row
     dist: str = "normal"        # normal | int4 | uniform1
     bias_sigma: float = 0.1
@@ -50,6 +50,7 @@ class Spec:
     ldb: int = 0
     ldc: int = 0
     ldd: int = 0
+    reduce: str = "none"        # none, or a '+'-joined subset of row, col, amax
     notes: str = ""
 
     # ----------------------------------------------------------- geometry --

@@ -79,7 +79,15 @@ typedef enum {
 typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3 } gemm_dtype_t;
 typedef enum { GEMM_COL_MAJOR = 0, GEMM_ROW_MAJOR = 1 } gemm_order_t;
 typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
-typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1 } gemm_act_t;
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 } gemm_act_t;
+/* Reductions of the epilogue value t = act(alpha*scale_a*scale_b*acc + beta*C + bias), fp32, taken before
+ * t is rounded to D's type; flags, combinable.  See gemm_run_ex. */
+typedef enum {
+    GEMM_REDUCE_NONE = 0,
+    GEMM_REDUCE_ROW_SUM = 1,      /* row_sum[l*M + m] = sum over n of t(l, m, n) */
+    GEMM_REDUCE_COL_SUM = 2,      /* col_sum[l*N + n] = sum over m of t(l, m, n) */
+    GEMM_REDUCE_ABS_MAX = 4       /* abs_max[l] = max over m, n of |t(l, m, n)| (NaN if any t is NaN) */
+} gemm_reduce_t;
 typedef enum { GEMM_BIAS_NONE = 0, GEMM_BIAS_COL = 1, GEMM_BIAS_ROW = 2 } gemm_bias_t;
 typedef enum {
     GEMM_SCHED_AUTO = 0,
@@ -100,6 +108,7 @@ typedef struct {
     float scale_a, scale_b;                        /* 1.0 unless 8-bit operands */
     int32_t act;                                   /* gemm_act_t */
     int32_t bias;                                  /* gemm_bias_t; bias is fp32 */
+    int32_t reduce;                                /* gemm_reduce_t flags; 0 = none */
 } gemm_desc_t;
 
 /* How a descriptor is executed; filled by gemm_plan (host only, no GPU). */
@@ -135,6 +144,25 @@ GEMM_API gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc);
  * Asynchronous; never allocates.  M == 0 or N == 0 launches nothing. */
 GEMM_API gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
                        const float* bias, void* stream);
+
+/* gemm_run plus the reductions the descriptor asks for (desc.reduce), into
+ * caller-owned fp32 device arrays: row_sum [batch*M], col_sum [batch*N],
+ * abs_max [batch]; an array the descriptor does not ask for may be NULL, one
+ * it asks for may not (GEMM_ERR_INVALID_ARG).  gemm_run on a descriptor with
+ * reductions returns GEMM_ERR_INVALID_ARG.
+ *
+ * The pages list per-row and per-column reductions among the epilogue
+ * fusions ("Technical Documentation: NVIDIA/cutlass", "What's New in CUTLASS
+ * 4.8"); what is reduced is this library's reading: t, the fp32 epilogue
+ * value after the activation and before rounding to D's type.  The GEMM
+ * kernel writes one partial per (row, 256- or 128-column tile) and per
+ * (32-row slab, column) into the handle's workspace (allocated by
+ * gemm_create) and a second, small kernel on the same stream adds them in
+ * index order, so the sums are the same on every run; the abs-max is an
+ * atomic maximum, also order-independent.  M == 0 or N == 0 launches nothing
+ * and leaves the outputs untouched. */
+GEMM_API gemm_status_t gemm_run_ex(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
+                                   const float* bias, float* row_sum, float* col_sum, float* abs_max, void* stream);
 
 /* Waits for the handle's last launch and reads its device status word:
  * GEMM_ERR_TIMEOUT if any bounded wait ran out (the word is then cleared),
@@ -216,7 +244,8 @@ GEMM_API uint64_t gemm_launch_count(gemm_handle_t h);
  * wait = 0: asynchronous; argument and launch errors are returned, an
  * in-kernel timeout is not reported.  wait = 1: the call synchronises
  * `stream` and returns GEMM_ERR_TIMEOUT if a bounded wait ran out.
- * Pointers, alignment and errors are as for gemm_run. */
+ * Pointers, alignment and errors are as for gemm_run; a descriptor with
+ * reductions (which need a handle's workspace) returns GEMM_ERR_UNSUPPORTED. */
 GEMM_API gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const void* B, const void* C,
                                         void* D, const float* bias, void* stream, int32_t wait);
 

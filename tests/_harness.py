@@ -34,12 +34,22 @@ def ulp(x, dtype):
     return np.exp2(e - MBITS[dtype])
 
 
-def tolerance(spec, inputs, d_ref):
+# An accumulation error e in the pre-activation value moves the output by at
+# most slope * e: 1 for none/ReLU, max |d/dx x*Phi(x)| < 1.13 for GELU.
+SLOPE = {"none": 1.0, "relu": 1.0, "gelu": 1.13}
+
+
+def accumulation_bound(spec, inputs):
+    """tau * sqrt(K) * max|A| * max|B|, times the activation's slope."""
     if spec.K == 0:
-        return ulp(d_ref, spec.dtype_d)
+        return 0.0
     a = inputs.A.to(torch.float32).abs().max().item() * inputs.scale_a
     b = inputs.B.to(torch.float32).abs().max().item() * inputs.scale_b
-    return TAU[spec.dtype_in] * math.sqrt(spec.K) * a * b + ulp(d_ref, spec.dtype_d)
+    return SLOPE[spec.act] * TAU[spec.dtype_in] * math.sqrt(spec.K) * a * b
+
+
+def tolerance(spec, inputs, d_ref):
+    return accumulation_bound(spec, inputs) + ulp(d_ref, spec.dtype_d)
 
 
 def canary_buffer(spec, extra=4096, device="cuda"):
