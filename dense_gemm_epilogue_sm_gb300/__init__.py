@@ -41,7 +41,7 @@ REDUCE_NONE, REDUCE_ROW_SUM, REDUCE_COL_SUM, REDUCE_ABS_MAX = 0, 1, 2, 4
 # gemm_bias_t
 BIAS_NONE, BIAS_COL, BIAS_ROW = 0, 1, 2
 # gemm_sched_t
-SCHED_AUTO, SCHED_DATA_PARALLEL, SCHED_STREAM_K, SCHED_SPLIT_TAIL = 0, 1, 2, 3
+SCHED_AUTO, SCHED_DATA_PARALLEL, SCHED_STREAM_K, SCHED_SPLIT_TAIL, SCHED_DYNAMIC = 0, 1, 2, 3, 4
 
 DTYPE_BYTES = {F32: 4, F16: 2, BF16: 2, E4M3: 1}
 

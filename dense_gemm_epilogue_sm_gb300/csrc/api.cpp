@@ -316,6 +316,7 @@ bool encode_map(CUtensorMap* map, const gl::Layout& lay, int dt, const void* bas
 int grid_for(const Plan& P, int sm_count, int max_clusters) {
     const int64_t tiles = P.info.tiles;
     const int cg = P.cta_group;
+    if (P.kp.clc) return (int)(tiles * cg);          // dynamic: one cluster per tile
     int64_t slots = sm_count / cg;
     if (max_clusters > 0 && max_clusters < slots) slots = max_clusters;
     if (slots < 1) slots = 1;
@@ -360,9 +361,14 @@ gemm_status_t apply_schedule(gemm_handle_s* h, int mode) {
     k.sk_ranges = 0;
     k.sk_part = nullptr;
     k.sk_flags = nullptr;
+    k.clc = 0;
     h->ws_dirty = false;
     const int64_t workers = grid_for(P, h->sm_count, h->max_clusters) / P.cta_group;
     h->workers = (int)workers;
+    if (mode == GEMM_SCHED_DYNAMIC) {      // whole tiles, one cluster launched per tile
+        k.clc = 1;
+        return GEMM_OK;
+    }
     const int64_t T = k.num_tiles, kb = k.num_kb;
     if (mode == GEMM_SCHED_DATA_PARALLEL || workers < 1 || kb < 1) return GEMM_OK;
     const int64_t waves = T / workers, rest = T % workers;
@@ -627,7 +633,7 @@ gemm_status_t gemm_check(gemm_handle_t h) {
 }
 
 gemm_status_t gemm_set_schedule(gemm_handle_t h, int32_t mode) {
-    if (!h || mode < GEMM_SCHED_AUTO || mode > GEMM_SCHED_SPLIT_TAIL) return GEMM_ERR_INVALID_ARG;
+    if (!h || mode < GEMM_SCHED_AUTO || mode > GEMM_SCHED_DYNAMIC) return GEMM_ERR_INVALID_ARG;
     if (h->launched && cudaStreamSynchronize(h->last_stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;

@@ -71,6 +71,7 @@ struct KernelParams {
     // by the worker that ran its first K block (its owner), which adds the
     // other workers' fp32 partial sums before the epilogue.  Without a split,
     // dp_tiles = num_tiles and sk_iters = 0.
+    int32_t clc;                  // 1: dynamic schedule (cluster launch control), grid = every tile
     int32_t dp_tiles;
     int64_t sk_iters;
     int32_t sk_ranges;            // ranges the iterations are cut into (<= workers); range r

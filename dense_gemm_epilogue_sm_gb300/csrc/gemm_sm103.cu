@@ -45,6 +45,10 @@ int stages_for(int cta_group, int tile_n) { return (cta_group == 1 && tile_n == 
 // main loop of the next (512 columns for BN = 256).
 constexpr int kPairAccBufs = 2;
 
+// Dynamic schedule: responses of cluster launch control kept for the roles
+// that have not read them yet.
+constexpr int kClcSlots = 4;
+
 template <int CG, int BN, int OB>
 struct Cfg {
     static constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
@@ -63,8 +67,9 @@ struct Cfg {
     // frees kGroup stages.
     static constexpr int kGroup = (kStages % 2 == 0 && kStages >= 6) ? 2 : 1;
     static constexpr int kGroups = kStages / kGroup;
-    static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps + 1;
-    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kNumBars * 8 + 16;
+    static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps + 1 + 2 * kClcSlots;
+    static constexpr int kSmemBytes =
+        1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kClcSlots * 16 + kNumBars * 8 + 16;
 };
 
 size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes) {
@@ -195,6 +200,108 @@ __device__ __forceinline__ bool sched_next(Sched& s, int& tile, int& kb0, int& k
     return false;
 }
 
+// Dynamic schedule ("Blackwell Cluster Launch Control": a launch holds one
+// cluster per tile; a running cluster that finishes a tile cancels the
+// launch of a cluster that has not started and takes its tile, so SMs that
+// another kernel holds do not leave their tiles behind).  The load thread of
+// the pair's leader issues one request at a time, at the start of each tile,
+// and none after a response that cancelled nothing.  The response goes to
+// slot n % kClcSlots of every CTA of the cluster; each role (load thread,
+// MMA thread, epilogue warps, in both CTAs) reads response n when it
+// finishes its n-th tile and then arrives on the leader's empty[slot], which
+// the issuer waits on before the slot's next use.
+struct Work {
+    Sched s;
+    bool dyn, producer, first;
+    uint32_t n;                   // responses read so far
+    uint32_t armed;               // requests this CTA expects (load thread only)
+    uint32_t resp0, full0, empty0;   // response slot 0 and its full / empty barriers
+    uint32_t rank;
+    int cg;
+};
+
+__device__ __forceinline__ Work work_make(const KernelParams& p, int worker, int workers, bool producer,
+                                          uint32_t resp0, uint32_t full0, uint32_t empty0, uint32_t rank, int cg) {
+    Work w;
+    w.s = sched_make(p, worker, workers);
+    w.dyn = p.clc != 0;
+    w.producer = producer;
+    w.first = true;
+    w.n = 0;
+    w.armed = 0;
+    w.resp0 = resp0;
+    w.full0 = full0;
+    w.empty0 = empty0;
+    w.rank = rank;
+    w.cg = cg;
+    return w;
+}
+
+// Request n: this CTA expects 16 bytes on full[slot]; the leader waits for
+// the slot's previous response to be read everywhere, then asks.
+__device__ __noinline__ bool clc_request(uint32_t n, uint32_t resp0, uint32_t full0, uint32_t empty0, uint32_t rank,
+                                         int cg, const KernelParams& p, volatile uint32_t* abort_flag,
+                                         uint32_t peer_abort) {
+    const uint32_t slot = n % kClcSlots;
+    ptx::mbar_arrive_expect_tx(full0 + 8u * slot, 16);
+    if (rank != 0) return true;
+    if (n >= kClcSlots &&
+        !wait_bar(empty0 + 8u * slot, ((n / kClcSlots) - 1u) & 1u, p, abort_flag, kStatusRoleLoad, peer_abort))
+        return false;
+    if (cg == 2)
+        ptx::clc_try_cancel_mc(resp0 + 16u * slot, full0 + 8u * slot);
+    else
+        ptx::clc_try_cancel(resp0 + 16u * slot, full0 + 8u * slot);
+    return true;
+}
+
+// The next work unit of this role.  `arrive`: this thread releases the
+// response slot for its role (one thread per role and CTA).
+__device__ __forceinline__ bool work_next(Work& w, const KernelParams& p, int& tile, int& kb0, int& kb1,
+                                          volatile uint32_t* abort_flag, uint32_t role, uint32_t peer_abort,
+                                          bool arrive) {
+    if (!w.dyn) return sched_next(w.s, tile, kb0, kb1);
+    kb0 = 0;
+    kb1 = p.num_kb;
+    if (w.first) {
+        w.first = false;
+        if (*abort_flag) return false;    // the launch already failed: do no work
+        tile = w.s.tile;                  // this cluster's own tile
+        if (w.producer) {
+            w.armed = 1;
+            if (!clc_request(0, w.resp0, w.full0, w.empty0, w.rank, w.cg, p, abort_flag, peer_abort)) return false;
+        }
+        return true;
+    }
+    const uint32_t slot = w.n % kClcSlots;
+    if (!wait_bar(w.full0 + 8u * slot, (w.n / kClcSlots) & 1u, p, abort_flag, role, peer_abort)) return false;
+    uint32_t x;
+    const bool cancelled = ptx::clc_query(w.resp0 + 16u * slot, x);
+    if (arrive) {
+        if (w.rank == 0)
+            ptx::mbar_arrive(w.empty0 + 8u * slot);
+        else
+            ptx::mbar_arrive_cluster(w.empty0 + 8u * slot, 0);
+    }
+    ++w.n;
+    if (!cancelled) return false;
+    tile = (int)(x / (uint32_t)w.cg);
+    if (w.producer) {
+        w.armed = w.n + 1;
+        if (!clc_request(w.n, w.resp0, w.full0, w.empty0, w.rank, w.cg, p, abort_flag, peer_abort)) return false;
+    }
+    return true;
+}
+
+// Before the load thread leaves: a response that is still on its way must
+// land before the CTA's shared memory is released (abort paths only; a
+// normal end has read every response).
+__device__ __forceinline__ void work_drain(const Work& w, const KernelParams& p) {
+    if (!w.dyn || !w.producer || w.armed <= w.n) return;
+    const uint32_t last = w.armed - 1;
+    drain_bar(w.full0 + 8u * (last % kClcSlots), (last / kClcSlots) & 1u, p);
+}
+
 // Partial-sum slot of `worker`, CTA `rank`, epilogue warp `q`: the warp's 32
 // accumulator rows, stored so that each warp-wide 16-byte access is one
 // contiguous 512-byte run: [subtile][4-column group][lane] float4.
@@ -309,6 +416,7 @@ struct MmaCtx {
     int first_tile, tile_step;
     volatile uint32_t* abort_flag;
     uint32_t peer_abort;
+    uint32_t resp0, clc_full0, clc_empty0;   // dynamic schedule ring
 };
 
 // The MMA issuer (one thread of the pair leader).  A tcgen05.mma blocks its
@@ -358,9 +466,9 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     int it = 0;
     bool issued = false;
     bool ready = ptx::mbar_test_wait(full_bar(0), 0);
-    Sched sc = sched_make(p, first_tile, tile_step);
+    Work wk = work_make(p, first_tile, tile_step, false, m.resp0, m.clc_full0, m.clc_empty0, 0u, CG);
     int tile, kb0, kb1;
-    for (; sched_next(sc, tile, kb0, kb1); ++it) {
+    for (; work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleMma, peer_abort, true); ++it) {
         const int buf = it % kAccBufs;
         const uint32_t acc_par = (uint32_t)(it / kAccBufs) & 1u;
         if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, abort_flag, kStatusRoleMma, peer_abort)) break;
@@ -423,7 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
     uint8_t* epi = ring + C::kRingBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::kEpiBytes);
+    uint8_t* clc_resp = epi + C::kEpiBytes;             // kClcSlots x 16 bytes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(clc_resp + kClcSlots * 16);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -434,6 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
     auto cfull_bar = [&](int i) { return bar0 + 8u * (2 * S + 4 + i); };
     const uint32_t drain = bar0 + 8u * (2 * S + 4 + 2 * kEpiWarps);
+    const uint32_t clc_full0 = drain + 8u, clc_empty0 = drain + 8u * (1 + kClcSlots);
+    const uint32_t resp0 = ptx::smem_addr(clc_resp);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -454,7 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2 * kEpiWarps; ++i) ptx::mbar_init(cfull_bar(i), 1);
         ptx::mbar_init(drain, 1);
-        *abort_flag = 0u;
+        // A dynamic launch starts clusters that nobody cancelled once others
+        // leave; after a recorded error they do no work (no chain of timeouts).
+        *abort_flag = p.clc && *reinterpret_cast<volatile uint32_t*>(p.status) != 0u ? 1u : 0u;
+        for (int i = 0; i < kClcSlots; ++i) {
+            ptx::mbar_init(clc_full0 + 8u * i, 1);
+            // readers of a response: load thread, MMA thread (leader) and the
+            // four epilogue warps of each CTA
+            ptx::mbar_init(clc_empty0 + 8u * i, CG == 2 ? 2 * (1 + kEpiWarps) + 1 : 2 + kEpiWarps);
+        }
         ptx::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -488,9 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool skip_first = p.inject != 0 && rank == 0;
-            Sched sc = sched_make(p, first_tile, tile_step);
+            Work wk = work_make(p, first_tile, tile_step, true, resp0, clc_full0, clc_empty0, rank, CG);
             int tile, kb0, kb1;
-            while (sched_next(sc, tile, kb0, kb1)) {
+            while (work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleLoad, peer_abort, true)) {
                 int mb, nb, l;
                 tile_coords(p, tile, mb, nb, l);
                 const int la = p.a_batched ? l : 0, lb = p.b_batched ? l : 0;
@@ -554,12 +673,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok_drain = drain_bar(full_bar(s), par, p);
                     if (!ok_drain) break;   // already past the time bound: stop waiting
                 }
+            work_drain(wk, p);
         }
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA -----
         if (lane == 0 && rank == 0) {
-            MmaCtx<CG, BN, S> m{p,         ptx::smem_addr(ring), C::kABytes, C::kStageBytes, bar0, tmem_base,
-                                first_tile, tile_step, abort_flag, peer_abort};
+            MmaCtx<CG, BN, S> m{p,          ptx::smem_addr(ring), C::kABytes, C::kStageBytes, bar0,
+                                tmem_base,  first_tile,           tile_step,   abort_flag,       peer_abort,
+                                resp0,      clc_full0,            clc_empty0};
             switch (p.mma_variant) {     // one loop per tcgen05 instruction descriptor
 #define GEMM_MMA_CASE(v)                                                         \
     case v:                                                                      \
@@ -623,9 +744,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return true;
             };
-            Sched sc = sched_make(p, first_tile, tile_step);
+            Work wk = work_make(p, first_tile, tile_step, false, resp0, clc_full0, clc_empty0, rank, CG);
             int tile, kb0, kb1;
-            for (; ok && sched_next(sc, tile, kb0, kb1); ++it) {
+            for (; ok; ++it) {
+                if (!__all_sync(0xffffffffu, work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleEpi, peer_abort,
+                                                       lane == 0)))
+                    break;
                 const int buf = it % C::kAccBufs;
                 const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
                 int mb, nb, l;

@@ -313,6 +313,43 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------- cluster launch control --
+// Ask the hardware to cancel the launch of one cluster that has not started
+// yet; the 16-byte response lands at `resp` and completes 16 bytes on `bar`.
+// The multicast form writes the response (and completes the bytes) at the
+// same offsets in every CTA of the issuing cluster.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void clc_try_cancel_mc(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 "
+        "[%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Decodes a response: true if a cluster was cancelled (then `x` is the x
+// index of its first CTA).
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& x) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t.reg .b64 lo, hi;\n\t"
+        "ld.shared.v2.b64 {lo, hi}, [%2];\n\t"
+        "mov.b128 r, {lo, hi};\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(x)
+        : "r"(resp)
+        : "memory");
+    return ok != 0;
+}
+
 // ------------------------------------------------------------ cluster -----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

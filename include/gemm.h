@@ -93,7 +93,8 @@ typedef enum {
     GEMM_SCHED_AUTO = 0,
     GEMM_SCHED_DATA_PARALLEL = 1,
     GEMM_SCHED_STREAM_K = 2,
-    GEMM_SCHED_SPLIT_TAIL = 3
+    GEMM_SCHED_SPLIT_TAIL = 3,
+    GEMM_SCHED_DYNAMIC = 4
 } gemm_sched_t;
 
 /* Problem descriptor.  Enumerations are carried as int32_t. */
@@ -192,6 +193,15 @@ GEMM_API gemm_status_t gemm_set_debug(gemm_handle_t h, int32_t inject_fault, uin
  *   GEMM_SCHED_STREAM_K       all full waves but the last are computed whole;
  *                             the K blocks of the remaining tiles are cut
  *                             into one equal contiguous range per worker.
+ *   GEMM_SCHED_DYNAMIC        whole tiles, scheduled by the hardware
+ *                             ("Technical Documentation: NVIDIA/cutlass",
+ *                             "Blackwell Cluster Launch Control"): the
+ *                             launch holds one cluster per tile and a running
+ *                             cluster that finishes a tile cancels the launch
+ *                             of one that has not started and computes its
+ *                             tile instead.  SMs held by other work on the
+ *                             GPU then delay no tile; with the GPU to itself
+ *                             it matches DATA_PARALLEL.  Needs no workspace.
  *   GEMM_SCHED_AUTO (default) SPLIT_TAIL when there is at least one full
  *                             wave, a ragged last wave, and it cuts each of
  *                             its tiles into two or more ranges of at least
