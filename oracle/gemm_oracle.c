@@ -32,6 +32,17 @@
  *    accumulator (the block-scaled form D = C + (A x SFA)(B x SFB) of
  *    "Blackwell SM100 GEMMs", "Block Scaled GEMMs", with one scale per
  *    tensor).
+ *  - Block scaling (sf_vec > 0), "Technical Documentation: NVIDIA/cutlass",
+ *    "Block Scaled GEMMs": acc = sum_k (a(m,k) * SFA(m, k/SV)) *
+ *    (b(k,n) * SFB(n, k/SV)), SV = sf_vec elements of K per scale factor.
+ *    "Blackwell Narrow Precision Data Types": mx_float8 pairs an 8-bit float
+ *    with a ue8m0 scale (8 exponent bits, no sign, no mantissa), SV = 32; the
+ *    value of a ue8m0 code e is 2^(e-127) and e = 255 is NaN (the OCP MX
+ *    definition the table points to).  "Scale Factor Layouts": each
+ *    512-byte basic block holds 128 rows x 4 scale factors, row r's four
+ *    factors at byte (r % 32) * 16 + ((r % 128) / 32) * 4 (M0SF0-3, M32SF0-3,
+ *    M64SF0-3, M96SF0-3, then M1...), and the blocks follow each other along
+ *    K first (K-major), then along M; one such tensor per batch.
  *
  * Every product of two operands (<= 11 significant bits each) is exact in
  * fp64, and the fp64 sum over K carries a relative error of order K * 2^-53,
@@ -55,7 +66,7 @@
 #endif
 
 /* Element type codes of this oracle's own interface. */
-enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3 };
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3, OR_UE8M0 = 4 };
 
 typedef struct {
     int64_t M, N, K, L;
@@ -68,6 +79,7 @@ typedef struct {
     int32_t has_bias;      /* bias is fp32 */
     int32_t bias_per_row;  /* 0: bias[n] broadcast down the columns; 1: bias[m] */
     int32_t act;           /* 0 = identity, 1 = ReLU, 2 = GELU */
+    int32_t sf_vec;        /* 0: no block scaling; 32: ue8m0 scale per 32 K elements */
 } oracle_problem_t;
 
 /* ---------------------------------------------------------------------------
@@ -88,6 +100,7 @@ static int type_bits(int dt, int* eb, int* mb, int* ieee) {
 
 double oracle_decode(int dt, uint32_t bits) {
     int eb, mb, ieee;
+    if (dt == OR_UE8M0) return (bits & 0xFFu) == 0xFFu ? NAN : ldexp(1.0, (int)(bits & 0xFFu) - 127);
     if (!type_bits(dt, &eb, &mb, &ieee)) return NAN;
     const uint32_t mant = bits & ((1u << mb) - 1u);
     const uint32_t expf = (bits >> mb) & ((1u << eb) - 1u);
@@ -196,6 +209,19 @@ static int nthreads_or_default(int nthreads) {
 
 int oracle_max_threads(void) { return nthreads_or_default(0); }
 
+/* Byte offset of scale factor (row, kf) of batch l in a tensor of `rows`
+ * rows and `sfk` factors per row (the basic-block layout above). */
+int64_t oracle_sf_index(int64_t l, int64_t row, int64_t kf, int64_t rows, int64_t sfk) {
+    const int64_t kblocks = (sfk + 3) / 4, mblocks = (rows + 127) / 128;
+    const int64_t block = (row / 128) * kblocks + kf / 4;
+    return l * mblocks * kblocks * 512 + block * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + kf % 4;
+}
+
+static double sf_value(const uint8_t* sf, int64_t l, int64_t row, int64_t k, int64_t rows, const oracle_problem_t* p) {
+    const int64_t sfk = (p->K + p->sf_vec - 1) / p->sf_vec;
+    return oracle_decode(OR_UE8M0, sf[oracle_sf_index(l, row, k / p->sf_vec, rows, sfk)]);
+}
+
 /*
  * b(l, k, n) decoded into a k-major fp64 panel (K x N).  The last panel is
  * kept and reused when the next call names the same storage with the same
@@ -207,9 +233,10 @@ static double* g_panel = NULL;
 static size_t g_panel_cap = 0;
 static struct {
     const void* base;
+    const void* sfb;
     int64_t K, N, l, ldb, stride_b;
-    int32_t op_b, order_b, dtype_b;
-    uint64_t hash;
+    int32_t op_b, order_b, dtype_b, sf_vec;
+    uint64_t hash, sf_hash;
     int valid;
 } g_key;
 
@@ -222,7 +249,7 @@ static uint64_t fnv1a(const uint8_t* p, size_t n) {
     return h;
 }
 
-static const double* b_panel(const oracle_problem_t* p, const void* B, int64_t l) {
+static const double* b_panel(const oracle_problem_t* p, const void* B, const uint8_t* SFB, int64_t l) {
     const int64_t K = p->K, N = p->N;
     int eb, mb, ieee;
     const int bytes = type_bits(p->dtype_b, &eb, &mb, &ieee) / 8;
@@ -233,9 +260,16 @@ static const double* b_panel(const oracle_problem_t* p, const void* B, int64_t l
     const int64_t span = outer > 0 && inner > 0 ? (outer - 1) * p->ldb + inner : 0;
     const uint8_t* first = (const uint8_t*)B + (size_t)(l * p->stride_b) * bytes;
     const uint64_t h = fnv1a(first, (size_t)span * bytes);
+    uint64_t sh = 0;
+    if (p->sf_vec > 0) {
+        const int64_t sfk = (K + p->sf_vec - 1) / p->sf_vec;
+        const int64_t per = ((N + 127) / 128) * ((sfk + 3) / 4) * 512;
+        sh = fnv1a(SFB + l * per, (size_t)per);
+    }
     if (g_key.valid && g_key.base == B && g_key.K == K && g_key.N == N && g_key.l == l && g_key.ldb == p->ldb &&
         g_key.stride_b == p->stride_b && g_key.op_b == p->op_b && g_key.order_b == p->order_b &&
-        g_key.dtype_b == p->dtype_b && g_key.hash == h)
+        g_key.dtype_b == p->dtype_b && g_key.hash == h && g_key.sf_vec == p->sf_vec &&
+        (p->sf_vec == 0 || (g_key.sfb == (const void*)SFB && g_key.sf_hash == sh)))
         return g_panel;
     const size_t need = (size_t)(K > 0 ? K : 1) * (size_t)N;
     if (need > g_panel_cap) {
@@ -246,9 +280,15 @@ static const double* b_panel(const oracle_problem_t* p, const void* B, int64_t l
         if (!g_panel) return NULL;
     }
     for (int64_t k = 0; k < K; ++k)
-        for (int64_t n = 0; n < N; ++n)
-            g_panel[k * N + n] = oracle_decode(p->dtype_b, load_bits(B, p->dtype_b, b_index(p, l, k, n)));
+        for (int64_t n = 0; n < N; ++n) {
+            double v = oracle_decode(p->dtype_b, load_bits(B, p->dtype_b, b_index(p, l, k, n)));
+            if (p->sf_vec > 0) v *= sf_value(SFB, l, n, k, N, p);      /* b(k,n) * SFB(n, k/SV) */
+            g_panel[k * N + n] = v;
+        }
     g_key.base = B;
+    g_key.sfb = SFB;
+    g_key.sf_vec = p->sf_vec;
+    g_key.sf_hash = sh;
     g_key.K = K;
     g_key.N = N;
     g_key.l = l;
@@ -269,9 +309,9 @@ static const double* b_panel(const oracle_problem_t* p, const void* B, int64_t l
  * The full GEMM is the call with every row listed.
  * Returns 0 on success, a negative code on bad arguments or allocation failure.
  */
-int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, const void* C,
-                     const float* bias, int64_t nrows, const int64_t* rows, void* Dout,
-                     double* Tout, int nthreads) {
+int oracle_gemm_rows_sf(const oracle_problem_t* p, const void* A, const void* B, const uint8_t* SFA,
+                        const uint8_t* SFB, const void* C, const float* bias, int64_t nrows, const int64_t* rows,
+                        void* Dout, double* Tout, int nthreads) {
     int eb, mb, ieee;
     if (!p || p->M < 0 || p->N < 0 || p->K < 0 || p->L < 1) return -1;
     if (!type_bits(p->dtype_a, &eb, &mb, &ieee) || !type_bits(p->dtype_b, &eb, &mb, &ieee)) return -2;
@@ -279,6 +319,7 @@ int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, co
     const int use_c = p->beta != 0.0;
     if (use_c && (!C || !type_bits(p->dtype_c, &eb, &mb, &ieee))) return -4;
     if (p->has_bias && !bias) return -5;
+    if (p->sf_vec < 0 || (p->sf_vec > 0 && (!SFA || !SFB))) return -7;
     const int64_t M = p->M, N = p->N, K = p->K;
     const double scale = p->alpha * p->scale_a * p->scale_b;
     const int nt = nthreads_or_default(nthreads);
@@ -289,7 +330,7 @@ int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, co
         int64_t in_batch = 0;
         for (int64_t i = 0; i < nrows; ++i) in_batch += (rows[i] / M) == l;
         if (!in_batch) continue;
-        const double* Bd = b_panel(p, B, l);
+        const double* Bd = b_panel(p, B, SFB, l);
         if (!Bd) return -6;
 
 #pragma omp parallel num_threads(nt)
@@ -306,7 +347,8 @@ int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, co
                 for (int64_t n = 0; n < N; ++n) acc[n] = 0.0;
                 /* i-k-j order: one a(m,k) times the k-th row of b, summed. */
                 for (int64_t k = 0; k < K; ++k) {
-                    const double a = oracle_decode(p->dtype_a, load_bits(A, p->dtype_a, a_index(p, l, m, k)));
+                    double a = oracle_decode(p->dtype_a, load_bits(A, p->dtype_a, a_index(p, l, m, k)));
+                    if (p->sf_vec > 0) a *= sf_value(SFA, l, m, k, M, p);     /* a(m,k) * SFA(m, k/SV) */
                     const double* brow = Bd + k * N;
                     for (int64_t n = 0; n < N; ++n) acc[n] += a * brow[n];
                 }
@@ -327,6 +369,12 @@ int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, co
         }
     }
     return status;
+}
+
+int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, const void* C, const float* bias,
+                     int64_t nrows, const int64_t* rows, void* Dout, double* Tout, int nthreads) {
+    if (p && p->sf_vec != 0) return -7;
+    return oracle_gemm_rows_sf(p, A, B, NULL, NULL, C, bias, nrows, rows, Dout, Tout, nthreads);
 }
 
 /* Scatters packed rows (as produced by oracle_gemm_rows for every row, in

@@ -14,8 +14,8 @@ import numpy as np
 from . import build as _build
 
 # The oracle's own element-type codes.
-F32, F16, BF16, E4M3 = 0, 1, 2, 3
-_NAMES = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3}
+F32, F16, BF16, E4M3, UE8M0 = 0, 1, 2, 3, 4
+_NAMES = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3, "ue8m0": UE8M0}
 _BYTES = {F32: 4, F16: 2, BF16: 2, E4M3: 1}
 _BITS_NP = {F32: np.uint32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8}
 
@@ -34,6 +34,7 @@ class Problem(ctypes.Structure):
         ("alpha", ctypes.c_double), ("beta", ctypes.c_double),
         ("scale_a", ctypes.c_double), ("scale_b", ctypes.c_double),
         ("has_bias", ctypes.c_int32), ("bias_per_row", ctypes.c_int32), ("act", ctypes.c_int32),
+        ("sf_vec", ctypes.c_int32),
     ]
 
 
@@ -49,6 +50,13 @@ def lib():
         l.oracle_gemm_rows.argtypes = [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        l.oracle_gemm_rows_sf.restype = ctypes.c_int
+        l.oracle_gemm_rows_sf.argtypes = [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_int]
+        l.oracle_sf_index.restype = ctypes.c_int64
+        l.oracle_sf_index.argtypes = [ctypes.c_int64] * 5
         l.oracle_decode.restype = ctypes.c_double
         l.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_uint32]
         l.oracle_encode.restype = ctypes.c_uint32
@@ -92,7 +100,7 @@ def make_problem(M, N, K, L=1, op_a="N", op_b="N", order_a="row", order_b="col",
                  stride_a=0, stride_b=0, stride_c=0, stride_d=0, stride_bias=0,
                  dtype_a="bf16", dtype_b="bf16", dtype_c="bf16", dtype_d="bf16",
                  alpha=1.0, beta=0.0, scale_a=1.0, scale_b=1.0, has_bias=False,
-                 bias_per_row=False, act="none"):
+                 bias_per_row=False, act="none", sf_vec=0):
     """Builds an oracle problem; leading dimensions default to the tight ones."""
 
     def tight(order, rows, cols):
@@ -116,24 +124,27 @@ def make_problem(M, N, K, L=1, op_a="N", op_b="N", order_a="row", order_b="col",
     p.alpha, p.beta, p.scale_a, p.scale_b = alpha, beta, scale_a, scale_b
     p.has_bias, p.bias_per_row = int(bool(has_bias)), int(bool(bias_per_row))
     p.act = {"none": 0, "relu": 1, "gelu": 2}[act]
+    p.sf_vec = sf_vec
     return p
 
 
-def gemm_rows(p: Problem, A, B, C=None, bias=None, rows=None, nthreads=0, want_t=False):
+def gemm_rows(p: Problem, A, B, C=None, bias=None, rows=None, nthreads=0, want_t=False, sfa=None, sfb=None):
     """Runs the oracle on the listed rows (l*M + m; default: all rows).
 
     Returns (bits, t): ``bits`` is a (len(rows), N) array of D's raw bit
     patterns (uint16 for 16-bit types, uint32 for fp32); ``t`` the fp64
-    values before rounding when ``want_t`` is set, else None.
+    values before rounding when ``want_t`` is set, else None.  ``sfa`` /
+    ``sfb``: the ue8m0 scale-factor bytes (basic-block layout, see
+    sf_index) when the problem is block-scaled (p.sf_vec > 0).
     """
     if rows is None:
         rows = np.arange(p.L * p.M, dtype=np.int64)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     out = np.zeros((len(rows), p.N), dtype=_BITS_NP[p.dtype_d])
     t = np.zeros((len(rows), p.N), dtype=np.float64) if want_t else None
-    rc = lib().oracle_gemm_rows(ctypes.byref(p), _addr(A), _addr(B), _addr(C), _addr(bias),
-                                len(rows), rows.ctypes.data, out.ctypes.data,
-                                None if t is None else t.ctypes.data, nthreads)
+    rc = lib().oracle_gemm_rows_sf(ctypes.byref(p), _addr(A), _addr(B), _addr(sfa), _addr(sfb), _addr(C),
+                                   _addr(bias), len(rows), rows.ctypes.data, out.ctypes.data,
+                                   None if t is None else t.ctypes.data, nthreads)
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_rows failed with code {rc}")
     return out, t
@@ -172,7 +183,17 @@ def problem_from_spec(spec, inputs):
 def run_spec_rows(spec, inputs, rows=None, nthreads=0, want_t=False):
     """Oracle rows (l*M + m) of a workload; returns (bits, t) as gemm_rows."""
     p = problem_from_spec(spec, inputs)
-    return gemm_rows(p, inputs.A, inputs.B, inputs.C, inputs.bias, rows=rows, nthreads=nthreads, want_t=want_t)
+    ex = getattr(inputs, "extras", None) or {}
+    if getattr(spec, "block_scale", "none") != "none":
+        p.sf_vec = 32
+    return gemm_rows(p, inputs.A, inputs.B, inputs.C, inputs.bias, rows=rows, nthreads=nthreads, want_t=want_t,
+                     sfa=ex.get("sfa"), sfb=ex.get("sfb"))
+
+
+def sf_index(l, row, kf, rows, sfk):
+    """Byte offset of scale factor (row, kf) of batch l in the basic-block
+    layout ("Scale Factor Layouts"): the oracle's own index function."""
+    return lib().oracle_sf_index(l, row, kf, rows, sfk)
 
 
 # ------------------------------------------------------------ reductions --

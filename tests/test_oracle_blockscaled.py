@@ -1,0 +1,120 @@
+"""Pins the oracle's block-scaled GEMM (no GPU): the ue8m0 scale-factor codec
+against exact powers of two, the scale-factor index against the byte order
+stated on "Technical Documentation: NVIDIA/cutlass", "Scale Factor Layouts",
+exact rational brute force of D = sum_k (A x SFA)(B x SFB) on small inputs,
+and the closed forms where all scale factors are one or constant."""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from _dtypes import from_bits, to_bits
+from _storage import to_storage
+from oracle import gemm_ref as g
+
+
+def test_ue8m0_decodes_to_powers_of_two_and_nan():
+    for e in range(255):
+        assert g.decode("ue8m0", e) == math.ldexp(1.0, e - 127)
+    assert math.isnan(g.decode("ue8m0", 255))
+
+
+def test_scale_factor_index_follows_the_stated_byte_order():
+    rows, sfk = 300, 10                     # 3 blocks of 128 rows, ceil(10/4) = 3 blocks of 4 factors
+    idx = lambda l, r, k: g.sf_index(l, r, k, rows, sfk)
+    # "M0SF0 to M0SF3, M32SF0 to M32SF3, M64SF0 to M64SF3, and M96SF0 to
+    # M96SF3 are stored consecutively"
+    order = [(0, k) for k in range(4)] + [(32, k) for k in range(4)] + [(64, k) for k in range(4)] + \
+            [(96, k) for k in range(4)] + [(1, k) for k in range(4)]
+    assert [idx(0, r, k) for r, k in order] == list(range(20))
+    assert idx(0, 127, 3) == 511                     # the basic block is 512 bytes
+    # blocks follow each other K-major: the next 4 factors of the same rows,
+    # then the next 128 rows
+    assert idx(0, 0, 4) == 512 and idx(0, 0, 8) == 1024 and idx(0, 128, 0) == 3 * 512
+    assert idx(1, 0, 0) == 3 * 3 * 512               # one tensor per batch
+    seen = {idx(0, r, k) for r in range(384) for k in range(12)}
+    assert seen == set(range(3 * 3 * 512))           # a bijection onto the padded tensor
+
+
+def _pack_sf(codes, pad=127):
+    """(L, rows, sfk) ue8m0 codes -> byte tensor; unused bytes hold `pad`."""
+    L, rows, sfk = codes.shape
+    size = ((rows + 127) // 128) * ((sfk + 3) // 4) * 512
+    out = np.full(L * size, pad, dtype=np.uint8)
+    for l in range(L):
+        for r in range(rows):
+            for k in range(sfk):
+                out[g.sf_index(l, r, k, rows, sfk)] = codes[l, r, k]
+    return out
+
+
+def _e4m3(rng, shape, scale=1.0):
+    return from_bits(to_bits(rng.uniform(-scale, scale, shape), "e4m3"), "e4m3").reshape(shape)
+
+
+def _run(a, b, sfa_codes, sfb_codes, *, op_a="N", op_b="N", order_a="row", order_b="col", sf_vec=32,
+         dt_out="f32", pad=127):
+    L, M, K = a.shape
+    N = b.shape[2]
+    sa, sb = (M, K) if op_a == "N" else (K, M), (K, N) if op_b == "N" else (N, K)
+    abuf, lda, bsa = to_storage(to_bits(a, "e4m3").reshape(a.shape), op_a, order_a,
+                                sa[1] if order_a == "row" else sa[0])
+    bbuf, ldb, bsb = to_storage(to_bits(b, "e4m3").reshape(b.shape), op_b, order_b,
+                                sb[1] if order_b == "row" else sb[0])
+    ldd = N
+    p = g.make_problem(M, N, K, L, op_a, op_b, order_a, order_b, "row", "row", lda, ldb, ldd, ldd,
+                       bsa, bsb, 0, M * N if L > 1 else 0, 0, "e4m3", "e4m3", dt_out, dt_out, sf_vec=sf_vec)
+    sfa = _pack_sf(sfa_codes, pad) if sf_vec else None
+    sfb = _pack_sf(sfb_codes, pad) if sf_vec else None
+    bits, t = g.gemm_rows(p, abuf, bbuf, want_t=True, sfa=sfa, sfb=sfb)
+    return bits.reshape(L, M, N), t.reshape(L, M, N)
+
+
+@pytest.mark.parametrize("op_a,op_b,order_a,order_b", [("N", "N", "row", "col"), ("T", "N", "row", "row"),
+                                                       ("N", "T", "col", "col"), ("T", "T", "col", "row")])
+def test_block_scaled_bruteforce_exact(op_a, op_b, order_a, order_b):
+    rng = np.random.default_rng(31)
+    L, M, N, K = 2, 5, 6, 96
+    a, b = _e4m3(rng, (L, M, K), 8), _e4m3(rng, (L, K, N), 8)
+    sfa = rng.integers(120, 135, (L, M, K // 32))
+    sfb = rng.integers(120, 135, (L, N, K // 32))
+    _, t = _run(a, b, sfa, sfb, op_a=op_a, op_b=op_b, order_a=order_a, order_b=order_b)
+    for l in range(L):
+        for m in range(M):
+            for n in range(N):
+                want = sum((Fraction(a[l, m, k]) * Fraction(2) ** int(sfa[l, m, k // 32] - 127)) *
+                           (Fraction(b[l, k, n]) * Fraction(2) ** int(sfb[l, n, k // 32] - 127)) for k in range(K))
+                assert Fraction(t[l, m, n]) == want
+
+
+def test_unit_scale_factors_reduce_to_the_plain_product():
+    rng = np.random.default_rng(32)
+    L, M, N, K = 1, 40, 36, 160
+    a, b = _e4m3(rng, (L, M, K), 4), _e4m3(rng, (L, K, N), 4)
+    ones_a, ones_b = np.full((L, M, K // 32), 127), np.full((L, N, K // 32), 127)
+    bits_s, t_s = _run(a, b, ones_a, ones_b)
+    bits_p, t_p = _run(a, b, None, None, sf_vec=0)
+    assert np.array_equal(t_s, t_p) and np.array_equal(bits_s, bits_p)
+
+
+def test_constant_scale_factors_scale_the_product_exactly():
+    rng = np.random.default_rng(33)
+    L, M, N, K = 1, 17, 19, 128
+    a, b = _e4m3(rng, (L, M, K), 4), _e4m3(rng, (L, K, N), 4)
+    _, t_p = _run(a, b, None, None, sf_vec=0)
+    _, t_s = _run(a, b, np.full((L, M, K // 32), 127 + 5), np.full((L, N, K // 32), 127 - 9))
+    assert np.array_equal(t_s, t_p * 2.0 ** (5 - 9))
+
+
+def test_k_not_a_multiple_of_the_block_reads_only_real_factors():
+    # K = 80: the third factor of each row covers 16 real elements; the
+    # padding factors (code 255 = NaN here) must not be read
+    rng = np.random.default_rng(34)
+    L, M, N, K = 1, 3, 4, 80
+    a, b = _e4m3(rng, (L, M, K), 2), _e4m3(rng, (L, K, N), 2)
+    sfa, sfb = rng.integers(124, 131, (L, M, 3)), rng.integers(124, 131, (L, N, 3))
+    _, t = _run(a, b, sfa, sfb, pad=255)
+    want = np.einsum("lmk,lkn->lmn", a * 2.0 ** (np.repeat(sfa, 32, axis=2)[:, :, :K] - 127),
+                     b * 2.0 ** (np.repeat(sfb, 32, axis=2)[:, :, :K].transpose(0, 2, 1) - 127))
+    assert np.all(np.isfinite(t)) and np.allclose(t, want, rtol=1e-14, atol=0)
