@@ -197,7 +197,7 @@ def run_reference(args):
     return 0
 
 
-def run_e2e(op, spec, inputs, dev, steps, flops):
+def run_e2e(launch, spec, inputs, dev, steps, flops):
     """The same GEMM end to end through the public API with host buffers:
     every step uploads its inputs from pinned host memory, runs the GEMM and
     reads D back.  Steps are pipelined on three streams (upload, compute,
@@ -205,9 +205,12 @@ def run_e2e(op, spec, inputs, dev, steps, flops):
     i-1's download overlap step i's GEMM."""
     import torch
 
+    ex = inputs.extras or {}
     host = [inputs.A.pin_memory(), inputs.B.pin_memory(),
             inputs.C.pin_memory() if inputs.C is not None else None,
-            inputs.bias.pin_memory() if inputs.bias is not None else None]
+            inputs.bias.pin_memory() if inputs.bias is not None else None,
+            ex["sfa"].pin_memory() if "sfa" in ex else None,
+            ex["sfb"].pin_memory() if "sfb" in ex else None]
     nbuf = 2
     dev_in = [[None if t is None else torch.empty(t.shape, dtype=t.dtype, device=dev) for t in host]
               for _ in range(nbuf)]
@@ -225,7 +228,7 @@ def run_e2e(op, spec, inputs, dev, steps, flops):
 
     def step(i):
         b = i % nbuf
-        A, B, C, bias = dev_in[b]
+        A, B, C, bias, sfa, sfb = dev_in[b]
         with torch.cuda.stream(s_in):
             if i >= nbuf:
                 s_in.wait_event(comp_done[b])       # the GEMM of step i-2 has read these inputs
@@ -237,7 +240,7 @@ def run_e2e(op, spec, inputs, dev, steps, flops):
             s_comp.wait_event(in_done[b])
             if i >= nbuf:
                 s_comp.wait_event(out_done[b])      # step i-2's D has been read back
-            op(A, B, C, dev_out[b], bias, s_comp)
+            launch(A, B, C, dev_out[b], bias, s_comp, sfa, sfb)
             comp_done[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
@@ -309,10 +312,22 @@ def run_ours(args):
     B = inputs.B.to(dev)
     C = inputs.C.to(dev) if inputs.C is not None else None
     bias = inputs.bias.to(dev) if inputs.bias is not None else None
+    ex = inputs.extras or {}
+    sfa_d = ex["sfa"].to(dev) if "sfa" in ex else None
+    sfb_d = ex["sfb"].to(dev) if "sfb" in ex else None
     D = torch.empty(spec.batch * spec.matrix_elems("d"), dtype=wl.DT[spec.dtype_d], device=dev)
     desc = desc_from_spec(spec, inputs.scale_a, inputs.scale_b)
     info = g.gemm_plan(desc)
     op = GemmOp(desc)
+
+    def launch(A, B, C, D, bias, stream, sfa=None, sfb=None):
+        # block-scaled descriptors carry their scale factors through gemm_run_args
+        if spec.block_scale != "none":
+            op.run_args(A, B, C, D, bias, sfa=sfa if sfa is not None else sfa_d,
+                        sfb=sfb if sfb is not None else sfb_d, stream=stream)
+        else:
+            op(A, B, C, D, bias, stream)
+
     stream = torch.cuda.current_stream(dev)
     flops = spec.flops()
     in_bytes = spec.algorithmic_bytes()
@@ -326,7 +341,7 @@ def run_ours(args):
             dist.barrier()
 
     for _ in range(max(3, args.warmup)):
-        op(A, B, C, D, bias, stream)
+        launch(A, B, C, D, bias, stream)
     op.check()
     torch.cuda.synchronize()
 
@@ -349,7 +364,7 @@ def run_ours(args):
         if flush is not None:
             flush.zero_()
         starts[i].record(stream)
-        op(A, B, C, D, bias, stream)
+        launch(A, B, C, D, bias, stream)
         ends[i].record(stream)
     total1.record(stream)
     torch.cuda.synchronize()
@@ -377,7 +392,7 @@ def run_ours(args):
     # the GEMM, D2H of the result, every step
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(op, spec, inputs, dev, max(1, min(args.steps, args.e2e_steps)), flops)
+        e2e = run_e2e(launch, spec, inputs, dev, max(1, min(args.steps, args.e2e_steps)), flops)
         op.check()
 
     # The bare GEMM of the same size (beta = 0, no bias, no activation) on the

@@ -38,6 +38,8 @@ OP_N, OP_T = 0, 1
 ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
 # gemm_reduce_t (flags)
 REDUCE_NONE, REDUCE_ROW_SUM, REDUCE_COL_SUM, REDUCE_ABS_MAX = 0, 1, 2, 4
+# gemm_block_scale_t
+BLOCK_SCALE_NONE, BLOCK_SCALE_MX = 0, 1
 # gemm_bias_t
 BIAS_NONE, BIAS_COL, BIAS_ROW = 0, 1, 2
 # gemm_sched_t
@@ -60,7 +62,13 @@ class GemmDesc(ctypes.Structure):
         ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
         ("scale_a", ctypes.c_float), ("scale_b", ctypes.c_float),
         ("act", ctypes.c_int32), ("bias", ctypes.c_int32), ("reduce", ctypes.c_int32),
+        ("block_scale", ctypes.c_int32),
     ]
+
+
+class GemmArgs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("A", "B", "C", "D", "bias", "sfa", "sfb", "row_sum", "col_sum",
+                                                "abs_max")]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -95,6 +103,7 @@ def _load():
         "gemm_create": (i32, [ctypes.POINTER(vp), ctypes.POINTER(GemmDesc)]),
         "gemm_run": (i32, [vp, vp, vp, vp, vp, vp, vp]),
         "gemm_run_ex": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+        "gemm_run_args": (i32, [vp, ctypes.POINTER(GemmArgs), vp]),
         "gemm_check": (i32, [vp]),
         "gemm_destroy": (i32, [vp]),
         "gemm_set_debug": (i32, [vp, i32, u32]),
@@ -118,7 +127,7 @@ def _load():
 
 
 lib = _load()
-EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_run_ex", "gemm_check", "gemm_destroy", "gemm_set_debug",
+EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_run_ex", "gemm_run_args", "gemm_check", "gemm_destroy", "gemm_set_debug",
             "gemm_set_schedule", "gemm_get_schedule", "gemm_launch_count", "gemm_status_str", "gemm_run_noalloc",
             "gemm_layout_query", "gemm_layout_eval", "gemm_layout_op", "gemm_layout_gather_f32")
 
@@ -127,7 +136,8 @@ def make_desc(M, N, K, batch=1, op_a=OP_N, op_b=OP_N, order_a=ROW_MAJOR, order_b
               order_c=ROW_MAJOR, order_d=ROW_MAJOR, lda=None, ldb=None, ldc=None, ldd=None,
               stride_a=0, stride_b=0, stride_c=0, stride_d=0, stride_bias=0,
               dtype_a=BF16, dtype_b=BF16, dtype_c=None, dtype_d=BF16, alpha=1.0, beta=0.0,
-              scale_a=1.0, scale_b=1.0, act=ACT_NONE, bias=BIAS_NONE, reduce=REDUCE_NONE):
+              scale_a=1.0, scale_b=1.0, act=ACT_NONE, bias=BIAS_NONE, reduce=REDUCE_NONE,
+              block_scale=BLOCK_SCALE_NONE):
     """Fills a GemmDesc; leading dimensions default to the tight ones and the
     batch strides of A, B, C, D to the tight matrix sizes when batch > 1."""
 
@@ -155,7 +165,7 @@ def make_desc(M, N, K, batch=1, op_a=OP_N, op_b=OP_N, order_a=ROW_MAJOR, order_b
     d.dtype_d = dtype_d
     d.dtype_c = dtype_d if dtype_c is None else dtype_c
     d.alpha, d.beta, d.scale_a, d.scale_b = alpha, beta, scale_a, scale_b
-    d.act, d.bias, d.reduce = act, bias, reduce
+    d.act, d.bias, d.reduce, d.block_scale = act, bias, reduce, block_scale
     return d
 
 
@@ -193,6 +203,15 @@ def gemm_run_ex(handle, A, B, C, D, bias, row_sum, col_sum, abs_max, stream):
     s = lib.gemm_run_ex(handle, A, B, C, D, bias, row_sum, col_sum, abs_max, stream)
     if s != OK:
         raise GemmError(s, "gemm_run_ex")
+
+
+def gemm_run_args(handle, stream, **buffers):
+    """Every buffer by name (A, B, C, D, bias, sfa, sfb, row_sum, col_sum,
+    abs_max: device addresses as integers, or None)."""
+    a = GemmArgs(**{k: v for k, v in buffers.items() if v is not None})
+    s = lib.gemm_run_args(handle, ctypes.byref(a), stream)
+    if s != OK:
+        raise GemmError(s, "gemm_run_args")
 
 
 def gemm_check(handle):

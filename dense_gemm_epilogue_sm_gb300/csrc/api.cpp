@@ -92,6 +92,9 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
         if (o != GEMM_ROW_MAJOR && o != GEMM_COL_MAJOR) return GEMM_ERR_INVALID_ARG;
     if (d.act != GEMM_ACT_NONE && d.act != GEMM_ACT_RELU && d.act != GEMM_ACT_GELU) return GEMM_ERR_INVALID_ARG;
     if (d.reduce & ~(GEMM_REDUCE_ROW_SUM | GEMM_REDUCE_COL_SUM | GEMM_REDUCE_ABS_MAX)) return GEMM_ERR_INVALID_ARG;
+    if (d.block_scale != GEMM_BLOCK_SCALE_NONE && d.block_scale != GEMM_BLOCK_SCALE_MX) return GEMM_ERR_INVALID_ARG;
+    if (d.block_scale == GEMM_BLOCK_SCALE_MX && (d.dtype_a != GEMM_E4M3 || d.dtype_b != GEMM_E4M3))
+        return GEMM_ERR_UNSUPPORTED;
     if (d.bias != GEMM_BIAS_NONE && d.bias != GEMM_BIAS_COL && d.bias != GEMM_BIAS_ROW) return GEMM_ERR_INVALID_ARG;
     for (int t : {d.dtype_a, d.dtype_b, d.dtype_d})
         if (!dtype_bytes(t)) return GEMM_ERR_INVALID_ARG;
@@ -177,6 +180,11 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     int cg = (P.Mk > 128 && P.Nk > 128 && tiles2 >= 64) ? 2 : 1;
     int tile_n = 256;
     if (cg == 1 && (P.Nk <= 128 || ((P.Mk + kTileM - 1) / kTileM) * ((P.Nk + 255) / 256) * L < 76)) tile_n = 128;
+    const int bs = d.block_scale != GEMM_BLOCK_SCALE_NONE;
+    if (bs) {     // the block-scaled kernel: one CTA, 128 x 128 tiles
+        cg = 1;
+        tile_n = 128;
+    }
     const int tile_m = kTileM * cg;
     P.cta_group = cg;
     P.tile_n = tile_n;
@@ -187,7 +195,7 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     P.info.tile_n = tile_n;
     P.info.tile_k = kStageKBytes / ab;
     P.info.cta_group = cg;
-    P.info.stages = stages_for(cg, tile_n);
+    P.info.stages = stages_for(cg, tile_n, bs);
     P.info.epi_cols = 128 / ob;
     P.info.tiles_m = tiles_m;
     P.info.tiles_n = tiles_n;
@@ -232,6 +240,9 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     }
     k.a_kmajor = a_kmaj;
     k.b_kmajor = b_kmaj;
+    k.block_scaled = bs;
+    k.sf_mblocks = (int32_t)((P.Mk + 127) / 128);
+    k.sf_nblocks = (int32_t)((P.Nk + 127) / 128);
     k.elem_bytes = ab;
     k.kind_f8 = d.dtype_a == GEMM_E4M3;
     k.mma_variant = (d.dtype_a == GEMM_E4M3 ? 8 : 0) + (d.dtype_a == GEMM_BF16 ? 4 : 0) + (a_kmaj ? 0 : 2) +
@@ -480,7 +491,7 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
         delete h;
         return GEMM_ERR_NO_DEVICE;
     }
-    if (prepare_kernel(h->plan.cta_group, h->plan.tile_n, h->plan.out_bytes) != cudaSuccess ||
+    if (prepare_kernel(h->plan.cta_group, h->plan.tile_n, h->plan.out_bytes, h->plan.kp.block_scaled) != cudaSuccess ||
         cudaMalloc(&h->status, sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) {
         cudaGetLastError();
@@ -489,7 +500,8 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
         return GEMM_ERR_CUDA;
     }
     h->plan.kp.status = h->status;
-    h->max_clusters = max_active_clusters(h->plan.cta_group, h->plan.tile_n, h->plan.out_bytes);
+    h->max_clusters =
+        max_active_clusters(h->plan.cta_group, h->plan.tile_n, h->plan.out_bytes, h->plan.kp.block_scaled);
     s = apply_schedule(h, GEMM_SCHED_AUTO);
     if (s == GEMM_OK) s = alloc_reductions(h);
     if (s != GEMM_OK) {
@@ -503,10 +515,15 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
 }
 
 static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
-                              const float* bias, float* row_sum, float* col_sum, float* abs_max, void* stream) {
+                              const float* bias, float* row_sum, float* col_sum, float* abs_max, const void* sfa,
+                              const void* sfb, void* stream) {
     if (!h) return GEMM_ERR_INVALID_ARG;
     Plan& P = h->plan;
     const gemm_desc_t& d = P.d;
+    if (P.kp.block_scaled && d.K > 0) {
+        if (!sfa || !sfb) return GEMM_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(sfa) | reinterpret_cast<uintptr_t>(sfb)) & 15u) return GEMM_ERR_MISALIGNED;
+    }
     if (((d.reduce & GEMM_REDUCE_ROW_SUM) && !row_sum) || ((d.reduce & GEMM_REDUCE_COL_SUM) && !col_sum) ||
         ((d.reduce & GEMM_REDUCE_ABS_MAX) && !abs_max))
         return GEMM_ERR_INVALID_ARG;
@@ -561,9 +578,13 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
     la.p = P.kp;
     la.p.bias = bias;
     la.p.d_ptr = D;
+    // kernel orientation: with D computed transposed, A's factors go with the kernel's B
+    la.p.sfa = static_cast<const uint8_t*>(swap ? sfb : sfa);
+    la.p.sfb = static_cast<const uint8_t*>(swap ? sfa : sfb);
     la.cta_group = P.cta_group;
     la.tile_n = P.tile_n;
     la.out_bytes = P.out_bytes;
+    la.block_scaled = P.kp.block_scaled;
     la.grid = grid_for(P, h->sm_count, h->max_clusters);
     la.stream = static_cast<cudaStream_t>(stream);
     if (la.grid < 1) return GEMM_OK;
@@ -605,12 +626,17 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
 
 gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D, const float* bias,
                        void* stream) {
-    return run_impl(h, A, B, C, D, bias, nullptr, nullptr, nullptr, stream);
+    return run_impl(h, A, B, C, D, bias, nullptr, nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 gemm_status_t gemm_run_ex(gemm_handle_t h, const void* A, const void* B, const void* C, void* D, const float* bias,
                           float* row_sum, float* col_sum, float* abs_max, void* stream) {
-    return run_impl(h, A, B, C, D, bias, row_sum, col_sum, abs_max, stream);
+    return run_impl(h, A, B, C, D, bias, row_sum, col_sum, abs_max, nullptr, nullptr, stream);
+}
+
+gemm_status_t gemm_run_args(gemm_handle_t h, const gemm_args_t* a, void* stream) {
+    if (!a) return GEMM_ERR_INVALID_ARG;
+    return run_impl(h, a->A, a->B, a->C, a->D, a->bias, a->row_sum, a->col_sum, a->abs_max, a->sfa, a->sfb, stream);
 }
 
 gemm_status_t gemm_check(gemm_handle_t h) {
@@ -699,6 +725,7 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
     const gemm_status_t s = validate_and_plan(desc, &P);
     if (s != GEMM_OK) return s;
     if (P.d.reduce) return GEMM_ERR_UNSUPPORTED;     // reductions need a handle's workspace
+    if (P.kp.block_scaled) return GEMM_ERR_UNSUPPORTED;   // no scale-factor arguments here
     const gemm_desc_t& d = P.d;
     if (d.M == 0 || d.N == 0) return GEMM_OK;
     if (!D || (d.K > 0 && (!A || !B)) || (P.has_c && !C) || (d.bias != GEMM_BIAS_NONE && !bias))
@@ -727,7 +754,7 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
         la.tmC = la.tmD;
     }
     if (!ok) return GEMM_ERR_CUDA;
-    if (prepare_kernel(P.cta_group, P.tile_n, P.out_bytes) != cudaSuccess) {
+    if (prepare_kernel(P.cta_group, P.tile_n, P.out_bytes, P.kp.block_scaled) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -738,7 +765,8 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
     la.cta_group = P.cta_group;
     la.tile_n = P.tile_n;
     la.out_bytes = P.out_bytes;
-    la.grid = grid_for(P, sm_count, max_active_clusters(P.cta_group, P.tile_n, P.out_bytes));
+    la.block_scaled = P.kp.block_scaled;
+    la.grid = grid_for(P, sm_count, max_active_clusters(P.cta_group, P.tile_n, P.out_bytes, P.kp.block_scaled));
     la.stream = stream;
     if (la.grid < 1) return GEMM_OK;
     if (launch(la) != cudaSuccess) {

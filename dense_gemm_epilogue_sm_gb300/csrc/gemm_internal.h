@@ -72,6 +72,13 @@ struct KernelParams {
     // other workers' fp32 partial sums before the epilogue.  Without a split,
     // dp_tiles = num_tiles and sk_iters = 0.
     int32_t clc;                  // 1: dynamic schedule (cluster launch control), grid = every tile
+    // Block scaling (block_scaled = 1): one ue8m0 factor per 32 K elements;
+    // the factors of 128 rows x one K stage (4 factors each) form one
+    // 512-byte block; a batch's tensor holds blocks (row/128) * num_kb + kb.
+    int32_t block_scaled;
+    int32_t sf_mblocks, sf_nblocks;    // 128-row blocks of the kernel's A and B
+    const uint8_t* sfa;
+    const uint8_t* sfb;
     int32_t dp_tiles;
     int64_t sk_iters;
     int32_t sk_ranges;            // ranges the iterations are cut into (<= workers); range r
@@ -96,6 +103,7 @@ struct LaunchArgs {
     int cta_group;                // 1 or 2 (CTA pair, cluster of 2)
     int tile_n;                   // 128 or 256
     int out_bytes;                // 2 or 4
+    int block_scaled;             // 1: the block-scaled (MX) kernel
     int grid;                     // CTAs (a multiple of cta_group)
     cudaStream_t stream;
 };
@@ -113,10 +121,10 @@ struct FinishParams {
 };
 cudaError_t launch_finish(const FinishParams& f, cudaStream_t stream);
 
-int stages_for(int cta_group, int tile_n);
-size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes);
-cudaError_t prepare_kernel(int cta_group, int tile_n, int out_bytes);
-int max_active_clusters(int cta_group, int tile_n, int out_bytes);   // 0 if unknown
+int stages_for(int cta_group, int tile_n, int block_scaled);
+size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes, int block_scaled);
+cudaError_t prepare_kernel(int cta_group, int tile_n, int out_bytes, int block_scaled);
+int max_active_clusters(int cta_group, int tile_n, int out_bytes, int block_scaled);   // 0 if unknown
 cudaError_t launch(const LaunchArgs& a);
 
 }  // namespace gemm_sm103

@@ -39,7 +39,9 @@
 
 namespace gemm_sm103 {
 
-int stages_for(int cta_group, int tile_n) { return (cta_group == 1 && tile_n == 256) ? 4 : 6; }
+int stages_for(int cta_group, int tile_n, int block_scaled) {
+    return block_scaled ? 5 : ((cta_group == 1 && tile_n == 256) ? 4 : 6);
+}
 
 // TMEM accumulators per CTA: two, so the epilogue of one tile overlaps the
 // main loop of the next (512 columns for BN = 256).
@@ -49,17 +51,25 @@ constexpr int kPairAccBufs = 2;
 // that have not read them yet.
 constexpr int kClcSlots = 4;
 
-template <int CG, int BN, int OB>
+// BS: block-scaled operands (e4m3 with one ue8m0 scale factor per 32 K
+// elements).  Each stage then also holds the 512-byte scale-factor blocks of
+// its A rows and B rows, which the MMA thread copies into TMEM columns after
+// the accumulators (8 columns per stage).
+template <int CG, int BN, int OB, bool BS = false>
 struct Cfg {
     static constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
     static constexpr int kBRows = BN / CG;                          // rows of B this CTA loads
-    static constexpr int kStages = (CG == 1 && BN == 256) ? 4 : 6;
+    static constexpr int kStages = BS ? 5 : ((CG == 1 && BN == 256) ? 4 : 6);
     static constexpr int kABytes = kTileM * kStageKBytes;           // 16 KiB
     static constexpr int kBBytes = kBRows * kStageKBytes;
-    static constexpr int kStageBytes = kABytes + kBBytes;           // this CTA's share of a stage
+    static constexpr int kSfBytes = BS ? 2 * 512 : 0;               // scale-factor blocks of A and B
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;   // this CTA's share of a stage
     static constexpr int kEpiCols = 128 / OB;                       // 64 (16-bit D) or 32 (fp32 D)
     static constexpr int kSubtiles = BN / kEpiCols;
-    static constexpr int kTmemCols = kAccBufs * BN;
+    static constexpr int kSfCol0 = kAccBufs * BN;                   // first TMEM column of the scale factors
+    static constexpr int kTmemCols = BS ? 512 : kAccBufs * BN;
+    static_assert(!BS || kSfCol0 + 8 * kStages <= 512, "TMEM");
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
     // Stages are released to the producer in groups: every tcgen05.commit
@@ -72,7 +82,8 @@ struct Cfg {
         1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kClcSlots * 16 + kNumBars * 8 + 16;
 };
 
-size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes) {
+size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes, int block_scaled) {
+    if (block_scaled) return out_bytes == 2 ? Cfg<1, 128, 2, true>::kSmemBytes : Cfg<1, 128, 4, true>::kSmemBytes;
     if (cta_group == 2) return out_bytes == 2 ? Cfg<2, 256, 2>::kSmemBytes : Cfg<2, 256, 4>::kSmemBytes;
     if (tile_n == 256) return out_bytes == 2 ? Cfg<1, 256, 2>::kSmemBytes : Cfg<1, 256, 4>::kSmemBytes;
     return out_bytes == 2 ? Cfg<1, 128, 2>::kSmemBytes : Cfg<1, 128, 4>::kSmemBytes;
@@ -404,6 +415,26 @@ __host__ __device__ constexpr uint32_t idesc_for(int cg, int bn, bool f8, uint32
            ((uint32_t)(bn >> 3) << 17) | ((uint32_t)((128 * cg) >> 4) << 24);
 }
 
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: scale-factor
+// byte of B (bits 4-5), A and B e4m3 (type 0, bits 7-9, 10-12), A / B
+// MN-major (15, 16), N >> 3 (17-22), ue8m0 scale factors (bit 23), M >> 4
+// (24-28), scale-factor byte of A (29-30).  The bytes select which of the
+// four factors in a TMEM word (four 32-element K blocks) an MMA uses.
+__host__ __device__ constexpr uint32_t idesc_mx(int cg, int bn, uint32_t a_mn, uint32_t b_mn, uint32_t sf_byte) {
+    return (sf_byte << 4) | (a_mn << 15) | (b_mn << 16) | ((uint32_t)(bn >> 3) << 17) | (1u << 23) |
+           ((uint32_t)((128 * cg) >> 4) << 24) | (sf_byte << 29);
+}
+
+// Shared-memory descriptor of a 512-byte scale-factor block read as 32 rows
+// of 16 bytes, no swizzle: 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t sf_desc(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // What the MMA issuer needs from the kernel.
 template <int CG, int BN, int S>
 struct MmaCtx {
@@ -430,7 +461,13 @@ struct MmaCtx {
 // and mbarrier wrappers clobber "memory", so a value read through `m` or `p`
 // (local and kernel-parameter memory behind a reference) would be re-loaded
 // after every MMA, a chain of dependent loads between two MMAs.
-template <int CG, int BN, int S, int G, bool F8, uint32_t IDESC>
+//
+// BS: block-scaled MMAs.  Each stage's two scale-factor blocks are copied
+// into TMEM (8 columns per stage after the accumulators) ahead of the
+// stage's four MMAs; tcgen05.cp and tcgen05.mma of one thread run in issue
+// order, so a copy never overtakes the MMAs that still read the columns it
+// overwrites one lap later.  MMA j reads factor byte j of each word.
+template <int CG, int BN, int S, int G, bool F8, uint32_t IDESC, bool BS = false>
 __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     const KernelParams& p = m.p;                 // slow paths (wait_bar) only
     const int first_tile = m.first_tile, tile_step = m.tile_step;
@@ -485,10 +522,23 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
             const uint64_t soff = (uint64_t)((stage * stage_bytes) >> 4);
             const uint64_t ad = a_base + soff, bd = b_base + soff;
             const uint32_t first = kb != kb0;
+            if constexpr (BS) {
+                constexpr uint32_t kSfCol0 = (uint32_t)(kAccBufs * BN);
+                const uint32_t sfs = ring + (uint32_t)stage * stage_bytes + stage_bytes - 1024u;
+                const uint32_t sfa = tmem_base + kSfCol0 + 8u * (uint32_t)stage, sfb = sfa + 4u;
+                ptx::tmem_cp_32x128b_x4<CG>(sfa, sf_desc(sfs));
+                ptx::tmem_cp_32x128b_x4<CG>(sfb, sf_desc(sfs + 512u));
+                ptx::mma_mx<CG, IDESC>(d_tmem, ad, bd, sfa, sfb, first);
+                ready = ptx::mbar_test_wait(full_bar(next), next_phase);
+                ptx::mma_mx<CG, IDESC | (1u << 4) | (1u << 29)>(d_tmem, ad + a_step, bd + b_step, sfa, sfb, 1u);
+                ptx::mma_mx<CG, IDESC | (2u << 4) | (2u << 29)>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, sfa, sfb, 1u);
+                ptx::mma_mx<CG, IDESC | (3u << 4) | (3u << 29)>(d_tmem, ad + 3 * a_step, bd + 3 * b_step, sfa, sfb, 1u);
+            } else {
 #pragma unroll
-            for (int j = 0; j < kStageKBytes / kKStepBytes; ++j) {
-                ptx::mma_imm<CG, F8, IDESC>(d_tmem, ad + j * a_step, bd + j * b_step, j ? 1u : first);
-                if (j == 0) ready = ptx::mbar_test_wait(full_bar(next), next_phase);
+                for (int j = 0; j < kStageKBytes / kKStepBytes; ++j) {
+                    ptx::mma_imm<CG, F8, IDESC>(d_tmem, ad + j * a_step, bd + j * b_step, j ? 1u : first);
+                    if (j == 0) ready = ptx::mbar_test_wait(full_bar(next), next_phase);
+                }
             }
             issued = true;
             if (stage % G == G - 1) release(stage / G);   // the group's last stage
@@ -519,12 +569,12 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     }
 }
 
-template <int CG, int BN, int OB>
+template <int CG, int BN, int OB, bool BS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                 const __grid_constant__ KernelParams p) {
-    using C = Cfg<CG, BN, OB>;
+    using C = Cfg<CG, BN, OB, BS>;
     constexpr int S = C::kStages;
     constexpr int kTileRows = kTileM * CG;               // output rows per tile
     extern __shared__ uint8_t smem_raw[];
@@ -649,6 +699,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < C::kBRows / mn_box; ++c)
                                 load(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb);
                         }
+                        if constexpr (BS) {
+                            // one 512-byte scale-factor block per 128 rows and K stage:
+                            // block (rows / 128) * num_kb + kb of the batch's tensor
+                            const uint32_t sf = sb + C::kBBytes;
+                            ptx::bulk_g2s(sf, p.sfa + (((int64_t)la * p.sf_mblocks + m0 / 128) * p.num_kb + kb) * 512,
+                                          512, fb);
+                            ptx::bulk_g2s(sf + 512, p.sfb + (((int64_t)lb * p.sf_nblocks + n0 / 128) * p.num_kb + kb) * 512,
+                                          512, fb);
+                        }
                         const uint32_t bit = 1u << pend_slot(stage);
                         pend |= bit;
                         pend_parity = phase ? (pend_parity | bit) : (pend_parity & ~bit);
@@ -681,17 +740,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             MmaCtx<CG, BN, S> m{p,          ptx::smem_addr(ring), C::kABytes, C::kStageBytes, bar0,
                                 tmem_base,  first_tile,           tile_step,   abort_flag,       peer_abort,
                                 resp0,      clc_full0,            clc_empty0};
-            switch (p.mma_variant) {     // one loop per tcgen05 instruction descriptor
+            if constexpr (BS) {
+                switch (p.mma_variant & 3) {     // A / B MN-major
+#define GEMM_MX_CASE(v)                                                                      \
+    case v:                                                                                  \
+        mma_role<CG, BN, S, C::kGroup, true, idesc_mx(CG, BN, ((v) >> 1) & 1, (v) & 1, 0), true>(m); \
+        break;
+                    GEMM_MX_CASE(0) GEMM_MX_CASE(1) GEMM_MX_CASE(2) GEMM_MX_CASE(3)
+#undef GEMM_MX_CASE
+                    default: break;
+                }
+            } else {
+                switch (p.mma_variant) {     // one loop per tcgen05 instruction descriptor
 #define GEMM_MMA_CASE(v)                                                         \
     case v:                                                                      \
         mma_role<CG, BN, S, C::kGroup, (v) >= 8, idesc_for(CG, BN, (v) >= 8, ((v) >> 2) & 1, \
                                                ((v) >> 1) & 1, (v) & 1)>(m);     \
         break;
-                GEMM_MMA_CASE(0) GEMM_MMA_CASE(1) GEMM_MMA_CASE(2) GEMM_MMA_CASE(3)
-                GEMM_MMA_CASE(4) GEMM_MMA_CASE(5) GEMM_MMA_CASE(6) GEMM_MMA_CASE(7)
-                GEMM_MMA_CASE(8) GEMM_MMA_CASE(9) GEMM_MMA_CASE(10) GEMM_MMA_CASE(11)
+                    GEMM_MMA_CASE(0) GEMM_MMA_CASE(1) GEMM_MMA_CASE(2) GEMM_MMA_CASE(3)
+                    GEMM_MMA_CASE(4) GEMM_MMA_CASE(5) GEMM_MMA_CASE(6) GEMM_MMA_CASE(7)
+                    GEMM_MMA_CASE(8) GEMM_MMA_CASE(9) GEMM_MMA_CASE(10) GEMM_MMA_CASE(11)
 #undef GEMM_MMA_CASE
-                default: break;
+                    default: break;
+                }
             }
         }
     } else {
@@ -970,24 +1041,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int CG, int BN, int OB>
+template <int CG, int BN, int OB, bool BS = false>
 static cudaError_t set_attrs() {
-    return cudaFuncSetAttribute(gemm_kernel<CG, BN, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg<CG, BN, OB>::kSmemBytes);
+    return cudaFuncSetAttribute(gemm_kernel<CG, BN, OB, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<CG, BN, OB, BS>::kSmemBytes);
 }
 
-cudaError_t prepare_kernel(int cta_group, int tile_n, int out_bytes) {
+cudaError_t prepare_kernel(int cta_group, int tile_n, int out_bytes, int block_scaled) {
+    if (block_scaled) return out_bytes == 2 ? set_attrs<1, 128, 2, true>() : set_attrs<1, 128, 4, true>();
     if (cta_group == 2) return out_bytes == 2 ? set_attrs<2, 256, 2>() : set_attrs<2, 256, 4>();
     if (tile_n == 256) return out_bytes == 2 ? set_attrs<1, 256, 2>() : set_attrs<1, 256, 4>();
     return out_bytes == 2 ? set_attrs<1, 128, 2>() : set_attrs<1, 128, 4>();
 }
 
-template <int CG, int BN, int OB>
+template <int CG, int BN, int OB, bool BS = false>
 static cudaLaunchConfig_t make_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<CG, BN, OB>::kSmemBytes;
+    cfg.dynamicSmemBytes = Cfg<CG, BN, OB, BS>::kSmemBytes;
     cfg.stream = stream;
     attr->id = cudaLaunchAttributeClusterDimension;
     attr->val.clusterDim.x = CG;
@@ -998,32 +1070,34 @@ static cudaLaunchConfig_t make_config(int grid, cudaStream_t stream, cudaLaunchA
     return cfg;
 }
 
-template <int CG, int BN, int OB>
+template <int CG, int BN, int OB, bool BS = false>
 static cudaError_t launch_t(const LaunchArgs& a) {
     cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = make_config<CG, BN, OB>(a.grid, a.stream, &attr);
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<CG, BN, OB>, a.tmA, a.tmB, a.tmC, a.tmD, a.p);
+    cudaLaunchConfig_t cfg = make_config<CG, BN, OB, BS>(a.grid, a.stream, &attr);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<CG, BN, OB, BS>, a.tmA, a.tmB, a.tmC, a.tmD, a.p);
 }
 
-template <int CG, int BN, int OB>
+template <int CG, int BN, int OB, bool BS = false>
 static int max_clusters_t() {
     cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = make_config<CG, BN, OB>(CG * 64, nullptr, &attr);
+    cudaLaunchConfig_t cfg = make_config<CG, BN, OB, BS>(CG * 64, nullptr, &attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<CG, BN, OB>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<CG, BN, OB, BS>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-int max_active_clusters(int cta_group, int tile_n, int out_bytes) {
+int max_active_clusters(int cta_group, int tile_n, int out_bytes, int block_scaled) {
+    if (block_scaled) return out_bytes == 2 ? max_clusters_t<1, 128, 2, true>() : max_clusters_t<1, 128, 4, true>();
     if (cta_group == 2) return out_bytes == 2 ? max_clusters_t<2, 256, 2>() : max_clusters_t<2, 256, 4>();
     if (tile_n == 256) return out_bytes == 2 ? max_clusters_t<1, 256, 2>() : max_clusters_t<1, 256, 4>();
     return out_bytes == 2 ? max_clusters_t<1, 128, 2>() : max_clusters_t<1, 128, 4>();
 }
 
 cudaError_t launch(const LaunchArgs& a) {
+    if (a.block_scaled) return a.out_bytes == 2 ? launch_t<1, 128, 2, true>(a) : launch_t<1, 128, 4, true>(a);
     if (a.cta_group == 2) return a.out_bytes == 2 ? launch_t<2, 256, 2>(a) : launch_t<2, 256, 4>(a);
     if (a.tile_n == 256) return a.out_bytes == 2 ? launch_t<1, 256, 2>(a) : launch_t<1, 256, 4>(a);
     return a.out_bytes == 2 ? launch_t<1, 128, 2>(a) : launch_t<1, 128, 4>(a);

@@ -146,6 +146,15 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int3
                  : "memory");
 }
 
+// 1-D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global memory into this CTA's shared memory, completing its
+// bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N committed bulk groups are still reading shared memory.
@@ -271,6 +280,38 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
             "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
+// Copies a 32-row x 128-bit block of shared memory (matrix descriptor
+// `sdesc`) into TMEM at `taddr`: row r's four 32-bit words go to columns
+// 0..3 of lane r of every 32-lane quadrant (.warpx4).
+template <int CG>
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Block-scaled MMA, kind::mxf8f6f4 with one scale factor per 32 K elements:
+// D[tmem] (+)= (A[smem] x SFA[tmem]) * (B[smem] x SFB[tmem])^T.
+template <int CG, uint32_t IDESC>
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t accumulate) {
+    if constexpr (CG == 1)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %6, [%3], [%4], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(sfa), "r"(sfb), "r"(accumulate), "n"(IDESC)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %6, [%3], [%4], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(sfa), "r"(sfb), "r"(accumulate), "n"(IDESC)
             : "memory");
 }
 

@@ -5,9 +5,9 @@ current CUDA stream.  Argument marshalling only; the GEMM runs in
 import torch
 
 from . import (ACT_GELU, ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E4M3, F16, F32, OP_N,
-               OP_T, REDUCE_ABS_MAX, REDUCE_COL_SUM, REDUCE_ROW_SUM, ROW_MAJOR, gemm_check, gemm_create,
-               gemm_destroy, gemm_get_schedule, gemm_launch_count, gemm_run, gemm_run_ex, gemm_set_schedule,
-               make_desc)
+               OP_T, REDUCE_ABS_MAX, REDUCE_COL_SUM, REDUCE_ROW_SUM, ROW_MAJOR, BLOCK_SCALE_MX, BLOCK_SCALE_NONE,
+               gemm_check, gemm_create, gemm_destroy, gemm_get_schedule, gemm_launch_count, gemm_run, gemm_run_args,
+               gemm_run_ex, gemm_set_schedule, make_desc)
 
 DTYPE_CODE = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3}
 ORDER_CODE = {"row": ROW_MAJOR, "col": COL_MAJOR}
@@ -38,7 +38,8 @@ def desc_from_spec(spec, scale_a=1.0, scale_b=1.0):
         stride("a"), stride("b"), stride("c"), stride("d"), bias_len if L > 1 else 0,
         DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_d], DTYPE_CODE[spec.dtype_d],
         spec.alpha, spec.beta, scale_a, scale_b, ACT_CODE[spec.act], BIAS_CODE[spec.bias],
-        reduce_code(getattr(spec, "reduce", "none")))
+        reduce_code(getattr(spec, "reduce", "none")),
+        BLOCK_SCALE_MX if getattr(spec, "block_scale", "none") == "mx" else BLOCK_SCALE_NONE)
 
 
 def _ptr(t):
@@ -61,6 +62,14 @@ class GemmOp:
         s = stream if stream is not None else torch.cuda.current_stream()
         gemm_run_ex(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(bias), _ptr(row_sum), _ptr(col_sum),
                     _ptr(abs_max), s.cuda_stream)
+
+    def run_args(self, A, B, C=None, D=None, bias=None, sfa=None, sfb=None, row_sum=None, col_sum=None,
+                 abs_max=None, stream=None):
+        """Every buffer by name (device tensors); the call for block-scaled descriptors."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        gemm_run_args(self.handle, s.cuda_stream, A=_ptr(A), B=_ptr(B), C=_ptr(C), D=_ptr(D), bias=_ptr(bias),
+                      sfa=_ptr(sfa), sfb=_ptr(sfb), row_sum=_ptr(row_sum), col_sum=_ptr(col_sum),
+                      abs_max=_ptr(abs_max))
 
     def check(self):
         gemm_check(self.handle)

@@ -51,6 +51,7 @@ class Spec:
     ldc: int = 0
     ldd: int = 0
     reduce: str = "none"        # none, or a '+'-joined subset of row, col, amax
+    block_scale: str = "none"   # none | mx (e4m3 data, ue8m0 scale per 32 elements of K)
     notes: str = ""
 
     # ----------------------------------------------------------- geometry --
@@ -93,6 +94,8 @@ class Spec:
             b += self.batch * self.M * self.N * e_d
         if self.bias != "none":
             b += 4 * (self.N if self.bias == "col" else self.M)
+        if self.block_scale != "none":      # one byte per 32 elements of K, per row of A and of B
+            b += self.batch * (self.M + self.N) * ((self.K + 31) // 32)
         return b
 
 
@@ -111,6 +114,9 @@ WORKLOADS = {
     "fp8_e4m3_8192": Spec(
         "fp8_e4m3_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e4m3",
         dist="uniform1", seed=3, notes="per-tensor scales folded into alpha"),
+    "mxfp8_8192": Spec(
+        "mxfp8_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e4m3", block_scale="mx", seed=7,
+        notes="mx_float8: e4m3 data, one ue8m0 scale factor per 32 elements of K"),
     "odd_1000_at": Spec(
         "odd_1000_at", 1000, 1000, 1000, op_a="T", order_a="col", order_b="col", seed=4,
         notes="A transposed: stored K x M column-major, lda = K"),
@@ -163,10 +169,96 @@ class Inputs:
         return 0 if s.bias == "none" else (s.N if s.bias == "col" else s.M)
 
 
+def _sf_offsets(L, rows, sfk):
+    """Byte offsets (L, rows, sfk) of the scale factors in the 512-byte
+    basic-block layout: 128 rows x 4 factors per block, row r's four factors
+    at (r % 32) * 16 + ((r % 128) // 32) * 4, blocks K-major, one tensor per
+    batch.  Returns (offsets, tensor bytes per batch)."""
+    kb, mb = (sfk + 3) // 4, (rows + 127) // 128
+    r = torch.arange(rows).view(1, rows, 1)
+    f = torch.arange(sfk).view(1, 1, sfk)
+    l = torch.arange(L).view(L, 1, 1)
+    off = ((r // 128) * kb + f // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + f % 4
+    return off + l * (mb * kb * 512), mb * kb * 512
+
+
+def _mx_quantise(x):
+    """(L, R, K) fp32 -> (e4m3 values, ue8m0 codes (L, R, ceil(K/32))): per
+    32-element block of K the shared exponent floor(log2 amax) - 8 (8 =
+    exponent of e4m3's largest power of two), elements divided by it and
+    rounded to e4m3, clamped to +-448."""
+    L, R, K = x.shape
+    sfk = (K + 31) // 32
+    xp = torch.zeros(L, R, sfk * 32)
+    xp[:, :, :K] = x
+    blk = xp.view(L, R, sfk, 32)
+    amax = blk.abs().amax(dim=3)
+    e = torch.where(amax > 0, torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - 8,
+                    torch.full_like(amax, -127.0))
+    code = (e + 127).clamp(0, 254)
+    scaled = (blk / torch.exp2(code - 127).unsqueeze(3)).clamp(-448.0, 448.0)
+    q = scaled.to(torch.float8_e4m3fn).view(L, R, sfk * 32)[:, :, :K]
+    return q, code.to(torch.uint8)
+
+
+def _to_storage(spec, which, logical):
+    """Logical (L, R, K) operand (A: R = M; B: R = N, i.e. op(B) transposed)
+    into the spec's flat storage, padding elements zero."""
+    L = spec.batch
+    op = spec.op_a if which == "a" else spec.op_b
+    order = spec.order(which)
+    ld = spec.ld(which)
+    per = spec.matrix_elems(which)
+    out = torch.zeros(L * per, dtype=logical.dtype)
+    R, K = logical.shape[1], logical.shape[2]
+    r = torch.arange(R).view(R, 1)
+    k = torch.arange(K).view(1, K)
+    # stored matrix: A op N is (M, K), op T is (K, M); B op N is (K, N), op T is (N, K)
+    rows_first = (op == "N") if which == "a" else (op == "T")
+    sr, sc = (r, k) if rows_first else (k, r)
+    idx = sr * ld + sc if order == "row" else sr + sc * ld
+    for l in range(L):
+        out[l * per + idx.reshape(-1)] = logical[l].reshape(-1)
+    return out
+
+
+def _make_mx_inputs(spec, gen):
+    L = spec.batch
+    ops = {}
+    for which, R in (("a", spec.M), ("b", spec.N)):
+        sfk = (spec.K + 31) // 32
+        if spec.dist == "int4":
+            # integers in [-4, 4] with factors 2^-1 .. 2^1: every sum exact in fp32
+            q = torch.randint(-4, 5, (L, R, spec.K), generator=gen).to(torch.float32).to(torch.float8_e4m3fn)
+            code = torch.randint(126, 129, (L, R, sfk), generator=gen).to(torch.uint8)
+        else:
+            x = torch.randn(L, R, spec.K, generator=gen, dtype=torch.float32)
+            # a power of two per 32-element block spreads the scale factors
+            shift = torch.randint(-4, 5, (L, R, sfk), generator=gen).to(torch.float32)
+            x = x * torch.exp2(shift.repeat_interleave(32, dim=2)[:, :, :spec.K])
+            q, code = _mx_quantise(x)
+        off, per = _sf_offsets(L, R, sfk)
+        sf = torch.full((L * per,), 127, dtype=torch.uint8)       # padding factors: 1.0
+        sf[off.reshape(-1)] = code.reshape(-1)
+        ops[which] = (_to_storage(spec, which, q), sf)
+    return ops
+
+
 def make_inputs(spec: Spec) -> Inputs:
     """Builds the storage buffers of one workload (CPU tensors).  Padding
     elements beyond each leading extent are drawn too (they are never read)."""
     gen = torch.Generator(device="cpu").manual_seed(spec.seed)
+    if spec.block_scale == "mx":
+        ops = _make_mx_inputs(spec, gen)
+        C = None
+        if spec.beta != 0:
+            C = _draw(gen, spec.batch * spec.matrix_elems("c"), "normal").to(DT[spec.dtype_d])
+        bias = None
+        if spec.bias != "none":
+            n = spec.N if spec.bias == "col" else spec.M
+            bias = torch.randn(spec.batch * n, generator=gen, dtype=torch.float32) * spec.bias_sigma
+        return Inputs(spec, ops["a"][0], ops["b"][0], C, bias, 1.0, 1.0,
+                      extras={"sfa": ops["a"][1], "sfb": ops["b"][1]})
     L = spec.batch
     out = {}
     scales = {}

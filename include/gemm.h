@@ -89,6 +89,21 @@ typedef enum {
     GEMM_REDUCE_ABS_MAX = 4       /* abs_max[l] = max over m, n of |t(l, m, n)| (NaN if any t is NaN) */
 } gemm_reduce_t;
 typedef enum { GEMM_BIAS_NONE = 0, GEMM_BIAS_COL = 1, GEMM_BIAS_ROW = 2 } gemm_bias_t;
+/* Block-scaled operands ("Technical Documentation: NVIDIA/cutlass", "Block
+ * Scaled GEMMs"): D = act(alpha * sum_k (A(m,k) SFA(m,k/32)) (B(k,n) SFB(n,k/32))
+ * + beta*C + bias).  GEMM_BLOCK_SCALE_MX: A and B e4m3 (mx_float8), scale
+ * factors ue8m0 (value 2^(code-127), code 255 = NaN), one per 32 elements of
+ * K.  Scale factors are passed to gemm_run_args as byte tensors in the
+ * pages' 512-byte basic-block layout ("Scale Factor Layouts"): for a matrix
+ * of R rows (M for A, N for B; rows of op(A) / columns of op(B)) and
+ * SFK = ceil(K/32) factors per row, factor (r, f) of batch l is at byte
+ *   l*ceil(R/128)*ceil(SFK/4)*512 + ((r/128)*ceil(SFK/4) + f/4)*512
+ *   + (r%32)*16 + ((r%128)/32)*4 + f%4
+ * Bytes of the padded tensor that name no real (r, f) are read by the
+ * kernel and must not be 255 (NaN).  A batch whose A (B) is shared
+ * (stride 0) shares SFA (SFB) too. */
+typedef enum { GEMM_BLOCK_SCALE_NONE = 0, GEMM_BLOCK_SCALE_MX = 1 } gemm_block_scale_t;
+
 typedef enum {
     GEMM_SCHED_AUTO = 0,
     GEMM_SCHED_DATA_PARALLEL = 1,
@@ -110,6 +125,7 @@ typedef struct {
     int32_t act;                                   /* gemm_act_t */
     int32_t bias;                                  /* gemm_bias_t; bias is fp32 */
     int32_t reduce;                                /* gemm_reduce_t flags; 0 = none */
+    int32_t block_scale;                           /* gemm_block_scale_t; 0 = none */
 } gemm_desc_t;
 
 /* How a descriptor is executed; filled by gemm_plan (host only, no GPU). */
@@ -255,9 +271,31 @@ GEMM_API uint64_t gemm_launch_count(gemm_handle_t h);
  * in-kernel timeout is not reported.  wait = 1: the call synchronises
  * `stream` and returns GEMM_ERR_TIMEOUT if a bounded wait ran out.
  * Pointers, alignment and errors are as for gemm_run; a descriptor with
- * reductions (which need a handle's workspace) returns GEMM_ERR_UNSUPPORTED. */
+ * reductions (which need a handle's workspace) or block scaling (no
+ * scale-factor arguments here) returns GEMM_ERR_UNSUPPORTED. */
 GEMM_API gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const void* B, const void* C,
                                         void* D, const float* bias, void* stream, int32_t wait);
+
+/* Every buffer of one launch.  Pointers as for gemm_run / gemm_run_ex;
+ * sfa / sfb: the scale-factor tensors of a block-scaled descriptor (16-byte
+ * aligned; NULL otherwise). */
+typedef struct {
+    const void* A;
+    const void* B;
+    const void* C;
+    void* D;
+    const float* bias;
+    const void* sfa;
+    const void* sfb;
+    float* row_sum;
+    float* col_sum;
+    float* abs_max;
+} gemm_args_t;
+
+/* gemm_run with every buffer in one struct: the entry point for
+ * block-scaled descriptors (gemm_run / gemm_run_ex return
+ * GEMM_ERR_INVALID_ARG for them, having no scale-factor arguments). */
+GEMM_API gemm_status_t gemm_run_args(gemm_handle_t h, const gemm_args_t* args, void* stream);
 
 /* Static string for a status code. */
 GEMM_API const char* gemm_status_str(gemm_status_t s);

@@ -162,3 +162,12 @@ def test_create_without_gpu_reports_no_device():
     with pytest.raises(g.GemmError) as e:
         g.gemm_create(d)
     assert e.value.status == g.ERR_INVALID_ARG
+
+
+def test_block_scaling_needs_e4m3_operands_and_plans_the_mx_kernel():
+    d = _desc(dtype_a=g.BF16, dtype_b=g.BF16, block_scale=g.BLOCK_SCALE_MX)
+    assert _status(d)[0] == g.ERR_UNSUPPORTED
+    d = _desc(dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=7)
+    assert _status(d)[0] == g.ERR_INVALID_ARG
+    s, info = _status(_desc(M=4096, N=4096, K=4096, dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=g.BLOCK_SCALE_MX))
+    assert s == g.OK and (info.cta_group, info.tile_m, info.tile_n, info.tile_k, info.stages) == (1, 128, 128, 128, 5)

@@ -118,3 +118,25 @@ def test_k_not_a_multiple_of_the_block_reads_only_real_factors():
     want = np.einsum("lmk,lkn->lmn", a * 2.0 ** (np.repeat(sfa, 32, axis=2)[:, :, :K] - 127),
                      b * 2.0 ** (np.repeat(sfb, 32, axis=2)[:, :, :K].transpose(0, 2, 1) - 127))
     assert np.all(np.isfinite(t)) and np.allclose(t, want, rtol=1e-14, atol=0)
+
+
+def test_input_generator_layout_agrees_with_the_oracle_index():
+    # the workload generator packs factors with its own code; both follow the page
+    from dense_gemm_epilogue_sm_gb300 import workloads as wl
+    for L, rows, sfk in [(1, 5, 3), (2, 300, 10), (1, 129, 4)]:
+        off, per = wl._sf_offsets(L, rows, sfk)
+        want = [[[g.sf_index(l, r, f, rows, sfk) for f in range(sfk)] for r in range(rows)] for l in range(L)]
+        assert off.tolist() == want
+        assert per == ((rows + 127) // 128) * ((sfk + 3) // 4) * 512
+
+
+def test_generated_mx_inputs_dequantise_close_to_their_source():
+    from dense_gemm_epilogue_sm_gb300 import workloads as wl
+    spec = wl.Spec("mx_small", 40, 36, 200, dtype_in="e4m3", block_scale="mx", seed=5)
+    inputs = wl.make_inputs(spec)
+    assert inputs.extras["sfa"].dtype == inputs.extras["sfb"].dtype
+    p = g.problem_from_spec(spec, inputs)
+    p.sf_vec = 32
+    bits, t = g.gemm_rows(p, inputs.A, inputs.B, want_t=True, sfa=inputs.extras["sfa"].numpy(),
+                          sfb=inputs.extras["sfb"].numpy())
+    assert np.all(np.isfinite(t)) and np.abs(t).max() > 0
