@@ -181,8 +181,11 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     int tile_n = 256;
     if (cg == 1 && (P.Nk <= 128 || ((P.Mk + kTileM - 1) / kTileM) * ((P.Nk + 255) / 256) * L < 76)) tile_n = 128;
     const int bs = d.block_scale != GEMM_BLOCK_SCALE_NONE;
-    if (bs) {     // the block-scaled kernel: one CTA, 128 x 128 tiles
-        cg = 1;
+    if (bs) {     // the block-scaled kernel: 128-wide tiles, a CTA pair (256 x 128) where that fills the GPU
+        const int64_t tiles_pair = ((P.Mk + 255) / 256) * ((P.Nk + 127) / 128) * L;
+        // A pair CTA holds 64 rows of B; an MN-major e4m3 B needs 128-element
+        // (one 128-byte swizzle row) boxes along N, so it stays on one CTA.
+        cg = (P.Mk > 128 && tiles_pair >= 64 && b_kmaj) ? 2 : 1;
         tile_n = 128;
     }
     const int tile_m = kTileM * cg;
@@ -322,6 +325,22 @@ bool encode_map(CUtensorMap* map, const gl::Layout& lay, int dt, const void* bas
     return r == CUDA_SUCCESS;
 }
 
+// Scale-factor tensor as TMA sees it: rows of 16 bytes, 32 rows (one
+// 512-byte block) per box, `blocks` blocks in all.
+// Rank 3 (a unit third dimension) like the operand maps, since the kernel
+// issues 3-D tensor copies for both.
+bool encode_sf_map(CUtensorMap* map, const void* base, int64_t blocks) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {16, (cuuint64_t)(blocks * 32), 1};
+    cuuint64_t strides[2] = {16, (cuuint64_t)(blocks * 512)};
+    cuuint32_t box[3] = {16, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more
 // than there are tiles.
 int grid_for(const Plan& P, int sm_count, int max_clusters) {
@@ -351,9 +370,9 @@ struct gemm_handle_s {
     bool launched = false;
     uint64_t launches = 0;
     // map cache, keyed by the pointers of the last run
-    const void* cached[4] = {nullptr, nullptr, nullptr, nullptr};
+    const void* cached[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     bool cache_valid = false;
-    CUtensorMap maps[4];
+    CUtensorMap maps[6];
 };
 
 namespace {
@@ -543,7 +562,11 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
     const void* kb = swap ? a_ptr : b_ptr;
     const int ab = P.a_bytes;
     const uint32_t kel = kStageKBytes / ab;
-    if (!h->cache_valid || h->cached[0] != ka || h->cached[1] != kb || h->cached[2] != c_ptr || h->cached[3] != D) {
+    // kernel orientation: with D computed transposed, A's factors go with the kernel's B
+    const void* ksfa = swap ? sfb : sfa;
+    const void* ksfb = swap ? sfa : sfb;
+    if (!h->cache_valid || h->cached[0] != ka || h->cached[1] != kb || h->cached[2] != c_ptr || h->cached[3] != D ||
+        h->cached[4] != ksfa || h->cached[5] != ksfb) {
         const int tn = P.tile_n;
         const uint32_t epi_cols = 128u / P.out_bytes;
         const int adt = d.dtype_a;
@@ -560,6 +583,14 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
         } else {
             h->maps[2] = h->maps[3];
         }
+        if (P.kp.block_scaled && d.K > 0) {
+            const int64_t la_n = P.kp.a_batched ? P.kp.L : 1, lb_n = P.kp.b_batched ? P.kp.L : 1;
+            ok = ok && encode_sf_map(&h->maps[4], ksfa, la_n * P.kp.sf_mblocks * (int64_t)P.kp.num_kb);
+            ok = ok && encode_sf_map(&h->maps[5], ksfb, lb_n * P.kp.sf_nblocks * (int64_t)P.kp.num_kb);
+        } else {
+            h->maps[4] = h->maps[0];
+            h->maps[5] = h->maps[0];
+        }
         if (!ok) {
             h->cache_valid = false;
             return GEMM_ERR_CUDA;
@@ -568,6 +599,8 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
         h->cached[1] = kb;
         h->cached[2] = c_ptr;
         h->cached[3] = D;
+        h->cached[4] = ksfa;
+        h->cached[5] = ksfb;
         h->cache_valid = true;
     }
     LaunchArgs la;
@@ -575,12 +608,13 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
     la.tmB = h->maps[1];
     la.tmC = h->maps[2];
     la.tmD = h->maps[3];
+    la.tmSA = h->maps[4];
+    la.tmSB = h->maps[5];
     la.p = P.kp;
     la.p.bias = bias;
     la.p.d_ptr = D;
-    // kernel orientation: with D computed transposed, A's factors go with the kernel's B
-    la.p.sfa = static_cast<const uint8_t*>(swap ? sfb : sfa);
-    la.p.sfb = static_cast<const uint8_t*>(swap ? sfa : sfb);
+    la.p.sfa = static_cast<const uint8_t*>(ksfa);
+    la.p.sfb = static_cast<const uint8_t*>(ksfb);
     la.cta_group = P.cta_group;
     la.tile_n = P.tile_n;
     la.out_bytes = P.out_bytes;
@@ -753,6 +787,8 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
     } else {
         la.tmC = la.tmD;
     }
+    la.tmSA = la.tmA;          // block scaling is refused above
+    la.tmSB = la.tmA;
     if (!ok) return GEMM_ERR_CUDA;
     if (prepare_kernel(P.cta_group, P.tile_n, P.out_bytes, P.kp.block_scaled) != cudaSuccess) {
         cudaGetLastError();

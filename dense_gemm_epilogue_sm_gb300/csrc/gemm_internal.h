@@ -77,7 +77,7 @@ struct KernelParams {
     // 512-byte block; a batch's tensor holds blocks (row/128) * num_kb + kb.
     int32_t block_scaled;
     int32_t sf_mblocks, sf_nblocks;    // 128-row blocks of the kernel's A and B
-    const uint8_t* sfa;
+    const uint8_t* sfa;                // (kept for reference; the kernel loads through tmSA / tmSB)
     const uint8_t* sfb;
     int32_t dp_tiles;
     int64_t sk_iters;
@@ -99,6 +99,7 @@ struct KernelParams {
 
 struct LaunchArgs {
     CUtensorMap tmA, tmB, tmC, tmD;
+    CUtensorMap tmSA, tmSB;       // scale-factor blocks (block-scaled kernel; else copies of tmA)
     KernelParams p;
     int cta_group;                // 1 or 2 (CTA pair, cluster of 2)
     int tile_n;                   // 128 or 256

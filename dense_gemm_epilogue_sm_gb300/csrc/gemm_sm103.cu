@@ -40,7 +40,7 @@
 namespace gemm_sm103 {
 
 int stages_for(int cta_group, int tile_n, int block_scaled) {
-    return block_scaled ? 5 : ((cta_group == 1 && tile_n == 256) ? 4 : 6);
+    return block_scaled ? (cta_group == 2 ? 6 : 5) : ((cta_group == 1 && tile_n == 256) ? 4 : 6);
 }
 
 // TMEM accumulators per CTA: two, so the epilogue of one tile overlaps the
@@ -59,7 +59,7 @@ template <int CG, int BN, int OB, bool BS = false>
 struct Cfg {
     static constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
     static constexpr int kBRows = BN / CG;                          // rows of B this CTA loads
-    static constexpr int kStages = BS ? 5 : ((CG == 1 && BN == 256) ? 4 : 6);
+    static constexpr int kStages = BS ? (CG == 2 ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
     static constexpr int kABytes = kTileM * kStageKBytes;           // 16 KiB
     static constexpr int kBBytes = kBRows * kStageKBytes;
     static constexpr int kSfBytes = BS ? 2 * 512 : 0;               // scale-factor blocks of A and B
@@ -83,6 +83,8 @@ struct Cfg {
 };
 
 size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes, int block_scaled) {
+    if (block_scaled && cta_group == 2)
+        return out_bytes == 2 ? Cfg<2, 128, 2, true>::kSmemBytes : Cfg<2, 128, 4, true>::kSmemBytes;
     if (block_scaled) return out_bytes == 2 ? Cfg<1, 128, 2, true>::kSmemBytes : Cfg<1, 128, 4, true>::kSmemBytes;
     if (cta_group == 2) return out_bytes == 2 ? Cfg<2, 256, 2>::kSmemBytes : Cfg<2, 256, 4>::kSmemBytes;
     if (tile_n == 256) return out_bytes == 2 ? Cfg<1, 256, 2>::kSmemBytes : Cfg<1, 256, 4>::kSmemBytes;
@@ -573,6 +575,7 @@ template <int CG, int BN, int OB, bool BS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                 const __grid_constant__ KernelParams p) {
     using C = Cfg<CG, BN, OB, BS>;
     constexpr int S = C::kStages;
@@ -631,6 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmB);
         ptx::prefetch_tensormap(&tmD);
         if (p.has_c) ptx::prefetch_tensormap(&tmC);
+        if constexpr (BS) {
+            ptx::prefetch_tensormap(&tmSA);
+            ptx::prefetch_tensormap(&tmSB);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), C::kTmemCols);
@@ -700,13 +707,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 load(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb);
                         }
                         if constexpr (BS) {
-                            // one 512-byte scale-factor block per 128 rows and K stage:
-                            // block (rows / 128) * num_kb + kb of the batch's tensor
+                            // One 512-byte scale-factor block per 128 rows and K stage:
+                            // block (rows / 128) * num_kb + kb of the batch's tensor, read
+                            // as 32 rows of 16 bytes.  Each CTA takes its own A rows'
+                            // block and the block of the tile's whole N range.
                             const uint32_t sf = sb + C::kBBytes;
-                            ptx::bulk_g2s(sf, p.sfa + (((int64_t)la * p.sf_mblocks + m0 / 128) * p.num_kb + kb) * 512,
-                                          512, fb);
-                            ptx::bulk_g2s(sf + 512, p.sfb + (((int64_t)lb * p.sf_nblocks + n0 / 128) * p.num_kb + kb) * 512,
-                                          512, fb);
+                            const int blk_a = (la * p.sf_mblocks + m0 / 128) * p.num_kb + kb;
+                            const int blk_b = (lb * p.sf_nblocks + nb * BN / 128) * p.num_kb + kb;
+                            load(sf, &tmSA, 0, blk_a * 32, 0);
+                            load(sf + 512, &tmSB, 0, blk_b * 32, 0);
                         }
                         const uint32_t bit = 1u << pend_slot(stage);
                         pend |= bit;
@@ -1048,6 +1057,8 @@ static cudaError_t set_attrs() {
 }
 
 cudaError_t prepare_kernel(int cta_group, int tile_n, int out_bytes, int block_scaled) {
+    if (block_scaled && cta_group == 2)
+        return out_bytes == 2 ? set_attrs<2, 128, 2, true>() : set_attrs<2, 128, 4, true>();
     if (block_scaled) return out_bytes == 2 ? set_attrs<1, 128, 2, true>() : set_attrs<1, 128, 4, true>();
     if (cta_group == 2) return out_bytes == 2 ? set_attrs<2, 256, 2>() : set_attrs<2, 256, 4>();
     if (tile_n == 256) return out_bytes == 2 ? set_attrs<1, 256, 2>() : set_attrs<1, 256, 4>();
@@ -1074,7 +1085,7 @@ template <int CG, int BN, int OB, bool BS = false>
 static cudaError_t launch_t(const LaunchArgs& a) {
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = make_config<CG, BN, OB, BS>(a.grid, a.stream, &attr);
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<CG, BN, OB, BS>, a.tmA, a.tmB, a.tmC, a.tmD, a.p);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<CG, BN, OB, BS>, a.tmA, a.tmB, a.tmC, a.tmD, a.tmSA, a.tmSB, a.p);
 }
 
 template <int CG, int BN, int OB, bool BS = false>
@@ -1090,6 +1101,8 @@ static int max_clusters_t() {
 }
 
 int max_active_clusters(int cta_group, int tile_n, int out_bytes, int block_scaled) {
+    if (block_scaled && cta_group == 2)
+        return out_bytes == 2 ? max_clusters_t<2, 128, 2, true>() : max_clusters_t<2, 128, 4, true>();
     if (block_scaled) return out_bytes == 2 ? max_clusters_t<1, 128, 2, true>() : max_clusters_t<1, 128, 4, true>();
     if (cta_group == 2) return out_bytes == 2 ? max_clusters_t<2, 256, 2>() : max_clusters_t<2, 256, 4>();
     if (tile_n == 256) return out_bytes == 2 ? max_clusters_t<1, 256, 2>() : max_clusters_t<1, 256, 4>();
@@ -1097,6 +1110,8 @@ int max_active_clusters(int cta_group, int tile_n, int out_bytes, int block_scal
 }
 
 cudaError_t launch(const LaunchArgs& a) {
+    if (a.block_scaled && a.cta_group == 2)
+        return a.out_bytes == 2 ? launch_t<2, 128, 2, true>(a) : launch_t<2, 128, 4, true>(a);
     if (a.block_scaled) return a.out_bytes == 2 ? launch_t<1, 128, 2, true>(a) : launch_t<1, 128, 4, true>(a);
     if (a.cta_group == 2) return a.out_bytes == 2 ? launch_t<2, 256, 2>(a) : launch_t<2, 256, 4>(a);
     if (a.tile_n == 256) return a.out_bytes == 2 ? launch_t<1, 256, 2>(a) : launch_t<1, 256, 4>(a);

@@ -84,19 +84,44 @@ SPECS = [
 ]
 
 
-@pytest.mark.parametrize("spec", SPECS, ids=lambda s: s.name)
+# big enough for the CTA-pair variant (256 x 128 tiles, at least 64 of them)
+PAIR_SPECS = [
+    wl.Spec("mx_pair_ragged_fused", 2100, 1300, 1024, dtype_in="e4m3", block_scale="mx", alpha=0.5, beta=1.0,
+            act="relu", bias="col", seed=101, pad=16),
+    wl.Spec("mx_pair_colmajor_f32", 1500, 2400, 768, dtype_in="e4m3", dtype_d="f32", block_scale="mx",
+            order_c="col", order_d="col", bias="row", seed=102),
+    wl.Spec("mx_pair_a_mn_major_batched", 1024, 1024, 512, batch=3, order_a="col", order_b="col", dtype_in="e4m3",
+            block_scale="mx", beta=1.0, seed=103),
+]
+
+
+def test_mn_major_b_stays_on_one_cta():
+    # each CTA of a pair holds 64 rows of B, narrower than one MN-major e4m3 box
+    spec = wl.Spec("mx_b_mn", 2048, 2048, 512, order_b="row", dtype_in="e4m3", block_scale="mx", seed=104)
+    info = g.gemm_plan(desc_from_spec(spec))
+    assert not info.b_k_major and info.cta_group == 1
+    inputs = wl.make_inputs(spec)
+    bits, op = _run(spec, inputs)
+    _check(spec, inputs, bits, rows=H.sample_rows(spec))
+    op.close()
+
+
+@pytest.mark.parametrize("spec", SPECS + PAIR_SPECS, ids=lambda s: s.name)
 def test_block_scaled_matches_oracle(spec):
     inputs = wl.make_inputs(spec)
     bits, op = _run(spec, inputs)
     info = g.gemm_plan(op.desc)
-    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (1, 128, 128, 128)
-    _check(spec, inputs, bits)
+    want_cg = 2 if spec in PAIR_SPECS else 1
+    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (want_cg, 128 * want_cg, 128, 128)
+    rows = H.sample_rows(spec) if spec in PAIR_SPECS else None
+    _check(spec, inputs, bits, rows=rows)
     op.close()
 
 
+@pytest.mark.parametrize("M,N", [(512, 384), (2304, 1152)])        # one CTA, and CTA pairs
 @pytest.mark.parametrize("order_d", ["row", "col"])
-def test_block_scaled_integer_sums_bit_exact(order_d):
-    spec = wl.Spec("mx_int", 512, 384, 1024, dtype_in="e4m3", dtype_d="f32", dist="int4", block_scale="mx",
+def test_block_scaled_integer_sums_bit_exact(order_d, M, N):
+    spec = wl.Spec("mx_int", M, N, 1024, dtype_in="e4m3", dtype_d="f32", dist="int4", block_scale="mx",
                    order_c=order_d, order_d=order_d, seed=97)
     inputs = wl.make_inputs(spec)
     bits, op = _run(spec, inputs, repeat=2)
