@@ -377,6 +377,35 @@ int oracle_gemm_rows(const oracle_problem_t* p, const void* A, const void* B, co
     return oracle_gemm_rows_sf(p, A, B, NULL, NULL, C, bias, nrows, rows, Dout, Tout, nthreads);
 }
 
+/* Round-to-nearest-even into e4m3 with saturation ("satfinite"): finite
+ * values beyond the largest finite magnitude 448 become +-448, NaN becomes
+ * the NaN code S.1111.111 (0x7F); e4m3 has no infinities.  Subnormals have
+ * quantum 2^-9 (exponent field 0, bias 7, 3 mantissa bits). */
+uint32_t oracle_encode_e4m3(double v) {
+    if (isnan(v)) return 0x7Fu;
+    const uint32_t sign = signbit(v) ? 0x80u : 0u;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    const int mb = 3, bias = 7, emin = 1 - bias;
+    int e2;
+    frexp(a, &e2);
+    int E = e2 - 1;
+    if (E < emin) E = emin;
+    double r = nearbyint(ldexp(a, mb - E));    /* exact scaling, ties to even */
+    double res = ldexp(r, E - mb);
+    if (res > 448.0 || isinf(a)) return sign | 0x7Eu;  /* satfinite: 1.1111.110 = 448 */
+    if (r == 0.0) return sign;
+    frexp(res, &e2);
+    E = e2 - 1;
+    if (E < emin) return sign | (uint32_t)ldexp(res, mb - emin);          /* subnormal */
+    const uint32_t mant = (uint32_t)(ldexp(res, mb - E) - ldexp(1.0, mb));
+    return sign | ((uint32_t)(E + bias) << mb) | mant;
+}
+
+void oracle_encode_e4m3_array(const double* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_encode_e4m3(v[i]);
+}
+
 /* Scatters packed rows (as produced by oracle_gemm_rows for every row, in
  * order) into D's own storage layout: D(l,m,n) at l*stride_d + (m,n) by
  * order_d and ldd.  Lets a test build a full D buffer the way a caller lays

@@ -57,6 +57,10 @@ def lib():
                                           ctypes.c_int]
         l.oracle_sf_index.restype = ctypes.c_int64
         l.oracle_sf_index.argtypes = [ctypes.c_int64] * 5
+        l.oracle_encode_e4m3.restype = ctypes.c_uint32
+        l.oracle_encode_e4m3.argtypes = [ctypes.c_double]
+        l.oracle_encode_e4m3_array.restype = None
+        l.oracle_encode_e4m3_array.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
         l.oracle_decode.restype = ctypes.c_double
         l.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_uint32]
         l.oracle_encode.restype = ctypes.c_uint32
@@ -218,3 +222,44 @@ def col_sums(t):
 def abs_max(t):
     """(L,): max over m, n of |t(l, m, n)| (NaN if any t is NaN)."""
     return np.max(np.abs(t), axis=(1, 2))
+
+
+# ------------------------------------------------- block-scaled output ----
+# MX output of the epilogue ("Technical Documentation: NVIDIA/cutlass",
+# "Blackwell SM100 GEMMs": an epilogue fusion that writes elements plus a
+# block scale factor per SFDVectorSize elements along an output dimension).
+# Reading for mx_float8 output: blocks of 32 consecutive elements of a D row
+# (D row-major), factor ue8m0 from the OCP MX rule (shared exponent
+# floor(log2 amax) - 8, where 8 is the exponent of e4m3's largest power of
+# two, code clamped to [0, 254]; a block with a NaN or infinite element gets
+# code 255 and NaN elements), elements = e4m3(t / 2^(code-127)) rounded to
+# nearest even and saturated at +-448.  The exponent is taken from t rounded
+# to fp32, the precision the epilogue computes t in.
+
+def encode_e4m3(values):
+    """fp64 array -> e4m3 codes (uint8), round to nearest even, saturating."""
+    v = np.ascontiguousarray(values, dtype=np.float64).reshape(-1)
+    out = np.empty(v.size, dtype=np.uint8)
+    lib().oracle_encode_e4m3_array(v.ctypes.data, v.size, out.ctypes.data)
+    return out.reshape(np.shape(values))
+
+
+def mx_quantise_rows(t):
+    """t: (R, N) epilogue values -> (codes (R, ceil(N/32)) uint8, elements
+    (R, N) e4m3 codes uint8)."""
+    t32 = np.asarray(t, dtype=np.float64).astype(np.float32).astype(np.float64)
+    R, N = t32.shape
+    nb = (N + 31) // 32
+    blk = np.zeros((R, nb * 32))
+    blk[:, :N] = t32
+    blk = blk.reshape(R, nb, 32)
+    a = np.abs(blk)
+    bad = ~np.isfinite(a).all(axis=2)
+    amax = np.where(bad, 0.0, a.max(axis=2))
+    _, e = np.frexp(amax)                        # amax = f * 2^e, f in [0.5, 1)
+    code = np.where(amax > 0, np.clip(e - 1 - 8 + 127, 0, 254), 0).astype(np.int64)
+    code = np.where(bad, 255, code)
+    scaled = blk / np.ldexp(1.0, (np.minimum(code, 254) - 127))[:, :, None]
+    q = encode_e4m3(scaled).reshape(R, nb * 32)[:, :N]
+    q = np.where(np.repeat(bad, 32, axis=1)[:, :N], np.uint8(0x7F), q)
+    return code.astype(np.uint8), q.astype(np.uint8)

@@ -140,3 +140,35 @@ def test_generated_mx_inputs_dequantise_close_to_their_source():
     bits, t = g.gemm_rows(p, inputs.A, inputs.B, want_t=True, sfa=inputs.extras["sfa"].numpy(),
                           sfb=inputs.extras["sfb"].numpy())
     assert np.all(np.isfinite(t)) and np.abs(t).max() > 0
+
+
+# ------------------------------------------------- block-scaled output ----
+def test_e4m3_encoder_round_trips_saturates_and_ties_to_even():
+    finite = [c for c in range(256) if (c & 0x7F) != 0x7F]
+    vals = np.array([g.decode("e4m3", c) for c in finite])
+    codes = g.encode_e4m3(vals)
+    assert [int(c) for c in codes] == finite                      # every finite code, -0 included
+    # halfway between 1.0 (0x38) and 1.125 (0x39) goes to the even code 0x38;
+    # halfway between 1.125 and 1.25 (0x3A) goes to 0x3A
+    assert g.encode_e4m3(np.array([1.0625, 1.1875])).tolist() == [0x38, 0x3A]
+    assert g.encode_e4m3(np.array([448.0, 464.0, 1e9, -1e9, np.inf])).tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0x7E]
+    assert g.encode_e4m3(np.array([np.nan])).tolist() == [0x7F]
+    assert g.encode_e4m3(np.array([2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10])).tolist() == [0x01, 0x00, 0x02]
+
+
+def test_mx_output_factor_follows_the_shared_exponent_rule():
+    t = np.zeros((3, 70))
+    t[0, :32] = np.linspace(-3.0, 3.0, 32)              # amax 3: floor(log2 3) - 8 = -7 -> code 120
+    t[0, 32:64] = 448.0 * 4                             # amax 1792 = 448 * 2^2: code 127 + 10 - 8
+    t[0, 64:] = 0.0                                     # all zero: code 0
+    t[1, 5] = np.nan                                    # a NaN: code 255, NaN elements
+    t[2, :] = 500.0                                     # 500 / 2^0 saturates to 448
+    codes, q = g.mx_quantise_rows(t)
+    assert codes.shape == (3, 3) and codes[0].tolist() == [120, 129, 0]
+    assert codes[1, 0] == 255 and np.all(q[1, :32] == 0x7F) and codes[1, 1] == 0
+    assert codes[2].tolist() == [127, 127, 127] and np.all(q[2] == 0x7E)
+    dq = np.array([g.decode("e4m3", int(c)) for c in q[0, :32]]) * 2.0 ** (int(codes[0, 0]) - 127)
+    assert np.array_equal(dq, np.array([g.decode("e4m3", int(c)) for c in g.encode_e4m3(t[0, :32] * 128)]) / 128)
+    assert np.all(np.abs(dq - t[0, :32]) <= 2.0 ** -4 * np.abs(t[0, :32]) + 2.0 ** -16)
+    dq1 = np.array([g.decode("e4m3", int(c)) for c in q[0, 32:64]]) * 2.0 ** (int(codes[0, 1]) - 127)
+    assert np.all(dq1 == 1792.0)
