@@ -104,7 +104,10 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     // One operand type per MMA: both f16, both bf16 or both e4m3.
     if (d.dtype_a != d.dtype_b) return GEMM_ERR_UNSUPPORTED;
     if (d.dtype_a == GEMM_F32) return GEMM_ERR_UNSUPPORTED;
-    if (d.dtype_d == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
+    if (d.out_scale != GEMM_OUT_SCALE_NONE && d.out_scale != GEMM_OUT_SCALE_MX) return GEMM_ERR_INVALID_ARG;
+    if ((d.dtype_d == GEMM_E4M3) != (d.out_scale == GEMM_OUT_SCALE_MX)) return GEMM_ERR_UNSUPPORTED;
+    if (d.out_scale == GEMM_OUT_SCALE_MX && (d.order_d != GEMM_ROW_MAJOR || d.beta != 0.0f || d.reduce))
+        return GEMM_ERR_UNSUPPORTED;
     if (has_c && (d.dtype_c != d.dtype_d || d.order_c != d.order_d)) return GEMM_ERR_UNSUPPORTED;
 
     const int ab = dtype_bytes(d.dtype_a), ob = dtype_bytes(d.dtype_d);
@@ -244,6 +247,12 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     k.a_kmajor = a_kmaj;
     k.b_kmajor = b_kmaj;
     k.block_scaled = bs;
+    k.out_f8 = d.out_scale == GEMM_OUT_SCALE_MX;
+    if (k.out_f8) {
+        const int64_t sfk = (P.Nk + 31) / 32;
+        k.sfd_kb4 = (int32_t)((sfk + 3) / 4);
+        k.sfd_bstride = ((P.Mk + 127) / 128) * (int64_t)k.sfd_kb4 * 512;
+    }
     k.sf_mblocks = (int32_t)((P.Mk + 127) / 128);
     k.sf_nblocks = (int32_t)((P.Nk + 127) / 128);
     k.elem_bytes = ab;
@@ -535,10 +544,11 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
 
 static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
                               const float* bias, float* row_sum, float* col_sum, float* abs_max, const void* sfa,
-                              const void* sfb, void* stream) {
+                              const void* sfb, void* sfd, void* stream) {
     if (!h) return GEMM_ERR_INVALID_ARG;
     Plan& P = h->plan;
     const gemm_desc_t& d = P.d;
+    if (P.kp.out_f8 && !sfd) return GEMM_ERR_INVALID_ARG;
     if (P.kp.block_scaled && d.K > 0) {
         if (!sfa || !sfb) return GEMM_ERR_INVALID_ARG;
         if ((reinterpret_cast<uintptr_t>(sfa) | reinterpret_cast<uintptr_t>(sfb)) & 15u) return GEMM_ERR_MISALIGNED;
@@ -615,6 +625,7 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
     la.p.d_ptr = D;
     la.p.sfa = static_cast<const uint8_t*>(ksfa);
     la.p.sfb = static_cast<const uint8_t*>(ksfb);
+    la.p.sfd = static_cast<uint8_t*>(sfd);
     la.cta_group = P.cta_group;
     la.tile_n = P.tile_n;
     la.out_bytes = P.out_bytes;
@@ -660,17 +671,18 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
 
 gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D, const float* bias,
                        void* stream) {
-    return run_impl(h, A, B, C, D, bias, nullptr, nullptr, nullptr, nullptr, nullptr, stream);
+    return run_impl(h, A, B, C, D, bias, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 gemm_status_t gemm_run_ex(gemm_handle_t h, const void* A, const void* B, const void* C, void* D, const float* bias,
                           float* row_sum, float* col_sum, float* abs_max, void* stream) {
-    return run_impl(h, A, B, C, D, bias, row_sum, col_sum, abs_max, nullptr, nullptr, stream);
+    return run_impl(h, A, B, C, D, bias, row_sum, col_sum, abs_max, nullptr, nullptr, nullptr, stream);
 }
 
 gemm_status_t gemm_run_args(gemm_handle_t h, const gemm_args_t* a, void* stream) {
     if (!a) return GEMM_ERR_INVALID_ARG;
-    return run_impl(h, a->A, a->B, a->C, a->D, a->bias, a->row_sum, a->col_sum, a->abs_max, a->sfa, a->sfb, stream);
+    return run_impl(h, a->A, a->B, a->C, a->D, a->bias, a->row_sum, a->col_sum, a->abs_max, a->sfa, a->sfb, a->sfd,
+                    stream);
 }
 
 gemm_status_t gemm_check(gemm_handle_t h) {
@@ -759,7 +771,7 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
     const gemm_status_t s = validate_and_plan(desc, &P);
     if (s != GEMM_OK) return s;
     if (P.d.reduce) return GEMM_ERR_UNSUPPORTED;     // reductions need a handle's workspace
-    if (P.kp.block_scaled) return GEMM_ERR_UNSUPPORTED;   // no scale-factor arguments here
+    if (P.kp.block_scaled || P.kp.out_f8) return GEMM_ERR_UNSUPPORTED;   // no scale-factor arguments here
     const gemm_desc_t& d = P.d;
     if (d.M == 0 || d.N == 0) return GEMM_OK;
     if (!D || (d.K > 0 && (!A || !B)) || (P.has_c && !C) || (d.bias != GEMM_BIAS_NONE && !bias))

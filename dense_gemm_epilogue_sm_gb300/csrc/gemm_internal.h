@@ -75,6 +75,13 @@ struct KernelParams {
     // Block scaling (block_scaled = 1): one ue8m0 factor per 32 K elements;
     // the factors of 128 rows x one K stage (4 factors each) form one
     // 512-byte block; a batch's tensor holds blocks (row/128) * num_kb + kb.
+    // MX output (out_f8 = 1): D in e4m3, factors written to sfd in the
+    // basic-block layout (rows = M, one factor per 32 columns; sfd_kb4 =
+    // ceil(ceil(N/32)/4) blocks along N; sfd_bstride bytes per batch).
+    int32_t out_f8;
+    uint8_t* sfd;
+    int64_t sfd_bstride;
+    int32_t sfd_kb4;
     int32_t block_scaled;
     int32_t sf_mblocks, sf_nblocks;    // 128-row blocks of the kernel's A and B
     const uint8_t* sfa;                // (kept for reference; the kernel loads through tmSA / tmSB)

@@ -64,7 +64,8 @@ struct Cfg {
     static constexpr int kBBytes = kBRows * kStageKBytes;
     static constexpr int kSfBytes = BS ? 2 * 512 : 0;               // scale-factor blocks of A and B
     static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;   // this CTA's share of a stage
-    static constexpr int kEpiCols = 128 / OB;                       // 64 (16-bit D) or 32 (fp32 D)
+    // 64 (16-bit D), 32 (fp32 D), or 64 (e4m3 D with MX factors, stored directly)
+    static constexpr int kEpiCols = OB == 1 ? 64 : 128 / OB;
     static constexpr int kSubtiles = BN / kEpiCols;
     static constexpr int kSfCol0 = kAccBufs * BN;                   // first TMEM column of the scale factors
     static constexpr int kTmemCols = BS ? 512 : kAccBufs * BN;
@@ -82,13 +83,19 @@ struct Cfg {
         1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kClcSlots * 16 + kNumBars * 8 + 16;
 };
 
+// Kernel variants by (CTA group, tile N, output bytes, block scaling).
+#define GEMM_OB3(EXPR1, EXPR2, EXPR4) (out_bytes == 1 ? (EXPR1) : out_bytes == 2 ? (EXPR2) : (EXPR4))
+
 size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes, int block_scaled) {
     if (block_scaled && cta_group == 2)
-        return out_bytes == 2 ? Cfg<2, 128, 2, true>::kSmemBytes : Cfg<2, 128, 4, true>::kSmemBytes;
-    if (block_scaled) return out_bytes == 2 ? Cfg<1, 128, 2, true>::kSmemBytes : Cfg<1, 128, 4, true>::kSmemBytes;
-    if (cta_group == 2) return out_bytes == 2 ? Cfg<2, 256, 2>::kSmemBytes : Cfg<2, 256, 4>::kSmemBytes;
-    if (tile_n == 256) return out_bytes == 2 ? Cfg<1, 256, 2>::kSmemBytes : Cfg<1, 256, 4>::kSmemBytes;
-    return out_bytes == 2 ? Cfg<1, 128, 2>::kSmemBytes : Cfg<1, 128, 4>::kSmemBytes;
+        return GEMM_OB3((Cfg<2, 128, 1, true>::kSmemBytes), (Cfg<2, 128, 2, true>::kSmemBytes),
+                        (Cfg<2, 128, 4, true>::kSmemBytes));
+    if (block_scaled)
+        return GEMM_OB3((Cfg<1, 128, 1, true>::kSmemBytes), (Cfg<1, 128, 2, true>::kSmemBytes),
+                        (Cfg<1, 128, 4, true>::kSmemBytes));
+    if (cta_group == 2) return GEMM_OB3((Cfg<2, 256, 1>::kSmemBytes), (Cfg<2, 256, 2>::kSmemBytes), (Cfg<2, 256, 4>::kSmemBytes));
+    if (tile_n == 256) return GEMM_OB3((Cfg<1, 256, 1>::kSmemBytes), (Cfg<1, 256, 2>::kSmemBytes), (Cfg<1, 256, 4>::kSmemBytes));
+    return GEMM_OB3((Cfg<1, 128, 1>::kSmemBytes), (Cfg<1, 128, 2>::kSmemBytes), (Cfg<1, 128, 4>::kSmemBytes));
 }
 
 // ------------------------------------------------------------------------
@@ -882,138 +889,211 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int sub = 0; sub < C::kSubtiles; ++sub) {
                     const int col0 = nb * BN + sub * C::kEpiCols;
                     if (row0 >= p.M || col0 >= p.N) continue;     // nothing of this subtile is in range
-                    // the subtile holding a ragged row end is stored element by element
-                    const bool direct = p.d_ragged && col0 + C::kEpiCols > p.N;
-                    const int sbi = sub_count & 1;
-                    ++sub_count;
-                    uint8_t* sbuf = epi + (ew * 2 + sbi) * kEpiBufBytes;
-                    const uint32_t sbuf_a = ptx::smem_addr(sbuf);
-                    if (lane == 0) ptx::bulk_wait_read<1>();       // the store that last used sbuf has read it
-                    __syncwarp();
-                    if (p.has_c) {
-                        const uint32_t cb = cfull_bar(ew * 2 + sbi);
-                        if (lane == 0) {
-                            ptx::mbar_arrive_expect_tx(cb, kEpiBufBytes);
-                            ptx::tma_load_3d(sbuf_a, &tmC, col0, row0, lc, cb);
+                    if constexpr (OB == 1) {
+                        // MX output: e4m3 elements and one ue8m0 factor per 32
+                        // columns of a row (no C; checked on the host).
+                        uint32_t acc[C::kEpiCols];
+                        if (p.num_kb > 0) {
+                            load_acc(buf, sub, acc);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
                         }
-                        ok = __all_sync(0xffffffffu, wait_bar(cb, c_phase[sbi], p, abort_flag, kStatusRoleEpi, peer_abort));
-                        c_phase[sbi] ^= 1u;
-                        if (!ok) break;
-                    }
-                    uint32_t acc[C::kEpiCols];
-                    if (p.num_kb > 0) {
-                        load_acc(buf, sub, acc);
-                    } else {
-    #pragma unroll
-                        for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
-                    }
-                    if (cut) {
-                        for_each_part(r_next, t_end, [&](int w) {
-                            const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
-    #pragma unroll
-                            for (int c = 0; c < C::kEpiCols / 4; ++c) {
-                                const float4 v4 = __ldcg(ps + c * 32);
-                                acc[4 * c] = __float_as_uint(__uint_as_float(acc[4 * c]) + v4.x);
-                                acc[4 * c + 1] = __float_as_uint(__uint_as_float(acc[4 * c + 1]) + v4.y);
-                                acc[4 * c + 2] = __float_as_uint(__uint_as_float(acc[4 * c + 2]) + v4.z);
-                                acc[4 * c + 3] = __float_as_uint(__uint_as_float(acc[4 * c + 3]) + v4.w);
+                        if (cut) {
+                            for_each_part(r_next, t_end, [&](int w) {
+                                const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
+#pragma unroll
+                                for (int c = 0; c < C::kEpiCols / 4; ++c) {
+                                    const float4 v4 = __ldcg(ps + c * 32);
+                                    acc[4 * c] = __float_as_uint(__uint_as_float(acc[4 * c]) + v4.x);
+                                    acc[4 * c + 1] = __float_as_uint(__uint_as_float(acc[4 * c + 1]) + v4.y);
+                                    acc[4 * c + 2] = __float_as_uint(__uint_as_float(acc[4 * c + 2]) + v4.z);
+                                    acc[4 * c + 3] = __float_as_uint(__uint_as_float(acc[4 * c + 3]) + v4.w);
+                                }
+                                return true;
+                            });
+                        }
+#pragma unroll
+                        for (int h = 0; h < C::kEpiCols / 32; ++h) {
+                            const int c0 = col0 + h * 32;
+                            if (c0 >= p.N) break;                 // the block lies past the row's end
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                float x = p.alpha * __uint_as_float(acc[h * 32 + i]);
+                                if (p.bias_mode == 1)
+                                    x += (c0 + i < p.N) ? __ldg(bias_l + c0 + i) : 0.f;
+                                else if (p.bias_mode == 2)
+                                    x += row_bias;
+                                if (p.act == 1)
+                                    x = fmaxf(x, 0.f);
+                                else if (EXT && p.act == 2)
+                                    x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+                                v[i] = (c0 + i < p.N) ? x : 0.f;   // columns past N join no block
                             }
-                            return true;
-                        });
-                    }
-                    // Row `lane` of the 32-row slab; 128-byte rows, 16-byte chunk c
-                    // stored at chunk c ^ (row % 8) (the TMA 128B swizzle).
-                    uint8_t* row_base = sbuf + lane * 128;
-    #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint4* slot = reinterpret_cast<uint4*>(row_base + ((ch ^ (lane & 7)) << 4));
-                        float v[VPC];
-    #pragma unroll
-                        for (int i = 0; i < VPC; ++i) v[i] = p.alpha * __uint_as_float(acc[ch * VPC + i]);
+                            // factor: the OCP MX shared exponent floor(log2 amax) - 8,
+                            // read off amax's biased fp32 exponent; 255 for NaN / inf
+                            uint32_t amax = 0u;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(fabsf(v[i])));
+                            const int be = (int)(amax >> 23);
+                            const uint32_t code = amax >= 0x7F800000u ? 255u : (be > 8 ? (uint32_t)(be - 8) : 0u);
+                            const float sc = __uint_as_float((254u - (code > 254u ? 254u : code)) << 23);   // 2^(127-code)
+                            uint32_t w[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                w[k] = code == 255u ? 0x7F7F7F7Fu
+                                                    : ptx::pack4_e4m3(v[4 * k] * sc, v[4 * k + 1] * sc, v[4 * k + 2] * sc,
+                                                                      v[4 * k + 3] * sc);
+                            if (row < p.M) {
+                                uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)l * p.d_bstride +
+                                                (int64_t)row * p.ldd;
+                                if (c0 + 32 <= p.N) {
+                                    *reinterpret_cast<uint4*>(drow + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+                                    *reinterpret_cast<uint4*>(drow + c0 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                                } else {
+                                    for (int i = 0; i < 32 && c0 + i < p.N; ++i)
+                                        drow[c0 + i] = (uint8_t)(w[i >> 2] >> ((i & 3) * 8));
+                                }
+                                const int f = c0 / 32;
+                                p.sfd[(int64_t)l * p.sfd_bstride + ((int64_t)(row / 128) * p.sfd_kb4 + f / 4) * 512 +
+                                      (row % 32) * 16 + ((row % 128) / 32) * 4 + f % 4] = (uint8_t)code;
+                            }
+                        }
+                    } else {
+                        // the subtile holding a ragged row end is stored element by element
+                        const bool direct = p.d_ragged && col0 + C::kEpiCols > p.N;
+                        const int sbi = sub_count & 1;
+                        ++sub_count;
+                        uint8_t* sbuf = epi + (ew * 2 + sbi) * kEpiBufBytes;
+                        const uint32_t sbuf_a = ptx::smem_addr(sbuf);
+                        if (lane == 0) ptx::bulk_wait_read<1>();       // the store that last used sbuf has read it
+                        __syncwarp();
                         if (p.has_c) {
-                            const uint4 craw = *slot;
-                            const uint32_t w[4] = {craw.x, craw.y, craw.z, craw.w};
+                            const uint32_t cb = cfull_bar(ew * 2 + sbi);
+                            if (lane == 0) {
+                                ptx::mbar_arrive_expect_tx(cb, kEpiBufBytes);
+                                ptx::tma_load_3d(sbuf_a, &tmC, col0, row0, lc, cb);
+                            }
+                            ok = __all_sync(0xffffffffu, wait_bar(cb, c_phase[sbi], p, abort_flag, kStatusRoleEpi, peer_abort));
+                            c_phase[sbi] ^= 1u;
+                            if (!ok) break;
+                        }
+                        uint32_t acc[C::kEpiCols];
+                        if (p.num_kb > 0) {
+                            load_acc(buf, sub, acc);
+                        } else {
+        #pragma unroll
+                            for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
+                        }
+                        if (cut) {
+                            for_each_part(r_next, t_end, [&](int w) {
+                                const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
+        #pragma unroll
+                                for (int c = 0; c < C::kEpiCols / 4; ++c) {
+                                    const float4 v4 = __ldcg(ps + c * 32);
+                                    acc[4 * c] = __float_as_uint(__uint_as_float(acc[4 * c]) + v4.x);
+                                    acc[4 * c + 1] = __float_as_uint(__uint_as_float(acc[4 * c + 1]) + v4.y);
+                                    acc[4 * c + 2] = __float_as_uint(__uint_as_float(acc[4 * c + 2]) + v4.z);
+                                    acc[4 * c + 3] = __float_as_uint(__uint_as_float(acc[4 * c + 3]) + v4.w);
+                                }
+                                return true;
+                            });
+                        }
+                        // Row `lane` of the 32-row slab; 128-byte rows, 16-byte chunk c
+                        // stored at chunk c ^ (row % 8) (the TMA 128B swizzle).
+                        uint8_t* row_base = sbuf + lane * 128;
+        #pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            uint4* slot = reinterpret_cast<uint4*>(row_base + ((ch ^ (lane & 7)) << 4));
+                            float v[VPC];
+        #pragma unroll
+                            for (int i = 0; i < VPC; ++i) v[i] = p.alpha * __uint_as_float(acc[ch * VPC + i]);
+                            if (p.has_c) {
+                                const uint4 craw = *slot;
+                                const uint32_t w[4] = {craw.x, craw.y, craw.z, craw.w};
+                                if constexpr (OB == 4) {
+        #pragma unroll
+                                    for (int i = 0; i < 4; ++i) v[i] = fmaf(p.beta, __uint_as_float(w[i]), v[i]);
+                                } else {
+        #pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        float lo, hi;
+                                        unpack2(w[i], f16_out, lo, hi);
+                                        v[2 * i] = fmaf(p.beta, lo, v[2 * i]);
+                                        v[2 * i + 1] = fmaf(p.beta, hi, v[2 * i + 1]);
+                                    }
+                                }
+                            }
+                            if (p.bias_mode == 1) {
+                                const int cb0 = col0 + ch * VPC;
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) v[i] += (cb0 + i < p.N) ? __ldg(bias_l + cb0 + i) : 0.f;
+                            } else if (p.bias_mode == 2) {
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) v[i] += row_bias;
+                            }
+                            if (p.act == 1) {
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) v[i] = fmaxf(v[i], 0.f);
+                            } else if (EXT && p.act == 2) {
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) v[i] = 0.5f * v[i] * (1.f + erff(v[i] * 0.70710678118654752f));
+                            }
+                            if (reducing) {
+                                // elements outside D count as 0
+                                const int c0 = col0 + ch * VPC;
+                                float r[VPC];
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) r[i] = (row < p.M && c0 + i < p.N) ? v[i] : 0.f;
+                                if (p.red_rows) {
+        #pragma unroll
+                                    for (int i = 0; i < VPC; ++i) row_acc += r[i];
+                                }
+                                if (p.red_amax) {
+        #pragma unroll
+                                    for (int i = 0; i < VPC; ++i) amax_bits = max(amax_bits, __float_as_uint(fabsf(r[i])));
+                                }
+                                if (p.red_cols) {
+                                    int j;
+                                    const float cs = chunk_col_sum<VPC>(r, lane, j);
+                                    if ((lane & (32 / VPC - 1)) == 0 && c0 + j < p.N)
+                                        p.red_col_ws[((int64_t)l * ((p.M + 31) / 32) + row0 / 32) * p.N + c0 + j] = cs;
+                                }
+                            }
+                            uint4 out;
                             if constexpr (OB == 4) {
-    #pragma unroll
-                                for (int i = 0; i < 4; ++i) v[i] = fmaf(p.beta, __uint_as_float(w[i]), v[i]);
+                                out = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                                                 __float_as_uint(v[3]));
                             } else {
-    #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    float lo, hi;
-                                    unpack2(w[i], f16_out, lo, hi);
-                                    v[2 * i] = fmaf(p.beta, lo, v[2 * i]);
-                                    v[2 * i + 1] = fmaf(p.beta, hi, v[2 * i + 1]);
+                                out = make_uint4(pack2(v[0], v[1], f16_out), pack2(v[2], v[3], f16_out),
+                                                 pack2(v[4], v[5], f16_out), pack2(v[6], v[7], f16_out));
+                            }
+                            if (!direct) {
+                                *slot = out;
+                            } else if (row < p.M) {
+                                const int c0 = col0 + ch * VPC;
+                                const uint32_t w[4] = {out.x, out.y, out.z, out.w};
+                                uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
+                                                ((int64_t)l * p.d_bstride + (int64_t)row * p.ldd) * OB;
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) {
+                                    if (c0 + i >= p.N) break;
+                                    if constexpr (OB == 4)
+                                        *reinterpret_cast<uint32_t*>(drow + (int64_t)(c0 + i) * 4) = w[i];
+                                    else
+                                        *reinterpret_cast<uint16_t*>(drow + (int64_t)(c0 + i) * 2) =
+                                            (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
                                 }
                             }
                         }
-                        if (p.bias_mode == 1) {
-                            const int cb0 = col0 + ch * VPC;
-    #pragma unroll
-                            for (int i = 0; i < VPC; ++i) v[i] += (cb0 + i < p.N) ? __ldg(bias_l + cb0 + i) : 0.f;
-                        } else if (p.bias_mode == 2) {
-    #pragma unroll
-                            for (int i = 0; i < VPC; ++i) v[i] += row_bias;
-                        }
-                        if (p.act == 1) {
-    #pragma unroll
-                            for (int i = 0; i < VPC; ++i) v[i] = fmaxf(v[i], 0.f);
-                        } else if (EXT && p.act == 2) {
-    #pragma unroll
-                            for (int i = 0; i < VPC; ++i) v[i] = 0.5f * v[i] * (1.f + erff(v[i] * 0.70710678118654752f));
-                        }
-                        if (reducing) {
-                            // elements outside D count as 0
-                            const int c0 = col0 + ch * VPC;
-                            float r[VPC];
-    #pragma unroll
-                            for (int i = 0; i < VPC; ++i) r[i] = (row < p.M && c0 + i < p.N) ? v[i] : 0.f;
-                            if (p.red_rows) {
-    #pragma unroll
-                                for (int i = 0; i < VPC; ++i) row_acc += r[i];
-                            }
-                            if (p.red_amax) {
-    #pragma unroll
-                                for (int i = 0; i < VPC; ++i) amax_bits = max(amax_bits, __float_as_uint(fabsf(r[i])));
-                            }
-                            if (p.red_cols) {
-                                int j;
-                                const float cs = chunk_col_sum<VPC>(r, lane, j);
-                                if ((lane & (32 / VPC - 1)) == 0 && c0 + j < p.N)
-                                    p.red_col_ws[((int64_t)l * ((p.M + 31) / 32) + row0 / 32) * p.N + c0 + j] = cs;
-                            }
-                        }
-                        uint4 out;
-                        if constexpr (OB == 4) {
-                            out = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
-                                             __float_as_uint(v[3]));
-                        } else {
-                            out = make_uint4(pack2(v[0], v[1], f16_out), pack2(v[2], v[3], f16_out),
-                                             pack2(v[4], v[5], f16_out), pack2(v[6], v[7], f16_out));
-                        }
                         if (!direct) {
-                            *slot = out;
-                        } else if (row < p.M) {
-                            const int c0 = col0 + ch * VPC;
-                            const uint32_t w[4] = {out.x, out.y, out.z, out.w};
-                            uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
-                                            ((int64_t)l * p.d_bstride + (int64_t)row * p.ldd) * OB;
-    #pragma unroll
-                            for (int i = 0; i < VPC; ++i) {
-                                if (c0 + i >= p.N) break;
-                                if constexpr (OB == 4)
-                                    *reinterpret_cast<uint32_t*>(drow + (int64_t)(c0 + i) * 4) = w[i];
-                                else
-                                    *reinterpret_cast<uint16_t*>(drow + (int64_t)(c0 + i) * 2) =
-                                        (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
+                            ptx::fence_async_shared();
+                            __syncwarp();
+                            if (lane == 0) {
+                                ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, l);
+                                ptx::bulk_commit();
                             }
-                        }
-                    }
-                    if (!direct) {
-                        ptx::fence_async_shared();
-                        __syncwarp();
-                        if (lane == 0) {
-                            ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, l);
-                            ptx::bulk_commit();
                         }
                     }
                 }
@@ -1058,11 +1138,12 @@ static cudaError_t set_attrs() {
 
 cudaError_t prepare_kernel(int cta_group, int tile_n, int out_bytes, int block_scaled) {
     if (block_scaled && cta_group == 2)
-        return out_bytes == 2 ? set_attrs<2, 128, 2, true>() : set_attrs<2, 128, 4, true>();
-    if (block_scaled) return out_bytes == 2 ? set_attrs<1, 128, 2, true>() : set_attrs<1, 128, 4, true>();
-    if (cta_group == 2) return out_bytes == 2 ? set_attrs<2, 256, 2>() : set_attrs<2, 256, 4>();
-    if (tile_n == 256) return out_bytes == 2 ? set_attrs<1, 256, 2>() : set_attrs<1, 256, 4>();
-    return out_bytes == 2 ? set_attrs<1, 128, 2>() : set_attrs<1, 128, 4>();
+        return GEMM_OB3((set_attrs<2, 128, 1, true>()), (set_attrs<2, 128, 2, true>()), (set_attrs<2, 128, 4, true>()));
+    if (block_scaled)
+        return GEMM_OB3((set_attrs<1, 128, 1, true>()), (set_attrs<1, 128, 2, true>()), (set_attrs<1, 128, 4, true>()));
+    if (cta_group == 2) return GEMM_OB3((set_attrs<2, 256, 1>()), (set_attrs<2, 256, 2>()), (set_attrs<2, 256, 4>()));
+    if (tile_n == 256) return GEMM_OB3((set_attrs<1, 256, 1>()), (set_attrs<1, 256, 2>()), (set_attrs<1, 256, 4>()));
+    return GEMM_OB3((set_attrs<1, 128, 1>()), (set_attrs<1, 128, 2>()), (set_attrs<1, 128, 4>()));
 }
 
 template <int CG, int BN, int OB, bool BS = false>
@@ -1102,20 +1183,27 @@ static int max_clusters_t() {
 
 int max_active_clusters(int cta_group, int tile_n, int out_bytes, int block_scaled) {
     if (block_scaled && cta_group == 2)
-        return out_bytes == 2 ? max_clusters_t<2, 128, 2, true>() : max_clusters_t<2, 128, 4, true>();
-    if (block_scaled) return out_bytes == 2 ? max_clusters_t<1, 128, 2, true>() : max_clusters_t<1, 128, 4, true>();
-    if (cta_group == 2) return out_bytes == 2 ? max_clusters_t<2, 256, 2>() : max_clusters_t<2, 256, 4>();
-    if (tile_n == 256) return out_bytes == 2 ? max_clusters_t<1, 256, 2>() : max_clusters_t<1, 256, 4>();
-    return out_bytes == 2 ? max_clusters_t<1, 128, 2>() : max_clusters_t<1, 128, 4>();
+        return GEMM_OB3((max_clusters_t<2, 128, 1, true>()), (max_clusters_t<2, 128, 2, true>()),
+                        (max_clusters_t<2, 128, 4, true>()));
+    if (block_scaled)
+        return GEMM_OB3((max_clusters_t<1, 128, 1, true>()), (max_clusters_t<1, 128, 2, true>()),
+                        (max_clusters_t<1, 128, 4, true>()));
+    if (cta_group == 2)
+        return GEMM_OB3((max_clusters_t<2, 256, 1>()), (max_clusters_t<2, 256, 2>()), (max_clusters_t<2, 256, 4>()));
+    if (tile_n == 256)
+        return GEMM_OB3((max_clusters_t<1, 256, 1>()), (max_clusters_t<1, 256, 2>()), (max_clusters_t<1, 256, 4>()));
+    return GEMM_OB3((max_clusters_t<1, 128, 1>()), (max_clusters_t<1, 128, 2>()), (max_clusters_t<1, 128, 4>()));
 }
 
 cudaError_t launch(const LaunchArgs& a) {
+    const int out_bytes = a.out_bytes;
     if (a.block_scaled && a.cta_group == 2)
-        return a.out_bytes == 2 ? launch_t<2, 128, 2, true>(a) : launch_t<2, 128, 4, true>(a);
-    if (a.block_scaled) return a.out_bytes == 2 ? launch_t<1, 128, 2, true>(a) : launch_t<1, 128, 4, true>(a);
-    if (a.cta_group == 2) return a.out_bytes == 2 ? launch_t<2, 256, 2>(a) : launch_t<2, 256, 4>(a);
-    if (a.tile_n == 256) return a.out_bytes == 2 ? launch_t<1, 256, 2>(a) : launch_t<1, 256, 4>(a);
-    return a.out_bytes == 2 ? launch_t<1, 128, 2>(a) : launch_t<1, 128, 4>(a);
+        return GEMM_OB3((launch_t<2, 128, 1, true>(a)), (launch_t<2, 128, 2, true>(a)), (launch_t<2, 128, 4, true>(a)));
+    if (a.block_scaled)
+        return GEMM_OB3((launch_t<1, 128, 1, true>(a)), (launch_t<1, 128, 2, true>(a)), (launch_t<1, 128, 4, true>(a)));
+    if (a.cta_group == 2) return GEMM_OB3((launch_t<2, 256, 1>(a)), (launch_t<2, 256, 2>(a)), (launch_t<2, 256, 4>(a)));
+    if (a.tile_n == 256) return GEMM_OB3((launch_t<1, 256, 1>(a)), (launch_t<1, 256, 2>(a)), (launch_t<1, 256, 4>(a)));
+    return GEMM_OB3((launch_t<1, 128, 1>(a)), (launch_t<1, 128, 2>(a)), (launch_t<1, 128, 4>(a)));
 }
 
 }  // namespace gemm_sm103

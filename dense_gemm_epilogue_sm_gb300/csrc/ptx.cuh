@@ -354,6 +354,15 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Four fp32 values to four e4m3 bytes (x0 in the lowest), rounded to
+// nearest even and saturated at +-448 (cvt ... satfinite).
+__device__ __forceinline__ uint32_t pack4_e4m3(float x0, float x1, float x2, float x3) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
 // ------------------------------------------------- cluster launch control --
 // Ask the hardware to cancel the launch of one cluster that has not started
 // yet; the 16-byte response lands at `resp` and completes 16 bytes on `bar`.

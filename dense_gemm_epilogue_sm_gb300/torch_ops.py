@@ -6,6 +6,7 @@ import torch
 
 from . import (ACT_GELU, ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E4M3, F16, F32, OP_N,
                OP_T, REDUCE_ABS_MAX, REDUCE_COL_SUM, REDUCE_ROW_SUM, ROW_MAJOR, BLOCK_SCALE_MX, BLOCK_SCALE_NONE,
+               OUT_SCALE_MX, OUT_SCALE_NONE,
                gemm_check, gemm_create, gemm_destroy, gemm_get_schedule, gemm_launch_count, gemm_run, gemm_run_args,
                gemm_run_ex, gemm_set_schedule, make_desc)
 
@@ -39,7 +40,8 @@ def desc_from_spec(spec, scale_a=1.0, scale_b=1.0):
         DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_d], DTYPE_CODE[spec.dtype_d],
         spec.alpha, spec.beta, scale_a, scale_b, ACT_CODE[spec.act], BIAS_CODE[spec.bias],
         reduce_code(getattr(spec, "reduce", "none")),
-        BLOCK_SCALE_MX if getattr(spec, "block_scale", "none") == "mx" else BLOCK_SCALE_NONE)
+        BLOCK_SCALE_MX if getattr(spec, "block_scale", "none") == "mx" else BLOCK_SCALE_NONE,
+        OUT_SCALE_MX if spec.dtype_d == "e4m3" else OUT_SCALE_NONE)
 
 
 def _ptr(t):
@@ -64,12 +66,12 @@ class GemmOp:
                     _ptr(abs_max), s.cuda_stream)
 
     def run_args(self, A, B, C=None, D=None, bias=None, sfa=None, sfb=None, row_sum=None, col_sum=None,
-                 abs_max=None, stream=None):
+                 abs_max=None, sfd=None, stream=None):
         """Every buffer by name (device tensors); the call for block-scaled descriptors."""
         s = stream if stream is not None else torch.cuda.current_stream()
         gemm_run_args(self.handle, s.cuda_stream, A=_ptr(A), B=_ptr(B), C=_ptr(C), D=_ptr(D), bias=_ptr(bias),
                       sfa=_ptr(sfa), sfb=_ptr(sfb), row_sum=_ptr(row_sum), col_sum=_ptr(col_sum),
-                      abs_max=_ptr(abs_max))
+                      abs_max=_ptr(abs_max), sfd=_ptr(sfd))
 
     def check(self):
         gemm_check(self.handle)

@@ -104,6 +104,20 @@ typedef enum { GEMM_BIAS_NONE = 0, GEMM_BIAS_COL = 1, GEMM_BIAS_ROW = 2 } gemm_b
  * (stride 0) shares SFA (SFB) too. */
 typedef enum { GEMM_BLOCK_SCALE_NONE = 0, GEMM_BLOCK_SCALE_MX = 1 } gemm_block_scale_t;
 
+/* Block-scaled output ("Technical Documentation: NVIDIA/cutlass", "Blackwell
+ * SM100 GEMMs": an epilogue that writes elements plus a block scale factor
+ * per SFDVectorSize elements).  GEMM_OUT_SCALE_MX: D is e4m3 (dtype_d =
+ * GEMM_E4M3, row-major) and every 32 consecutive elements of a D row share
+ * one ue8m0 factor, written to gemm_args_t.sfd in the same basic-block
+ * layout as the input factors (rows = M, factors per row = ceil(N/32)).
+ * Factor: the OCP MX rule on the fp32 epilogue value t of the block (shared
+ * exponent floor(log2 max|t|) - 8, code clamped to [0, 254]; 255 and NaN
+ * elements for a block holding NaN or inf); elements e4m3(t / 2^(code-127))
+ * rounded to nearest even, saturated at +-448.  Needs beta = 0 and no
+ * reductions (else GEMM_ERR_UNSUPPORTED).  Only the factors of real
+ * (row, block) pairs are written. */
+typedef enum { GEMM_OUT_SCALE_NONE = 0, GEMM_OUT_SCALE_MX = 1 } gemm_out_scale_t;
+
 typedef enum {
     GEMM_SCHED_AUTO = 0,
     GEMM_SCHED_DATA_PARALLEL = 1,
@@ -126,6 +140,7 @@ typedef struct {
     int32_t bias;                                  /* gemm_bias_t; bias is fp32 */
     int32_t reduce;                                /* gemm_reduce_t flags; 0 = none */
     int32_t block_scale;                           /* gemm_block_scale_t; 0 = none */
+    int32_t out_scale;                             /* gemm_out_scale_t; 0 = none */
 } gemm_desc_t;
 
 /* How a descriptor is executed; filled by gemm_plan (host only, no GPU). */
@@ -290,6 +305,7 @@ typedef struct {
     float* row_sum;
     float* col_sum;
     float* abs_max;
+    void* sfd;                     /* output factors of a GEMM_OUT_SCALE_MX descriptor */
 } gemm_args_t;
 
 /* gemm_run with every buffer in one struct: the entry point for

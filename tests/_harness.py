@@ -24,7 +24,7 @@ MBITS = {"f32": 23, "f16": 10, "bf16": 7}
 EMIN = {"f32": -126, "f16": -14, "bf16": -126}
 # a bit pattern no correct result takes (a NaN with a payload), used to see
 # which elements the kernel wrote
-CANARY = {"f32": 0x7FC0DEAD, "f16": 0x7E5A, "bf16": 0x7FA5}
+CANARY = {"f32": 0x7FC0DEAD, "f16": 0x7E5A, "bf16": 0x7FA5, "e4m3": 0xFF}
 
 
 def ulp(x, dtype):

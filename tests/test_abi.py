@@ -173,3 +173,15 @@ def test_block_scaling_needs_e4m3_operands_and_plans_the_mx_kernel():
     assert s == g.OK and (info.cta_group, info.tile_m, info.tile_n, info.tile_k, info.stages) == (2, 256, 128, 128, 6)
     s, info = _status(_desc(M=512, N=512, K=512, dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=g.BLOCK_SCALE_MX))
     assert s == g.OK and (info.cta_group, info.tile_m, info.tile_n, info.tile_k, info.stages) == (1, 128, 128, 128, 5)
+
+
+def test_mx_output_needs_e4m3_row_major_d_without_c_or_reductions():
+    ok = _desc(dtype_d=g.E4M3, out_scale=g.OUT_SCALE_MX, ldd=512)
+    assert _status(ok)[0] == g.OK
+    assert _status(_desc(dtype_d=g.E4M3))[0] == g.ERR_UNSUPPORTED                 # e4m3 D needs factors
+    assert _status(_desc(out_scale=g.OUT_SCALE_MX))[0] == g.ERR_UNSUPPORTED      # factors need e4m3 D
+    assert _status(_desc(dtype_d=g.E4M3, out_scale=g.OUT_SCALE_MX, beta=1.0, dtype_c=g.E4M3))[0] == g.ERR_UNSUPPORTED
+    assert _status(_desc(dtype_d=g.E4M3, out_scale=g.OUT_SCALE_MX, order_d=g.COL_MAJOR, ldd=256))[0] == \
+        g.ERR_UNSUPPORTED
+    assert _status(_desc(dtype_d=g.E4M3, out_scale=g.OUT_SCALE_MX, reduce=g.REDUCE_ROW_SUM))[0] == g.ERR_UNSUPPORTED
+    assert _status(_desc(dtype_d=g.E4M3, out_scale=3))[0] == g.ERR_INVALID_ARG
