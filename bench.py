@@ -315,6 +315,11 @@ def run_ours(args):
     ex = inputs.extras or {}
     sfa_d = ex["sfa"].to(dev) if "sfa" in ex else None
     sfb_d = ex["sfb"].to(dev) if "sfb" in ex else None
+    sfd_d = None
+    if spec.dtype_d == "e4m3":        # MX output: the factor tensor beside D
+        sfk = (spec.N + 31) // 32
+        sfd_d = torch.empty(spec.batch * ((spec.M + 127) // 128) * ((sfk + 3) // 4) * 512, dtype=torch.uint8,
+                            device=dev)
     D = torch.empty(spec.batch * spec.matrix_elems("d"), dtype=wl.DT[spec.dtype_d], device=dev)
     desc = desc_from_spec(spec, inputs.scale_a, inputs.scale_b)
     info = g.gemm_plan(desc)
@@ -322,9 +327,9 @@ def run_ours(args):
 
     def launch(A, B, C, D, bias, stream, sfa=None, sfb=None):
         # block-scaled descriptors carry their scale factors through gemm_run_args
-        if spec.block_scale != "none":
+        if spec.block_scale != "none" or sfd_d is not None:
             op.run_args(A, B, C, D, bias, sfa=sfa if sfa is not None else sfa_d,
-                        sfb=sfb if sfb is not None else sfb_d, stream=stream)
+                        sfb=sfb if sfb is not None else sfb_d, sfd=sfd_d, stream=stream)
         else:
             op(A, B, C, D, bias, stream)
 
@@ -391,7 +396,7 @@ def run_ours(args):
     # end to end through the public API with host buffers: H2D of the inputs,
     # the GEMM, D2H of the result, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and spec.dtype_d != "e4m3":     # (MX output: not measured end to end)
         e2e = run_e2e(launch, spec, inputs, dev, max(1, min(args.steps, args.e2e_steps)), flops)
         op.check()
 

@@ -117,6 +117,10 @@ WORKLOADS = {
     "mxfp8_8192": Spec(
         "mxfp8_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e4m3", block_scale="mx", seed=7,
         notes="mx_float8: e4m3 data, one ue8m0 scale factor per 32 elements of K"),
+    "mxfp8_to_mxfp8_8192": Spec(
+        "mxfp8_to_mxfp8_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e4m3", block_scale="mx",
+        dtype_d="e4m3", act="relu", seed=8,
+        notes="MX in, MX out: e4m3 D with a ue8m0 factor per 32 elements of a row"),
     "odd_1000_at": Spec(
         "odd_1000_at", 1000, 1000, 1000, op_a="T", order_a="col", order_b="col", seed=4,
         notes="A transposed: stored K x M column-major, lda = K"),
