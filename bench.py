@@ -24,7 +24,7 @@ sys.path.insert(0, ROOT)
 DEFAULT_WORKLOAD = "fused_bf16_8192"
 METRIC = "GEMM TFLOP/s (2MNK/s) bf16 8192^3 and % of GB300 dense tensor peak"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-KERNEL_SOURCES = ["dense_gemm_epilogue_sm_gb300/csrc/gemm_sm103.cu", "dense_gemm_epilogue_sm_gb300/csrc/ptx.cuh",
+KERNEL_SOURCES = ["dense_gemm_epilogue_sm_gb300/csrc/gemm_kernel.cuh", "dense_gemm_epilogue_sm_gb300/csrc/ptx.cuh",
                   "dense_gemm_epilogue_sm_gb300/csrc/gemm_internal.h"]
 
 

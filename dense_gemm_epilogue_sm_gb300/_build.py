@@ -14,8 +14,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgemm_sm103.so")
-SOURCES = ["gemm_sm103.cu", "api.cpp", "layout_api.cu", "noalloc.cu", "reduce_finish.cu"]
-HEADERS = ["gemm_internal.h", "layout.hpp", "ptx.cuh"]
+SOURCES = ["gemm_ob2.cu", "gemm_ob4.cu", "gemm_ob1.cu", "gemm_sm103.cu", "api.cpp", "layout_api.cu", "noalloc.cu",
+           "reduce_finish.cu"]
+HEADERS = ["gemm_internal.h", "gemm_kernel.cuh", "gemm_variants.h", "layout.hpp", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

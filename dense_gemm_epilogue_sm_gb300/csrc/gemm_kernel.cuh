@@ -1,0 +1,1169 @@
+// gemm_kernel.cuh - persistent, warp-specialised fused-epilogue GEMM for
+// sm_103a (GB300): TMA -> shared-memory ring -> tcgen05.mma (fp32
+// accumulator in TMEM) -> TMEM loads -> fused alpha/beta/bias/ReLU -> TMA
+// store.
+//
+// Two variants share this source.  CG = 1: one CTA computes a 128 x BN tile
+// with tcgen05 cta_group::1.  CG = 2: a cluster of two CTAs computes a
+// 256 x BN tile with cta_group::2 MMAs issued by the even CTA (the leader);
+// each CTA loads its own 128 rows of A and BN/2 rows of B, the leader's
+// full[s] barrier counts both CTAs' bytes, commits are multicast to both
+// CTAs, and each CTA's epilogue reads the 128 accumulator rows in its own
+// TMEM and signals the leader's acc_empty barrier.
+//
+// Structure (the roles of "Technical Documentation: NVIDIA/cutlass",
+// "Blackwell Warp-specialized Persistent Kernel", re-split for this kernel):
+//   warp 0      one lane issues TMA loads of A and B tiles into a STAGES-deep
+//               ring; full[s] counts the bytes, empty[s] is released by the
+//               MMA's commit;
+//   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma into
+//               one of two TMEM accumulators (double buffering lets the
+//               epilogue of tile i overlap the main loop of tile i+1);
+//   warps 2..5  the epilogue: each warp owns one 32-lane TMEM quadrant
+//               (rows 32q..32q+31 of the 128-row tile), loads the source C
+//               subtile by TMA, applies the fusion in registers, stages D in
+//               swizzled shared memory and stores it by TMA.
+// The persistent loop is the static scheduler of "Blackwell Cluster Launch
+// Control", "Static Persistent Kernel": CTA b takes tiles b, b+grid, ...,
+// in a grouped raster order given as a layout (raster_full / raster_tail).
+//
+// Every mbarrier wait is bounded: on expiry the waiting thread sets the
+// kernel's status word and a shared abort flag, all roles leave their loops,
+// outstanding TMA loads are awaited (bounded), the MMA pipe is drained, and
+// TMEM is freed before the CTA exits.  Nothing traps.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemm_internal.h"
+#include "gemm_variants.h"
+#include "ptx.cuh"
+
+namespace gemm_sm103 {
+
+
+// TMEM accumulators per CTA: two, so the epilogue of one tile overlaps the
+// main loop of the next (512 columns for BN = 256).
+constexpr int kPairAccBufs = 2;
+
+// Dynamic schedule: responses of cluster launch control kept for the roles
+// that have not read them yet.
+constexpr int kClcSlots = 4;
+
+// BS: block-scaled operands (e4m3 with one ue8m0 scale factor per 32 K
+// elements).  Each stage then also holds the 512-byte scale-factor blocks of
+// its A rows and B rows, which the MMA thread copies into TMEM columns after
+// the accumulators (8 columns per stage).
+template <int CG, int BN, int OB, bool BS = false>
+struct Cfg {
+    static constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
+    static constexpr int kBRows = BN / CG;                          // rows of B this CTA loads
+    static constexpr int kStages = BS ? (CG == 2 ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
+    static constexpr int kABytes = kTileM * kStageKBytes;           // 16 KiB
+    static constexpr int kBBytes = kBRows * kStageKBytes;
+    static constexpr int kSfBytes = BS ? 2 * 512 : 0;               // scale-factor blocks of A and B
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;   // this CTA's share of a stage
+    // 64 (16-bit D), 32 (fp32 D), or 64 (e4m3 D with MX factors, stored directly)
+    static constexpr int kEpiCols = OB == 1 ? 64 : 128 / OB;
+    static constexpr int kSubtiles = BN / kEpiCols;
+    static constexpr int kSfCol0 = kAccBufs * BN;                   // first TMEM column of the scale factors
+    static constexpr int kTmemCols = BS ? 512 : kAccBufs * BN;
+    static_assert(!BS || kSfCol0 + 8 * kStages <= 512, "TMEM");
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+    // Stages are released to the producer in groups: every tcgen05.commit
+    // costs the tensor front end cycles that MMAs cannot use, so one commit
+    // frees kGroup stages.
+    static constexpr int kGroup = (kStages % 2 == 0 && kStages >= 6) ? 2 : 1;
+    static constexpr int kGroups = kStages / kGroup;
+    static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps + 1 + 2 * kClcSlots;
+    static constexpr int kSmemBytes =
+        1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kClcSlots * 16 + kNumBars * 8 + 16;
+};
+
+
+// ------------------------------------------------------------------------
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand tile
+// (tcgen05 "matrix descriptor": start address, leading- and stride-dimension
+// byte offsets, all >> 4; version 1 at bit 46; swizzle mode 2 = 128B at bits
+// 61-63).  K-major: rows of 128 bytes, 8-row groups 1024 bytes apart (SBO);
+// LBO unused.  MN-major: 128-byte rows along M/N, one row per K index;
+// 8-row K groups 1024 bytes apart (SBO), 128-byte-wide M/N chunks LBO apart.
+// ------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Bounded wait on phase `parity` of `bar`.  Gives up when another role has
+// aborted or after p.timeout_ns; on timeout records `role` in the status word
+// and raises the abort flag.  Waiting threads sleep in try_wait (suspend
+// hint) rather than re-polling: polling threads slow the barrier and tensor
+// front end that the MMA issuer depends on.
+// `peer_abort` (0 outside a CTA pair) is the peer CTA's abort flag as a
+// shared::cluster address: a timeout raises it too, so the peer stops
+// waiting for work that will not come.
+constexpr uint32_t kSleepHintNs = 200000;
+static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const KernelParams& p,
+                                      volatile uint32_t* abort_flag, uint32_t role, uint32_t peer_abort) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1u;
+            if (peer_abort) ptx::st_cluster_u32(peer_abort, 1u);
+            atomicOr(p.status, kStatusTimeout | role);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight copies
+// and MMAs before the CTA releases its resources).
+static __device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, const KernelParams& p) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            atomicOr(p.status, kStatusTimeout | kStatusRoleDrain);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int& mb, int& nb, int& l) {
+    l = tile / p.tiles_per_batch;
+    const int t = tile - l * p.tiles_per_batch;
+    const int64_t idx = t < p.raster_full_count ? p.raster_full(t)
+                                                : p.raster_tail(t - p.raster_full_count) + p.raster_tail_offset;
+    mb = (int)(idx % p.tiles_m);
+    nb = (int)(idx / p.tiles_m);
+}
+
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
+// ---------------------------------------------------------------- work ---
+// The sequence of work units (tile, K blocks [kb0, kb1)) of one worker (a CTA,
+// or a CTA pair).  Every role of the worker walks the same sequence.  First
+// the whole tiles w, w + workers, ... below dp_tiles; then the worker's range
+// of the split iterations (K blocks of the tiles from dp_tiles on, tile by
+// tile), cut at tile boundaries.  Range r goes to worker workers - 1 - r, so
+// the owner of a cut tile (the worker that ran its first K block) waits only
+// for workers of lower index, which were launched no later than itself.
+struct Sched {
+    int tile, step, dp_end, num_kb;
+    int64_t it, it_end;
+};
+
+__device__ __forceinline__ int64_t sk_range_start(int64_t sk_iters, int64_t r, int ranges) {
+    return sk_iters * r / ranges;
+}
+
+__device__ __forceinline__ Sched sched_make(const KernelParams& p, int worker, int workers) {
+    Sched s;
+    s.tile = worker;
+    s.step = workers;
+    s.dp_end = p.dp_tiles;
+    s.num_kb = p.num_kb;
+    const int64_t r = workers - 1 - worker;
+    if (r < p.sk_ranges) {
+        s.it = sk_range_start(p.sk_iters, r, p.sk_ranges);
+        s.it_end = sk_range_start(p.sk_iters, r + 1, p.sk_ranges);
+    } else {
+        s.it = s.it_end = 0;
+    }
+    return s;
+}
+
+__device__ __forceinline__ bool sched_next(Sched& s, int& tile, int& kb0, int& kb1) {
+    if (s.tile < s.dp_end) {
+        tile = s.tile;
+        kb0 = 0;
+        kb1 = s.num_kb;
+        s.tile += s.step;
+        return true;
+    }
+    if (s.it < s.it_end) {
+        const int64_t t = s.it / s.num_kb;
+        kb0 = (int)(s.it - t * s.num_kb);
+        const int64_t left = s.it_end - s.it;
+        kb1 = left < (int64_t)(s.num_kb - kb0) ? kb0 + (int)left : s.num_kb;
+        tile = s.dp_end + (int)t;
+        s.it += kb1 - kb0;
+        return true;
+    }
+    return false;
+}
+
+// Dynamic schedule ("Blackwell Cluster Launch Control": a launch holds one
+// cluster per tile; a running cluster that finishes a tile cancels the
+// launch of a cluster that has not started and takes its tile, so SMs that
+// another kernel holds do not leave their tiles behind).  The load thread of
+// the pair's leader issues one request at a time, at the start of each tile,
+// and none after a response that cancelled nothing.  The response goes to
+// slot n % kClcSlots of every CTA of the cluster; each role (load thread,
+// MMA thread, epilogue warps, in both CTAs) reads response n when it
+// finishes its n-th tile and then arrives on the leader's empty[slot], which
+// the issuer waits on before the slot's next use.
+struct Work {
+    Sched s;
+    bool dyn, producer, first;
+    uint32_t n;                   // responses read so far
+    uint32_t armed;               // requests this CTA expects (load thread only)
+    uint32_t resp0, full0, empty0;   // response slot 0 and its full / empty barriers
+    uint32_t rank;
+    int cg;
+};
+
+__device__ __forceinline__ Work work_make(const KernelParams& p, int worker, int workers, bool producer,
+                                          uint32_t resp0, uint32_t full0, uint32_t empty0, uint32_t rank, int cg) {
+    Work w;
+    w.s = sched_make(p, worker, workers);
+    w.dyn = p.clc != 0;
+    w.producer = producer;
+    w.first = true;
+    w.n = 0;
+    w.armed = 0;
+    w.resp0 = resp0;
+    w.full0 = full0;
+    w.empty0 = empty0;
+    w.rank = rank;
+    w.cg = cg;
+    return w;
+}
+
+// Request n: this CTA expects 16 bytes on full[slot]; the leader waits for
+// the slot's previous response to be read everywhere, then asks.
+static __device__ __noinline__ bool clc_request(uint32_t n, uint32_t resp0, uint32_t full0, uint32_t empty0, uint32_t rank,
+                                         int cg, const KernelParams& p, volatile uint32_t* abort_flag,
+                                         uint32_t peer_abort) {
+    const uint32_t slot = n % kClcSlots;
+    ptx::mbar_arrive_expect_tx(full0 + 8u * slot, 16);
+    if (rank != 0) return true;
+    if (n >= kClcSlots &&
+        !wait_bar(empty0 + 8u * slot, ((n / kClcSlots) - 1u) & 1u, p, abort_flag, kStatusRoleLoad, peer_abort))
+        return false;
+    if (cg == 2)
+        ptx::clc_try_cancel_mc(resp0 + 16u * slot, full0 + 8u * slot);
+    else
+        ptx::clc_try_cancel(resp0 + 16u * slot, full0 + 8u * slot);
+    return true;
+}
+
+// The next work unit of this role.  `arrive`: this thread releases the
+// response slot for its role (one thread per role and CTA).
+__device__ __forceinline__ bool work_next(Work& w, const KernelParams& p, int& tile, int& kb0, int& kb1,
+                                          volatile uint32_t* abort_flag, uint32_t role, uint32_t peer_abort,
+                                          bool arrive) {
+    if (!w.dyn) return sched_next(w.s, tile, kb0, kb1);
+    kb0 = 0;
+    kb1 = p.num_kb;
+    if (w.first) {
+        w.first = false;
+        if (*abort_flag) return false;    // the launch already failed: do no work
+        tile = w.s.tile;                  // this cluster's own tile
+        if (w.producer) {
+            w.armed = 1;
+            if (!clc_request(0, w.resp0, w.full0, w.empty0, w.rank, w.cg, p, abort_flag, peer_abort)) return false;
+        }
+        return true;
+    }
+    const uint32_t slot = w.n % kClcSlots;
+    if (!wait_bar(w.full0 + 8u * slot, (w.n / kClcSlots) & 1u, p, abort_flag, role, peer_abort)) return false;
+    uint32_t x;
+    const bool cancelled = ptx::clc_query(w.resp0 + 16u * slot, x);
+    if (arrive) {
+        if (w.rank == 0)
+            ptx::mbar_arrive(w.empty0 + 8u * slot);
+        else
+            ptx::mbar_arrive_cluster(w.empty0 + 8u * slot, 0);
+    }
+    ++w.n;
+    if (!cancelled) return false;
+    tile = (int)(x / (uint32_t)w.cg);
+    if (w.producer) {
+        w.armed = w.n + 1;
+        if (!clc_request(w.n, w.resp0, w.full0, w.empty0, w.rank, w.cg, p, abort_flag, peer_abort)) return false;
+    }
+    return true;
+}
+
+// Before the load thread leaves: a response that is still on its way must
+// land before the CTA's shared memory is released (abort paths only; a
+// normal end has read every response).
+__device__ __forceinline__ void work_drain(const Work& w, const KernelParams& p) {
+    if (!w.dyn || !w.producer || w.armed <= w.n) return;
+    const uint32_t last = w.armed - 1;
+    drain_bar(w.full0 + 8u * (last % kClcSlots), (last / kClcSlots) & 1u, p);
+}
+
+// Partial-sum slot of `worker`, CTA `rank`, epilogue warp `q`: the warp's 32
+// accumulator rows, stored so that each warp-wide 16-byte access is one
+// contiguous 512-byte run: [subtile][4-column group][lane] float4.
+template <int BN>
+__device__ __forceinline__ float4* part_slot(const KernelParams& p, int worker, int cg, uint32_t rank, int q) {
+    return reinterpret_cast<float4*>(p.sk_part) + ((size_t)(worker * cg + (int)rank) * kEpiWarps + q) * (kEpiRows * BN / 4);
+}
+
+__device__ __forceinline__ uint32_t* part_flag(const KernelParams& p, int worker, int cg, uint32_t rank, int q) {
+    return p.sk_flags + ((size_t)(worker * cg + (int)rank) * kEpiWarps + q);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* a) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(uint32_t* a, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// Bounded wait (all lanes of a warp) for another worker's partial sum.
+static __device__ __noinline__ bool wait_part(const uint32_t* flag, const KernelParams& p, volatile uint32_t* abort_flag,
+                                       uint32_t peer_abort) {
+    if (ld_acquire(flag)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        __nanosleep(256);
+        if (ld_acquire(flag)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1u;
+            if (peer_abort) ptx::st_cluster_u32(peer_abort, 1u);
+            atomicOr(p.status, kStatusTimeout | kStatusRoleFixup);
+            return false;
+        }
+    }
+}
+
+// Column sums of one 16-byte chunk over the warp's 32 rows: lane i holds
+// row i's V values.  Halving exchanges (lanes 16, 8, ... apart) leave each
+// lane the sum of one column over the lanes that share its high bits; the
+// remaining steps sum across the rest.  Returns that column sum; `j` is its
+// column within the chunk.  Lanes whose low log2(32/V) bits are zero hold
+// distinct columns.  Fixed order: the sums are the same on every run.
+template <int V>
+__device__ __forceinline__ float chunk_col_sum(float (&r)[V], int lane, int& j) {
+    j = 0;
+    int off = 16;
+#pragma unroll
+    for (int width = V; width > 1; width >>= 1, off >>= 1) {
+        const bool hi = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < width / 2; ++i) {
+            const float send = hi ? r[i] : r[width / 2 + i];
+            const float keep = hi ? r[width / 2 + i] : r[i];
+            r[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+        if (hi) j += width / 2;
+    }
+#pragma unroll
+    for (; off >= 1; off >>= 1) r[0] += __shfl_xor_sync(0xffffffffu, r[0], off);
+    return r[0];
+}
+
+__device__ __forceinline__ void unpack2(uint32_t w, bool f16, float& lo, float& hi) {
+    if (f16) {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w);
+        const float2 f = __half22float2(h);
+        lo = f.x;
+        hi = f.y;
+    } else {
+        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w);
+        const float2 f = __bfloat1622float2(h);
+        lo = f.x;
+        hi = f.y;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
+    uint32_t w;
+    if (f16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        w = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        w = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return w;
+}
+
+// tcgen05 instruction descriptor (kind::f16 / kind::f8f6f4, dense): D fp32
+// (bits 4-5 = 1), A and B type (bits 7-9, 10-12: f16 0 / bf16 1 for kind::f16,
+// e4m3 0 for kind::f8f6f4), A / B MN-major (bits 15, 16), N >> 3 (bits
+// 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_for(int cg, int bn, bool f8, uint32_t bf16, uint32_t a_mn,
+                                                 uint32_t b_mn) {
+    return (1u << 4) | ((f8 ? 0u : bf16) << 7) | ((f8 ? 0u : bf16) << 10) | (a_mn << 15) | (b_mn << 16) |
+           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)((128 * cg) >> 4) << 24);
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: scale-factor
+// byte of B (bits 4-5), A and B e4m3 (type 0, bits 7-9, 10-12), A / B
+// MN-major (15, 16), N >> 3 (17-22), ue8m0 scale factors (bit 23), M >> 4
+// (24-28), scale-factor byte of A (29-30).  The bytes select which of the
+// four factors in a TMEM word (four 32-element K blocks) an MMA uses.
+__host__ __device__ constexpr uint32_t idesc_mx(int cg, int bn, uint32_t a_mn, uint32_t b_mn, uint32_t sf_byte) {
+    return (sf_byte << 4) | (a_mn << 15) | (b_mn << 16) | ((uint32_t)(bn >> 3) << 17) | (1u << 23) |
+           ((uint32_t)((128 * cg) >> 4) << 24) | (sf_byte << 29);
+}
+
+// Shared-memory descriptor of a 512-byte scale-factor block read as 32 rows
+// of 16 bytes, no swizzle: 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t sf_desc(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// What the MMA issuer needs from the kernel.
+template <int CG, int BN, int S>
+struct MmaCtx {
+    const KernelParams& p;
+    uint32_t ring;          // shared address of stage 0
+    uint32_t a_bytes;       // A tile bytes at the front of a stage
+    uint32_t stage_bytes;
+    uint32_t bar0;          // barrier block
+    uint32_t tmem_base;
+    int first_tile, tile_step;
+    volatile uint32_t* abort_flag;
+    uint32_t peer_abort;
+    uint32_t resp0, clc_full0, clc_empty0;   // dynamic schedule ring
+};
+
+// The MMA issuer (one thread of the pair leader).  A tcgen05.mma blocks its
+// issuing thread until the tensor core takes it (the queue is about one
+// instruction deep), so any work between two MMAs is tensor-pipe idle time:
+// the loop asks for the next stage's barrier while the current stage's MMAs
+// issue, builds descriptors by adding offsets to a precomputed base, and
+// carries the instruction descriptor as an immediate.
+//
+// Every scalar the loop reads is copied into a register first.  The tcgen05
+// and mbarrier wrappers clobber "memory", so a value read through `m` or `p`
+// (local and kernel-parameter memory behind a reference) would be re-loaded
+// after every MMA, a chain of dependent loads between two MMAs.
+//
+// BS: block-scaled MMAs.  Each stage's two scale-factor blocks are copied
+// into TMEM (8 columns per stage after the accumulators) ahead of the
+// stage's four MMAs; tcgen05.cp and tcgen05.mma of one thread run in issue
+// order, so a copy never overtakes the MMAs that still read the columns it
+// overwrites one lap later.  MMA j reads factor byte j of each word.
+template <int CG, int BN, int S, int G, bool F8, uint32_t IDESC, bool BS = false>
+__device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
+    const KernelParams& p = m.p;                 // slow paths (wait_bar) only
+    const int first_tile = m.first_tile, tile_step = m.tile_step;
+    const uint32_t bar0 = m.bar0, ring = m.ring, a_bytes = m.a_bytes, stage_bytes = m.stage_bytes;
+    const uint32_t tmem_base = m.tmem_base, peer_abort = m.peer_abort;
+    volatile uint32_t* const abort_flag = m.abort_flag;
+    constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
+    auto full_bar = [=](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [=](int s) { return bar0 + 8u * (S + s); };
+    auto accf_bar = [=](int b) { return bar0 + 8u * (2 * S + b); };
+    auto acce_bar = [=](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+    const uint32_t drain = bar0 + 8u * (2 * S + 4 + 2 * kEpiWarps);
+    constexpr bool a_mn = (IDESC >> 15) & 1u, b_mn = (IDESC >> 16) & 1u;
+    constexpr int eb = F8 ? 1 : 2;
+    constexpr int kel = kStageKBytes / eb;
+    // per-K-step advance of the descriptors' start address, in 16-byte units
+    constexpr uint32_t a_step = (a_mn ? (kKStepBytes / eb) * 128u : kKStepBytes) >> 4;
+    constexpr uint32_t b_step = (b_mn ? (kKStepBytes / eb) * 128u : kKStepBytes) >> 4;
+    // shared addresses stay below 2^18, so offsets added to the 14-bit
+    // start-address field never carry into the other fields
+    const uint64_t a_base = smem_desc(ring, a_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
+    const uint64_t b_base = smem_desc(ring + a_bytes, b_mn ? (uint32_t)(kel * 128) : 16u, 1024u);
+    // One commit releases a whole group of G stages (empty[] is indexed by
+    // group); the commit covers every earlier MMA of this thread.
+    auto release = [=](int g) {
+        if constexpr (CG == 2)
+            ptx::mma_commit_mc(empty_bar(g), 0x3);
+        else
+            ptx::mma_commit(empty_bar(g));
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool issued = false;
+    bool ready = ptx::mbar_test_wait(full_bar(0), 0);
+    Work wk = work_make(p, first_tile, tile_step, false, m.resp0, m.clc_full0, m.clc_empty0, 0u, CG);
+    int tile, kb0, kb1;
+    for (; work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleMma, peer_abort, true); ++it) {
+        const int buf = it % kAccBufs;
+        const uint32_t acc_par = (uint32_t)(it / kAccBufs) & 1u;
+        if (!wait_bar(acce_bar(buf), acc_par ^ 1u, p, abort_flag, kStatusRoleMma, peer_abort)) break;
+        ptx::tc_fence_after();   // the epilogue's reads of this accumulator come first
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        bool stop = false;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (!ready && !wait_bar(full_bar(stage), phase, p, abort_flag, kStatusRoleMma, peer_abort)) {
+                stop = true;
+                break;
+            }
+            const int next = stage + 1 == S ? 0 : stage + 1;
+            const uint32_t next_phase = stage + 1 == S ? phase ^ 1u : phase;
+            const uint64_t soff = (uint64_t)((stage * stage_bytes) >> 4);
+            const uint64_t ad = a_base + soff, bd = b_base + soff;
+            const uint32_t first = kb != kb0;
+            if constexpr (BS) {
+                constexpr uint32_t kSfCol0 = (uint32_t)(kAccBufs * BN);
+                const uint32_t sfs = ring + (uint32_t)stage * stage_bytes + stage_bytes - 1024u;
+                const uint32_t sfa = tmem_base + kSfCol0 + 8u * (uint32_t)stage, sfb = sfa + 4u;
+                ptx::tmem_cp_32x128b_x4<CG>(sfa, sf_desc(sfs));
+                ptx::tmem_cp_32x128b_x4<CG>(sfb, sf_desc(sfs + 512u));
+                ptx::mma_mx<CG, IDESC>(d_tmem, ad, bd, sfa, sfb, first);
+                ready = ptx::mbar_test_wait(full_bar(next), next_phase);
+                ptx::mma_mx<CG, IDESC | (1u << 4) | (1u << 29)>(d_tmem, ad + a_step, bd + b_step, sfa, sfb, 1u);
+                ptx::mma_mx<CG, IDESC | (2u << 4) | (2u << 29)>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, sfa, sfb, 1u);
+                ptx::mma_mx<CG, IDESC | (3u << 4) | (3u << 29)>(d_tmem, ad + 3 * a_step, bd + 3 * b_step, sfa, sfb, 1u);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kStageKBytes / kKStepBytes; ++j) {
+                    ptx::mma_imm<CG, F8, IDESC>(d_tmem, ad + j * a_step, bd + j * b_step, j ? 1u : first);
+                    if (j == 0) ready = ptx::mbar_test_wait(full_bar(next), next_phase);
+                }
+            }
+            issued = true;
+            if (stage % G == G - 1) release(stage / G);   // the group's last stage
+            stage = next;
+            phase = next_phase;
+        }
+        if (stop) break;
+        if (kb1 > kb0) {                         // accumulator complete
+            if constexpr (CG == 2)
+                ptx::mma_commit_mc(accf_bar(buf), 0x3);
+            else
+                ptx::mma_commit(accf_bar(buf));
+        } else {                                  // K == 0: nothing accumulated
+            ptx::mbar_arrive(accf_bar(buf));
+            if constexpr (CG == 2) ptx::mbar_arrive_cluster(accf_bar(buf), 1);
+        }
+    }
+    // A group left partly issued is released too, so a producer waiting to
+    // drain its copies is not left waiting.
+    if (issued && stage % G != 0) release(stage / G);
+    // Drain: every MMA issued above must finish before TMEM is freed.
+    if (issued) {
+        if constexpr (CG == 2)
+            ptx::mma_commit_cg2(drain);
+        else
+            ptx::mma_commit(drain);
+        drain_bar(drain, 0, p);
+    }
+}
+
+template <int CG, int BN, int OB, bool BS = false>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                const __grid_constant__ KernelParams p) {
+    using C = Cfg<CG, BN, OB, BS>;
+    constexpr int S = C::kStages;
+    constexpr int kTileRows = kTileM * CG;               // output rows per tile
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = smem;
+    uint8_t* epi = ring + C::kRingBytes;
+    uint8_t* clc_resp = epi + C::kEpiBytes;             // kClcSlots x 16 bytes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(clc_resp + kClcSlots * 16);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+    auto cfull_bar = [&](int i) { return bar0 + 8u * (2 * S + 4 + i); };
+    const uint32_t drain = bar0 + 8u * (2 * S + 4 + 2 * kEpiWarps);
+    const uint32_t clc_full0 = drain + 8u, clc_empty0 = drain + 8u * (1 + kClcSlots);
+    const uint32_t resp0 = ptx::smem_addr(clc_resp);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // CTA pair bookkeeping (CG == 2): rank 0 is the leader that issues MMAs.
+    const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;
+    const int first_tile = CG == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int tile_step = CG == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const uint32_t peer_abort = CG == 2 ? ptx::mapa(ptx::smem_addr(tmem_slot + 1), rank ^ 1u) : 0u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(accf_bar(b), 1);
+            ptx::mbar_init(acce_bar(b), kEpiWarps * CG);   // every epilogue warp of the pair
+        }
+        for (int i = 0; i < 2 * kEpiWarps; ++i) ptx::mbar_init(cfull_bar(i), 1);
+        ptx::mbar_init(drain, 1);
+        // A dynamic launch starts clusters that nobody cancelled once others
+        // leave; after a recorded error they do no work (no chain of timeouts).
+        *abort_flag = p.clc && *reinterpret_cast<volatile uint32_t*>(p.status) != 0u ? 1u : 0u;
+        for (int i = 0; i < kClcSlots; ++i) {
+            ptx::mbar_init(clc_full0 + 8u * i, 1);
+            // readers of a response: load thread, MMA thread (leader) and the
+            // four epilogue warps of each CTA
+            ptx::mbar_init(clc_empty0 + 8u * i, CG == 2 ? 2 * (1 + kEpiWarps) + 1 : 2 + kEpiWarps);
+        }
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmD);
+        if (p.has_c) ptx::prefetch_tensormap(&tmC);
+        if constexpr (BS) {
+            ptx::prefetch_tensormap(&tmSA);
+            ptx::prefetch_tensormap(&tmSB);
+        }
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), C::kTmemCols);
+        ptx::tmem_relinquish<CG>();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if constexpr (CG == 2) ptx::cluster_sync();   // the peer's barriers exist before anyone signals them
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA loads --
+        if (lane == 0) {
+            const int eb = p.elem_bytes;
+            const int kel = kStageKBytes / eb;          // K elements per stage
+            const int mn_box = kStageKBytes / eb;       // M/N elements per 128-byte row (MN-major)
+            // Latest fill of each stage (single CTA: drained on full[s]) or of
+            // each release group (pair: drained on empty[g], which a later
+            // fill of any stage of the group moves on).
+            // (bit masks, so they stay in registers)
+            uint32_t pend = 0u, pend_parity = 0u;
+            auto pend_slot = [&](int st) { return CG == 2 ? st / C::kGroup : st; };
+            int stage = 0;
+            uint32_t phase = 0;
+            bool skip_first = p.inject != 0 && rank == 0;
+            Work wk = work_make(p, first_tile, tile_step, true, resp0, clc_full0, clc_empty0, rank, CG);
+            int tile, kb0, kb1;
+            while (work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleLoad, peer_abort, true)) {
+                int mb, nb, l;
+                tile_coords(p, tile, mb, nb, l);
+                const int la = p.a_batched ? l : 0, lb = p.b_batched ? l : 0;
+                const int m0 = mb * kTileRows + (int)rank * kTileM;
+                const int n0 = nb * BN + (int)rank * C::kBRows;
+                bool stop = false;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    // a group of stages is released together: wait at its first stage
+                    if (stage % C::kGroup == 0 &&
+                        !wait_bar(empty_bar(stage / C::kGroup), phase ^ 1u, p, abort_flag, kStatusRoleLoad, peer_abort)) {
+                        stop = true;
+                        break;
+                    }
+                    if (skip_first) {
+                        skip_first = false;       // test hook: this stage is never filled
+                    } else {
+                        // the pair's leader counts both CTAs' bytes
+                        const uint32_t fb = CG == 2 ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes * CG);
+                        const uint32_t sa = ptx::smem_addr(ring + stage * C::kStageBytes);
+                        const uint32_t sb = sa + C::kABytes;
+                        const int k0 = kb * kel;
+                        auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
+                            if constexpr (CG == 2)
+                                ptx::tma_load_3d_cg2(dst, map, c0, c1, c2, fb);
+                            else
+                                ptx::tma_load_3d(dst, map, c0, c1, c2, fb);
+                        };
+                        if (p.a_kmajor) {
+                            load(sa, &tmA, k0, m0, la);
+                        } else {
+                            for (int c = 0; c < kTileM / mn_box; ++c) load(sa + c * (kel * 128), &tmA, m0 + c * mn_box, k0, la);
+                        }
+                        if (p.b_kmajor) {
+                            load(sb, &tmB, k0, n0, lb);
+                        } else {
+                            for (int c = 0; c < C::kBRows / mn_box; ++c)
+                                load(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb);
+                        }
+                        if constexpr (BS) {
+                            // One 512-byte scale-factor block per 128 rows and K stage:
+                            // block (rows / 128) * num_kb + kb of the batch's tensor, read
+                            // as 32 rows of 16 bytes.  Each CTA takes its own A rows'
+                            // block and the block of the tile's whole N range.
+                            const uint32_t sf = sb + C::kBBytes;
+                            const int blk_a = (la * p.sf_mblocks + m0 / 128) * p.num_kb + kb;
+                            const int blk_b = (lb * p.sf_nblocks + nb * BN / 128) * p.num_kb + kb;
+                            load(sf, &tmSA, 0, blk_a * 32, 0);
+                            load(sf + 512, &tmSB, 0, blk_b * 32, 0);
+                        }
+                        const uint32_t bit = 1u << pend_slot(stage);
+                        pend |= bit;
+                        pend_parity = phase ? (pend_parity | bit) : (pend_parity & ~bit);
+                    }
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (stop) break;
+            }
+            // Every issued copy must land before the CTA may exit.  In a pair
+            // the copies complete on the leader's barrier, so each CTA waits
+            // for the MMA to have consumed its stages instead.
+            for (int s = 0; s < S; ++s)
+                if ((pend >> s) & 1u) {
+                    const uint32_t par = (pend_parity >> s) & 1u;
+                    bool ok_drain;
+                    if constexpr (CG == 2)
+                        ok_drain = drain_bar(empty_bar(s), par, p);   // s indexes a group here
+                    else
+                        ok_drain = drain_bar(full_bar(s), par, p);
+                    if (!ok_drain) break;   // already past the time bound: stop waiting
+                }
+            work_drain(wk, p);
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA -----
+        if (lane == 0 && rank == 0) {
+            MmaCtx<CG, BN, S> m{p,          ptx::smem_addr(ring), C::kABytes, C::kStageBytes, bar0,
+                                tmem_base,  first_tile,           tile_step,   abort_flag,       peer_abort,
+                                resp0,      clc_full0,            clc_empty0};
+            if constexpr (BS) {
+                switch (p.mma_variant & 3) {     // A / B MN-major
+#define GEMM_MX_CASE(v)                                                                      \
+    case v:                                                                                  \
+        mma_role<CG, BN, S, C::kGroup, true, idesc_mx(CG, BN, ((v) >> 1) & 1, (v) & 1, 0), true>(m); \
+        break;
+                    GEMM_MX_CASE(0) GEMM_MX_CASE(1) GEMM_MX_CASE(2) GEMM_MX_CASE(3)
+#undef GEMM_MX_CASE
+                    default: break;
+                }
+            } else {
+                switch (p.mma_variant) {     // one loop per tcgen05 instruction descriptor
+#define GEMM_MMA_CASE(v)                                                         \
+    case v:                                                                      \
+        mma_role<CG, BN, S, C::kGroup, (v) >= 8, idesc_for(CG, BN, (v) >= 8, ((v) >> 2) & 1, \
+                                               ((v) >> 1) & 1, (v) & 1)>(m);     \
+        break;
+                    GEMM_MMA_CASE(0) GEMM_MMA_CASE(1) GEMM_MMA_CASE(2) GEMM_MMA_CASE(3)
+                    GEMM_MMA_CASE(4) GEMM_MMA_CASE(5) GEMM_MMA_CASE(6) GEMM_MMA_CASE(7)
+                    GEMM_MMA_CASE(8) GEMM_MMA_CASE(9) GEMM_MMA_CASE(10) GEMM_MMA_CASE(11)
+#undef GEMM_MMA_CASE
+                    default: break;
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue -----
+        constexpr int VPC = 16 / OB;                    // output values per 16-byte chunk
+        const int ew = warp - 2;                        // staging-buffer owner
+        const int q = warp & 3;                         // TMEM lane quadrant this warp may read
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const bool f16_out = p.out_f16 != 0;
+        // Compiled twice: EXT adds GELU and the reductions, so the plain
+        // epilogue carries none of their code.
+        auto epilogue = [&](auto ext_tag) {
+            constexpr bool EXT = decltype(ext_tag)::value;
+            [[maybe_unused]] uint32_t c_phase[2] = {0u, 0u};
+            [[maybe_unused]] int sub_count = 0;
+            int it = 0;
+            bool ok = true;
+            const int workers = tile_step;
+            // this warp's 32 rows of accumulator `b`, columns [32*..)
+            auto load_acc = [&](int b, int sub, uint32_t (&acc)[C::kEpiCols]) {
+                const uint32_t taddr = tmem_base + lane_off + (uint32_t)(b * BN + sub * C::kEpiCols);
+                ptx::tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
+                if constexpr (C::kEpiCols == 64)
+                    ptx::tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
+                ptx::tmem_ld_wait();
+            };
+            // This warp is done reading accumulator `b`: tell the MMA issuer.
+            auto release_acc = [&](int b) {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CG == 2) {
+                        if (rank == 0)
+                            ptx::mbar_arrive(acce_bar(b));
+                        else
+                            ptx::mbar_arrive_cluster(acce_bar(b), 0);
+                    } else {
+                        ptx::mbar_arrive(acce_bar(b));
+                    }
+                }
+            };
+            // The workers whose stream-K ranges hold the later K blocks of a cut
+            // tile: ranges r_next, r_next + 1, ... that start before t_end.
+            auto for_each_part = [&](int64_t r_next, int64_t t_end, auto&& fn) {
+                for (int64_t j = r_next; j < p.sk_ranges; ++j) {
+                    const int64_t js = sk_range_start(p.sk_iters, j, p.sk_ranges);
+                    if (js >= t_end) break;
+                    if (sk_range_start(p.sk_iters, j + 1, p.sk_ranges) == js) continue;     // empty range
+                    if (!fn(workers - 1 - (int)j)) return false;
+                }
+                return true;
+            };
+            Work wk = work_make(p, first_tile, tile_step, false, resp0, clc_full0, clc_empty0, rank, CG);
+            int tile, kb0, kb1;
+            for (; ok; ++it) {
+                if (!__all_sync(0xffffffffu, work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleEpi, peer_abort,
+                                                       lane == 0)))
+                    break;
+                const int buf = it % C::kAccBufs;
+                const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
+                int mb, nb, l;
+                tile_coords(p, tile, mb, nb, l);
+                ok = __all_sync(0xffffffffu, wait_bar(accf_bar(buf), acc_par, p, abort_flag, kStatusRoleEpi, peer_abort));
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if (kb0 > 0) {
+                    // Stream-K: this tile's first K blocks belong to another worker,
+                    // its owner, which finishes the tile; hand it the raw sums.
+                    float4* slot = part_slot<BN>(p, first_tile, CG, rank, q) + lane;
+    #pragma unroll 1
+                    for (int sub = 0; sub < C::kSubtiles; ++sub) {
+                        uint32_t acc[C::kEpiCols];
+                        load_acc(buf, sub, acc);
+    #pragma unroll
+                        for (int c = 0; c < C::kEpiCols / 4; ++c)
+                            __stcg(slot + (sub * (C::kEpiCols / 4) + c) * 32,
+                                   make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
+                                               __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3])));
+                    }
+                    release_acc(buf);
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) st_release(part_flag(p, first_tile, CG, rank, q), 1u);
+                    continue;
+                }
+                // A tile cut short (kb1 < num_kb, stream-K region only): its later
+                // K blocks come from the next workers' partial sums.
+                const bool cut = kb1 < p.num_kb;
+                const int64_t t_end = cut ? (int64_t)(tile - p.dp_tiles + 1) * p.num_kb : 0;
+                const int64_t r_next = workers - first_tile;        // this worker's range index + 1
+                if (cut) {
+                    ok = for_each_part(r_next, t_end, [&](int w) {
+                        return wait_part(part_flag(p, w, CG, rank, q), p, abort_flag, peer_abort);
+                    });
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
+                [[maybe_unused]] const bool reducing = EXT && (p.red_rows | p.red_cols | p.red_amax) != 0;
+                float row_acc = 0.f;          // sum of t over this tile's columns of row `row`
+                uint32_t amax_bits = 0u;      // max |t| as fp32 bits (NaN sorts above inf)
+                const int row0 = mb * kTileRows + (int)rank * kTileM + q * kEpiRows;
+                const int row = row0 + lane;
+                float row_bias = 0.f;
+                if (p.bias_mode == 2 && row < p.M) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
+                const float* bias_l = p.bias_mode == 1 ? p.bias + (int64_t)l * p.bias_stride : nullptr;
+                [[maybe_unused]] const int lc = p.c_batched ? l : 0;
+    #pragma unroll 1
+                for (int sub = 0; sub < C::kSubtiles; ++sub) {
+                    const int col0 = nb * BN + sub * C::kEpiCols;
+                    if (row0 >= p.M || col0 >= p.N) continue;     // nothing of this subtile is in range
+                    if constexpr (OB == 1) {
+                        // MX output: e4m3 elements and one ue8m0 factor per 32
+                        // columns of a row (no C; checked on the host).
+                        uint32_t acc[C::kEpiCols];
+                        if (p.num_kb > 0) {
+                            load_acc(buf, sub, acc);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
+                        }
+                        if (cut) {
+                            for_each_part(r_next, t_end, [&](int w) {
+                                const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
+#pragma unroll
+                                for (int c = 0; c < C::kEpiCols / 4; ++c) {
+                                    const float4 v4 = __ldcg(ps + c * 32);
+                                    acc[4 * c] = __float_as_uint(__uint_as_float(acc[4 * c]) + v4.x);
+                                    acc[4 * c + 1] = __float_as_uint(__uint_as_float(acc[4 * c + 1]) + v4.y);
+                                    acc[4 * c + 2] = __float_as_uint(__uint_as_float(acc[4 * c + 2]) + v4.z);
+                                    acc[4 * c + 3] = __float_as_uint(__uint_as_float(acc[4 * c + 3]) + v4.w);
+                                }
+                                return true;
+                            });
+                        }
+#pragma unroll
+                        for (int h = 0; h < C::kEpiCols / 32; ++h) {
+                            const int c0 = col0 + h * 32;
+                            if (c0 >= p.N) break;                 // the block lies past the row's end
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                float x = p.alpha * __uint_as_float(acc[h * 32 + i]);
+                                if (p.bias_mode == 1)
+                                    x += (c0 + i < p.N) ? __ldg(bias_l + c0 + i) : 0.f;
+                                else if (p.bias_mode == 2)
+                                    x += row_bias;
+                                if (p.act == 1)
+                                    x = fmaxf(x, 0.f);
+                                else if (EXT && p.act == 2)
+                                    x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+                                v[i] = (c0 + i < p.N) ? x : 0.f;   // columns past N join no block
+                            }
+                            // factor: the OCP MX shared exponent floor(log2 amax) - 8,
+                            // read off amax's biased fp32 exponent; 255 for NaN / inf
+                            uint32_t amax = 0u;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(fabsf(v[i])));
+                            const int be = (int)(amax >> 23);
+                            const uint32_t code = amax >= 0x7F800000u ? 255u : (be > 8 ? (uint32_t)(be - 8) : 0u);
+                            const float sc = __uint_as_float((254u - (code > 254u ? 254u : code)) << 23);   // 2^(127-code)
+                            uint32_t w[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                w[k] = code == 255u ? 0x7F7F7F7Fu
+                                                    : ptx::pack4_e4m3(v[4 * k] * sc, v[4 * k + 1] * sc, v[4 * k + 2] * sc,
+                                                                      v[4 * k + 3] * sc);
+                            if (row < p.M) {
+                                uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)l * p.d_bstride +
+                                                (int64_t)row * p.ldd;
+                                if (c0 + 32 <= p.N) {
+                                    *reinterpret_cast<uint4*>(drow + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+                                    *reinterpret_cast<uint4*>(drow + c0 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                                } else {
+                                    for (int i = 0; i < 32 && c0 + i < p.N; ++i)
+                                        drow[c0 + i] = (uint8_t)(w[i >> 2] >> ((i & 3) * 8));
+                                }
+                                const int f = c0 / 32;
+                                p.sfd[(int64_t)l * p.sfd_bstride + ((int64_t)(row / 128) * p.sfd_kb4 + f / 4) * 512 +
+                                      (row % 32) * 16 + ((row % 128) / 32) * 4 + f % 4] = (uint8_t)code;
+                            }
+                        }
+                    } else {
+                        // the subtile holding a ragged row end is stored element by element
+                        const bool direct = p.d_ragged && col0 + C::kEpiCols > p.N;
+                        const int sbi = sub_count & 1;
+                        ++sub_count;
+                        uint8_t* sbuf = epi + (ew * 2 + sbi) * kEpiBufBytes;
+                        const uint32_t sbuf_a = ptx::smem_addr(sbuf);
+                        if (lane == 0) ptx::bulk_wait_read<1>();       // the store that last used sbuf has read it
+                        __syncwarp();
+                        if (p.has_c) {
+                            const uint32_t cb = cfull_bar(ew * 2 + sbi);
+                            if (lane == 0) {
+                                ptx::mbar_arrive_expect_tx(cb, kEpiBufBytes);
+                                ptx::tma_load_3d(sbuf_a, &tmC, col0, row0, lc, cb);
+                            }
+                            ok = __all_sync(0xffffffffu, wait_bar(cb, c_phase[sbi], p, abort_flag, kStatusRoleEpi, peer_abort));
+                            c_phase[sbi] ^= 1u;
+                            if (!ok) break;
+                        }
+                        uint32_t acc[C::kEpiCols];
+                        if (p.num_kb > 0) {
+                            load_acc(buf, sub, acc);
+                        } else {
+        #pragma unroll
+                            for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
+                        }
+                        if (cut) {
+                            for_each_part(r_next, t_end, [&](int w) {
+                                const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
+        #pragma unroll
+                                for (int c = 0; c < C::kEpiCols / 4; ++c) {
+                                    const float4 v4 = __ldcg(ps + c * 32);
+                                    acc[4 * c] = __float_as_uint(__uint_as_float(acc[4 * c]) + v4.x);
+                                    acc[4 * c + 1] = __float_as_uint(__uint_as_float(acc[4 * c + 1]) + v4.y);
+                                    acc[4 * c + 2] = __float_as_uint(__uint_as_float(acc[4 * c + 2]) + v4.z);
+                                    acc[4 * c + 3] = __float_as_uint(__uint_as_float(acc[4 * c + 3]) + v4.w);
+                                }
+                                return true;
+                            });
+                        }
+                        // Row `lane` of the 32-row slab; 128-byte rows, 16-byte chunk c
+                        // stored at chunk c ^ (row % 8) (the TMA 128B swizzle).
+                        uint8_t* row_base = sbuf + lane * 128;
+        #pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            uint4* slot = reinterpret_cast<uint4*>(row_base + ((ch ^ (lane & 7)) << 4));
+                            float v[VPC];
+        #pragma unroll
+                            for (int i = 0; i < VPC; ++i) v[i] = p.alpha * __uint_as_float(acc[ch * VPC + i]);
+                            if (p.has_c) {
+                                const uint4 craw = *slot;
+                                const uint32_t w[4] = {craw.x, craw.y, craw.z, craw.w};
+                                if constexpr (OB == 4) {
+        #pragma unroll
+                                    for (int i = 0; i < 4; ++i) v[i] = fmaf(p.beta, __uint_as_float(w[i]), v[i]);
+                                } else {
+        #pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        float lo, hi;
+                                        unpack2(w[i], f16_out, lo, hi);
+                                        v[2 * i] = fmaf(p.beta, lo, v[2 * i]);
+                                        v[2 * i + 1] = fmaf(p.beta, hi, v[2 * i + 1]);
+                                    }
+                                }
+                            }
+                            if (p.bias_mode == 1) {
+                                const int cb0 = col0 + ch * VPC;
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) v[i] += (cb0 + i < p.N) ? __ldg(bias_l + cb0 + i) : 0.f;
+                            } else if (p.bias_mode == 2) {
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) v[i] += row_bias;
+                            }
+                            if (p.act == 1) {
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) v[i] = fmaxf(v[i], 0.f);
+                            } else if (EXT && p.act == 2) {
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) v[i] = 0.5f * v[i] * (1.f + erff(v[i] * 0.70710678118654752f));
+                            }
+                            if (reducing) {
+                                // elements outside D count as 0
+                                const int c0 = col0 + ch * VPC;
+                                float r[VPC];
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) r[i] = (row < p.M && c0 + i < p.N) ? v[i] : 0.f;
+                                if (p.red_rows) {
+        #pragma unroll
+                                    for (int i = 0; i < VPC; ++i) row_acc += r[i];
+                                }
+                                if (p.red_amax) {
+        #pragma unroll
+                                    for (int i = 0; i < VPC; ++i) amax_bits = max(amax_bits, __float_as_uint(fabsf(r[i])));
+                                }
+                                if (p.red_cols) {
+                                    int j;
+                                    const float cs = chunk_col_sum<VPC>(r, lane, j);
+                                    if ((lane & (32 / VPC - 1)) == 0 && c0 + j < p.N)
+                                        p.red_col_ws[((int64_t)l * ((p.M + 31) / 32) + row0 / 32) * p.N + c0 + j] = cs;
+                                }
+                            }
+                            uint4 out;
+                            if constexpr (OB == 4) {
+                                out = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                                                 __float_as_uint(v[3]));
+                            } else {
+                                out = make_uint4(pack2(v[0], v[1], f16_out), pack2(v[2], v[3], f16_out),
+                                                 pack2(v[4], v[5], f16_out), pack2(v[6], v[7], f16_out));
+                            }
+                            if (!direct) {
+                                *slot = out;
+                            } else if (row < p.M) {
+                                const int c0 = col0 + ch * VPC;
+                                const uint32_t w[4] = {out.x, out.y, out.z, out.w};
+                                uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
+                                                ((int64_t)l * p.d_bstride + (int64_t)row * p.ldd) * OB;
+        #pragma unroll
+                                for (int i = 0; i < VPC; ++i) {
+                                    if (c0 + i >= p.N) break;
+                                    if constexpr (OB == 4)
+                                        *reinterpret_cast<uint32_t*>(drow + (int64_t)(c0 + i) * 4) = w[i];
+                                    else
+                                        *reinterpret_cast<uint16_t*>(drow + (int64_t)(c0 + i) * 2) =
+                                            (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
+                                }
+                            }
+                        }
+                        if (!direct) {
+                            ptx::fence_async_shared();
+                            __syncwarp();
+                            if (lane == 0) {
+                                ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, l);
+                                ptx::bulk_commit();
+                            }
+                        }
+                    }
+                }
+                if (!ok) break;
+                release_acc(buf);
+                if (EXT && p.red_rows && row < p.M) p.red_row_ws[((int64_t)l * p.tiles_n + nb) * p.M + row] = row_acc;
+                if (EXT && p.red_amax) {
+    #pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1)
+                        amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, off));
+                    if (lane == 0 && amax_bits) atomicMax(p.red_amax_ws + l, amax_bits);
+                }
+                // the partial sums are consumed: clear their flags for the next launch
+                if (cut && lane == 0)
+                    for_each_part(r_next, t_end, [&](int w) {
+                        *part_flag(p, w, CG, rank, q) = 0u;
+                        return true;
+                    });
+            }
+        };
+        if (p.act == 2 || p.red_rows || p.red_cols || p.red_amax)
+            epilogue(BoolTag<true>{});
+        else
+            epilogue(BoolTag<false>{});
+        if (lane == 0) ptx::bulk_wait<0>();
+        ptx::tc_fence_before();
+    }
+
+    __syncthreads();
+    if constexpr (CG == 2) ptx::cluster_sync();   // no CTA leaves while its peer may still touch its memory
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<CG>(tmem_base, C::kTmemCols);
+    }
+}
+
+
+// The host-side operations of one kernel variant (declared in
+// gemm_variants.h; instantiated in gemm_ob1.cu, gemm_ob2.cu, gemm_ob4.cu).
+template <int CG, int BN, int OB, bool BS>
+static cudaLaunchConfig_t variant_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<CG, BN, OB, BS>::kSmemBytes;
+    cfg.stream = stream;
+    attr->id = cudaLaunchAttributeClusterDimension;
+    attr->val.clusterDim.x = CG;
+    attr->val.clusterDim.y = 1;
+    attr->val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CG == 2 ? 1 : 0;      // CTA pairs are launched as clusters of two
+    return cfg;
+}
+
+template <int CG, int BN, int OB, bool BS>
+size_t Variant<CG, BN, OB, BS>::smem() {
+    return Cfg<CG, BN, OB, BS>::kSmemBytes;
+}
+
+template <int CG, int BN, int OB, bool BS>
+cudaError_t Variant<CG, BN, OB, BS>::prepare() {
+    return cudaFuncSetAttribute(gemm_kernel<CG, BN, OB, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<CG, BN, OB, BS>::kSmemBytes);
+}
+
+template <int CG, int BN, int OB, bool BS>
+cudaError_t Variant<CG, BN, OB, BS>::launch(const LaunchArgs& a) {
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = variant_config<CG, BN, OB, BS>(a.grid, a.stream, &attr);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<CG, BN, OB, BS>, a.tmA, a.tmB, a.tmC, a.tmD, a.tmSA, a.tmSB, a.p);
+}
+
+template <int CG, int BN, int OB, bool BS>
+int Variant<CG, BN, OB, BS>::max_clusters() {
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = variant_config<CG, BN, OB, BS>(CG * 64, nullptr, &attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<CG, BN, OB, BS>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+
+}  // namespace gemm_sm103
