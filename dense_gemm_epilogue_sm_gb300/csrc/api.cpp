@@ -184,12 +184,21 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     int tile_n = 256;
     if (cg == 1 && (P.Nk <= 128 || ((P.Mk + kTileM - 1) / kTileM) * ((P.Nk + 255) / 256) * L < 76)) tile_n = 128;
     const int bs = d.block_scale != GEMM_BLOCK_SCALE_NONE;
-    if (bs) {     // the block-scaled kernel: 128-wide tiles, a CTA pair (256 x 128) where that fills the GPU
-        const int64_t tiles_pair = ((P.Mk + 255) / 256) * ((P.Nk + 127) / 128) * L;
-        // A pair CTA holds 64 rows of B; an MN-major e4m3 B needs 128-element
-        // (one 128-byte swizzle row) boxes along N, so it stays on one CTA.
-        cg = (P.Mk > 128 && tiles_pair >= 64 && b_kmaj) ? 2 : 1;
-        tile_n = 128;
+    if (bs) {
+        // The block-scaled kernel: CTA pairs with 256 x 256 tiles (one TMEM
+        // accumulator beside the scale factors) where at least 64 of them fill
+        // the GPU, else pairs with 256 x 128 tiles, else one CTA (128 x 128).
+        // A pair CTA of a 256 x 128 tile holds 64 rows of B, narrower than one
+        // 128-element MN-major e4m3 box, so an MN-major B stays on one CTA.
+        const int64_t tiles_256 = ((P.Mk + 255) / 256) * ((P.Nk + 255) / 256) * L;
+        const int64_t tiles_128 = ((P.Mk + 255) / 256) * ((P.Nk + 127) / 128) * L;
+        if (P.Mk > 128 && P.Nk > 128 && tiles_256 >= 64) {
+            cg = 2;
+            tile_n = 256;
+        } else {
+            cg = (P.Mk > 128 && tiles_128 >= 64 && b_kmaj) ? 2 : 1;
+            tile_n = 128;
+        }
     }
     const int tile_m = kTileM * cg;
     P.cta_group = cg;

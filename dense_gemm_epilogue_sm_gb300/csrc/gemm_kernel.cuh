@@ -55,21 +55,32 @@ constexpr int kClcSlots = 4;
 // elements).  Each stage then also holds the 512-byte scale-factor blocks of
 // its A rows and B rows, which the MMA thread copies into TMEM columns after
 // the accumulators (8 columns per stage).
+// TMEM accumulators: two, except for block-scaled 256-wide tiles, whose
+// 256-column accumulator leaves room for one only beside the scale factors.
+__host__ __device__ constexpr int acc_bufs(int cg, int bn, bool bs) {
+    return (bs && bn == 256) ? 1 : (cg == 2 ? kPairAccBufs : 2);
+}
+
 template <int CG, int BN, int OB, bool BS = false>
 struct Cfg {
-    static constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
+    static constexpr int kAccBufs = acc_bufs(CG, BN, BS);
     static constexpr int kBRows = BN / CG;                          // rows of B this CTA loads
-    static constexpr int kStages = BS ? (CG == 2 ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
+    static constexpr int kStages = BS ? ((CG == 2 && BN == 128) ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
     static constexpr int kABytes = kTileM * kStageKBytes;           // 16 KiB
     static constexpr int kBBytes = kBRows * kStageKBytes;
-    static constexpr int kSfBytes = BS ? 2 * 512 : 0;               // scale-factor blocks of A and B
+    // scale-factor blocks: A's 128 rows and the tile's BN columns, 512 bytes
+    // per 128; the stage keeps 1024-byte alignment
+    static constexpr int kSfTxBytes = BS ? 512 + 512 * (BN / 128) : 0;
+    static constexpr int kSfBytes = (kSfTxBytes + 1023) / 1024 * 1024;
+    static constexpr int kSfCols = BS ? 4 + 4 * (BN / 128) : 0;    // TMEM columns of one stage's factors
     static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;   // this CTA's share of a stage
+    static constexpr int kTxBytes = kABytes + kBBytes + kSfTxBytes;    // bytes one stage's copies bring
     // 64 (16-bit D), 32 (fp32 D), or 64 (e4m3 D with MX factors, stored directly)
     static constexpr int kEpiCols = OB == 1 ? 64 : 128 / OB;
     static constexpr int kSubtiles = BN / kEpiCols;
     static constexpr int kSfCol0 = kAccBufs * BN;                   // first TMEM column of the scale factors
     static constexpr int kTmemCols = BS ? 512 : kAccBufs * BN;
-    static_assert(!BS || kSfCol0 + 8 * kStages <= 512, "TMEM");
+    static_assert(!BS || kSfCol0 + kSfCols * kStages <= 512, "TMEM");
     static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
@@ -469,7 +480,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     const uint32_t bar0 = m.bar0, ring = m.ring, a_bytes = m.a_bytes, stage_bytes = m.stage_bytes;
     const uint32_t tmem_base = m.tmem_base, peer_abort = m.peer_abort;
     volatile uint32_t* const abort_flag = m.abort_flag;
-    constexpr int kAccBufs = CG == 2 ? kPairAccBufs : 2;
+    constexpr int kAccBufs = acc_bufs(CG, BN, BS);
     auto full_bar = [=](int s) { return bar0 + 8u * s; };
     auto empty_bar = [=](int s) { return bar0 + 8u * (S + s); };
     auto accf_bar = [=](int b) { return bar0 + 8u * (2 * S + b); };
@@ -519,10 +530,13 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
             const uint32_t first = kb != kb0;
             if constexpr (BS) {
                 constexpr uint32_t kSfCol0 = (uint32_t)(kAccBufs * BN);
-                const uint32_t sfs = ring + (uint32_t)stage * stage_bytes + stage_bytes - 1024u;
-                const uint32_t sfa = tmem_base + kSfCol0 + 8u * (uint32_t)stage, sfb = sfa + 4u;
+                constexpr uint32_t kSfCols = 4u + 4u * (BN / 128), kSfBytes = (512u + 512u * (BN / 128) + 1023u) / 1024u * 1024u;
+                const uint32_t sfs = ring + (uint32_t)stage * stage_bytes + stage_bytes - kSfBytes;
+                const uint32_t sfa = tmem_base + kSfCol0 + kSfCols * (uint32_t)stage, sfb = sfa + 4u;
                 ptx::tmem_cp_32x128b_x4<CG>(sfa, sf_desc(sfs));
-                ptx::tmem_cp_32x128b_x4<CG>(sfb, sf_desc(sfs + 512u));
+#pragma unroll
+                for (int jb = 0; jb < BN / 128; ++jb)           // columns 128 jb .. 128 jb + 127 of the tile
+                    ptx::tmem_cp_32x128b_x4<CG>(sfb + 4u * jb, sf_desc(sfs + 512u + 512u * jb));
                 ptx::mma_mx<CG, IDESC>(d_tmem, ad, bd, sfa, sfb, first);
                 ready = ptx::mbar_test_wait(full_bar(next), next_phase);
                 ptx::mma_mx<CG, IDESC | (1u << 4) | (1u << 29)>(d_tmem, ad + a_step, bd + b_step, sfa, sfb, 1u);
@@ -678,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         // the pair's leader counts both CTAs' bytes
                         const uint32_t fb = CG == 2 ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
-                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes * CG);
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes * CG);
                         const uint32_t sa = ptx::smem_addr(ring + stage * C::kStageBytes);
                         const uint32_t sb = sa + C::kABytes;
                         const int k0 = kb * kel;
@@ -706,9 +720,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // block and the block of the tile's whole N range.
                             const uint32_t sf = sb + C::kBBytes;
                             const int blk_a = (la * p.sf_mblocks + m0 / 128) * p.num_kb + kb;
-                            const int blk_b = (lb * p.sf_nblocks + nb * BN / 128) * p.num_kb + kb;
                             load(sf, &tmSA, 0, blk_a * 32, 0);
-                            load(sf + 512, &tmSB, 0, blk_b * 32, 0);
+#pragma unroll
+                            for (int j = 0; j < BN / 128; ++j) {
+                                // (a block past N multiplies zero-filled B columns only)
+                                const int blk_b = (lb * p.sf_nblocks + nb * BN / 128 + j) * p.num_kb + kb;
+                                load(sf + 512 + 512 * j, &tmSB, 0, blk_b * 32, 0);
+                            }
                         }
                         const uint32_t bit = 1u << pend_slot(stage);
                         pend |= bit;

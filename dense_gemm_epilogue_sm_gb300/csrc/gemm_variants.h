@@ -18,8 +18,9 @@ struct Variant {
     static int max_clusters();
 };
 
-#define GEMM_FOR_EACH_VARIANT(X, OB) \
-    X(2, 256, OB, false) X(1, 256, OB, false) X(1, 128, OB, false) X(2, 128, OB, true) X(1, 128, OB, true)
+#define GEMM_FOR_EACH_VARIANT(X, OB)                                                                  \
+    X(2, 256, OB, false) X(1, 256, OB, false) X(1, 128, OB, false) X(2, 256, OB, true) X(2, 128, OB, true) \
+        X(1, 128, OB, true)
 #define GEMM_EXTERN_VARIANT(CG, BN, OB, BS) extern template struct Variant<CG, BN, OB, BS>;
 #define GEMM_INSTANTIATE_VARIANT(CG, BN, OB, BS) template struct Variant<CG, BN, OB, BS>;
 

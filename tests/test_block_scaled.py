@@ -84,7 +84,13 @@ SPECS = [
 ]
 
 
-# big enough for the CTA-pair variant (256 x 128 tiles, at least 64 of them)
+# big enough for the CTA-pair variants: 256 x 256 tiles (one accumulator)
+# where at least 64 of them exist, else 256 x 128
+PAIR256_SPECS = [
+    wl.Spec("mx_pair256_ragged_fused", 2300, 2100, 1024, dtype_in="e4m3", block_scale="mx", alpha=0.5, beta=1.0,
+            act="gelu", bias="col", seed=105, pad=16),
+    wl.Spec("mx_pair256_b_mn_major", 2048, 2048, 640, order_b="row", dtype_in="e4m3", block_scale="mx", seed=106),
+]
 PAIR_SPECS = [
     wl.Spec("mx_pair_ragged_fused", 2100, 1300, 1024, dtype_in="e4m3", block_scale="mx", alpha=0.5, beta=1.0,
             act="relu", bias="col", seed=101, pad=16),
@@ -96,8 +102,9 @@ PAIR_SPECS = [
 
 
 def test_mn_major_b_stays_on_one_cta():
-    # each CTA of a pair holds 64 rows of B, narrower than one MN-major e4m3 box
-    spec = wl.Spec("mx_b_mn", 2048, 2048, 512, order_b="row", dtype_in="e4m3", block_scale="mx", seed=104)
+    # too few 256 x 256 tiles; each CTA of a 256 x 128 pair would hold 64 rows
+    # of B, narrower than one MN-major e4m3 box
+    spec = wl.Spec("mx_b_mn", 2048, 1024, 512, order_b="row", dtype_in="e4m3", block_scale="mx", seed=104)
     info = g.gemm_plan(desc_from_spec(spec))
     assert not info.b_k_major and info.cta_group == 1
     inputs = wl.make_inputs(spec)
@@ -106,19 +113,20 @@ def test_mn_major_b_stays_on_one_cta():
     op.close()
 
 
-@pytest.mark.parametrize("spec", SPECS + PAIR_SPECS, ids=lambda s: s.name)
+@pytest.mark.parametrize("spec", SPECS + PAIR_SPECS + PAIR256_SPECS, ids=lambda s: s.name)
 def test_block_scaled_matches_oracle(spec):
     inputs = wl.make_inputs(spec)
     bits, op = _run(spec, inputs)
     info = g.gemm_plan(op.desc)
-    want_cg = 2 if spec in PAIR_SPECS else 1
-    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (want_cg, 128 * want_cg, 128, 128)
-    rows = H.sample_rows(spec) if spec in PAIR_SPECS else None
+    want_cg = 1 if spec in SPECS else 2
+    want_n = 256 if spec in PAIR256_SPECS else 128
+    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (want_cg, 128 * want_cg, want_n, 128)
+    rows = H.sample_rows(spec) if want_cg == 2 else None
     _check(spec, inputs, bits, rows=rows)
     op.close()
 
 
-@pytest.mark.parametrize("M,N", [(512, 384), (2304, 1152)])        # one CTA, and CTA pairs
+@pytest.mark.parametrize("M,N", [(512, 384), (2304, 1152), (2304, 2176)])   # one CTA, pairs 256x128, 256x256
 @pytest.mark.parametrize("order_d", ["row", "col"])
 def test_block_scaled_integer_sums_bit_exact(order_d, M, N):
     spec = wl.Spec("mx_int", M, N, 1024, dtype_in="e4m3", dtype_d="f32", dist="int4", block_scale="mx",
