@@ -65,7 +65,7 @@ template <int CG, int BN, int OB, bool BS = false>
 struct Cfg {
     static constexpr int kAccBufs = acc_bufs(CG, BN, BS);
     static constexpr int kBRows = BN / CG;                          // rows of B this CTA loads
-    static constexpr int kStages = BS ? ((CG == 2 && BN == 128) ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
+    static constexpr int kStages = BS ? (CG == 2 ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
     static constexpr int kABytes = kTileM * kStageKBytes;           // 16 KiB
     static constexpr int kBBytes = kBRows * kStageKBytes;
     // scale-factor blocks: A's 128 rows and the tile's BN columns, 512 bytes
@@ -83,7 +83,10 @@ struct Cfg {
     static_assert(!BS || kSfCol0 + kSfCols * kStages <= 512, "TMEM");
     static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+    // epilogue staging buffers per warp: two (a store drains while the next
+    // subtile fills), one where the ring needs the room (block-scaled 256-wide)
+    static constexpr int kEpiBufs = (BS && BN == 256) ? 1 : 2;
+    static constexpr int kEpiBytes = kEpiWarps * kEpiBufs * kEpiBufBytes;
     // Stages are released to the producer in groups: every tcgen05.commit
     // costs the tensor front end cycles that MMAs cannot use, so one commit
     // frees kGroup stages.
@@ -967,11 +970,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         // the subtile holding a ragged row end is stored element by element
                         const bool direct = p.d_ragged && col0 + C::kEpiCols > p.N;
-                        const int sbi = sub_count & 1;
+                        const int sbi = sub_count % C::kEpiBufs;
                         ++sub_count;
-                        uint8_t* sbuf = epi + (ew * 2 + sbi) * kEpiBufBytes;
+                        uint8_t* sbuf = epi + (ew * C::kEpiBufs + sbi) * kEpiBufBytes;
                         const uint32_t sbuf_a = ptx::smem_addr(sbuf);
-                        if (lane == 0) ptx::bulk_wait_read<1>();       // the store that last used sbuf has read it
+                        if (lane == 0) ptx::bulk_wait_read<C::kEpiBufs - 1>();   // the store that last used sbuf has read it
                         __syncwarp();
                         if (p.has_c) {
                             const uint32_t cb = cfull_bar(ew * 2 + sbi);

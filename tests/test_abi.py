@@ -170,7 +170,7 @@ def test_block_scaling_needs_e4m3_operands_and_plans_the_mx_kernel():
     d = _desc(dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=7)
     assert _status(d)[0] == g.ERR_INVALID_ARG
     s, info = _status(_desc(M=4096, N=4096, K=4096, dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=g.BLOCK_SCALE_MX))
-    assert s == g.OK and (info.cta_group, info.tile_m, info.tile_n, info.tile_k, info.stages) == (2, 256, 256, 128, 5)
+    assert s == g.OK and (info.cta_group, info.tile_m, info.tile_n, info.tile_k, info.stages) == (2, 256, 256, 128, 6)
     s, info = _status(_desc(M=2048, N=1024, K=4096, dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=g.BLOCK_SCALE_MX))
     assert s == g.OK and (info.cta_group, info.tile_m, info.tile_n, info.tile_k, info.stages) == (2, 256, 128, 128, 6)
     s, info = _status(_desc(M=512, N=512, K=512, dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=g.BLOCK_SCALE_MX))
