@@ -892,6 +892,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.bias_mode == 2 && row < p.M) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
                 const float* bias_l = p.bias_mode == 1 ? p.bias + (int64_t)l * p.bias_stride : nullptr;
                 [[maybe_unused]] const int lc = p.c_batched ? l : 0;
+                // With a single accumulator the MMA waits for the whole
+                // epilogue, so it is released right after its last subtile's
+                // TMEM load, before that subtile's math and stores.  With two
+                // the MMA works on the other one meanwhile and the release
+                // stays at the end of the tile.
+                const int n_end = nb * BN + BN < p.N ? nb * BN + BN : p.N;
+                const int last_sub = (row0 < p.M && n_end > nb * BN) ? (n_end - 1 - nb * BN) / C::kEpiCols : -1;
+                bool released = false;
+                auto early_release = [&](int sub) {
+                    if constexpr (C::kAccBufs == 1) {
+                        if (sub == last_sub) {
+                            release_acc(buf);
+                            released = true;
+                        }
+                    }
+                };
     #pragma unroll 1
                 for (int sub = 0; sub < C::kSubtiles; ++sub) {
                     const int col0 = nb * BN + sub * C::kEpiCols;
@@ -906,6 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
                         }
+                        early_release(sub);
                         if (cut) {
                             for_each_part(r_next, t_end, [&](int w) {
                                 const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
@@ -993,6 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         #pragma unroll
                             for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0u;
                         }
+                        early_release(sub);
                         if (cut) {
                             for_each_part(r_next, t_end, [&](int w) {
                                 const float4* ps = part_slot<BN>(p, w, CG, rank, q) + sub * (C::kEpiCols / 4) * 32 + lane;
@@ -1105,7 +1123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                release_acc(buf);
+                if (!released) release_acc(buf);
                 if (EXT && p.red_rows && row < p.M) p.red_row_ws[((int64_t)l * p.tiles_n + nb) * p.M + row] = row_acc;
                 if (EXT && p.red_amax) {
     #pragma unroll
