@@ -9,7 +9,9 @@ order, A, B, C, bias as fp32 in storage order; 16-bit operands are the fp32
 draws rounded to nearest-even.  8-bit (e4m3) operands are quantised with a
 per-tensor scale s = 448 / max|x| (q = e4m3(clamp(x*s, +-448)), rounded to
 nearest-even by torch) and the dequantisation factors 1/s are handed to the
-GEMM as scale_a / scale_b.
+GEMM as scale_a / scale_b.  Block-scaled operands (mx_float8, nv_float4)
+are quantised per block of K from N(0,1) draws spread by a random power of
+two per block; the factors are laid out in the 512-byte basic-block layout.
 
 The named workloads are the five configurations the method is measured on:
 a tiny exact fp16 GEMM, plain bf16 4096^3, the fused-epilogue bf16 8192^3
@@ -19,8 +21,11 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
-ESIZE = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
+# e2m1 (nv_float4) operands are stored as bytes, two elements per byte
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn,
+      "e2m1": torch.uint8}
+ESIZE = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1, "e2m1": 0.5}
+SF_VEC = {"mx": 32, "nv": 16}
 
 
 @dataclass
@@ -52,6 +57,7 @@ class Spec:
     ldd: int = 0
     reduce: str = "none"        # none, or a '+'-joined subset of row, col, amax
     block_scale: str = "none"   # none | mx (e4m3 data, ue8m0 scale per 32 elements of K)
+                                # | nv (e2m1 data, ue4m3 scale per 16 elements of K)
     notes: str = ""
 
     # ----------------------------------------------------------- geometry --
@@ -73,7 +79,7 @@ class Spec:
         r, c = self.stored(which)
         tight = c if self.order(which) == "row" else r
         esz = ESIZE[self.dtype_in if which in "ab" else self.dtype_d]
-        align = 16 // esz
+        align = int(16 / esz)
         return max(align, -(-(tight + self.pad) // align) * align)
 
     def outer(self, which):
@@ -94,9 +100,10 @@ class Spec:
             b += self.batch * self.M * self.N * e_d
         if self.bias != "none":
             b += 4 * (self.N if self.bias == "col" else self.M)
-        if self.block_scale != "none":      # one byte per 32 elements of K, per row of A and of B
-            b += self.batch * (self.M + self.N) * ((self.K + 31) // 32)
-        return b
+        if self.block_scale != "none":      # one byte per SV elements of K, per row of A and of B
+            sv = SF_VEC[self.block_scale]
+            b += self.batch * (self.M + self.N) * ((self.K + sv - 1) // sv)
+        return int(b)
 
 
 WORKLOADS = {
@@ -121,6 +128,9 @@ WORKLOADS = {
         "mxfp8_to_mxfp8_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e4m3", block_scale="mx",
         dtype_d="e4m3", act="relu", seed=8,
         notes="MX in, MX out: e4m3 D with a ue8m0 factor per 32 elements of a row"),
+    "nvfp4_8192": Spec(
+        "nvfp4_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e2m1", block_scale="nv", seed=9,
+        notes="nv_float4: e2m1 data, one ue4m3 scale factor per 16 elements of K, fp32 global scales"),
     "odd_1000_at": Spec(
         "odd_1000_at", 1000, 1000, 1000, op_a="T", order_a="col", order_b="col", seed=4,
         notes="A transposed: stored K x M column-major, lda = K"),
@@ -205,6 +215,45 @@ def _mx_quantise(x):
     return q, code.to(torch.uint8)
 
 
+# e2m1 magnitudes by code 0..7 (sign in bit 3)
+E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _encode_e2m1(v):
+    """fp32 -> e2m1 codes (uint8, 0..15): nearest of the grid, ties to the
+    even code, magnitudes beyond 6 saturated to 6."""
+    a = v.abs()
+    code = torch.zeros_like(a, dtype=torch.int64)
+    for i in range(7):
+        t = 0.5 * (E2M1_GRID[i] + E2M1_GRID[i + 1])
+        code += ((a > t) | ((a == t) & (i % 2 == 1))).to(torch.int64)
+    return (code | torch.where(v < 0, 8, 0)).to(torch.uint8)
+
+
+def _nv_quantise(x):
+    """(L, R, K) fp32 -> (e2m1 codes, ue4m3 codes (L, R, ceil(K/16)), global
+    scale g): g = amax / (448 * 6) over the tensor, a block's factor
+    e4m3(amax_block / (6 g)), elements e2m1(x / (factor * g))."""
+    L, R, K = x.shape
+    sfk = (K + 15) // 16
+    amax = float(x.abs().max())
+    g = float(torch.tensor(amax / (448.0 * 6.0) if amax > 0 else 1.0, dtype=torch.float32))
+    xp = torch.zeros(L, R, sfk * 16)
+    xp[:, :, :K] = x
+    blk = xp.view(L, R, sfk, 16)
+    sf = (blk.abs().amax(dim=3) / (6.0 * g)).clamp(0.0, 448.0).to(torch.float8_e4m3fn)
+    sf_val = sf.to(torch.float32) * g
+    q = _encode_e2m1(torch.where(sf_val.unsqueeze(3) > 0, blk / sf_val.unsqueeze(3), torch.zeros_like(blk)))
+    return q.view(L, R, sfk * 16)[:, :, :K], sf.view(torch.uint8), g
+
+
+def _pack_e2m1(codes):
+    """Flat e2m1 codes (one per element, storage order) -> bytes, the element
+    of lower index in the low nibble."""
+    c = codes.view(-1, 2)
+    return (c[:, 0] | (c[:, 1] << 4)).contiguous()
+
+
 def _to_storage(spec, which, logical):
     """Logical (L, R, K) operand (A: R = M; B: R = N, i.e. op(B) transposed)
     into the spec's flat storage, padding elements zero."""
@@ -248,12 +297,39 @@ def _make_mx_inputs(spec, gen):
     return ops
 
 
+def _make_nv_inputs(spec, gen):
+    L = spec.batch
+    ops = {}
+    for which, R in (("a", spec.M), ("b", spec.N)):
+        sfk = (spec.K + 15) // 16
+        if spec.dist == "int4":
+            # any e2m1 code with factors 0.5, 1, 2: every sum exact in fp32
+            q = torch.randint(0, 16, (L, R, spec.K), generator=gen).to(torch.uint8)
+            code = torch.tensor([0x30, 0x38, 0x40], dtype=torch.uint8)[torch.randint(0, 3, (L, R, sfk), generator=gen)]
+            g = 1.0
+        else:
+            x = torch.randn(L, R, spec.K, generator=gen, dtype=torch.float32)
+            shift = torch.randint(-4, 5, (L, R, sfk), generator=gen).to(torch.float32)
+            x = x * torch.exp2(shift.repeat_interleave(16, dim=2)[:, :, :spec.K])
+            q, code, g = _nv_quantise(x)
+        off, per = _sf_offsets(L, R, sfk)
+        sf = torch.full((L * per,), 0x38, dtype=torch.uint8)      # padding factors: 1.0
+        sf[off.reshape(-1)] = code.reshape(-1)
+        ops[which] = (_pack_e2m1(_to_storage(spec, which, q)), sf, g)
+    return ops
+
+
 def make_inputs(spec: Spec) -> Inputs:
     """Builds the storage buffers of one workload (CPU tensors).  Padding
     elements beyond each leading extent are drawn too (they are never read)."""
     gen = torch.Generator(device="cpu").manual_seed(spec.seed)
-    if spec.block_scale == "mx":
-        ops = _make_mx_inputs(spec, gen)
+    if spec.block_scale in ("mx", "nv"):
+        if spec.block_scale == "nv":
+            ops = _make_nv_inputs(spec, gen)
+            sa, sb = ops["a"][2], ops["b"][2]
+        else:
+            ops = _make_mx_inputs(spec, gen)
+            sa = sb = 1.0
         C = None
         if spec.beta != 0:
             C = _draw(gen, spec.batch * spec.matrix_elems("c"), "normal").to(DT[spec.dtype_d])
@@ -261,7 +337,7 @@ def make_inputs(spec: Spec) -> Inputs:
         if spec.bias != "none":
             n = spec.N if spec.bias == "col" else spec.M
             bias = torch.randn(spec.batch * n, generator=gen, dtype=torch.float32) * spec.bias_sigma
-        return Inputs(spec, ops["a"][0], ops["b"][0], C, bias, 1.0, 1.0,
+        return Inputs(spec, ops["a"][0], ops["b"][0], C, bias, sa, sb,
                       extras={"sfa": ops["a"][1], "sfb": ops["b"][1]})
     L = spec.batch
     out = {}

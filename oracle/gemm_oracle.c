@@ -43,6 +43,13 @@
  *    factors at byte (r % 32) * 16 + ((r % 128) / 32) * 4 (M0SF0-3, M32SF0-3,
  *    M64SF0-3, M96SF0-3, then M1...), and the blocks follow each other along
  *    K first (K-major), then along M; one such tensor per batch.
+ *    nv_float4 pairs e2m1 data (2 exponent bits, 1 mantissa bit, signed)
+ *    with a ue4m3 scale (4 exponent bits, 3 mantissa bits, no sign), SV =
+ *    16 (same table and "Blackwell Block Scaled Narrow Precision Data
+ *    Types").  Reading: e2m1 has bias 1 and no inf or NaN, so its codes are
+ *    +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}; ue4m3 is e4m3 without the sign bit
+ *    (bias 7, 0x7F NaN).  Two e2m1 elements share a byte, the one of lower
+ *    storage index in the low nibble.
  *
  * Every product of two operands (<= 11 significant bits each) is exact in
  * fp64, and the fp64 sum over K carries a relative error of order K * 2^-53,
@@ -66,7 +73,7 @@
 #endif
 
 /* Element type codes of this oracle's own interface. */
-enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3, OR_UE8M0 = 4 };
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3, OR_UE8M0 = 4, OR_E2M1 = 5, OR_UE4M3 = 6 };
 
 typedef struct {
     int64_t M, N, K, L;
@@ -79,14 +86,16 @@ typedef struct {
     int32_t has_bias;      /* bias is fp32 */
     int32_t bias_per_row;  /* 0: bias[n] broadcast down the columns; 1: bias[m] */
     int32_t act;           /* 0 = identity, 1 = ReLU, 2 = GELU */
-    int32_t sf_vec;        /* 0: no block scaling; 32: ue8m0 scale per 32 K elements */
+    int32_t sf_vec;        /* 0: no block scaling; 32: ue8m0 scale per 32 K elements;
+                              16: ue4m3 scale per 16 K elements */
 } oracle_problem_t;
 
 /* ---------------------------------------------------------------------------
  * Bit-level codecs.  A binary float with `eb` exponent bits and `mb` stored
  * mantissa bits has bias 2^(eb-1)-1; a zero exponent field means subnormal
  * (value = mant * 2^(1-bias-mb)).  IEEE formats reserve the all-ones exponent
- * for inf/NaN; e4m3 uses it for normal numbers except mantissa 111 (NaN).
+ * for inf/NaN; e4m3 uses it for normal numbers except mantissa 111 (NaN);
+ * e2m1 has no special values at all.  `ieee`: 1 IEEE, 0 e4m3's rule, -1 none.
  * ------------------------------------------------------------------------- */
 static int type_bits(int dt, int* eb, int* mb, int* ieee) {
     switch (dt) {
@@ -94,6 +103,7 @@ static int type_bits(int dt, int* eb, int* mb, int* ieee) {
         case OR_F16:  *eb = 5; *mb = 10; *ieee = 1; return 16;
         case OR_BF16: *eb = 8; *mb = 7;  *ieee = 1; return 16;
         case OR_E4M3: *eb = 4; *mb = 3;  *ieee = 0; return 8;
+        case OR_E2M1: *eb = 2; *mb = 1;  *ieee = -1; return 4;
         default: return 0;
     }
 }
@@ -101,6 +111,7 @@ static int type_bits(int dt, int* eb, int* mb, int* ieee) {
 double oracle_decode(int dt, uint32_t bits) {
     int eb, mb, ieee;
     if (dt == OR_UE8M0) return (bits & 0xFFu) == 0xFFu ? NAN : ldexp(1.0, (int)(bits & 0xFFu) - 127);
+    if (dt == OR_UE4M3) return oracle_decode(OR_E4M3, bits & 0x7Fu);     /* no sign bit */
     if (!type_bits(dt, &eb, &mb, &ieee)) return NAN;
     const uint32_t mant = bits & ((1u << mb) - 1u);
     const uint32_t expf = (bits >> mb) & ((1u << eb) - 1u);
@@ -108,9 +119,9 @@ double oracle_decode(int dt, uint32_t bits) {
     const int bias = (1 << (eb - 1)) - 1;
     const uint32_t all_ones = (1u << eb) - 1u;
     double v;
-    if (expf == all_ones && ieee) {
+    if (expf == all_ones && ieee == 1) {
         v = mant ? NAN : INFINITY;
-    } else if (expf == all_ones && !ieee && mant == (1u << mb) - 1u) {
+    } else if (expf == all_ones && ieee == 0 && mant == (1u << mb) - 1u) {
         v = NAN;
     } else if (expf == 0) {
         v = ldexp((double)mant, 1 - bias - mb);
@@ -124,7 +135,7 @@ double oracle_decode(int dt, uint32_t bits) {
  * Overflow goes to infinity as IEEE 754 prescribes for this rounding mode. */
 uint32_t oracle_encode(int dt, double v) {
     int eb, mb, ieee;
-    if (!type_bits(dt, &eb, &mb, &ieee) || !ieee) return 0xFFFFFFFFu;
+    if (!type_bits(dt, &eb, &mb, &ieee) || ieee != 1) return 0xFFFFFFFFu;
     const int bias = (1 << (eb - 1)) - 1;
     const uint32_t sign = signbit(v) ? (1u << (eb + mb)) : 0u;
     const uint32_t inf_bits = sign | (((1u << eb) - 1u) << mb);
@@ -160,6 +171,10 @@ static uint32_t load_bits(const void* base, int dt, int64_t idx) {
         case OR_F16:
         case OR_BF16: { uint16_t x; memcpy(&x, (const char*)base + 2 * idx, 2); return x; }
         case OR_E4M3: return ((const uint8_t*)base)[idx];
+        case OR_E2M1: {
+            const uint8_t byte = ((const uint8_t*)base)[idx / 2];
+            return idx % 2 ? (uint32_t)(byte >> 4) : (uint32_t)(byte & 0xFu);
+        }
         default: return 0;
     }
 }
@@ -219,7 +234,8 @@ int64_t oracle_sf_index(int64_t l, int64_t row, int64_t kf, int64_t rows, int64_
 
 static double sf_value(const uint8_t* sf, int64_t l, int64_t row, int64_t k, int64_t rows, const oracle_problem_t* p) {
     const int64_t sfk = (p->K + p->sf_vec - 1) / p->sf_vec;
-    return oracle_decode(OR_UE8M0, sf[oracle_sf_index(l, row, k / p->sf_vec, rows, sfk)]);
+    const int sf_type = p->sf_vec == 16 ? OR_UE4M3 : OR_UE8M0;      /* nv_float4 : mx types */
+    return oracle_decode(sf_type, sf[oracle_sf_index(l, row, k / p->sf_vec, rows, sfk)]);
 }
 
 /*
@@ -252,14 +268,15 @@ static uint64_t fnv1a(const uint8_t* p, size_t n) {
 static const double* b_panel(const oracle_problem_t* p, const void* B, const uint8_t* SFB, int64_t l) {
     const int64_t K = p->K, N = p->N;
     int eb, mb, ieee;
-    const int bytes = type_bits(p->dtype_b, &eb, &mb, &ieee) / 8;
-    /* the storage span this batch of B occupies */
+    const int bits = type_bits(p->dtype_b, &eb, &mb, &ieee);
+    /* the storage span this batch of B occupies (whole bytes) */
     const int64_t srows = p->op_b == 0 ? K : N, scols = p->op_b == 0 ? N : K;
     const int64_t outer = p->order_b == 1 ? srows : scols;
     const int64_t inner = p->order_b == 1 ? scols : srows;
     const int64_t span = outer > 0 && inner > 0 ? (outer - 1) * p->ldb + inner : 0;
-    const uint8_t* first = (const uint8_t*)B + (size_t)(l * p->stride_b) * bytes;
-    const uint64_t h = fnv1a(first, (size_t)span * bytes);
+    const int64_t bit0 = l * p->stride_b * bits;
+    const uint8_t* first = (const uint8_t*)B + (size_t)(bit0 / 8);
+    const uint64_t h = fnv1a(first, (size_t)((bit0 % 8 + span * bits + 7) / 8));
     uint64_t sh = 0;
     if (p->sf_vec > 0) {
         const int64_t sfk = (K + p->sf_vec - 1) / p->sf_vec;
@@ -315,7 +332,7 @@ int oracle_gemm_rows_sf(const oracle_problem_t* p, const void* A, const void* B,
     int eb, mb, ieee;
     if (!p || p->M < 0 || p->N < 0 || p->K < 0 || p->L < 1) return -1;
     if (!type_bits(p->dtype_a, &eb, &mb, &ieee) || !type_bits(p->dtype_b, &eb, &mb, &ieee)) return -2;
-    if (!type_bits(p->dtype_d, &eb, &mb, &ieee) || !ieee) return -3;
+    if (!type_bits(p->dtype_d, &eb, &mb, &ieee) || ieee != 1) return -3;
     const int use_c = p->beta != 0.0;
     if (use_c && (!C || !type_bits(p->dtype_c, &eb, &mb, &ieee))) return -4;
     if (p->has_bias && !bias) return -5;

@@ -14,8 +14,11 @@ import numpy as np
 from . import build as _build
 
 # The oracle's own element-type codes.
-F32, F16, BF16, E4M3, UE8M0 = 0, 1, 2, 3, 4
-_NAMES = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3, "ue8m0": UE8M0}
+F32, F16, BF16, E4M3, UE8M0, E2M1, UE4M3 = 0, 1, 2, 3, 4, 5, 6
+_NAMES = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3, "ue8m0": UE8M0, "e2m1": E2M1, "ue4m3": UE4M3}
+# scale-factor vector size of each block-scaled format: mx_float8 (ue8m0
+# per 32), nv_float4 (ue4m3 per 16)
+SF_VEC = {"mx": 32, "nv": 16}
 _BYTES = {F32: 4, F16: 2, BF16: 2, E4M3: 1}
 _BITS_NP = {F32: np.uint32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8}
 
@@ -138,8 +141,8 @@ def gemm_rows(p: Problem, A, B, C=None, bias=None, rows=None, nthreads=0, want_t
     Returns (bits, t): ``bits`` is a (len(rows), N) array of D's raw bit
     patterns (uint16 for 16-bit types, uint32 for fp32); ``t`` the fp64
     values before rounding when ``want_t`` is set, else None.  ``sfa`` /
-    ``sfb``: the ue8m0 scale-factor bytes (basic-block layout, see
-    sf_index) when the problem is block-scaled (p.sf_vec > 0).
+    ``sfb``: the scale-factor bytes (ue8m0 for p.sf_vec = 32, ue4m3 for 16;
+    basic-block layout, see sf_index) when the problem is block-scaled.
     """
     if rows is None:
         rows = np.arange(p.L * p.M, dtype=np.int64)
@@ -189,7 +192,7 @@ def run_spec_rows(spec, inputs, rows=None, nthreads=0, want_t=False):
     p = problem_from_spec(spec, inputs)
     ex = getattr(inputs, "extras", None) or {}
     if getattr(spec, "block_scale", "none") != "none":
-        p.sf_vec = 32
+        p.sf_vec = SF_VEC[spec.block_scale]
     return gemm_rows(p, inputs.A, inputs.B, inputs.C, inputs.bias, rows=rows, nthreads=nthreads, want_t=want_t,
                      sfa=ex.get("sfa"), sfb=ex.get("sfb"))
 

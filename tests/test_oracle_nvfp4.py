@@ -1,0 +1,162 @@
+"""Pins the oracle's NVFP4 path (no GPU): the e2m1 and ue4m3 codecs against
+the values the format definitions fix, the nibble order of packed e2m1
+storage, exact rational brute force of D = sum_k (A x SFA)(B x SFB) with
+16-element scale vectors ("Technical Documentation: NVIDIA/cutlass", "Block
+Scaled GEMMs" and "Blackwell Narrow Precision Data Types"), and the special
+case that reduces to an e4m3 product.  Also checks the input generator's
+e2m1 rounding, which both sides consume."""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gemm_ref as g
+
+# E2M1 values by code, as tabulated by the OCP microscaling specification the
+# page's narrow-precision table points to (sign in bit 3)
+E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decodes_every_code():
+    for c in range(16):
+        want = E2M1[c & 7] * (-1.0 if c & 8 else 1.0)
+        got = g.decode("e2m1", c)
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want)
+
+
+def test_ue4m3_is_e4m3_without_a_sign():
+    assert [g.decode("ue4m3", c) for c in (0x38, 0x30, 0x40, 0x7E, 0x01, 0x08, 0x00)] == \
+        [1.0, 0.5, 2.0, 448.0, 2.0 ** -9, 2.0 ** -6, 0.0]
+    assert math.isnan(g.decode("ue4m3", 0x7F))
+    for c in range(0x80):
+        x, y = g.decode("ue4m3", c), g.decode("e4m3", c)
+        assert (math.isnan(x) and math.isnan(y)) or x == y
+
+
+def _pack(codes):
+    """Flat nibble codes -> bytes, the element of lower index in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8).reshape(-1, 2)
+    return (c[:, 0] | (c[:, 1] << 4)).astype(np.uint8)
+
+
+def _pack_sf(codes, pad=0x38):
+    L, rows, sfk = codes.shape
+    size = ((rows + 127) // 128) * ((sfk + 3) // 4) * 512
+    out = np.full(L * size, pad, dtype=np.uint8)
+    for l in range(L):
+        for r in range(rows):
+            for k in range(sfk):
+                out[g.sf_index(l, r, k, rows, sfk)] = codes[l, r, k]
+    return out
+
+
+def _ue4m3_fraction(c):
+    e, m = (c >> 3) & 15, c & 7
+    return Fraction(m, 8) * Fraction(2) ** -6 if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+
+
+def _run(ca, cb, sfa, sfb, L, M, N, K, kmajor_a=("N", "row"), kmajor_b=("N", "col"), sf_vec=16, dt="e2m1",
+         pad=0x38):
+    """ca: (L, M, K), cb: (L, N, K) element codes; A and B K-contiguous."""
+    op_a, order_a = kmajor_a
+    op_b, order_b = kmajor_b
+    lda = ldb = K
+    # K-contiguous storage of rows of op(A) and columns of op(B)
+    a_store = np.asarray(ca).reshape(-1)
+    b_store = np.asarray(cb).reshape(-1)
+    if dt == "e2m1":
+        a_store, b_store = _pack(a_store), _pack(b_store)
+    p = g.make_problem(M, N, K, L, op_a, op_b, order_a, order_b, "row", "row", lda, ldb, N, N,
+                       M * K if L > 1 else 0, N * K if L > 1 else 0, 0, M * N if L > 1 else 0, 0,
+                       dt, dt, "f32", "f32", sf_vec=sf_vec)
+    sa = _pack_sf(sfa, pad) if sf_vec else None
+    sb = _pack_sf(sfb, pad) if sf_vec else None
+    bits, t = g.gemm_rows(p, a_store, b_store, want_t=True, sfa=sa, sfb=sb)
+    return t.reshape(L, M, N)
+
+
+@pytest.mark.parametrize("layout", ["NN_row_col", "TT_col_row"])
+@pytest.mark.parametrize("K", [48, 40])          # three full factor blocks; a last block of 8 elements
+def test_nvfp4_bruteforce_exact(layout, K):
+    rng = np.random.default_rng(41)
+    L, M, N = 2, 5, 6
+    ca = rng.integers(0, 16, (L, M, K))
+    cb = rng.integers(0, 16, (L, N, K))
+    sfk = (K + 15) // 16
+    sfa = rng.integers(0x20, 0x50, (L, M, sfk))
+    sfb = rng.integers(0x20, 0x50, (L, N, sfk))
+    kw = {} if layout == "NN_row_col" else {"kmajor_a": ("T", "col"), "kmajor_b": ("T", "row")}
+    t = _run(ca, cb, sfa, sfb, L, M, N, K, **kw)
+    e2m1 = lambda c: Fraction(E2M1[c & 7]) * (-1 if c & 8 else 1)
+    for l in range(L):
+        for m in range(M):
+            for n in range(N):
+                want = sum(e2m1(int(ca[l, m, k])) * _ue4m3_fraction(int(sfa[l, m, k // 16])) *
+                           e2m1(int(cb[l, n, k])) * _ue4m3_fraction(int(sfb[l, n, k // 16])) for k in range(K))
+                assert Fraction(t[l, m, n]) == want
+
+
+def test_swapped_nibbles_change_the_result():
+    # a reader of the high nibble first would see a different product
+    rng = np.random.default_rng(42)
+    L, M, N, K = 1, 3, 3, 32
+    ca, cb = rng.integers(1, 8, (L, M, K)), rng.integers(1, 8, (L, N, K))
+    ones = lambda R: np.full((L, R, 2), 0x38)
+    t = _run(ca, cb, ones(M), ones(N), L, M, N, K)
+    swapped = ca.reshape(L, M, K // 2, 2)[..., ::-1].reshape(L, M, K)
+    t_sw = _run(swapped, cb, ones(M), ones(N), L, M, N, K)
+    assert not np.array_equal(t, t_sw)
+
+
+def test_unit_factors_reduce_to_the_e4m3_product_of_the_same_values():
+    # every e2m1 value is exact in e4m3; with factors 1.0 the block-scaled
+    # e2m1 GEMM equals the plain e4m3 GEMM of the same numbers
+    rng = np.random.default_rng(43)
+    L, M, N, K = 1, 20, 24, 96
+    ca, cb = rng.integers(0, 16, (L, M, K)), rng.integers(0, 16, (L, N, K))
+    t = _run(ca, cb, np.full((L, M, 6), 0x38), np.full((L, N, 6), 0x38), L, M, N, K)
+    e4 = {}
+    for c in range(16):
+        v = E2M1[c & 7] * (-1.0 if c & 8 else 1.0)
+        code = [x for x in range(256) if g.decode("e4m3", x) == v and math.copysign(1, g.decode("e4m3", x)) ==
+                math.copysign(1, v)][0]
+        e4[c] = code
+    ea = np.vectorize(e4.get)(ca).astype(np.uint8)
+    eb = np.vectorize(e4.get)(cb).astype(np.uint8)
+    t_e4 = _run(ea, eb, None, None, L, M, N, K, sf_vec=0, dt="e4m3")
+    assert np.array_equal(t, t_e4)
+
+
+def test_padding_factors_past_k_are_not_read():
+    rng = np.random.default_rng(44)
+    L, M, N, K = 1, 4, 4, 36                       # factors 0..2 real, the fourth slot is padding
+    ca, cb = rng.integers(0, 16, (L, M, K)), rng.integers(0, 16, (L, N, K))
+    sfa, sfb = rng.integers(0x30, 0x41, (L, M, 3)), rng.integers(0x30, 0x41, (L, N, 3))
+    t = _run(ca, cb, sfa, sfb, L, M, N, K, pad=0x7F)     # NaN padding
+    assert np.all(np.isfinite(t))
+
+
+def test_generator_e2m1_rounding_ties_to_even_and_saturates():
+    from dense_gemm_epilogue_sm_gb300 import workloads as wl
+    v = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, -0.3, -5.1, 0.0, 6.0, 1e9])
+    codes = wl._encode_e2m1(v).tolist()
+    got = [g.decode("e2m1", c) for c in codes]
+    assert got == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0, -0.5, -6.0, 0.0, 6.0, 6.0]
+    grid = torch.tensor([E2M1[c & 7] * (-1.0 if c & 8 else 1.0) for c in range(16)])
+    back = wl._encode_e2m1(grid).tolist()
+    assert [c if c != 8 else 0 for c in back] == [c if c != 8 else 0 for c in range(16)]
+
+
+def test_generated_nvfp4_inputs_dequantise_close_to_their_source():
+    from dense_gemm_epilogue_sm_gb300 import workloads as wl
+    gen = torch.Generator().manual_seed(5)
+    x = torch.randn(1, 8, 64, generator=gen)
+    q, sf, gs = wl._nv_quantise(x)
+    deq = torch.tensor([[g.decode("e2m1", int(c)) for c in row] for row in q[0]])
+    scale = torch.tensor([[g.decode("ue4m3", int(c)) for c in row] for row in sf[0]]).repeat_interleave(16, dim=1)
+    deq = deq * scale * gs
+    blk_amax = x[0].abs().view(8, 4, 16).amax(dim=2).repeat_interleave(16, dim=1)
+    # half the widest e2m1 step (2 of 6) of the block's range, plus the factor's own rounding
+    assert torch.all((deq - x[0]).abs() <= blk_amax * (1.0 / 6.0 + 1.0 / 16.0) + 1e-6)
