@@ -29,7 +29,7 @@ LIBRARY_PATH = os.path.join(_HERE, "libgemm_sm103.so")
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_DEVICE = range(7)
 # gemm_dtype_t
-F32, F16, BF16, E4M3 = 0, 1, 2, 3
+F32, F16, BF16, E4M3, E2M1 = 0, 1, 2, 3, 4
 # gemm_order_t
 COL_MAJOR, ROW_MAJOR = 0, 1
 # gemm_op_t
@@ -39,7 +39,7 @@ ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
 # gemm_reduce_t (flags)
 REDUCE_NONE, REDUCE_ROW_SUM, REDUCE_COL_SUM, REDUCE_ABS_MAX = 0, 1, 2, 4
 # gemm_block_scale_t
-BLOCK_SCALE_NONE, BLOCK_SCALE_MX = 0, 1
+BLOCK_SCALE_NONE, BLOCK_SCALE_MX, BLOCK_SCALE_NV = 0, 1, 2
 # gemm_out_scale_t
 OUT_SCALE_NONE, OUT_SCALE_MX = 0, 1
 # gemm_bias_t

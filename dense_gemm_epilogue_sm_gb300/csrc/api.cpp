@@ -83,7 +83,30 @@ bool aligned16(int64_t elems, int bytes) { return ((elems * bytes) % 16) == 0; }
 
 gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     if (!desc || !out) return GEMM_ERR_INVALID_ARG;
-    const gemm_desc_t& d = *desc;
+    // NVFP4 operands are planned as bytes: two e2m1 elements per byte along
+    // K (both operands K-contiguous), so K, the leading dimensions and the
+    // batch strides of A and B are halved and the byte view is planned like
+    // an 8-bit operand.  A stage's 128 bytes of K then hold 256 elements.
+    gemm_desc_t view = *desc;
+    const bool nv = desc->block_scale == GEMM_BLOCK_SCALE_NV;
+    if (nv) {
+        if (desc->dtype_a != GEMM_E2M1 || desc->dtype_b != GEMM_E2M1) return GEMM_ERR_UNSUPPORTED;
+        if (desc->K < 0 || desc->lda < 0 || desc->ldb < 0) return GEMM_ERR_INVALID_ARG;
+        if (desc->K % 2) return GEMM_ERR_UNSUPPORTED;
+        // K-contiguous storage of both operands (the pages' TN layout)
+        const bool a_k = (desc->op_a == GEMM_OP_N) == (desc->order_a == GEMM_ROW_MAJOR);
+        const bool b_k = (desc->op_b == GEMM_OP_N) == (desc->order_b == GEMM_COL_MAJOR);
+        if (!a_k || !b_k) return GEMM_ERR_UNSUPPORTED;
+        if (desc->lda % 32 || desc->ldb % 32 || (desc->batch > 1 && (desc->stride_a % 32 || desc->stride_b % 32)))
+            return GEMM_ERR_MISALIGNED;
+        view.K /= 2;
+        view.lda /= 2;
+        view.ldb /= 2;
+        view.stride_a /= 2;
+        view.stride_b /= 2;
+        view.dtype_a = view.dtype_b = GEMM_E4M3;
+    }
+    const gemm_desc_t& d = view;
     if (d.M < 0 || d.N < 0 || d.K < 0 || d.batch < 1) return GEMM_ERR_INVALID_ARG;
     if (d.M > INT32_MAX || d.N > INT32_MAX || d.K > INT32_MAX || d.batch > 65535) return GEMM_ERR_UNSUPPORTED;
     if ((d.op_a != GEMM_OP_N && d.op_a != GEMM_OP_T) || (d.op_b != GEMM_OP_N && d.op_b != GEMM_OP_T))
@@ -92,7 +115,9 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
         if (o != GEMM_ROW_MAJOR && o != GEMM_COL_MAJOR) return GEMM_ERR_INVALID_ARG;
     if (d.act != GEMM_ACT_NONE && d.act != GEMM_ACT_RELU && d.act != GEMM_ACT_GELU) return GEMM_ERR_INVALID_ARG;
     if (d.reduce & ~(GEMM_REDUCE_ROW_SUM | GEMM_REDUCE_COL_SUM | GEMM_REDUCE_ABS_MAX)) return GEMM_ERR_INVALID_ARG;
-    if (d.block_scale != GEMM_BLOCK_SCALE_NONE && d.block_scale != GEMM_BLOCK_SCALE_MX) return GEMM_ERR_INVALID_ARG;
+    if (d.block_scale != GEMM_BLOCK_SCALE_NONE && d.block_scale != GEMM_BLOCK_SCALE_MX &&
+        d.block_scale != GEMM_BLOCK_SCALE_NV)
+        return GEMM_ERR_INVALID_ARG;
     if (d.block_scale == GEMM_BLOCK_SCALE_MX && (d.dtype_a != GEMM_E4M3 || d.dtype_b != GEMM_E4M3))
         return GEMM_ERR_UNSUPPORTED;
     if (d.bias != GEMM_BIAS_NONE && d.bias != GEMM_BIAS_COL && d.bias != GEMM_BIAS_ROW) return GEMM_ERR_INVALID_ARG;
@@ -183,7 +208,9 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     int cg = (P.Mk > 128 && P.Nk > 128 && tiles2 >= 64) ? 2 : 1;
     int tile_n = 256;
     if (cg == 1 && (P.Nk <= 128 || ((P.Mk + kTileM - 1) / kTileM) * ((P.Nk + 255) / 256) * L < 76)) tile_n = 128;
-    const int bs = d.block_scale != GEMM_BLOCK_SCALE_NONE;
+    // 0 dense, 1 MXFP8, 2 NVFP4
+    const int bs = d.block_scale == GEMM_BLOCK_SCALE_NONE ? 0 : (nv ? 2 : 1);
+    if (nv && (!a_kmaj || !b_kmaj)) return GEMM_ERR_UNSUPPORTED;     // the pages' TN layout only
     if (bs) {
         // The block-scaled kernel: CTA pairs with 256 x 256 tiles (one TMEM
         // accumulator beside the scale factors) where at least 64 of them fill
@@ -208,7 +235,7 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
 
     P.info.tile_m = tile_m;
     P.info.tile_n = tile_n;
-    P.info.tile_k = kStageKBytes / ab;
+    P.info.tile_k = kStageKBytes / ab * (nv ? 2 : 1);
     P.info.cta_group = cg;
     P.info.stages = stages_for(cg, tile_n, bs);
     P.info.epi_cols = 128 / ob;
@@ -353,6 +380,23 @@ bool encode_sf_map(CUtensorMap* map, const void* base, int64_t blocks) {
     cuuint64_t dims[3] = {16, (cuuint64_t)(blocks * 32), 1};
     cuuint64_t strides[2] = {16, (cuuint64_t)(blocks * 512)};
     cuuint32_t box[3] = {16, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// NVFP4 factors: one ue4m3 per 16 K elements, so a 256-element K stage
+// takes four 512-byte blocks per 128 rows, adjacent in the tensor.  Seen as
+// rows of 16 bytes: dimension 1 walks a 128-row block's K blocks (32 rows
+// each, `kblocks` of them), dimension 2 the 128-row blocks; a box of 128 rows
+// is one stage's four blocks, and blocks past the last K block read as zero.
+bool encode_sf_map_nv(CUtensorMap* map, const void* base, int64_t kblocks, int64_t row_blocks) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {16, (cuuint64_t)(kblocks * 32), (cuuint64_t)row_blocks};
+    cuuint64_t strides[2] = {16, (cuuint64_t)(kblocks * 512)};
+    cuuint32_t box[3] = {16, 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -604,8 +648,15 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
         }
         if (P.kp.block_scaled && d.K > 0) {
             const int64_t la_n = P.kp.a_batched ? P.kp.L : 1, lb_n = P.kp.b_batched ? P.kp.L : 1;
-            ok = ok && encode_sf_map(&h->maps[4], ksfa, la_n * P.kp.sf_mblocks * (int64_t)P.kp.num_kb);
-            ok = ok && encode_sf_map(&h->maps[5], ksfb, lb_n * P.kp.sf_nblocks * (int64_t)P.kp.num_kb);
+            if (P.kp.block_scaled == 2) {
+                // K here counts bytes (two elements each): ceil(K/16) factors, four per block
+                const int64_t kblocks = (2 * d.K + 63) / 64;
+                ok = ok && encode_sf_map_nv(&h->maps[4], ksfa, kblocks, la_n * P.kp.sf_mblocks);
+                ok = ok && encode_sf_map_nv(&h->maps[5], ksfb, kblocks, lb_n * P.kp.sf_nblocks);
+            } else {
+                ok = ok && encode_sf_map(&h->maps[4], ksfa, la_n * P.kp.sf_mblocks * (int64_t)P.kp.num_kb);
+                ok = ok && encode_sf_map(&h->maps[5], ksfb, lb_n * P.kp.sf_nblocks * (int64_t)P.kp.num_kb);
+            }
         } else {
             h->maps[4] = h->maps[0];
             h->maps[5] = h->maps[0];

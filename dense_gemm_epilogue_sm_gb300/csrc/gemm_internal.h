@@ -72,9 +72,12 @@ struct KernelParams {
     // other workers' fp32 partial sums before the epilogue.  Without a split,
     // dp_tiles = num_tiles and sk_iters = 0.
     int32_t clc;                  // 1: dynamic schedule (cluster launch control), grid = every tile
-    // Block scaling (block_scaled = 1): one ue8m0 factor per 32 K elements;
-    // the factors of 128 rows x one K stage (4 factors each) form one
-    // 512-byte block; a batch's tensor holds blocks (row/128) * num_kb + kb.
+    // Block scaling.  block_scaled = 1 (MXFP8): one ue8m0 factor per 32 K
+    // elements; the factors of 128 rows x one K stage (4 factors each) form
+    // one 512-byte block; a batch's tensor holds blocks (row/128) * num_kb + kb.
+    // block_scaled = 2 (NVFP4): operands are planned as bytes (two e2m1 per
+    // byte, K and num_kb in bytes), one ue4m3 factor per 16 elements, four
+    // blocks per 128 rows and K stage, loaded through a map of their own.
     // MX output (out_f8 = 1): D in e4m3, factors written to sfd in the
     // basic-block layout (rows = M, one factor per 32 columns; sfd_kb4 =
     // ceil(ceil(N/32)/4) blocks along N; sfd_bstride bytes per batch).
@@ -111,7 +114,7 @@ struct LaunchArgs {
     int cta_group;                // 1 or 2 (CTA pair, cluster of 2)
     int tile_n;                   // 128 or 256
     int out_bytes;                // 2 or 4
-    int block_scaled;             // 1: the block-scaled (MX) kernel
+    int block_scaled;             // 1: MXFP8, 2: NVFP4 block-scaled kernel
     int grid;                     // CTAs (a multiple of cta_group)
     cudaStream_t stream;
 };

@@ -51,28 +51,31 @@ constexpr int kPairAccBufs = 2;
 // that have not read them yet.
 constexpr int kClcSlots = 4;
 
-// BS: block-scaled operands (e4m3 with one ue8m0 scale factor per 32 K
-// elements).  Each stage then also holds the 512-byte scale-factor blocks of
-// its A rows and B rows, which the MMA thread copies into TMEM columns after
-// the accumulators (8 columns per stage).
+// BS: block-scaled operands.  1: MXFP8, e4m3 with one ue8m0 scale factor per
+// 32 K elements; 2: NVFP4, e2m1 (two per byte) with one ue4m3 factor per 16.
+// Each stage then also holds the 512-byte scale-factor blocks of its A rows
+// and B rows (one per 128 rows for MXFP8, whose 128-element stage has four
+// factors a row; four for NVFP4, whose 256-element stage has sixteen), which
+// the MMA thread copies into TMEM columns after the accumulators.
 // TMEM accumulators: two, except for block-scaled 256-wide tiles, whose
 // 256-column accumulator leaves room for one only beside the scale factors.
-__host__ __device__ constexpr int acc_bufs(int cg, int bn, bool bs) {
+__host__ __device__ constexpr int acc_bufs(int cg, int bn, int bs) {
     return (bs && bn == 256) ? 1 : (cg == 2 ? kPairAccBufs : 2);
 }
 
-template <int CG, int BN, int OB, bool BS = false>
+template <int CG, int BN, int OB, int BS = 0>
 struct Cfg {
     static constexpr int kAccBufs = acc_bufs(CG, BN, BS);
     static constexpr int kBRows = BN / CG;                          // rows of B this CTA loads
-    static constexpr int kStages = BS ? (CG == 2 ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
+    static constexpr int kStages = BS == 2 ? 5 : BS ? (CG == 2 ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
     static constexpr int kABytes = kTileM * kStageKBytes;           // 16 KiB
     static constexpr int kBBytes = kBRows * kStageKBytes;
-    // scale-factor blocks: A's 128 rows and the tile's BN columns, 512 bytes
-    // per 128; the stage keeps 1024-byte alignment
-    static constexpr int kSfTxBytes = BS ? 512 + 512 * (BN / 128) : 0;
+    // scale-factor blocks of A's 128 rows and the tile's BN columns, per K
+    // stage; the stage keeps 1024-byte alignment
+    static constexpr int kSfK = BS == 2 ? 4 : 1;                    // blocks per 128 rows and stage
+    static constexpr int kSfTxBytes = BS ? kSfK * (512 + 512 * (BN / 128)) : 0;
     static constexpr int kSfBytes = (kSfTxBytes + 1023) / 1024 * 1024;
-    static constexpr int kSfCols = BS ? 4 + 4 * (BN / 128) : 0;    // TMEM columns of one stage's factors
+    static constexpr int kSfCols = BS ? kSfK * (4 + 4 * (BN / 128)) : 0;   // TMEM columns of one stage's factors
     static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;   // this CTA's share of a stage
     static constexpr int kTxBytes = kABytes + kBBytes + kSfTxBytes;    // bytes one stage's copies bring
     // 64 (16-bit D), 32 (fp32 D), or 64 (e4m3 D with MX factors, stored directly)
@@ -84,8 +87,8 @@ struct Cfg {
     static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static constexpr int kRingBytes = kStages * kStageBytes;
     // epilogue staging buffers per warp: two (a store drains while the next
-    // subtile fills), one where the ring needs the room (block-scaled 256-wide)
-    static constexpr int kEpiBufs = (BS && BN == 256) ? 1 : 2;
+    // subtile fills), one where the ring needs the room (MXFP8 256-wide)
+    static constexpr int kEpiBufs = (BS == 1 && BN == 256) ? 1 : 2;
     static constexpr int kEpiBytes = kEpiWarps * kEpiBufs * kEpiBufBytes;
     // Stages are released to the producer in groups: every tcgen05.commit
     // costs the tensor front end cycles that MMAs cannot use, so one commit
@@ -95,6 +98,7 @@ struct Cfg {
     static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps + 1 + 2 * kClcSlots;
     static constexpr int kSmemBytes =
         1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kClcSlots * 16 + kNumBars * 8 + 16;
+    static_assert(kSmemBytes <= 232448, "227 KB of shared memory per CTA");
 };
 
 
@@ -434,6 +438,15 @@ __host__ __device__ constexpr uint32_t idesc_mx(int cg, int bn, uint32_t a_mn, u
            ((uint32_t)((128 * cg) >> 4) << 24) | (sf_byte << 29);
 }
 
+// Instruction descriptor for kind::mxf4nvf4 with 16-element scale vectors
+// (scale_vec::4X): A and B e2m1 (type 1 of this kind, bits 7-9, 10-12), both
+// K-major, N >> 3 (17-22), ue4m3 scale factors (bit 23 clear), M >> 4
+// (24-28).  Each MMA (K = 64) reads all four factor bytes of its TMEM words,
+// so the factor byte selectors stay 0.
+__host__ __device__ constexpr uint32_t idesc_nv(int cg, int bn) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)((128 * cg) >> 4) << 24);
+}
+
 // Shared-memory descriptor of a 512-byte scale-factor block read as 32 rows
 // of 16 bytes, no swizzle: 8-row core matrices 128 bytes apart.
 __device__ __forceinline__ uint64_t sf_desc(uint32_t addr) {
@@ -471,12 +484,15 @@ struct MmaCtx {
 // (local and kernel-parameter memory behind a reference) would be re-loaded
 // after every MMA, a chain of dependent loads between two MMAs.
 //
-// BS: block-scaled MMAs.  Each stage's two scale-factor blocks are copied
-// into TMEM (8 columns per stage after the accumulators) ahead of the
+// BS: block-scaled MMAs.  Each stage's scale-factor blocks are copied into
+// TMEM (one slot of columns per stage after the accumulators) ahead of the
 // stage's four MMAs; tcgen05.cp and tcgen05.mma of one thread run in issue
 // order, so a copy never overtakes the MMAs that still read the columns it
-// overwrites one lap later.  MMA j reads factor byte j of each word.
-template <int CG, int BN, int S, int G, bool F8, uint32_t IDESC, bool BS = false>
+// overwrites one lap later.  MXFP8 (BS = 1): one block each for A and for
+// every 128 columns of B, 4 columns apiece; MMA j (32 elements of K) reads
+// factor byte j of each word.  NVFP4 (BS = 2): four blocks each, and MMA j
+// (64 elements of K) reads the whole words of block j.
+template <int CG, int BN, int S, int G, bool F8, uint32_t IDESC, int BS = 0>
 __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     const KernelParams& p = m.p;                 // slow paths (wait_bar) only
     const int first_tile = m.first_tile, tile_step = m.tile_step;
@@ -531,7 +547,28 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
             const uint64_t soff = (uint64_t)((stage * stage_bytes) >> 4);
             const uint64_t ad = a_base + soff, bd = b_base + soff;
             const uint32_t first = kb != kb0;
-            if constexpr (BS) {
+            if constexpr (BS == 2) {
+                // slot columns: A's block j at 4 j, B's block j at 16 + kNB*4 j
+                // (+4 per 128 columns of the tile); shared memory holds A's four
+                // blocks, then each 128 columns' four blocks of B
+                constexpr uint32_t kNB = BN / 128;
+                constexpr uint32_t kSfCol0 = (uint32_t)(kAccBufs * BN);
+                constexpr uint32_t kSfCols = 16u + 16u * kNB, kSfBytes = (2048u + 2048u * kNB + 1023u) / 1024u * 1024u;
+                const uint32_t sfs = ring + (uint32_t)stage * stage_bytes + stage_bytes - kSfBytes;
+                const uint32_t sfa = tmem_base + kSfCol0 + kSfCols * (uint32_t)stage, sfb = sfa + 16u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    ptx::tmem_cp_32x128b_x4<CG>(sfa + 4u * j, sf_desc(sfs + 512u * j));
+#pragma unroll
+                    for (int jb = 0; jb < (int)kNB; ++jb)
+                        ptx::tmem_cp_32x128b_x4<CG>(sfb + 4u * (kNB * j + jb), sf_desc(sfs + 2048u * (1 + jb) + 512u * j));
+                }
+                ptx::mma_nv<CG, IDESC>(d_tmem, ad, bd, sfa, sfb, first);
+                ready = ptx::mbar_test_wait(full_bar(next), next_phase);
+                ptx::mma_nv<CG, IDESC>(d_tmem, ad + a_step, bd + b_step, sfa + 4u, sfb + 4u * kNB, 1u);
+                ptx::mma_nv<CG, IDESC>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, sfa + 8u, sfb + 8u * kNB, 1u);
+                ptx::mma_nv<CG, IDESC>(d_tmem, ad + 3 * a_step, bd + 3 * b_step, sfa + 12u, sfb + 12u * kNB, 1u);
+            } else if constexpr (BS == 1) {
                 constexpr uint32_t kSfCol0 = (uint32_t)(kAccBufs * BN);
                 constexpr uint32_t kSfCols = 4u + 4u * (BN / 128), kSfBytes = (512u + 512u * (BN / 128) + 1023u) / 1024u * 1024u;
                 const uint32_t sfs = ring + (uint32_t)stage * stage_bytes + stage_bytes - kSfBytes;
@@ -581,7 +618,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     }
 }
 
-template <int CG, int BN, int OB, bool BS = false>
+template <int CG, int BN, int OB, int BS = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -716,7 +753,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < C::kBRows / mn_box; ++c)
                                 load(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb);
                         }
-                        if constexpr (BS) {
+                        if constexpr (BS == 2) {
+                            // Four 512-byte blocks per 128 rows and K stage, one box
+                            // at (K block 4 kb, 128-row block) of the batch's tensor
+                            const uint32_t sf = sb + C::kBBytes;
+                            load(sf, &tmSA, 0, kb * 128, la * p.sf_mblocks + m0 / 128);
+#pragma unroll
+                            for (int j = 0; j < BN / 128; ++j)
+                                load(sf + 2048 * (1 + j), &tmSB, 0, kb * 128, lb * p.sf_nblocks + nb * BN / 128 + j);
+                        } else if constexpr (BS == 1) {
                             // One 512-byte scale-factor block per 128 rows and K stage:
                             // block (rows / 128) * num_kb + kb of the batch's tensor, read
                             // as 32 rows of 16 bytes.  Each CTA takes its own A rows'
@@ -763,11 +808,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             MmaCtx<CG, BN, S> m{p,          ptx::smem_addr(ring), C::kABytes, C::kStageBytes, bar0,
                                 tmem_base,  first_tile,           tile_step,   abort_flag,       peer_abort,
                                 resp0,      clc_full0,            clc_empty0};
-            if constexpr (BS) {
+            if constexpr (BS == 2) {
+                mma_role<CG, BN, S, C::kGroup, true, idesc_nv(CG, BN), 2>(m);   // K-major only
+            } else if constexpr (BS == 1) {
                 switch (p.mma_variant & 3) {     // A / B MN-major
 #define GEMM_MX_CASE(v)                                                                      \
     case v:                                                                                  \
-        mma_role<CG, BN, S, C::kGroup, true, idesc_mx(CG, BN, ((v) >> 1) & 1, (v) & 1, 0), true>(m); \
+        mma_role<CG, BN, S, C::kGroup, true, idesc_mx(CG, BN, ((v) >> 1) & 1, (v) & 1, 0), 1>(m); \
         break;
                     GEMM_MX_CASE(0) GEMM_MX_CASE(1) GEMM_MX_CASE(2) GEMM_MX_CASE(3)
 #undef GEMM_MX_CASE
@@ -1158,7 +1205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // The host-side operations of one kernel variant (declared in
 // gemm_variants.h; instantiated in gemm_ob1.cu, gemm_ob2.cu, gemm_ob4.cu).
-template <int CG, int BN, int OB, bool BS>
+template <int CG, int BN, int OB, int BS>
 static cudaLaunchConfig_t variant_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -1174,25 +1221,25 @@ static cudaLaunchConfig_t variant_config(int grid, cudaStream_t stream, cudaLaun
     return cfg;
 }
 
-template <int CG, int BN, int OB, bool BS>
+template <int CG, int BN, int OB, int BS>
 size_t Variant<CG, BN, OB, BS>::smem() {
     return Cfg<CG, BN, OB, BS>::kSmemBytes;
 }
 
-template <int CG, int BN, int OB, bool BS>
+template <int CG, int BN, int OB, int BS>
 cudaError_t Variant<CG, BN, OB, BS>::prepare() {
     return cudaFuncSetAttribute(gemm_kernel<CG, BN, OB, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Cfg<CG, BN, OB, BS>::kSmemBytes);
 }
 
-template <int CG, int BN, int OB, bool BS>
+template <int CG, int BN, int OB, int BS>
 cudaError_t Variant<CG, BN, OB, BS>::launch(const LaunchArgs& a) {
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = variant_config<CG, BN, OB, BS>(a.grid, a.stream, &attr);
     return cudaLaunchKernelEx(&cfg, gemm_kernel<CG, BN, OB, BS>, a.tmA, a.tmB, a.tmC, a.tmD, a.tmSA, a.tmSB, a.p);
 }
 
-template <int CG, int BN, int OB, bool BS>
+template <int CG, int BN, int OB, int BS>
 int Variant<CG, BN, OB, BS>::max_clusters() {
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = variant_config<CG, BN, OB, BS>(CG * 64, nullptr, &attr);

@@ -9,8 +9,9 @@
 namespace gemm_sm103 {
 
 // CG: CTAs per MMA (1, or a pair), BN: tile columns, OB: output element
-// bytes (1 = e4m3 with MX factors), BS: block-scaled (MX) operands.
-template <int CG, int BN, int OB, bool BS>
+// bytes (1 = e4m3 with MX factors), BS: block-scaled operands (0 none,
+// 1 MXFP8, 2 NVFP4).
+template <int CG, int BN, int OB, int BS>
 struct Variant {
     static size_t smem();
     static cudaError_t prepare();
@@ -19,8 +20,8 @@ struct Variant {
 };
 
 #define GEMM_FOR_EACH_VARIANT(X, OB)                                                                  \
-    X(2, 256, OB, false) X(1, 256, OB, false) X(1, 128, OB, false) X(2, 256, OB, true) X(2, 128, OB, true) \
-        X(1, 128, OB, true)
+    X(2, 256, OB, 0) X(1, 256, OB, 0) X(1, 128, OB, 0) X(2, 256, OB, 1) X(2, 128, OB, 1) X(1, 128, OB, 1)  \
+        X(2, 256, OB, 2) X(2, 128, OB, 2) X(1, 128, OB, 2)
 #define GEMM_EXTERN_VARIANT(CG, BN, OB, BS) extern template struct Variant<CG, BN, OB, BS>;
 #define GEMM_INSTANTIATE_VARIANT(CG, BN, OB, BS) template struct Variant<CG, BN, OB, BS>;
 

@@ -315,6 +315,27 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
             : "memory");
 }
 
+// Block-scaled e2m1 MMA with 16-element scale vectors (NVFP4, ue4m3
+// factors), K = 64 per instruction; factors as for mma_mx.
+template <int CG, uint32_t IDESC>
+__device__ __forceinline__ void mma_nv(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t accumulate) {
+    if constexpr (CG == 1)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %6, [%3], [%4], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(sfa), "r"(sfb), "r"(accumulate), "n"(IDESC)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %6, [%3], [%4], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(sfa), "r"(sfb), "r"(accumulate), "n"(IDESC)
+            : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

@@ -4,13 +4,14 @@ current CUDA stream.  Argument marshalling only; the GEMM runs in
 ``libgemm_sm103.so``."""
 import torch
 
-from . import (ACT_GELU, ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E4M3, F16, F32, OP_N,
-               OP_T, REDUCE_ABS_MAX, REDUCE_COL_SUM, REDUCE_ROW_SUM, ROW_MAJOR, BLOCK_SCALE_MX, BLOCK_SCALE_NONE,
+from . import (ACT_GELU, ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E2M1, E4M3, F16, F32, OP_N,
+               OP_T, REDUCE_ABS_MAX, REDUCE_COL_SUM, REDUCE_ROW_SUM, ROW_MAJOR, BLOCK_SCALE_MX, BLOCK_SCALE_NONE, BLOCK_SCALE_NV,
                OUT_SCALE_MX, OUT_SCALE_NONE,
                gemm_check, gemm_create, gemm_destroy, gemm_get_schedule, gemm_launch_count, gemm_run, gemm_run_args,
                gemm_run_ex, gemm_set_schedule, make_desc)
 
-DTYPE_CODE = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3}
+DTYPE_CODE = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1}
+BLOCK_SCALE_CODE = {"none": BLOCK_SCALE_NONE, "mx": BLOCK_SCALE_MX, "nv": BLOCK_SCALE_NV}
 ORDER_CODE = {"row": ROW_MAJOR, "col": COL_MAJOR}
 OP_CODE = {"N": OP_N, "T": OP_T}
 ACT_CODE = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU}
@@ -40,7 +41,7 @@ def desc_from_spec(spec, scale_a=1.0, scale_b=1.0):
         DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_d], DTYPE_CODE[spec.dtype_d],
         spec.alpha, spec.beta, scale_a, scale_b, ACT_CODE[spec.act], BIAS_CODE[spec.bias],
         reduce_code(getattr(spec, "reduce", "none")),
-        BLOCK_SCALE_MX if getattr(spec, "block_scale", "none") == "mx" else BLOCK_SCALE_NONE,
+        BLOCK_SCALE_CODE[getattr(spec, "block_scale", "none")],
         OUT_SCALE_MX if spec.dtype_d == "e4m3" else OUT_SCALE_NONE)
 
 

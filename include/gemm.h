@@ -76,7 +76,12 @@ typedef enum {
     GEMM_ERR_NO_DEVICE = 6
 } gemm_status_t;
 
-typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3 } gemm_dtype_t;
+/* GEMM_E2M1: 4-bit float (sign, 2 exponent bits with bias 1, 1 mantissa bit;
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; "Blackwell Narrow Precision Data
+ * Types"), two per byte along K, the element of lower K index in the low
+ * nibble.  Operand type of GEMM_BLOCK_SCALE_NV only; leading dimensions and
+ * batch strides still count elements. */
+typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3, GEMM_E2M1 = 4 } gemm_dtype_t;
 typedef enum { GEMM_COL_MAJOR = 0, GEMM_ROW_MAJOR = 1 } gemm_order_t;
 typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
 typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 } gemm_act_t;
@@ -90,19 +95,26 @@ typedef enum {
 } gemm_reduce_t;
 typedef enum { GEMM_BIAS_NONE = 0, GEMM_BIAS_COL = 1, GEMM_BIAS_ROW = 2 } gemm_bias_t;
 /* Block-scaled operands ("Technical Documentation: NVIDIA/cutlass", "Block
- * Scaled GEMMs"): D = act(alpha * sum_k (A(m,k) SFA(m,k/32)) (B(k,n) SFB(n,k/32))
- * + beta*C + bias).  GEMM_BLOCK_SCALE_MX: A and B e4m3 (mx_float8), scale
- * factors ue8m0 (value 2^(code-127), code 255 = NaN), one per 32 elements of
- * K.  Scale factors are passed to gemm_run_args as byte tensors in the
- * pages' 512-byte basic-block layout ("Scale Factor Layouts"): for a matrix
- * of R rows (M for A, N for B; rows of op(A) / columns of op(B)) and
- * SFK = ceil(K/32) factors per row, factor (r, f) of batch l is at byte
+ * Scaled GEMMs"): D = act(alpha * sum_k (A(m,k) SFA(m,k/SV)) (B(k,n) SFB(n,k/SV))
+ * + beta*C + bias), SV the scale-factor vector size.
+ *   GEMM_BLOCK_SCALE_MX: A and B e4m3 (mx_float8), scale factors ue8m0
+ *     (value 2^(code-127), code 255 = NaN), SV = 32.
+ *   GEMM_BLOCK_SCALE_NV: A and B GEMM_E2M1 (nv_float4), scale factors ue4m3
+ *     (e4m3 without its sign bit: code 0x7F = NaN, bit 7 must be 0), SV = 16.
+ *     Both operands K-contiguous (the pages' TN layout), K even, leading
+ *     dimensions and batch strides multiples of 32 elements (16 bytes);
+ *     otherwise GEMM_ERR_UNSUPPORTED / GEMM_ERR_MISALIGNED.  A per-tensor
+ *     fp32 global scale goes in scale_a / scale_b.
+ * Scale factors are passed to gemm_run_args as byte tensors in the pages'
+ * 512-byte basic-block layout ("Scale Factor Layouts"): for a matrix of R
+ * rows (M for A, N for B; rows of op(A) / columns of op(B)) and
+ * SFK = ceil(K/SV) factors per row, factor (r, f) of batch l is at byte
  *   l*ceil(R/128)*ceil(SFK/4)*512 + ((r/128)*ceil(SFK/4) + f/4)*512
  *   + (r%32)*16 + ((r%128)/32)*4 + f%4
  * Bytes of the padded tensor that name no real (r, f) are read by the
- * kernel and must not be 255 (NaN).  A batch whose A (B) is shared
+ * kernel and must not be NaN codes.  A batch whose A (B) is shared
  * (stride 0) shares SFA (SFB) too. */
-typedef enum { GEMM_BLOCK_SCALE_NONE = 0, GEMM_BLOCK_SCALE_MX = 1 } gemm_block_scale_t;
+typedef enum { GEMM_BLOCK_SCALE_NONE = 0, GEMM_BLOCK_SCALE_MX = 1, GEMM_BLOCK_SCALE_NV = 2 } gemm_block_scale_t;
 
 /* Block-scaled output ("Technical Documentation: NVIDIA/cutlass", "Blackwell
  * SM100 GEMMs": an epilogue that writes elements plus a block scale factor

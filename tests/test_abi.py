@@ -187,3 +187,37 @@ def test_mx_output_needs_e4m3_row_major_d_without_c_or_reductions():
         g.ERR_UNSUPPORTED
     assert _status(_desc(dtype_d=g.E4M3, out_scale=g.OUT_SCALE_MX, reduce=g.REDUCE_ROW_SUM))[0] == g.ERR_UNSUPPORTED
     assert _status(_desc(dtype_d=g.E4M3, out_scale=3))[0] == g.ERR_INVALID_ARG
+
+
+def _nv(**kw):
+    base = dict(M=4096, N=4096, K=4096, dtype_a=g.E2M1, dtype_b=g.E2M1, block_scale=g.BLOCK_SCALE_NV,
+                lda=4096, ldb=4096, ldd=4096)
+    base.update(kw)
+    return _desc(**base)
+
+
+def test_nvfp4_plans_k_major_e2m1_with_256_element_stages():
+    s, info = _status(_nv())
+    assert s == g.OK and (info.cta_group, info.tile_m, info.tile_n, info.tile_k, info.stages) == (2, 256, 256, 256, 5)
+    assert info.a_k_major and info.b_k_major
+    s, info = _status(_nv(M=2048, N=1024, ldd=1024))
+    assert s == g.OK and (info.cta_group, info.tile_n, info.tile_k) == (2, 128, 256)
+    s, info = _status(_nv(M=512, N=512, K=1000, lda=1024, ldb=1024, ldd=512))
+    assert s == g.OK and (info.cta_group, info.tile_n, info.tile_k, info.stages) == (1, 128, 256, 5)
+    # column-major D: computed transposed, still K-major on both sides
+    s, info = _status(_nv(order_d=g.COL_MAJOR))
+    assert s == g.OK and info.swapped and info.a_k_major and info.b_k_major
+
+
+def test_nvfp4_argument_rules():
+    assert _status(_nv(dtype_a=g.E4M3, dtype_b=g.E4M3))[0] == g.ERR_UNSUPPORTED      # e2m1 only
+    assert _status(_nv(block_scale=g.BLOCK_SCALE_MX))[0] == g.ERR_UNSUPPORTED        # mx_float8 is e4m3
+    assert _status(_nv(block_scale=g.BLOCK_SCALE_NONE))[0] == g.ERR_INVALID_ARG      # e2m1 needs its factors
+    assert _status(_nv(dtype_d=g.E2M1))[0] == g.ERR_INVALID_ARG
+    assert _status(_nv(K=4095))[0] == g.ERR_UNSUPPORTED                              # odd K: half a byte
+    assert _status(_nv(lda=4112))[0] == g.ERR_MISALIGNED                             # 2056 bytes
+    assert _status(_nv(order_a=g.COL_MAJOR, lda=4096))[0] == g.ERR_UNSUPPORTED       # MN-major A
+    assert _status(_nv(order_b=g.ROW_MAJOR, ldb=4096))[0] == g.ERR_UNSUPPORTED       # MN-major B
+    assert _status(_nv(lda=2048))[0] == g.ERR_INVALID_ARG                            # lda < K
+    assert _status(_nv(batch=2, stride_a=4096 * 4096 + 16, stride_b=4096 * 4096, stride_d=4096 * 4096))[0] == \
+        g.ERR_MISALIGNED

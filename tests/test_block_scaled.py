@@ -1,14 +1,16 @@
-"""Block-scaled (MX) GEMM on the GPU: e4m3 operands with one ue8m0 scale
-factor per 32 elements of K, through gemm_run_args, against the oracle.
+"""Block-scaled GEMM on the GPU, through gemm_run_args, against the oracle:
+MXFP8 (e4m3 operands, one ue8m0 scale factor per 32 elements of K) and
+NVFP4 (e2m1 operands two per byte, one ue4m3 factor per 16, fp32 global
+scales in scale_a / scale_b).
 
-Both sides read the same e4m3 bytes and scale-factor bytes, so the only
+Both sides read the same operand bytes and scale-factor bytes, so the only
 difference is fp32 accumulation order: per element
     |D - D_ref| <= 2 K u |alpha| sum_k |a_k b_k| + 4 u |t| + ulp_D(|D_ref|)
 with u = 2^-24 and sum_k |a_k b_k| (scale factors included) taken from the
-oracle run on the operands with their sign bits cleared.  Integer data with
-factors 2^-1..2^1 makes every sum exact in fp32: compared bit for bit.  The
-exact case catches any misplaced scale factor, since factors differ by
-powers of two from block to block."""
+oracle run on the operands with their sign bits cleared.  Integer data
+(MXFP8) or any e2m1 code (NVFP4) with factors 2^-1..2^1 makes every sum
+exact in fp32: compared bit for bit.  The exact case catches any misplaced
+scale factor, since factors differ by powers of two from block to block."""
 import dataclasses
 
 import numpy as np
@@ -31,7 +33,7 @@ def _dev(t):
 
 
 def _run(spec, inputs, op=None, repeat=1):
-    op = op or GemmOp(desc_from_spec(spec))
+    op = op or GemmOp(desc_from_spec(spec, inputs.scale_a, inputs.scale_b))
     A, B, C, bias = (_dev(t) for t in (inputs.A, inputs.B, inputs.C, inputs.bias))
     sfa, sfb = _dev(inputs.extras["sfa"]), _dev(inputs.extras["sfb"])
     D = H.canary_buffer(spec)
@@ -43,6 +45,8 @@ def _run(spec, inputs, op=None, repeat=1):
 
 
 def _clear_sign(t):
+    if t.dtype == torch.uint8:                  # two e2m1 codes per byte, sign in bit 3 of each
+        return t & 0x77
     return (t.view(torch.uint8) & 0x7F).view(torch.float8_e4m3fn)
 
 
@@ -55,8 +59,8 @@ def _check(spec, inputs, bits, rows=None, exact=False):
         return
     abs_spec = dataclasses.replace(spec, alpha=1.0, beta=0.0, bias="none", act="none", dtype_d="f32",
                                    order_c="row", order_d="row", pad=0, ldc=0, ldd=0)
-    abs_inputs = wl.Inputs(abs_spec, _clear_sign(inputs.A), _clear_sign(inputs.B), None, None, 1.0, 1.0,
-                           extras=inputs.extras)
+    abs_inputs = wl.Inputs(abs_spec, _clear_sign(inputs.A), _clear_sign(inputs.B), None, None, inputs.scale_a,
+                           inputs.scale_b, extras=inputs.extras)
     _, tabs = gemm_ref.run_spec_rows(abs_spec, abs_inputs, rows=rows, want_t=True)
     got = d.reshape(spec.batch * spec.M, spec.N)
     if rows is not None:
@@ -167,3 +171,60 @@ def test_block_scaled_argument_errors():
     with pytest.raises(g.GemmError) as e:
         g.gemm_run_noalloc(desc, A.data_ptr(), B.data_ptr(), None, D.data_ptr(), None, None)
     assert e.value.status == g.ERR_UNSUPPORTED
+
+
+# ----------------------------------------------------------------- NVFP4 --
+NV_SPECS = [
+    wl.Spec("nv_one_tile", 128, 128, 256, dtype_in="e2m1", block_scale="nv", seed=111),
+    wl.Spec("nv_ragged_fused", 300, 520, 1000, dtype_in="e2m1", block_scale="nv", alpha=0.5, beta=1.0, act="relu",
+            bias="col", seed=112, pad=32),
+    wl.Spec("nv_short_k_colmajor_f32", 257, 190, 176, dtype_in="e2m1", dtype_d="f32", block_scale="nv",
+            order_c="col", order_d="col", beta=0.75, bias="row", seed=113),
+    wl.Spec("nv_transposed_gelu", 200, 272, 512, op_a="T", op_b="T", order_a="col", order_b="row",
+            dtype_in="e2m1", block_scale="nv", act="gelu", seed=114),
+    wl.Spec("nv_batched", 256, 384, 320, batch=3, dtype_in="e2m1", block_scale="nv", beta=1.0, seed=115),
+]
+NV_PAIR_SPECS = [
+    wl.Spec("nv_pair_ragged_fused", 2100, 1300, 1024, dtype_in="e2m1", block_scale="nv", alpha=0.5, beta=1.0,
+            act="relu", bias="col", seed=116, pad=32),
+    wl.Spec("nv_pair_batched_f32", 1024, 1024, 768, batch=3, dtype_in="e2m1", dtype_d="f32", block_scale="nv",
+            beta=1.0, seed=117),
+]
+NV_PAIR256_SPECS = [
+    wl.Spec("nv_pair256_ragged_fused", 2300, 2100, 1056, dtype_in="e2m1", block_scale="nv", alpha=0.5, beta=1.0,
+            act="gelu", bias="col", seed=118, pad=32),
+    wl.Spec("nv_pair256_colmajor", 2048, 2304, 2048, dtype_in="e2m1", block_scale="nv", order_c="col",
+            order_d="col", beta=1.0, bias="row", seed=119),
+]
+
+
+@pytest.mark.parametrize("spec", NV_SPECS + NV_PAIR_SPECS + NV_PAIR256_SPECS, ids=lambda s: s.name)
+def test_nvfp4_matches_oracle(spec):
+    inputs = wl.make_inputs(spec)
+    bits, op = _run(spec, inputs)
+    info = g.gemm_plan(op.desc)
+    want_cg = 1 if spec in NV_SPECS else 2
+    want_n = 256 if spec in NV_PAIR256_SPECS else 128
+    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (want_cg, 128 * want_cg, want_n, 256)
+    rows = H.sample_rows(spec) if want_cg == 2 else None
+    _check(spec, inputs, bits, rows=rows)
+    op.close()
+
+
+@pytest.mark.parametrize("M,N", [(512, 384), (2304, 1152), (2304, 2176)])   # one CTA, pairs 256x128, 256x256
+@pytest.mark.parametrize("order_d", ["row", "col"])
+def test_nvfp4_exact_sums_bit_exact(order_d, M, N):
+    spec = wl.Spec("nv_int", M, N, 1024, dtype_in="e2m1", dtype_d="f32", dist="int4", block_scale="nv",
+                   order_c=order_d, order_d=order_d, seed=120)
+    inputs = wl.make_inputs(spec)
+    bits, op = _run(spec, inputs, repeat=2)
+    _check(spec, inputs, bits, exact=True)
+    op.close()
+
+
+def test_nvfp4_full_size_sampled_rows():
+    spec = wl.get("nvfp4_8192")
+    inputs = wl.make_inputs(spec)
+    bits, op = _run(spec, inputs)
+    _check(spec, inputs, bits, rows=H.sample_rows(spec, per_tile=1))
+    op.close()
