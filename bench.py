@@ -410,13 +410,15 @@ def run_ours(args):
     long_region = total_ms > 1000.0
     pkey = "bf16_tflops_sustained" if long_region else "bf16_tflops"
     peak = float(peaks.get(pkey, FALLBACK_PEAKS[pkey]))
-    if spec.dtype_in == "e4m3":
-        peak *= 2.0       # nominal fp8:bf16 dense ratio 4.5 : 2.25
+    # nominal dense ratios to bf16: fp8 4.5 : 2.25, fp4 13.5 : 2.25
+    ratio = {"e4m3": 2.0, "e2m1": 6.0}.get(spec.dtype_in, 1.0)
+    peak *= ratio
     achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
     traffic = load_traffic(spec.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peak_src} {pkey}" + (" x2 (fp8 nominal ratio)" if spec.dtype_in == "e4m3" else ""),
+                "peak_source": f"{peak_src} {pkey}" + (f" x{ratio:g} ({spec.dtype_in} nominal ratio)" if ratio != 1.0
+                                                       else ""),
                 "algorithmic_bytes": in_bytes,
                 "hbm_frac": (in_bytes / (avg_kernel_ms * 1e-3)) / (float(peaks.get("hbm_gbs", 6800)) * 1e9)}
 
