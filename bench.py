@@ -129,6 +129,22 @@ def dist_setup():
     return world, rank, local
 
 
+def oracle_view(spec, inputs):
+    """The problem the oracle samples rows of: the workload itself, or for a
+    grouped workload its first group (the whole A with B and bias of group
+    0; rows of that group only).  Returns (spec, inputs, rows to draw from)."""
+    if not getattr(spec, "groups", 0):
+        return spec, inputs, spec.batch * spec.M
+    import dataclasses
+
+    from dense_gemm_epilogue_sm_gb300 import workloads as wl
+    sub = dataclasses.replace(spec, groups=0, group_sizes=())
+    per = spec.matrix_elems("b")
+    bias = None if inputs.bias is None else inputs.bias[: spec.N].contiguous()
+    sub_in = wl.Inputs(sub, inputs.A, inputs.B[:per].contiguous(), inputs.C, bias, inputs.scale_a, inputs.scale_b)
+    return sub, sub_in, int(inputs.extras["group_rows"][1])
+
+
 def oracle_sample(spec, inputs, rows_target_s=12.0):
     """Times the oracle on a bounded random row sample sized for about
     `rows_target_s` seconds; returns (tflops, rows, secs, threads)."""
@@ -138,7 +154,7 @@ def oracle_sample(spec, inputs, rows_target_s=12.0):
 
     threads = gemm_ref.max_threads()
     rng = np.random.default_rng(0)
-    total_rows = spec.batch * spec.M
+    spec, inputs, total_rows = oracle_view(spec, inputs)
     gemm_ref.run_spec_rows(spec, inputs, rows=np.array([0]))       # decodes B once (kept by the oracle)
     probe = np.sort(rng.choice(total_rows, size=min(total_rows, 2 * threads), replace=False))
     t0 = time.perf_counter()
@@ -166,7 +182,9 @@ def run_reference(args):
     inputs = wl.make_inputs(spec)
     threads = gemm_ref.max_threads()
     rng = np.random.default_rng(1)
-    total_rows = spec.batch * spec.M
+    grouped = getattr(spec, "groups", 0) > 0
+    wname = spec.name
+    spec, inputs, total_rows = oracle_view(spec, inputs)
     # size each step so the whole --steps/--warmup run stays within about two minutes
     probe = np.sort(rng.choice(total_rows, size=min(total_rows, threads), replace=False))
     gemm_ref.run_spec_rows(spec, inputs, rows=probe[:1])     # decodes B once (kept by the oracle)
@@ -184,12 +202,13 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     flops = 2.0 * nrows * spec.N * spec.K * args.steps
     value = flops / dt / 1e12
-    sample = f"{nrows} random full rows of the {spec.M}x{spec.N}x{spec.K} workload per step"
+    sample = f"{nrows} random full rows of the {spec.M}x{spec.N}x{spec.K} workload per step" + \
+        (" (rows of group 0)" if grouped else "")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": spec.name, "M": spec.M, "N": spec.N, "K": spec.K},
+        "data": "synthetic", "config": {"workload": wname, "M": spec.M, "N": spec.N, "K": spec.K},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -210,7 +229,8 @@ def run_e2e(launch, spec, inputs, dev, steps, flops):
             inputs.C.pin_memory() if inputs.C is not None else None,
             inputs.bias.pin_memory() if inputs.bias is not None else None,
             ex["sfa"].pin_memory() if "sfa" in ex else None,
-            ex["sfb"].pin_memory() if "sfb" in ex else None]
+            ex["sfb"].pin_memory() if "sfb" in ex else None,
+            ex["group_rows"].pin_memory() if "group_rows" in ex else None]
     nbuf = 2
     dev_in = [[None if t is None else torch.empty(t.shape, dtype=t.dtype, device=dev) for t in host]
               for _ in range(nbuf)]
@@ -228,7 +248,7 @@ def run_e2e(launch, spec, inputs, dev, steps, flops):
 
     def step(i):
         b = i % nbuf
-        A, B, C, bias, sfa, sfb = dev_in[b]
+        A, B, C, bias, sfa, sfb, gr = dev_in[b]
         with torch.cuda.stream(s_in):
             if i >= nbuf:
                 s_in.wait_event(comp_done[b])       # the GEMM of step i-2 has read these inputs
@@ -240,7 +260,7 @@ def run_e2e(launch, spec, inputs, dev, steps, flops):
             s_comp.wait_event(in_done[b])
             if i >= nbuf:
                 s_comp.wait_event(out_done[b])      # step i-2's D has been read back
-            launch(A, B, C, dev_out[b], bias, s_comp, sfa, sfb)
+            launch(A, B, C, dev_out[b], bias, s_comp, sfa, sfb, gr)
             comp_done[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
@@ -323,11 +343,15 @@ def run_ours(args):
     D = torch.empty(spec.batch * spec.matrix_elems("d"), dtype=wl.DT[spec.dtype_d], device=dev)
     desc = desc_from_spec(spec, inputs.scale_a, inputs.scale_b)
     info = g.gemm_plan(desc)
-    op = GemmOp(desc)
+    groups = getattr(spec, "groups", 0)
+    op = GemmOp(desc, groups=groups)
+    gr_d = ex["group_rows"].to(dev) if "group_rows" in ex else None
 
-    def launch(A, B, C, D, bias, stream, sfa=None, sfb=None):
+    def launch(A, B, C, D, bias, stream, sfa=None, sfb=None, gr=None):
         # block-scaled descriptors carry their scale factors through gemm_run_args
-        if spec.block_scale != "none" or sfd_d is not None:
+        if groups:
+            op.run_grouped(A, B, C, D, gr if gr is not None else gr_d, bias, stream=stream)
+        elif spec.block_scale != "none" or sfd_d is not None:
             op.run_args(A, B, C, D, bias, sfa=sfa if sfa is not None else sfa_d,
                         sfb=sfb if sfb is not None else sfb_d, sfd=sfd_d, stream=stream)
         else:
@@ -428,6 +452,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": spec.dtype_in if spec.dtype_in != "e4m3" else "e4m3",
         "data": "synthetic (seeded torch CPU generator; N(0,1) operands, bias N(0,0.1))",
         "config": {"workload": spec.name, "M": spec.M, "N": spec.N, "K": spec.K, "batch": spec.batch,
+                   **({"groups": groups} if groups else {}),
                    "alpha": spec.alpha, "beta": spec.beta, "act": spec.act, "bias": spec.bias,
                    "out": spec.dtype_d, "l2": "inputs larger than L2" if flush is None else "L2 flushed between steps",
                    "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "stages": info.stages,

@@ -106,6 +106,8 @@ def _load():
         "gemm_run": (i32, [vp, vp, vp, vp, vp, vp, vp]),
         "gemm_run_ex": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "gemm_run_args": (i32, [vp, ctypes.POINTER(GemmArgs), vp]),
+        "gemm_grouped_create": (i32, [ctypes.POINTER(vp), ctypes.POINTER(GemmDesc), i32]),
+        "gemm_grouped_run": (i32, [vp, vp, vp, vp, vp, vp, vp, vp]),
         "gemm_check": (i32, [vp]),
         "gemm_destroy": (i32, [vp]),
         "gemm_set_debug": (i32, [vp, i32, u32]),
@@ -129,7 +131,8 @@ def _load():
 
 
 lib = _load()
-EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_run_ex", "gemm_run_args", "gemm_check", "gemm_destroy", "gemm_set_debug",
+EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_run_ex", "gemm_run_args", "gemm_grouped_create",
+            "gemm_grouped_run", "gemm_check", "gemm_destroy", "gemm_set_debug",
             "gemm_set_schedule", "gemm_get_schedule", "gemm_launch_count", "gemm_status_str", "gemm_run_noalloc",
             "gemm_layout_query", "gemm_layout_eval", "gemm_layout_op", "gemm_layout_gather_f32")
 
@@ -214,6 +217,21 @@ def gemm_run_args(handle, stream, **buffers):
     s = lib.gemm_run_args(handle, ctypes.byref(a), stream)
     if s != OK:
         raise GemmError(s, "gemm_run_args")
+
+
+def gemm_grouped_create(desc, groups):
+    h = ctypes.c_void_p()
+    s = lib.gemm_grouped_create(ctypes.byref(h), ctypes.byref(desc), groups)
+    if s != OK:
+        raise GemmError(s, "gemm_grouped_create")
+    return h
+
+
+def gemm_grouped_run(handle, A, B, C, D, bias, group_rows, stream):
+    """group_rows: device address of groups + 1 int64 row offsets."""
+    s = lib.gemm_grouped_run(handle, A, B, C, D, bias, group_rows, stream)
+    if s != OK:
+        raise GemmError(s, "gemm_grouped_run")
 
 
 def gemm_check(handle):

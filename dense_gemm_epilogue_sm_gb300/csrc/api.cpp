@@ -81,8 +81,24 @@ struct Plan {
 
 bool aligned16(int64_t elems, int bytes) { return ((elems * bytes) % 16) == 0; }
 
-gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
+// groups > 0: a grouped GEMM (gemm_grouped_create); desc.batch must be 1,
+// B and the bias get `groups` batches (strides stride_b, stride_bias).
+gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out, int32_t groups = 0) {
     if (!desc || !out) return GEMM_ERR_INVALID_ARG;
+    if (groups < 0 || groups > 65535) return GEMM_ERR_INVALID_ARG;
+    if (groups > 0) {
+        // one A, C and D split by rows; no swap (row-major D), no splits of K
+        // across workers, none of the extensions that keep per-batch state
+        if (desc->batch != 1 || desc->stride_a || desc->stride_c || desc->stride_d) return GEMM_ERR_INVALID_ARG;
+        if (desc->order_d != GEMM_ROW_MAJOR || (desc->beta != 0.0f && desc->order_c != GEMM_ROW_MAJOR))
+            return GEMM_ERR_UNSUPPORTED;
+        if (desc->block_scale != GEMM_BLOCK_SCALE_NONE || desc->out_scale != GEMM_OUT_SCALE_NONE || desc->reduce ||
+            desc->bias == GEMM_BIAS_ROW)
+            return GEMM_ERR_UNSUPPORTED;
+        // A K-contiguous: a group's first row is any offset, and a tensor copy
+        // may start at any row but only at 16-byte-aligned inner coordinates
+        if ((desc->op_a == GEMM_OP_N) != (desc->order_a == GEMM_ROW_MAJOR)) return GEMM_ERR_UNSUPPORTED;
+    }
     // NVFP4 operands are planned as bytes: two e2m1 elements per byte along
     // K (both operands K-contiguous), so K, the leading dimensions and the
     // batch strides of A and B are halved and the byte view is planned like
@@ -169,8 +185,10 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     P.out_bytes = ob;
 
     const int64_t L = d.batch;
+    const int64_t Lb = groups > 0 ? groups : L;             // batches of B (and of the bias)
+    if (groups > 1 && (d.stride_b < 0 || !aligned16(d.stride_b, ab))) return GEMM_ERR_MISALIGNED;
     gl::Layout la = logical_layout(d.op_a, d.order_a, d.M, d.K, d.lda, L, L > 1 ? d.stride_a : 0);  // (M,K,L)
-    gl::Layout lbt = transpose2(logical_layout(d.op_b, d.order_b, d.K, d.N, d.ldb, L, L > 1 ? d.stride_b : 0));  // (N,K,L)
+    gl::Layout lbt = transpose2(logical_layout(d.op_b, d.order_b, d.K, d.N, d.ldb, Lb, Lb > 1 ? d.stride_b : 0));  // (N,K,Lb)
     gl::Layout ld_ = logical_layout(GEMM_OP_N, d.order_d, d.M, d.N, d.ldd, L, d.stride_d);   // (M,N,L)
 
     // The kernel writes D with N contiguous.  A column-major D is the
@@ -296,7 +314,8 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out) {
     k.mma_variant = (d.dtype_a == GEMM_E4M3 ? 8 : 0) + (d.dtype_a == GEMM_BF16 ? 4 : 0) + (a_kmaj ? 0 : 2) +
                     (b_kmaj ? 0 : 1);
     k.a_batched = L > 1 && mode_stride(P.a, 2) != 0;
-    k.b_batched = L > 1 && mode_stride(P.b, 2) != 0;
+    k.b_batched = Lb > 1 && mode_stride(P.b, 2) != 0;
+    k.groups = groups;
     k.c_batched = L > 1 && d.stride_c != 0;
     k.alpha = d.alpha * d.scale_a * d.scale_b;            // per-tensor dequantisation folded into alpha
     k.beta = d.beta;
@@ -404,7 +423,8 @@ bool encode_sf_map_nv(CUtensorMap* map, const void* base, int64_t kblocks, int64
 }
 
 // Persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more
-// than there are tiles.
+// than there are tiles.  A grouped launch counts its tiles on the device, so
+// it takes every slot.
 int grid_for(const Plan& P, int sm_count, int max_clusters) {
     const int64_t tiles = P.info.tiles;
     const int cg = P.cta_group;
@@ -412,6 +432,7 @@ int grid_for(const Plan& P, int sm_count, int max_clusters) {
     int64_t slots = sm_count / cg;
     if (max_clusters > 0 && max_clusters < slots) slots = max_clusters;
     if (slots < 1) slots = 1;
+    if (P.kp.groups > 0) return (int)(slots * cg);
     return (int)((tiles < slots ? tiles : slots) * cg);
 }
 
@@ -462,7 +483,7 @@ gemm_status_t apply_schedule(gemm_handle_s* h, int mode) {
         return GEMM_OK;
     }
     const int64_t T = k.num_tiles, kb = k.num_kb;
-    if (mode == GEMM_SCHED_DATA_PARALLEL || workers < 1 || kb < 1) return GEMM_OK;
+    if (mode == GEMM_SCHED_DATA_PARALLEL || k.groups > 0 || workers < 1 || kb < 1) return GEMM_OK;
     const int64_t waves = T / workers, rest = T % workers;
     int64_t dp, sk, ranges;
     if (mode == GEMM_SCHED_STREAM_K) {
@@ -543,12 +564,12 @@ gemm_status_t gemm_plan(const gemm_desc_t* desc, gemm_plan_info_t* info) {
     return s;
 }
 
-gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
+static gemm_status_t create_impl(gemm_handle_t* out, const gemm_desc_t* desc, int32_t groups) {
     if (!out) return GEMM_ERR_INVALID_ARG;
     *out = nullptr;
     gemm_handle_s* h = new (std::nothrow) gemm_handle_s;
     if (!h) return GEMM_ERR_INVALID_ARG;
-    gemm_status_t s = validate_and_plan(desc, &h->plan);
+    gemm_status_t s = validate_and_plan(desc, &h->plan, groups);
     if (s != GEMM_OK) {
         delete h;
         return s;
@@ -595,12 +616,24 @@ gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) {
     return GEMM_OK;
 }
 
+gemm_status_t gemm_create(gemm_handle_t* out, const gemm_desc_t* desc) { return create_impl(out, desc, 0); }
+
+gemm_status_t gemm_grouped_create(gemm_handle_t* out, const gemm_desc_t* desc, int32_t groups) {
+    if (groups < 1) {
+        if (out) *out = nullptr;
+        return GEMM_ERR_INVALID_ARG;
+    }
+    return create_impl(out, desc, groups);
+}
+
 static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
                               const float* bias, float* row_sum, float* col_sum, float* abs_max, const void* sfa,
-                              const void* sfb, void* sfd, void* stream) {
+                              const void* sfb, void* sfd, void* stream, const int64_t* group_rows = nullptr) {
     if (!h) return GEMM_ERR_INVALID_ARG;
     Plan& P = h->plan;
     const gemm_desc_t& d = P.d;
+    if ((P.kp.groups > 0) != (group_rows != nullptr)) return GEMM_ERR_INVALID_ARG;
+    if (group_rows && (reinterpret_cast<uintptr_t>(group_rows) & 7u)) return GEMM_ERR_MISALIGNED;
     if (P.kp.out_f8 && !sfd) return GEMM_ERR_INVALID_ARG;
     if (P.kp.block_scaled && d.K > 0) {
         if (!sfa || !sfb) return GEMM_ERR_INVALID_ARG;
@@ -686,6 +719,7 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
     la.p.sfa = static_cast<const uint8_t*>(ksfa);
     la.p.sfb = static_cast<const uint8_t*>(ksfb);
     la.p.sfd = static_cast<uint8_t*>(sfd);
+    la.p.group_rows = group_rows;
     la.cta_group = P.cta_group;
     la.tile_n = P.tile_n;
     la.out_bytes = P.out_bytes;
@@ -739,6 +773,12 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, const void* A, const void* B, const v
     return run_impl(h, A, B, C, D, bias, row_sum, col_sum, abs_max, nullptr, nullptr, nullptr, stream);
 }
 
+gemm_status_t gemm_grouped_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
+                               const float* bias, const int64_t* group_rows, void* stream) {
+    if (!group_rows) return GEMM_ERR_INVALID_ARG;
+    return run_impl(h, A, B, C, D, bias, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, stream, group_rows);
+}
+
 gemm_status_t gemm_run_args(gemm_handle_t h, const gemm_args_t* a, void* stream) {
     if (!a) return GEMM_ERR_INVALID_ARG;
     return run_impl(h, a->A, a->B, a->C, a->D, a->bias, a->row_sum, a->col_sum, a->abs_max, a->sfa, a->sfb, a->sfd,
@@ -766,6 +806,8 @@ gemm_status_t gemm_check(gemm_handle_t h) {
 
 gemm_status_t gemm_set_schedule(gemm_handle_t h, int32_t mode) {
     if (!h || mode < GEMM_SCHED_AUTO || mode > GEMM_SCHED_DYNAMIC) return GEMM_ERR_INVALID_ARG;
+    if (h->plan.kp.groups > 0 && mode != GEMM_SCHED_AUTO && mode != GEMM_SCHED_DATA_PARALLEL)
+        return GEMM_ERR_UNSUPPORTED;          // grouped: whole tiles only
     if (h->launched && cudaStreamSynchronize(h->last_stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;

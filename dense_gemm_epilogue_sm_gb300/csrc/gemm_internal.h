@@ -1,5 +1,5 @@
 // gemm_internal.h - what the host planner (api.cpp) hands the sm_103a kernel
-// (gemm_sm103.cu).  Not part of the public ABI.
+// (gemm_kernel.cuh).  Not part of the public ABI.
 #pragma once
 
 #include <cuda.h>
@@ -105,6 +105,13 @@ struct KernelParams {
     float* red_col_ws;
     uint32_t* red_amax_ws;
     int32_t inject;               // 1: skip the first load (bounded-wait test)
+    // Grouped GEMM (groups > 0): group g owns rows [group_rows[g],
+    // group_rows[g+1]) of A, C and D (one matrix each; offsets clamped to
+    // [0, M], each group starting where the previous one ends at the latest) and
+    // batch g of B and of the bias.  Its tiles follow those of group g - 1,
+    // M-block fastest; each CTA counts the tiles itself (data parallel only).
+    int32_t groups;
+    const int64_t* group_rows;    // device, groups + 1 entries
 };
 
 struct LaunchArgs {
@@ -113,7 +120,7 @@ struct LaunchArgs {
     KernelParams p;
     int cta_group;                // 1 or 2 (CTA pair, cluster of 2)
     int tile_n;                   // 128 or 256
-    int out_bytes;                // 2 or 4
+    int out_bytes;                // 1 (e4m3 with MX factors), 2 or 4
     int block_scaled;             // 1: MXFP8, 2: NVFP4 block-scaled kernel
     int grid;                     // CTAs (a multiple of cta_group)
     cudaStream_t stream;

@@ -166,6 +166,93 @@ __device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int
     nb = (int)(idx / p.tiles_m);
 }
 
+// Where a tile sits: M and N block, batch (group) index, and the tile's row
+// range in A, C and D (rows [m_base, m_end) for a grouped GEMM, [0, M)
+// otherwise).
+struct TilePos {
+    int mb, nb, l;
+    int m_base, m_end;
+    int cd_l;        // batch index of C and D (0 when grouped: one matrix)
+};
+
+// Group offsets as the kernel reads them: each clamped to [0, M], and group
+// g covers [e_(g-1), e_g) with e_g the running maximum of the clamped
+// offsets 0..g+1 (e_(-1) the first offset), so groups never overlap and
+// every access stays inside A, C and D whatever offsets the caller passes.
+__device__ __forceinline__ int clamp_row(const KernelParams& p, int i) {
+    const int64_t a = __ldg(p.group_rows + i);
+    return (int)(a < 0 ? 0 : (a > p.M ? (int64_t)p.M : a));
+}
+
+__device__ __forceinline__ int group_tiles(const KernelParams& p, int r0, int r1, int tile_rows) {
+    return (r1 - r0 + tile_rows - 1) / tile_rows * p.tiles_n;
+}
+
+// Tiles of every group (grouped GEMM), counted by one warp at the start:
+// 32 groups at a time, the running maximum by a warp scan.
+__device__ __forceinline__ int grouped_tile_count(const KernelParams& p, int tile_rows, int lane) {
+    int carry = clamp_row(p, 0);
+    int n = 0;
+    for (int c = 0; c < p.groups; c += 32) {
+        const int g = c + lane;
+        int e = g < p.groups ? clamp_row(p, g + 1) : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, e, off);
+            if (lane >= off) e = max(e, o);
+        }
+        e = max(e, carry);
+        int st = __shfl_up_sync(0xffffffffu, e, 1);
+        if (lane == 0) st = carry;
+        if (g < p.groups) n += group_tiles(p, st, e, tile_rows);
+        carry = __shfl_sync(0xffffffffu, e, 31);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    return n;
+}
+
+// A role's walk over the groups: tiles come in increasing order, so the
+// group of the next tile is found by moving forward from the last one.
+struct GroupWalk {
+    int g, base, tiles, r0, r1;
+};
+
+__device__ __forceinline__ GroupWalk group_walk_make(const KernelParams& p, int tile_rows) {
+    GroupWalk w{0, 0, 0, 0, 0};
+    if (p.groups > 0) {
+        w.r0 = clamp_row(p, 0);
+        w.r1 = max(w.r0, clamp_row(p, 1));
+        w.tiles = group_tiles(p, w.r0, w.r1, tile_rows);
+    }
+    return w;
+}
+
+__device__ __forceinline__ void tile_pos(const KernelParams& p, GroupWalk& w, int tile, int tile_rows, TilePos& t) {
+    if (p.groups == 0) {
+        tile_coords(p, tile, t.mb, t.nb, t.l);
+        t.m_base = 0;
+        t.m_end = p.M;
+        t.cd_l = t.l;
+        return;
+    }
+    while (tile >= w.base + w.tiles && w.g + 1 < p.groups) {
+        w.base += w.tiles;
+        ++w.g;
+        w.r0 = w.r1;
+        w.r1 = max(w.r1, clamp_row(p, w.g + 1));
+        w.tiles = group_tiles(p, w.r0, w.r1, tile_rows);
+    }
+    const int local = tile - w.base;
+    const int tm = (w.r1 - w.r0 + tile_rows - 1) / tile_rows;
+    t.mb = tm > 0 ? local % tm : 0;
+    t.nb = tm > 0 ? local / tm : 0;
+    t.l = w.g;
+    t.m_base = w.r0;
+    t.m_end = w.r1;
+    t.cd_l = 0;
+}
+
 template <bool B>
 struct BoolTag {
     static constexpr bool value = B;
@@ -188,11 +275,11 @@ __device__ __forceinline__ int64_t sk_range_start(int64_t sk_iters, int64_t r, i
     return sk_iters * r / ranges;
 }
 
-__device__ __forceinline__ Sched sched_make(const KernelParams& p, int worker, int workers) {
+__device__ __forceinline__ Sched sched_make(const KernelParams& p, int worker, int workers, int dp_tiles) {
     Sched s;
     s.tile = worker;
     s.step = workers;
-    s.dp_end = p.dp_tiles;
+    s.dp_end = dp_tiles;
     s.num_kb = p.num_kb;
     const int64_t r = workers - 1 - worker;
     if (r < p.sk_ranges) {
@@ -245,9 +332,10 @@ struct Work {
 };
 
 __device__ __forceinline__ Work work_make(const KernelParams& p, int worker, int workers, bool producer,
-                                          uint32_t resp0, uint32_t full0, uint32_t empty0, uint32_t rank, int cg) {
+                                          uint32_t resp0, uint32_t full0, uint32_t empty0, uint32_t rank, int cg,
+                                          int dp_tiles) {
     Work w;
-    w.s = sched_make(p, worker, workers);
+    w.s = sched_make(p, worker, workers, dp_tiles);
     w.dyn = p.clc != 0;
     w.producer = producer;
     w.first = true;
@@ -470,6 +558,7 @@ struct MmaCtx {
     volatile uint32_t* abort_flag;
     uint32_t peer_abort;
     uint32_t resp0, clc_full0, clc_empty0;   // dynamic schedule ring
+    int dp_tiles;           // whole tiles of the launch (counted in the kernel when grouped)
 };
 
 // The MMA issuer (one thread of the pair leader).  A tcgen05.mma blocks its
@@ -528,7 +617,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     int it = 0;
     bool issued = false;
     bool ready = ptx::mbar_test_wait(full_bar(0), 0);
-    Work wk = work_make(p, first_tile, tile_step, false, m.resp0, m.clc_full0, m.clc_empty0, 0u, CG);
+    Work wk = work_make(p, first_tile, tile_step, false, m.resp0, m.clc_full0, m.clc_empty0, 0u, CG, m.dp_tiles);
     int tile, kb0, kb1;
     for (; work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleMma, peer_abort, true); ++it) {
         const int buf = it % kAccBufs;
@@ -690,11 +779,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish<CG>();
     }
+    // grouped GEMM: the launch's tiles, from the group offsets in device memory
+    if (warp == 2 && p.groups > 0) {
+        const int n = grouped_tile_count(p, kTileRows, lane);
+        if (lane == 0) tmem_slot[2] = (uint32_t)n;
+    }
     ptx::tc_fence_before();
     __syncthreads();
     if constexpr (CG == 2) ptx::cluster_sync();   // the peer's barriers exist before anyone signals them
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const int dp_tiles = p.groups > 0 ? (int)tmem_slot[2] : p.dp_tiles;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA loads --
@@ -711,13 +806,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool skip_first = p.inject != 0 && rank == 0;
-            Work wk = work_make(p, first_tile, tile_step, true, resp0, clc_full0, clc_empty0, rank, CG);
+            Work wk = work_make(p, first_tile, tile_step, true, resp0, clc_full0, clc_empty0, rank, CG, dp_tiles);
+            GroupWalk gw = group_walk_make(p, kTileRows);
             int tile, kb0, kb1;
             while (work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleLoad, peer_abort, true)) {
-                int mb, nb, l;
-                tile_coords(p, tile, mb, nb, l);
+                TilePos tp;
+                tile_pos(p, gw, tile, kTileRows, tp);
+                const int mb = tp.mb, nb = tp.nb, l = tp.l;
                 const int la = p.a_batched ? l : 0, lb = p.b_batched ? l : 0;
-                const int m0 = mb * kTileRows + (int)rank * kTileM;
+                const int m0 = tp.m_base + mb * kTileRows + (int)rank * kTileM;
                 const int n0 = nb * BN + (int)rank * C::kBRows;
                 bool stop = false;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -807,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && rank == 0) {
             MmaCtx<CG, BN, S> m{p,          ptx::smem_addr(ring), C::kABytes, C::kStageBytes, bar0,
                                 tmem_base,  first_tile,           tile_step,   abort_flag,       peer_abort,
-                                resp0,      clc_full0,            clc_empty0};
+                                resp0,      clc_full0,            clc_empty0,  dp_tiles};
             if constexpr (BS == 2) {
                 mma_role<CG, BN, S, C::kGroup, true, idesc_nv(CG, BN), 2>(m);   // K-major only
             } else if constexpr (BS == 1) {
@@ -885,7 +982,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return true;
             };
-            Work wk = work_make(p, first_tile, tile_step, false, resp0, clc_full0, clc_empty0, rank, CG);
+            Work wk = work_make(p, first_tile, tile_step, false, resp0, clc_full0, clc_empty0, rank, CG, dp_tiles);
+            GroupWalk gw = group_walk_make(p, kTileRows);
             int tile, kb0, kb1;
             for (; ok; ++it) {
                 if (!__all_sync(0xffffffffu, work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleEpi, peer_abort,
@@ -893,8 +991,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 const int buf = it % C::kAccBufs;
                 const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
-                int mb, nb, l;
-                tile_coords(p, tile, mb, nb, l);
+                TilePos tp;
+                tile_pos(p, gw, tile, kTileRows, tp);
+                const int mb = tp.mb, nb = tp.nb, l = tp.l;
+                const int m_end = tp.m_end;        // rows past it belong to no output of this tile
+                const int dl = tp.cd_l;            // batch index of D
                 ok = __all_sync(0xffffffffu, wait_bar(accf_bar(buf), acc_par, p, abort_flag, kStatusRoleEpi, peer_abort));
                 if (!ok) break;
                 ptx::tc_fence_after();
@@ -933,10 +1034,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 [[maybe_unused]] const bool reducing = EXT && (p.red_rows | p.red_cols | p.red_amax) != 0;
                 float row_acc = 0.f;          // sum of t over this tile's columns of row `row`
                 uint32_t amax_bits = 0u;      // max |t| as fp32 bits (NaN sorts above inf)
-                const int row0 = mb * kTileRows + (int)rank * kTileM + q * kEpiRows;
+                const int row0 = tp.m_base + mb * kTileRows + (int)rank * kTileM + q * kEpiRows;
                 const int row = row0 + lane;
                 float row_bias = 0.f;
-                if (p.bias_mode == 2 && row < p.M) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
+                if (p.bias_mode == 2 && row < m_end) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
                 const float* bias_l = p.bias_mode == 1 ? p.bias + (int64_t)l * p.bias_stride : nullptr;
                 [[maybe_unused]] const int lc = p.c_batched ? l : 0;
                 // With a single accumulator the MMA waits for the whole
@@ -945,7 +1046,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the MMA works on the other one meanwhile and the release
                 // stays at the end of the tile.
                 const int n_end = nb * BN + BN < p.N ? nb * BN + BN : p.N;
-                const int last_sub = (row0 < p.M && n_end > nb * BN) ? (n_end - 1 - nb * BN) / C::kEpiCols : -1;
+                const int last_sub = (row0 < m_end && n_end > nb * BN) ? (n_end - 1 - nb * BN) / C::kEpiCols : -1;
                 bool released = false;
                 auto early_release = [&](int sub) {
                     if constexpr (C::kAccBufs == 1) {
@@ -958,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll 1
                 for (int sub = 0; sub < C::kSubtiles; ++sub) {
                     const int col0 = nb * BN + sub * C::kEpiCols;
-                    if (row0 >= p.M || col0 >= p.N) continue;     // nothing of this subtile is in range
+                    if (row0 >= m_end || col0 >= p.N) continue;     // nothing of this subtile is in range
                     if constexpr (OB == 1) {
                         // MX output: e4m3 elements and one ue8m0 factor per 32
                         // columns of a row (no C; checked on the host).
@@ -1016,8 +1117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 w[k] = code == 255u ? 0x7F7F7F7Fu
                                                     : ptx::pack4_e4m3(v[4 * k] * sc, v[4 * k + 1] * sc, v[4 * k + 2] * sc,
                                                                       v[4 * k + 3] * sc);
-                            if (row < p.M) {
-                                uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)l * p.d_bstride +
+                            if (row < m_end) {
+                                uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)dl * p.d_bstride +
                                                 (int64_t)row * p.ldd;
                                 if (c0 + 32 <= p.N) {
                                     *reinterpret_cast<uint4*>(drow + c0) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -1027,13 +1128,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         drow[c0 + i] = (uint8_t)(w[i >> 2] >> ((i & 3) * 8));
                                 }
                                 const int f = c0 / 32;
-                                p.sfd[(int64_t)l * p.sfd_bstride + ((int64_t)(row / 128) * p.sfd_kb4 + f / 4) * 512 +
+                                p.sfd[(int64_t)dl * p.sfd_bstride + ((int64_t)(row / 128) * p.sfd_kb4 + f / 4) * 512 +
                                       (row % 32) * 16 + ((row % 128) / 32) * 4 + f % 4] = (uint8_t)code;
                             }
                         }
                     } else {
-                        // the subtile holding a ragged row end is stored element by element
-                        const bool direct = p.d_ragged && col0 + C::kEpiCols > p.N;
+                        // the subtile holding a ragged row end, or a group's last rows
+                        // short of the end of D, is stored element by element
+                        const bool direct = (p.d_ragged && col0 + C::kEpiCols > p.N) ||
+                                            (row0 + kEpiRows > m_end && m_end < p.M);
                         const int sbi = sub_count % C::kEpiBufs;
                         ++sub_count;
                         uint8_t* sbuf = epi + (ew * C::kEpiBufs + sbi) * kEpiBufBytes;
@@ -1117,7 +1220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const int c0 = col0 + ch * VPC;
                                 float r[VPC];
         #pragma unroll
-                                for (int i = 0; i < VPC; ++i) r[i] = (row < p.M && c0 + i < p.N) ? v[i] : 0.f;
+                                for (int i = 0; i < VPC; ++i) r[i] = (row < m_end && c0 + i < p.N) ? v[i] : 0.f;
                                 if (p.red_rows) {
         #pragma unroll
                                     for (int i = 0; i < VPC; ++i) row_acc += r[i];
@@ -1143,11 +1246,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             if (!direct) {
                                 *slot = out;
-                            } else if (row < p.M) {
+                            } else if (row < m_end) {
                                 const int c0 = col0 + ch * VPC;
                                 const uint32_t w[4] = {out.x, out.y, out.z, out.w};
                                 uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
-                                                ((int64_t)l * p.d_bstride + (int64_t)row * p.ldd) * OB;
+                                                ((int64_t)dl * p.d_bstride + (int64_t)row * p.ldd) * OB;
         #pragma unroll
                                 for (int i = 0; i < VPC; ++i) {
                                     if (c0 + i >= p.N) break;
@@ -1163,7 +1266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::fence_async_shared();
                             __syncwarp();
                             if (lane == 0) {
-                                ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, l);
+                                ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, dl);
                                 ptx::bulk_commit();
                             }
                         }
@@ -1171,7 +1274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 if (!released) release_acc(buf);
-                if (EXT && p.red_rows && row < p.M) p.red_row_ws[((int64_t)l * p.tiles_n + nb) * p.M + row] = row_acc;
+                if (EXT && p.red_rows && row < m_end) p.red_row_ws[((int64_t)l * p.tiles_n + nb) * p.M + row] = row_acc;
                 if (EXT && p.red_amax) {
     #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1)

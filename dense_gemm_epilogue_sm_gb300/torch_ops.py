@@ -7,8 +7,8 @@ import torch
 from . import (ACT_GELU, ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E2M1, E4M3, F16, F32, OP_N,
                OP_T, REDUCE_ABS_MAX, REDUCE_COL_SUM, REDUCE_ROW_SUM, ROW_MAJOR, BLOCK_SCALE_MX, BLOCK_SCALE_NONE, BLOCK_SCALE_NV,
                OUT_SCALE_MX, OUT_SCALE_NONE,
-               gemm_check, gemm_create, gemm_destroy, gemm_get_schedule, gemm_launch_count, gemm_run, gemm_run_args,
-               gemm_run_ex, gemm_set_schedule, make_desc)
+               gemm_check, gemm_create, gemm_destroy, gemm_get_schedule, gemm_grouped_create, gemm_grouped_run,
+               gemm_launch_count, gemm_run, gemm_run_args, gemm_run_ex, gemm_set_schedule, make_desc)
 
 DTYPE_CODE = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1}
 BLOCK_SCALE_CODE = {"none": BLOCK_SCALE_NONE, "mx": BLOCK_SCALE_MX, "nv": BLOCK_SCALE_NV}
@@ -31,13 +31,15 @@ BIAS_CODE = {"none": BIAS_NONE, "col": BIAS_COL, "row": BIAS_ROW}
 
 def desc_from_spec(spec, scale_a=1.0, scale_b=1.0):
     L = spec.batch
-    stride = lambda w: spec.matrix_elems(w) if L > 1 else 0
+    grouped = getattr(spec, "groups", 0) > 0
+    # grouped: A, C, D one matrix each; B and the bias one per group
+    stride = lambda w: spec.matrix_elems(w) if (L > 1 and not grouped) or (grouped and w == "b") else 0
     bias_len = 0 if spec.bias == "none" else (spec.N if spec.bias == "col" else spec.M)
     return make_desc(
         spec.M, spec.N, spec.K, L, OP_CODE[spec.op_a], OP_CODE[spec.op_b], ORDER_CODE[spec.order_a],
         ORDER_CODE[spec.order_b], ORDER_CODE[spec.order_c], ORDER_CODE[spec.order_d],
         spec.ld("a"), spec.ld("b"), spec.ld("c"), spec.ld("d"),
-        stride("a"), stride("b"), stride("c"), stride("d"), bias_len if L > 1 else 0,
+        stride("a"), stride("b"), stride("c"), stride("d"), bias_len if (L > 1 or grouped) else 0,
         DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_in], DTYPE_CODE[spec.dtype_d], DTYPE_CODE[spec.dtype_d],
         spec.alpha, spec.beta, scale_a, scale_b, ACT_CODE[spec.act], BIAS_CODE[spec.bias],
         reduce_code(getattr(spec, "reduce", "none")),
@@ -52,9 +54,16 @@ def _ptr(t):
 class GemmOp:
     """One planned GEMM (a handle) bound to a device; call with device tensors."""
 
-    def __init__(self, desc):
+    def __init__(self, desc, groups=0):
         self.desc = desc
-        self.handle = gemm_create(desc)
+        self.groups = groups
+        self.handle = gemm_grouped_create(desc, groups) if groups else gemm_create(desc)
+
+    def run_grouped(self, A, B, C, D, group_rows, bias=None, stream=None):
+        """Grouped handle: group_rows is an int64 device tensor of groups + 1 row offsets."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        gemm_grouped_run(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(bias), _ptr(group_rows),
+                         s.cuda_stream)
 
     def __call__(self, A, B, C, D, bias=None, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream()

@@ -58,6 +58,8 @@ class Spec:
     reduce: str = "none"        # none, or a '+'-joined subset of row, col, amax
     block_scale: str = "none"   # none | mx (e4m3 data, ue8m0 scale per 32 elements of K)
                                 # | nv (e2m1 data, ue4m3 scale per 16 elements of K)
+    groups: int = 0             # > 0: grouped GEMM; M = rows of all groups, B and bias per group
+    group_sizes: tuple = ()     # grouped: explicit rows per group (else drawn by the generator)
     notes: str = ""
 
     # ----------------------------------------------------------- geometry --
@@ -96,10 +98,12 @@ class Spec:
         """Each operand read once, D written once (bias and C included)."""
         e_in, e_d = ESIZE[self.dtype_in], ESIZE[self.dtype_d]
         b = self.batch * (self.M * self.K * e_in + self.K * self.N * e_in + self.M * self.N * e_d)
+        if self.groups:                     # one B per group
+            b += (self.groups - 1) * self.K * self.N * e_in
         if self.beta != 0:
             b += self.batch * self.M * self.N * e_d
         if self.bias != "none":
-            b += 4 * (self.N if self.bias == "col" else self.M)
+            b += 4 * (self.N if self.bias == "col" else self.M) * max(1, self.groups)
         if self.block_scale != "none":      # one byte per SV elements of K, per row of A and of B
             sv = SF_VEC[self.block_scale]
             b += self.batch * (self.M + self.N) * ((self.K + sv - 1) // sv)
@@ -131,6 +135,9 @@ WORKLOADS = {
     "nvfp4_8192": Spec(
         "nvfp4_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e2m1", block_scale="nv", seed=9,
         notes="nv_float4: e2m1 data, one ue4m3 scale factor per 16 elements of K, fp32 global scales"),
+    "grouped_16x_bf16": Spec(
+        "grouped_16x_bf16", 32768, 4096, 4096, order_a="row", order_b="col", groups=16, act="relu", bias="col",
+        seed=10, notes="16 groups of ragged row counts (32768 rows in all), one 4096x4096 B and bias per group"),
     "odd_1000_at": Spec(
         "odd_1000_at", 1000, 1000, 1000, op_a="T", order_a="col", order_b="col", seed=4,
         notes="A transposed: stored K x M column-major, lda = K"),
@@ -319,10 +326,41 @@ def _make_nv_inputs(spec, gen):
     return ops
 
 
+def group_rows_of(spec, gen):
+    """Row offsets (groups + 1, int64) of a grouped workload: the given sizes,
+    else weights drawn uniform in [0.25, 1.75] scaled to M rows (floors, the
+    remainder to the last group)."""
+    if spec.group_sizes:
+        sizes = list(spec.group_sizes)
+    else:
+        w = torch.rand(spec.groups, generator=gen, dtype=torch.float64) * 1.5 + 0.25
+        sizes = [int(x) for x in torch.floor(w / w.sum() * spec.M).tolist()]
+        sizes[-1] += spec.M - sum(sizes)
+    rows = [0]
+    for n in sizes:
+        rows.append(rows[-1] + n)
+    return torch.tensor(rows, dtype=torch.int64)
+
+
+def _make_grouped_inputs(spec, gen):
+    rows = group_rows_of(spec, gen)
+    a = _draw(gen, spec.matrix_elems("a"), spec.dist).to(DT[spec.dtype_in])
+    b = _draw(gen, spec.groups * spec.matrix_elems("b"), spec.dist).to(DT[spec.dtype_in])
+    C = None
+    if spec.beta != 0:
+        C = _draw(gen, spec.matrix_elems("c"), "normal" if spec.dist != "int4" else "int4").to(DT[spec.dtype_d])
+    bias = None
+    if spec.bias != "none":
+        bias = torch.randn(spec.groups * spec.N, generator=gen, dtype=torch.float32) * spec.bias_sigma
+    return Inputs(spec, a, b, C, bias, 1.0, 1.0, extras={"group_rows": rows})
+
+
 def make_inputs(spec: Spec) -> Inputs:
     """Builds the storage buffers of one workload (CPU tensors).  Padding
     elements beyond each leading extent are drawn too (they are never read)."""
     gen = torch.Generator(device="cpu").manual_seed(spec.seed)
+    if spec.groups:
+        return _make_grouped_inputs(spec, gen)
     if spec.block_scale in ("mx", "nv"):
         if spec.block_scale == "nv":
             ops = _make_nv_inputs(spec, gen)

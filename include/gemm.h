@@ -325,6 +325,33 @@ typedef struct {
  * GEMM_ERR_INVALID_ARG for them, having no scale-factor arguments). */
 GEMM_API gemm_status_t gemm_run_args(gemm_handle_t h, const gemm_args_t* args, void* stream);
 
+/* Grouped GEMM ("Technical Documentation: NVIDIA/cutlass", "What's New in
+ * CUTLASS 4.8": grouped GEMM with contiguous offsets).  `groups` problems in
+ * one launch that share N, K, types, layouts and epilogue: group g owns rows
+ * [group_rows[g], group_rows[g+1]) of one A, one C and one D (desc.M rows
+ * each, the rows of all groups one after another) and uses batch g of B
+ * (desc.stride_b elements apart; 0 = one B for all) and of the bias
+ * (desc.stride_bias apart; 0 = shared):
+ *   D[r, :] = act(alpha * A[r, :] op(B_g) + beta * C[r, :] + bias_g)   for r in group g.
+ * Descriptor rules: desc.batch = 1 and stride_a = stride_c = stride_d = 0
+ * (else GEMM_ERR_INVALID_ARG); D (and C) row-major; no block scaling, MX
+ * output, reductions or per-row bias (else GEMM_ERR_UNSUPPORTED); groups in
+ * [1, 65535].  The handle runs whole tiles (gemm_set_schedule accepts
+ * GEMM_SCHED_AUTO and GEMM_SCHED_DATA_PARALLEL only) and sizes its grid to the
+ * GPU, since the tile count is known only on the device.
+ * gemm_grouped_run: group_rows is a DEVICE array of groups + 1 int64 row
+ * offsets, 8-byte aligned, read by the kernel (so it may be written by an
+ * earlier kernel on the same stream).  Offsets are clamped to [0, desc.M]
+ * and group g covers [e(g-1), e(g)), e(g) the running maximum of the
+ * clamped offsets 0..g+1 (e(-1) = the first), so groups never overlap and
+ * no row outside D is ever written; rows of D that no group covers are left
+ * untouched.  gemm_run / gemm_run_ex /
+ * gemm_run_args on a grouped handle, and gemm_grouped_run on another one,
+ * return GEMM_ERR_INVALID_ARG.  Other arguments as for gemm_run. */
+GEMM_API gemm_status_t gemm_grouped_create(gemm_handle_t* out, const gemm_desc_t* desc, int32_t groups);
+GEMM_API gemm_status_t gemm_grouped_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
+                                        const float* bias, const int64_t* group_rows, void* stream);
+
 /* Static string for a status code. */
 GEMM_API const char* gemm_status_str(gemm_status_t s);
 

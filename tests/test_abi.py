@@ -221,3 +221,31 @@ def test_nvfp4_argument_rules():
     assert _status(_nv(lda=2048))[0] == g.ERR_INVALID_ARG                            # lda < K
     assert _status(_nv(batch=2, stride_a=4096 * 4096 + 16, stride_b=4096 * 4096, stride_d=4096 * 4096))[0] == \
         g.ERR_MISALIGNED
+
+
+def _grouped_status(desc, groups):
+    h = ctypes.c_void_p()
+    s = g.lib.gemm_grouped_create(ctypes.byref(h), ctypes.byref(desc), groups)
+    if s == g.OK:
+        g.lib.gemm_destroy(h)
+    return s
+
+
+def test_grouped_descriptor_rules():
+    import torch
+    ok = g.ERR_NO_DEVICE if not torch.cuda.is_available() else g.OK
+    base = dict(M=4096, N=512, K=256, stride_b=512 * 256)
+    assert _grouped_status(_desc(**base), 8) == ok
+    assert _grouped_status(_desc(**base), 0) == g.ERR_INVALID_ARG
+    assert _grouped_status(_desc(**base), 65536) == g.ERR_INVALID_ARG
+    assert _grouped_status(_desc(**dict(base, stride_b=0)), 8) == ok                       # one B for all
+    assert _grouped_status(_desc(**dict(base, batch=2)), 8) == g.ERR_INVALID_ARG
+    assert _grouped_status(_desc(**dict(base, stride_a=100)), 8) == g.ERR_INVALID_ARG
+    assert _grouped_status(_desc(**dict(base, order_d=g.COL_MAJOR, ldd=4096)), 8) == g.ERR_UNSUPPORTED
+    assert _grouped_status(_desc(**dict(base, order_a=g.COL_MAJOR, lda=4096)), 8) == g.ERR_UNSUPPORTED   # MN-major A
+    assert _grouped_status(_desc(**dict(base, op_a=g.OP_T, order_a=g.COL_MAJOR, lda=256)), 8) == ok   # K-major A
+    assert _grouped_status(_desc(**dict(base, reduce=g.REDUCE_ROW_SUM)), 8) == g.ERR_UNSUPPORTED
+    assert _grouped_status(_desc(**dict(base, bias=g.BIAS_ROW)), 8) == g.ERR_UNSUPPORTED
+    assert _grouped_status(_desc(**dict(base, dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=g.BLOCK_SCALE_MX)), 8) == \
+        g.ERR_UNSUPPORTED
+    assert _grouped_status(_desc(**dict(base, stride_b=512 * 256 + 4)), 8) == g.ERR_MISALIGNED
