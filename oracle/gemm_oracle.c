@@ -423,6 +423,34 @@ void oracle_encode_e4m3_array(const double* v, int64_t n, uint8_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_encode_e4m3(v[i]);
 }
 
+/* Round-to-nearest-even into e2m1 with saturation: magnitudes from 6 up
+ * become 6 (code 7), the sign goes to bit 3.  Bias 1 and one mantissa bit:
+ * below 1 the quantum is 0.5 (code 1 = 0.5), then 2^(E-1) for values in
+ * [2^E, 2^(E+1)).  NaN has no code; it is given 0 (callers never pass one). */
+uint32_t oracle_encode_e2m1(double v) {
+    if (isnan(v)) return 0u;
+    const uint32_t sign = signbit(v) ? 0x8u : 0u;
+    const double a = fabs(v);
+    if (a >= 6.0) return sign | 0x7u;
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);
+    int E = e2 - 1;
+    if (E < 0) E = 0;                          /* subnormal range shares exponent 0's quantum */
+    const double r = nearbyint(ldexp(a, 1 - E));    /* exact scaling, ties to even */
+    const double res = ldexp(r, E - 1);
+    if (res == 0.0) return sign;
+    frexp(res, &e2);
+    E = e2 - 1;
+    if (E < 0) return sign | 0x1u;             /* 0.5 */
+    const uint32_t mant = (uint32_t)(ldexp(res, 1 - E) - 2.0);
+    return sign | ((uint32_t)(E + 1) << 1) | mant;
+}
+
+void oracle_encode_e2m1_array(const double* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_encode_e2m1(v[i]);
+}
+
 /* Scatters packed rows (as produced by oracle_gemm_rows for every row, in
  * order) into D's own storage layout: D(l,m,n) at l*stride_d + (m,n) by
  * order_d and ldd.  Lets a test build a full D buffer the way a caller lays

@@ -64,6 +64,8 @@ def lib():
         l.oracle_encode_e4m3.argtypes = [ctypes.c_double]
         l.oracle_encode_e4m3_array.restype = None
         l.oracle_encode_e4m3_array.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        l.oracle_encode_e2m1_array.restype = None
+        l.oracle_encode_e2m1_array.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
         l.oracle_decode.restype = ctypes.c_double
         l.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_uint32]
         l.oracle_encode.restype = ctypes.c_uint32
@@ -265,4 +267,51 @@ def mx_quantise_rows(t):
     scaled = blk / np.ldexp(1.0, (np.minimum(code, 254) - 127))[:, :, None]
     q = encode_e4m3(scaled).reshape(R, nb * 32)[:, :N]
     q = np.where(np.repeat(bad, 32, axis=1)[:, :N], np.uint8(0x7F), q)
+    return code.astype(np.uint8), q.astype(np.uint8)
+
+
+# NVFP4 output ("Blackwell SM100 GEMMs": LinCombBlockScaleFactor with
+# SFDVectorSize = 16).  Reading (the page leaves the rule open): blocks of 16
+# consecutive elements of a D row; with the output's fp32 global scale g,
+# factor = e4m3(amax / (6 g)) (ue4m3, nearest even, saturating at 448) and
+# elements = e2m1(t / (factor * g)) (nearest even, saturating at 6), zero
+# where the factor is 0; a block holding NaN or inf gets factor 0x7F and zero
+# elements.  Every step is taken in fp32, the epilogue's precision: t is
+# rounded to fp32 first, and 6 g, the quotient, the factor's value times g and
+# the element quotients are each one fp32 operation, so both sides take the
+# same integer decisions.
+
+def encode_e2m1(values):
+    """fp64 array -> e2m1 codes (uint8, 0..15), round to nearest even, saturating."""
+    v = np.ascontiguousarray(values, dtype=np.float64).reshape(-1)
+    out = np.empty(v.size, dtype=np.uint8)
+    lib().oracle_encode_e2m1_array(v.ctypes.data, v.size, out.ctypes.data)
+    return out.reshape(np.shape(values))
+
+
+def nv_quantise_rows(t, scale_d):
+    """t: (R, N) epilogue values, scale_d: the output's global scale ->
+    (factor codes (R, ceil(N/16)) uint8, element codes (R, N) uint8)."""
+    f32 = np.float32
+    t32 = np.asarray(t, dtype=np.float64).astype(f32)
+    R, N = t32.shape
+    nb = (N + 15) // 16
+    blk = np.zeros((R, nb * 16), dtype=f32)
+    blk[:, :N] = t32
+    blk = blk.reshape(R, nb, 16)
+    with np.errstate(invalid="ignore"):
+        a = np.abs(blk)
+        bad = ~np.isfinite(a).all(axis=2)
+        amax = np.where(bad, f32(0), a.max(axis=2)).astype(f32)
+    g = f32(scale_d)
+    sfv = (amax / (f32(6) * g)).astype(f32)
+    code = encode_e4m3(sfv.astype(np.float64)).astype(np.uint8)
+    code = np.where(bad, np.uint8(0x7F), code)
+    dec = np.array([decode("e4m3", int(c)) if c != 0x7F else 0.0 for c in code.reshape(-1)],
+                   dtype=np.float64).reshape(code.shape).astype(f32)
+    denom = (dec * g).astype(f32)
+    safe = np.where(denom > 0, denom, f32(1))
+    x = np.where((denom > 0)[:, :, None], blk / safe[:, :, None], f32(0)).astype(f32)
+    q = encode_e2m1(x.astype(np.float64)).reshape(R, nb * 16)[:, :N]
+    q = np.where(np.repeat(bad, 16, axis=1)[:, :N], np.uint8(0), q)
     return code.astype(np.uint8), q.astype(np.uint8)

@@ -160,3 +160,50 @@ def test_generated_nvfp4_inputs_dequantise_close_to_their_source():
     blk_amax = x[0].abs().view(8, 4, 16).amax(dim=2).repeat_interleave(16, dim=1)
     # half the widest e2m1 step (2 of 6) of the block's range, plus the factor's own rounding
     assert torch.all((deq - x[0]).abs() <= blk_amax * (1.0 / 6.0 + 1.0 / 16.0) + 1e-6)
+
+
+# ------------------------------------------------------- NVFP4 output ----
+def test_e2m1_encoder_round_trips_ties_to_even_and_saturates():
+    vals = np.array([g.decode("e2m1", c) for c in range(16)])
+    assert g.encode_e2m1(vals).tolist() == list(range(16))          # -0 included (code 8)
+    # halfway points go to the even code; 6 and beyond saturate
+    got = g.encode_e2m1(np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 5.5, 7.0, 1e9, -1e9])).tolist()
+    assert got == [0, 2, 2, 4, 4, 6, 6, 7, 7, 7, 15]
+    assert g.encode_e2m1(np.array([0.2, 0.3, 2.9, 3.1])).tolist() == [0, 1, 5, 5]
+
+
+def test_nv_output_factor_and_elements_follow_the_rule():
+    t = np.zeros((3, 40))
+    t[0, :16] = np.linspace(-6.0, 6.0, 16)          # amax 6, g = 1: factor 1.0 (0x38), elements e2m1(t)
+    t[0, 16:32] = 6.0 * 448 * 3                     # amax/6 = 1344 saturates to 448 (0x7E); elements 18 -> 6
+    t[0, 32:] = 0.0                                 # zeros: factor 0, elements 0
+    t[1, 3] = np.nan                                # a NaN: factor 0x7F, elements 0
+    t[2, :] = 0.75                                  # amax/6 = 0.125 = 2^-3 exactly (0x20); elements 6.0
+    codes, q = g.nv_quantise_rows(t, 1.0)
+    assert codes.shape == (3, 3) and q.shape == (3, 40)
+    assert codes[0].tolist() == [0x38, 0x7E, 0x00]
+    assert q[0, :16].tolist() == g.encode_e2m1(np.float32(t[0, :16]).astype(np.float64)).tolist()
+    assert np.all(q[0, 16:32] == 7) and np.all(q[0, 32:] == 0)
+    assert codes[1, 0] == 0x7F and np.all(q[1, :16] == 0) and codes[1, 1] == 0
+    assert codes[2].tolist() == [0x20, 0x20, 0x20] and np.all(q[2] == 7)
+
+
+def test_nv_output_global_scale_is_a_pure_rescaling():
+    rng = np.random.default_rng(45)
+    t = rng.normal(size=(4, 64)) * 3.0
+    c1, q1 = g.nv_quantise_rows(t, 1.0)
+    c2, q2 = g.nv_quantise_rows(t * 2.0 ** 7, 2.0 ** 7)   # powers of two: every fp32 step exact
+    assert np.array_equal(c1, c2) and np.array_equal(q1, q2)
+
+
+def test_nv_output_dequantises_within_half_a_step():
+    rng = np.random.default_rng(46)
+    t = rng.normal(size=(6, 96)) * np.exp2(rng.integers(-3, 4, (6, 1)))
+    gs = float(np.abs(t).max()) / (448.0 * 6.0)      # the tensor's global scale: no factor saturates
+    codes, q = g.nv_quantise_rows(t, gs)
+    fac = np.array([[g.decode("e4m3", int(c)) for c in row] for row in codes]).repeat(16, axis=1)[:, :96]
+    dq = np.array([[g.decode("e2m1", int(c)) for c in row] for row in q]) * fac * gs
+    amax = np.abs(t).reshape(6, 6, 16).max(axis=2).repeat(16, axis=1)
+    # one e2m1 step is at most 2 at the top of the range (4 -> 6) in units of
+    # factor * g ~ amax / 6; the factor's own rounding adds at most 1/16
+    assert np.all(np.abs(dq - t) <= amax * (1.0 / 6.0) * (1 + 1.0 / 16.0) + 1e-12)
