@@ -41,7 +41,7 @@ REDUCE_NONE, REDUCE_ROW_SUM, REDUCE_COL_SUM, REDUCE_ABS_MAX = 0, 1, 2, 4
 # gemm_block_scale_t
 BLOCK_SCALE_NONE, BLOCK_SCALE_MX, BLOCK_SCALE_NV = 0, 1, 2
 # gemm_out_scale_t
-OUT_SCALE_NONE, OUT_SCALE_MX = 0, 1
+OUT_SCALE_NONE, OUT_SCALE_MX, OUT_SCALE_NV = 0, 1, 2
 # gemm_bias_t
 BIAS_NONE, BIAS_COL, BIAS_ROW = 0, 1, 2
 # gemm_sched_t
@@ -64,7 +64,7 @@ class GemmDesc(ctypes.Structure):
         ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
         ("scale_a", ctypes.c_float), ("scale_b", ctypes.c_float),
         ("act", ctypes.c_int32), ("bias", ctypes.c_int32), ("reduce", ctypes.c_int32),
-        ("block_scale", ctypes.c_int32), ("out_scale", ctypes.c_int32),
+        ("block_scale", ctypes.c_int32), ("out_scale", ctypes.c_int32), ("scale_d", ctypes.c_float),
     ]
 
 
@@ -142,7 +142,7 @@ def make_desc(M, N, K, batch=1, op_a=OP_N, op_b=OP_N, order_a=ROW_MAJOR, order_b
               stride_a=0, stride_b=0, stride_c=0, stride_d=0, stride_bias=0,
               dtype_a=BF16, dtype_b=BF16, dtype_c=None, dtype_d=BF16, alpha=1.0, beta=0.0,
               scale_a=1.0, scale_b=1.0, act=ACT_NONE, bias=BIAS_NONE, reduce=REDUCE_NONE,
-              block_scale=BLOCK_SCALE_NONE, out_scale=OUT_SCALE_NONE):
+              block_scale=BLOCK_SCALE_NONE, out_scale=OUT_SCALE_NONE, scale_d=1.0):
     """Fills a GemmDesc; leading dimensions default to the tight ones and the
     batch strides of A, B, C, D to the tight matrix sizes when batch > 1."""
 
@@ -171,6 +171,7 @@ def make_desc(M, N, K, batch=1, op_a=OP_N, op_b=OP_N, order_a=ROW_MAJOR, order_b
     d.dtype_c = dtype_d if dtype_c is None else dtype_c
     d.alpha, d.beta, d.scale_a, d.scale_b = alpha, beta, scale_a, scale_b
     d.act, d.bias, d.reduce, d.block_scale, d.out_scale = act, bias, reduce, block_scale, out_scale
+    d.scale_d = scale_d
     return d
 
 

@@ -137,21 +137,31 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out, int32_t grou
     if (d.block_scale == GEMM_BLOCK_SCALE_MX && (d.dtype_a != GEMM_E4M3 || d.dtype_b != GEMM_E4M3))
         return GEMM_ERR_UNSUPPORTED;
     if (d.bias != GEMM_BIAS_NONE && d.bias != GEMM_BIAS_COL && d.bias != GEMM_BIAS_ROW) return GEMM_ERR_INVALID_ARG;
-    for (int t : {d.dtype_a, d.dtype_b, d.dtype_d})
+    // e2m1 D exists only with its block factors (GEMM_OUT_SCALE_NV)
+    if (d.out_scale != GEMM_OUT_SCALE_NONE && d.out_scale != GEMM_OUT_SCALE_MX && d.out_scale != GEMM_OUT_SCALE_NV)
+        return GEMM_ERR_INVALID_ARG;
+    const bool out_nv = d.out_scale == GEMM_OUT_SCALE_NV;
+    if ((d.dtype_d == GEMM_E2M1) != out_nv) return GEMM_ERR_UNSUPPORTED;
+    for (int t : {d.dtype_a, d.dtype_b})
         if (!dtype_bytes(t)) return GEMM_ERR_INVALID_ARG;
+    if (!out_nv && !dtype_bytes(d.dtype_d)) return GEMM_ERR_INVALID_ARG;
     const bool has_c = d.beta != 0.0f;
     if (has_c && !dtype_bytes(d.dtype_c)) return GEMM_ERR_INVALID_ARG;
 
     // One operand type per MMA: both f16, both bf16 or both e4m3.
     if (d.dtype_a != d.dtype_b) return GEMM_ERR_UNSUPPORTED;
     if (d.dtype_a == GEMM_F32) return GEMM_ERR_UNSUPPORTED;
-    if (d.out_scale != GEMM_OUT_SCALE_NONE && d.out_scale != GEMM_OUT_SCALE_MX) return GEMM_ERR_INVALID_ARG;
     if ((d.dtype_d == GEMM_E4M3) != (d.out_scale == GEMM_OUT_SCALE_MX)) return GEMM_ERR_UNSUPPORTED;
-    if (d.out_scale == GEMM_OUT_SCALE_MX && (d.order_d != GEMM_ROW_MAJOR || d.beta != 0.0f || d.reduce))
+    if (d.out_scale != GEMM_OUT_SCALE_NONE && (d.order_d != GEMM_ROW_MAJOR || d.beta != 0.0f || d.reduce))
         return GEMM_ERR_UNSUPPORTED;
+    if (out_nv) {
+        if (!(d.scale_d > 0.0f) || !(d.scale_d < 3.0e38f)) return GEMM_ERR_INVALID_ARG;
+        if (d.N % 2) return GEMM_ERR_UNSUPPORTED;                  // whole bytes per row
+        if (d.ldd % 32 || (d.batch > 1 && d.stride_d % 32)) return GEMM_ERR_MISALIGNED;
+    }
     if (has_c && (d.dtype_c != d.dtype_d || d.order_c != d.order_d)) return GEMM_ERR_UNSUPPORTED;
 
-    const int ab = dtype_bytes(d.dtype_a), ob = dtype_bytes(d.dtype_d);
+    const int ab = dtype_bytes(d.dtype_a), ob = out_nv ? 1 : dtype_bytes(d.dtype_d);   // e2m1 D: the 1-byte kernel
 
     // Leading dimensions must cover the stored rows (BLAS rule).
     auto ld_ok = [](int order, int64_t srows, int64_t scols, int64_t ld) {
@@ -301,9 +311,12 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out, int32_t grou
     k.a_kmajor = a_kmaj;
     k.b_kmajor = b_kmaj;
     k.block_scaled = bs;
-    k.out_f8 = d.out_scale == GEMM_OUT_SCALE_MX;
+    // 1: e4m3 D with ue8m0 factors per 32; 2: e2m1 D with ue4m3 factors per 16
+    k.out_f8 = d.out_scale == GEMM_OUT_SCALE_MX ? 1 : (out_nv ? 2 : 0);
+    k.scale_d = d.scale_d;
     if (k.out_f8) {
-        const int64_t sfk = (P.Nk + 31) / 32;
+        const int64_t sv = out_nv ? 16 : 32;
+        const int64_t sfk = (P.Nk + sv - 1) / sv;
         k.sfd_kb4 = (int32_t)((sfk + 3) / 4);
         k.sfd_bstride = ((P.Mk + 127) / 128) * (int64_t)k.sfd_kb4 * 512;
     }
@@ -333,6 +346,10 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out, int32_t grou
     k.d_ragged = ((P.Nk * ob) % 16) != 0;
     k.ldd = mode_stride(P.cd, 0);
     k.d_bstride = mode_stride(P.cd, 2);
+    if (out_nv) {                              // the kernel addresses e2m1 D in bytes
+        k.ldd /= 2;
+        k.d_bstride /= 2;
+    }
     k.timeout_ns = kDefaultTimeoutNs;
     return GEMM_OK;
 }
@@ -671,7 +688,14 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
         ok = ok && encode_map(&h->maps[0], P.a, adt, ka, kel, P.kp.a_kmajor ? kTileM : kel, P.kp.a_batched);
         ok = ok && encode_map(&h->maps[1], P.b, adt, kb, kel, P.kp.b_kmajor ? (uint32_t)(tn / P.cta_group) : kel,
                               P.kp.b_batched);
-        ok = ok && encode_map(&h->maps[3], P.cd, d.dtype_d, D, epi_cols, kEpiRows, d.batch > 1);
+        if (P.kp.out_f8 == 2) {
+            // e2m1 D (stored by the kernel directly): a map over its bytes
+            const gl::Layout lb = logical_layout(GEMM_OP_N, GEMM_ROW_MAJOR, d.M, d.N / 2, d.ldd / 2, d.batch,
+                                                 d.stride_d / 2);
+            ok = ok && encode_map(&h->maps[3], lb, GEMM_E4M3, D, epi_cols, kEpiRows, d.batch > 1);
+        } else {
+            ok = ok && encode_map(&h->maps[3], P.cd, d.dtype_d, D, epi_cols, kEpiRows, d.batch > 1);
+        }
         if (P.has_c) {
             gl::Layout lc = logical_layout(GEMM_OP_N, d.order_c, d.M, d.N, d.ldc, d.batch, d.stride_c);
             if (swap) lc = transpose2(lc);

@@ -81,7 +81,10 @@ struct KernelParams {
     // MX output (out_f8 = 1): D in e4m3, factors written to sfd in the
     // basic-block layout (rows = M, one factor per 32 columns; sfd_kb4 =
     // ceil(ceil(N/32)/4) blocks along N; sfd_bstride bytes per batch).
+    // NVFP4 output (out_f8 = 2): D in e2m1 (two per byte; ldd and d_bstride
+    // then count bytes), one ue4m3 factor per 16 columns, global scale scale_d.
     int32_t out_f8;
+    float scale_d;
     uint8_t* sfd;
     int64_t sfd_bstride;
     int32_t sfd_kb4;

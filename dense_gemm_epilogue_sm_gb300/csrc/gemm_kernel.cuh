@@ -1085,6 +1085,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 return true;
                             });
                         }
+                        if (p.out_f8 == 2) {
+                            // NVFP4 output: e2m1 elements and one ue4m3 factor per 16
+                            // columns of a row under the global scale g = scale_d, each
+                            // step one fp32 operation rounded to nearest:
+                            // factor = e4m3(amax / (6 g)), elements e2m1(t / (factor g))
+                            const float six_g = __fmul_rn(6.0f, p.scale_d);
+#pragma unroll
+                            for (int h = 0; h < C::kEpiCols / 16; ++h) {
+                                const int c0 = col0 + h * 16;
+                                if (c0 >= p.N) break;             // the block lies past the row's end
+                                float v[16];
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    float x = p.alpha * __uint_as_float(acc[h * 16 + i]);
+                                    if (p.bias_mode == 1)
+                                        x += (c0 + i < p.N) ? __ldg(bias_l + c0 + i) : 0.f;
+                                    else if (p.bias_mode == 2)
+                                        x += row_bias;
+                                    if (p.act == 1)
+                                        x = fmaxf(x, 0.f);
+                                    else if (EXT && p.act == 2)
+                                        x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+                                    v[i] = (c0 + i < p.N) ? x : 0.f;   // columns past N join no block
+                                }
+                                uint32_t amax = 0u;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) amax = max(amax, __float_as_uint(fabsf(v[i])));
+                                uint32_t code = 0x7Fu;            // NaN / inf in the block
+                                uint2 out = make_uint2(0u, 0u);
+                                if (amax < 0x7F800000u) {
+                                    const float sfv = __fdiv_rn(__uint_as_float(amax), six_g);
+                                    code = ptx::pack4_e4m3(sfv, 0.f, 0.f, 0.f) & 0xFFu;
+                                    // the factor's value, from its bits (code <= 0x7E, sign 0)
+                                    const uint32_t fe = code >> 3, fm = code & 7u;
+                                    const float fval = fe ? __uint_as_float(((fe + 120u) << 23) | (fm << 20))
+                                                          : (float)fm * 0.001953125f;     // m * 2^-9
+                                    const float denom = __fmul_rn(fval, p.scale_d);
+                                    if (denom > 0.f) {
+                                        float x[16];
+#pragma unroll
+                                        for (int i = 0; i < 16; ++i) x[i] = __fdiv_rn(v[i], denom);
+                                        out.x = ptx::pack8_e2m1(x);
+                                        out.y = ptx::pack8_e2m1(x + 8);
+                                    }
+                                }
+                                if (row < m_end) {
+                                    uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)dl * p.d_bstride +
+                                                    (int64_t)row * p.ldd;          // bytes: two elements each
+                                    if (c0 + 16 <= p.N) {
+                                        *reinterpret_cast<uint2*>(drow + c0 / 2) = out;
+                                    } else {
+                                        for (int i = 0; i < 8 && c0 + 2 * i < p.N; ++i)
+                                            drow[c0 / 2 + i] = (uint8_t)((i < 4 ? out.x : out.y) >> ((i & 3) * 8));
+                                    }
+                                    const int f = c0 / 16;
+                                    p.sfd[(int64_t)dl * p.sfd_bstride + ((int64_t)(row / 128) * p.sfd_kb4 + f / 4) * 512 +
+                                          (row % 32) * 16 + ((row % 128) / 32) * 4 + f % 4] = (uint8_t)code;
+                                }
+                            }
+                            continue;
+                        }
 #pragma unroll
                         for (int h = 0; h < C::kEpiCols / 32; ++h) {
                             const int c0 = col0 + h * 32;

@@ -315,6 +315,22 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
             : "memory");
 }
 
+// Eight fp32 values to e2m1 (round to nearest even, saturating at +-6),
+// x[0] in the low nibble of the result, x[7] in the high one (each cvt puts
+// its first operand in the upper nibble of its byte).
+__device__ __forceinline__ uint32_t pack8_e2m1(const float* x) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
+    return r;
+}
+
 // Block-scaled e2m1 MMA with 16-element scale vectors (NVFP4, ue4m3
 // factors), K = 64 per instruction; factors as for mma_mx.
 template <int CG, uint32_t IDESC>

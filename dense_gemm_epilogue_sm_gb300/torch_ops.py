@@ -6,7 +6,7 @@ import torch
 
 from . import (ACT_GELU, ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW, COL_MAJOR, E2M1, E4M3, F16, F32, OP_N,
                OP_T, REDUCE_ABS_MAX, REDUCE_COL_SUM, REDUCE_ROW_SUM, ROW_MAJOR, BLOCK_SCALE_MX, BLOCK_SCALE_NONE, BLOCK_SCALE_NV,
-               OUT_SCALE_MX, OUT_SCALE_NONE,
+               OUT_SCALE_MX, OUT_SCALE_NONE, OUT_SCALE_NV,
                gemm_check, gemm_create, gemm_destroy, gemm_get_schedule, gemm_grouped_create, gemm_grouped_run,
                gemm_launch_count, gemm_run, gemm_run_args, gemm_run_ex, gemm_set_schedule, make_desc)
 
@@ -44,7 +44,8 @@ def desc_from_spec(spec, scale_a=1.0, scale_b=1.0):
         spec.alpha, spec.beta, scale_a, scale_b, ACT_CODE[spec.act], BIAS_CODE[spec.bias],
         reduce_code(getattr(spec, "reduce", "none")),
         BLOCK_SCALE_CODE[getattr(spec, "block_scale", "none")],
-        OUT_SCALE_MX if spec.dtype_d == "e4m3" else OUT_SCALE_NONE)
+        {"e4m3": OUT_SCALE_MX, "e2m1": OUT_SCALE_NV}.get(spec.dtype_d, OUT_SCALE_NONE),
+        scale_d=getattr(spec, "scale_d", 1.0))
 
 
 def _ptr(t):

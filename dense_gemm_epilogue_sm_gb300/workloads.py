@@ -58,6 +58,7 @@ class Spec:
     reduce: str = "none"        # none, or a '+'-joined subset of row, col, amax
     block_scale: str = "none"   # none | mx (e4m3 data, ue8m0 scale per 32 elements of K)
                                 # | nv (e2m1 data, ue4m3 scale per 16 elements of K)
+    scale_d: float = 1.0        # e2m1 D (NVFP4 output): the output's global scale
     groups: int = 0             # > 0: grouped GEMM; M = rows of all groups, B and bias per group
     group_sizes: tuple = ()     # grouped: explicit rows per group (else drawn by the generator)
     notes: str = ""

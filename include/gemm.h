@@ -127,8 +127,22 @@ typedef enum { GEMM_BLOCK_SCALE_NONE = 0, GEMM_BLOCK_SCALE_MX = 1, GEMM_BLOCK_SC
  * elements for a block holding NaN or inf); elements e4m3(t / 2^(code-127))
  * rounded to nearest even, saturated at +-448.  Needs beta = 0 and no
  * reductions (else GEMM_ERR_UNSUPPORTED).  Only the factors of real
- * (row, block) pairs are written. */
-typedef enum { GEMM_OUT_SCALE_NONE = 0, GEMM_OUT_SCALE_MX = 1 } gemm_out_scale_t;
+ * (row, block) pairs are written.
+ * GEMM_OUT_SCALE_NV (the page's example, SFDVectorSize = 16): D is e2m1
+ * (dtype_d = GEMM_E2M1, row-major, two elements per byte, the lower column
+ * in the low nibble; N even and ldd / stride_d multiples of 32 elements,
+ * else GEMM_ERR_UNSUPPORTED / GEMM_ERR_MISALIGNED) and every 16 consecutive
+ * elements of a D row share one ue4m3 factor, written to gemm_args_t.sfd in
+ * the basic-block layout (rows = M, factors per row = ceil(N/16)).  With the
+ * output's fp32 global scale g = desc.scale_d (> 0 and finite, else
+ * GEMM_ERR_INVALID_ARG), each step one fp32 operation rounded to nearest:
+ * factor = e4m3(amax / (6 g)) (nearest even, saturating at 448; amax = the
+ * block's max |t|), elements e2m1(t / (factor * g)) (nearest even,
+ * saturating at +-6), 0 where the factor is 0; a block holding NaN or inf
+ * gets factor 0x7F and zero elements.  So D * factor * g ~ t, and D with its
+ * factors and g is an NVFP4 operand (GEMM_BLOCK_SCALE_NV) for the next GEMM.
+ * Same restrictions as GEMM_OUT_SCALE_MX. */
+typedef enum { GEMM_OUT_SCALE_NONE = 0, GEMM_OUT_SCALE_MX = 1, GEMM_OUT_SCALE_NV = 2 } gemm_out_scale_t;
 
 typedef enum {
     GEMM_SCHED_AUTO = 0,
@@ -153,6 +167,7 @@ typedef struct {
     int32_t reduce;                                /* gemm_reduce_t flags; 0 = none */
     int32_t block_scale;                           /* gemm_block_scale_t; 0 = none */
     int32_t out_scale;                             /* gemm_out_scale_t; 0 = none */
+    float scale_d;                                 /* output global scale of GEMM_OUT_SCALE_NV; else unused */
 } gemm_desc_t;
 
 /* How a descriptor is executed; filled by gemm_plan (host only, no GPU). */
@@ -317,7 +332,7 @@ typedef struct {
     float* row_sum;
     float* col_sum;
     float* abs_max;
-    void* sfd;                     /* output factors of a GEMM_OUT_SCALE_MX descriptor */
+    void* sfd;                     /* output factors of a GEMM_OUT_SCALE_MX / _NV descriptor */
 } gemm_args_t;
 
 /* gemm_run with every buffer in one struct: the entry point for

@@ -213,7 +213,7 @@ def test_nvfp4_argument_rules():
     assert _status(_nv(dtype_a=g.E4M3, dtype_b=g.E4M3))[0] == g.ERR_UNSUPPORTED      # e2m1 only
     assert _status(_nv(block_scale=g.BLOCK_SCALE_MX))[0] == g.ERR_UNSUPPORTED        # mx_float8 is e4m3
     assert _status(_nv(block_scale=g.BLOCK_SCALE_NONE))[0] == g.ERR_INVALID_ARG      # e2m1 needs its factors
-    assert _status(_nv(dtype_d=g.E2M1))[0] == g.ERR_INVALID_ARG
+    assert _status(_nv(dtype_d=g.E2M1))[0] == g.ERR_UNSUPPORTED                      # e2m1 D needs its factors
     assert _status(_nv(K=4095))[0] == g.ERR_UNSUPPORTED                              # odd K: half a byte
     assert _status(_nv(lda=4112))[0] == g.ERR_MISALIGNED                             # 2056 bytes
     assert _status(_nv(order_a=g.COL_MAJOR, lda=4096))[0] == g.ERR_UNSUPPORTED       # MN-major A
@@ -249,3 +249,22 @@ def test_grouped_descriptor_rules():
     assert _grouped_status(_desc(**dict(base, dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=g.BLOCK_SCALE_MX)), 8) == \
         g.ERR_UNSUPPORTED
     assert _grouped_status(_desc(**dict(base, stride_b=512 * 256 + 4)), 8) == g.ERR_MISALIGNED
+
+
+def test_nv_output_rules():
+    ok = _desc(dtype_d=g.E2M1, out_scale=g.OUT_SCALE_NV, scale_d=0.5, ldd=512)
+    s, info = _status(ok)
+    assert s == g.OK and info.cta_group in (1, 2)
+    assert _status(_desc(dtype_d=g.E2M1, out_scale=g.OUT_SCALE_NV, scale_d=0.0, ldd=512))[0] == g.ERR_INVALID_ARG
+    assert _status(_desc(dtype_d=g.E2M1, out_scale=g.OUT_SCALE_NV, scale_d=float("inf"), ldd=512))[0] == \
+        g.ERR_INVALID_ARG
+    assert _status(_desc(out_scale=g.OUT_SCALE_NV, scale_d=1.0))[0] == g.ERR_UNSUPPORTED        # factors need e2m1 D
+    assert _status(_desc(N=511, dtype_d=g.E2M1, out_scale=g.OUT_SCALE_NV, scale_d=1.0, ldd=512))[0] == \
+        g.ERR_UNSUPPORTED                                                                       # half a byte
+    assert _status(_desc(dtype_d=g.E2M1, out_scale=g.OUT_SCALE_NV, scale_d=1.0, ldd=528))[0] == g.ERR_MISALIGNED
+    assert _status(_desc(dtype_d=g.E2M1, out_scale=g.OUT_SCALE_NV, scale_d=1.0, ldd=512, beta=1.0,
+                         dtype_c=g.BF16))[0] == g.ERR_UNSUPPORTED
+    assert _status(_desc(dtype_d=g.E2M1, out_scale=g.OUT_SCALE_NV, scale_d=1.0, order_d=g.COL_MAJOR,
+                         ldd=256))[0] == g.ERR_UNSUPPORTED
+    assert _status(_desc(dtype_d=g.E2M1, out_scale=g.OUT_SCALE_NV, scale_d=1.0, ldd=512,
+                         reduce=g.REDUCE_ABS_MAX))[0] == g.ERR_UNSUPPORTED
