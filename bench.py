@@ -132,17 +132,35 @@ def dist_setup():
 def oracle_view(spec, inputs):
     """The problem the oracle samples rows of: the workload itself, or for a
     grouped workload its first group (the whole A with B and bias of group
-    0; rows of that group only).  Returns (spec, inputs, rows to draw from)."""
-    if not getattr(spec, "groups", 0):
-        return spec, inputs, spec.batch * spec.M
+    0; rows of that group only).  A block-scaled D (e4m3 or e2m1 with
+    factors) is the oracle's fp32 t followed by its output quantiser.
+    Returns (spec, inputs, rows to draw from, rows -> result function)."""
     import dataclasses
 
     from dense_gemm_epilogue_sm_gb300 import workloads as wl
-    sub = dataclasses.replace(spec, groups=0, group_sizes=())
-    per = spec.matrix_elems("b")
-    bias = None if inputs.bias is None else inputs.bias[: spec.N].contiguous()
-    sub_in = wl.Inputs(sub, inputs.A, inputs.B[:per].contiguous(), inputs.C, bias, inputs.scale_a, inputs.scale_b)
-    return sub, sub_in, int(inputs.extras["group_rows"][1])
+    from oracle import gemm_ref
+
+    total = spec.batch * spec.M
+    if getattr(spec, "groups", 0):
+        sub = dataclasses.replace(spec, groups=0, group_sizes=())
+        per = spec.matrix_elems("b")
+        bias = None if inputs.bias is None else inputs.bias[: spec.N].contiguous()
+        total = int(inputs.extras["group_rows"][1])
+        inputs = wl.Inputs(sub, inputs.A, inputs.B[:per].contiguous(), inputs.C, bias, inputs.scale_a,
+                           inputs.scale_b)
+        spec = sub
+    quant = None
+    if spec.dtype_d == "e4m3":
+        quant = gemm_ref.mx_quantise_rows
+    elif spec.dtype_d == "e2m1":
+        quant = lambda t, g=spec.scale_d: gemm_ref.nv_quantise_rows(t, g)
+    if quant is not None:
+        spec = dataclasses.replace(spec, dtype_d="f32")
+
+    def run(rows):
+        bits, t = gemm_ref.run_spec_rows(spec, inputs, rows=rows, want_t=quant is not None)
+        return quant(t) if quant is not None else bits
+    return spec, inputs, total, run
 
 
 def oracle_sample(spec, inputs, rows_target_s=12.0):
@@ -154,16 +172,16 @@ def oracle_sample(spec, inputs, rows_target_s=12.0):
 
     threads = gemm_ref.max_threads()
     rng = np.random.default_rng(0)
-    spec, inputs, total_rows = oracle_view(spec, inputs)
-    gemm_ref.run_spec_rows(spec, inputs, rows=np.array([0]))       # decodes B once (kept by the oracle)
+    spec, inputs, total_rows, run = oracle_view(spec, inputs)
+    run(np.array([0]))                                             # decodes B once (kept by the oracle)
     probe = np.sort(rng.choice(total_rows, size=min(total_rows, 2 * threads), replace=False))
     t0 = time.perf_counter()
-    gemm_ref.run_spec_rows(spec, inputs, rows=probe)
+    run(probe)
     rows_per_s = len(probe) / (time.perf_counter() - t0)
     n = int(min(total_rows, max(len(probe), rows_target_s * rows_per_s)))
     rows = np.sort(rng.choice(total_rows, size=n, replace=False))
     t0 = time.perf_counter()
-    gemm_ref.run_spec_rows(spec, inputs, rows=rows)
+    run(rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * len(rows) * spec.N * spec.K
     return flops / dt / 1e12, len(rows), dt, threads
@@ -184,21 +202,21 @@ def run_reference(args):
     rng = np.random.default_rng(1)
     grouped = getattr(spec, "groups", 0) > 0
     wname = spec.name
-    spec, inputs, total_rows = oracle_view(spec, inputs)
+    spec, inputs, total_rows, run = oracle_view(spec, inputs)
     # size each step so the whole --steps/--warmup run stays within about two minutes
     probe = np.sort(rng.choice(total_rows, size=min(total_rows, threads), replace=False))
-    gemm_ref.run_spec_rows(spec, inputs, rows=probe[:1])     # decodes B once (kept by the oracle)
+    run(probe[:1])                                           # decodes B once (kept by the oracle)
     t0 = time.perf_counter()
-    gemm_ref.run_spec_rows(spec, inputs, rows=probe)
+    run(probe)
     per_row = (time.perf_counter() - t0) / len(probe)
     budget = 100.0 / max(1, args.steps + args.warmup)
     nrows = int(min(total_rows, max(1, budget / max(per_row, 1e-9))))
     samples = [np.sort(rng.choice(total_rows, size=nrows, replace=False)) for _ in range(args.steps + args.warmup)]
     for s in samples[: args.warmup]:
-        gemm_ref.run_spec_rows(spec, inputs, rows=s)
+        run(s)
     t0 = time.perf_counter()
     for s in samples[args.warmup:]:
-        gemm_ref.run_spec_rows(spec, inputs, rows=s)
+        run(s)
     dt = time.perf_counter() - t0
     flops = 2.0 * nrows * spec.N * spec.K * args.steps
     value = flops / dt / 1e12
@@ -336,11 +354,12 @@ def run_ours(args):
     sfa_d = ex["sfa"].to(dev) if "sfa" in ex else None
     sfb_d = ex["sfb"].to(dev) if "sfb" in ex else None
     sfd_d = None
-    if spec.dtype_d == "e4m3":        # MX output: the factor tensor beside D
-        sfk = (spec.N + 31) // 32
+    if spec.dtype_d in ("e4m3", "e2m1"):        # MX / NVFP4 output: the factor tensor beside D
+        sfk = (spec.N + (31 if spec.dtype_d == "e4m3" else 15)) // (32 if spec.dtype_d == "e4m3" else 16)
         sfd_d = torch.empty(spec.batch * ((spec.M + 127) // 128) * ((sfk + 3) // 4) * 512, dtype=torch.uint8,
                             device=dev)
-    D = torch.empty(spec.batch * spec.matrix_elems("d"), dtype=wl.DT[spec.dtype_d], device=dev)
+    d_elems = spec.batch * spec.matrix_elems("d")
+    D = torch.empty(d_elems // 2 if spec.dtype_d == "e2m1" else d_elems, dtype=wl.DT[spec.dtype_d], device=dev)
     desc = desc_from_spec(spec, inputs.scale_a, inputs.scale_b)
     info = g.gemm_plan(desc)
     groups = getattr(spec, "groups", 0)
@@ -420,7 +439,7 @@ def run_ours(args):
     # end to end through the public API with host buffers: H2D of the inputs,
     # the GEMM, D2H of the result, every step
     e2e = None
-    if not args.no_e2e and spec.dtype_d != "e4m3":     # (MX output: not measured end to end)
+    if not args.no_e2e and spec.dtype_d not in ("e4m3", "e2m1"):     # (block-scaled output: not measured end to end)
         e2e = run_e2e(launch, spec, inputs, dev, max(1, min(args.steps, args.e2e_steps)), flops)
         op.check()
 

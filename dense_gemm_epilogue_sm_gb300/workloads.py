@@ -136,6 +136,10 @@ WORKLOADS = {
     "nvfp4_8192": Spec(
         "nvfp4_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e2m1", block_scale="nv", seed=9,
         notes="nv_float4: e2m1 data, one ue4m3 scale factor per 16 elements of K, fp32 global scales"),
+    "nvfp4_to_nvfp4_8192": Spec(
+        "nvfp4_to_nvfp4_8192", 8192, 8192, 8192, order_a="row", order_b="col", dtype_in="e2m1", block_scale="nv",
+        dtype_d="e2m1", act="relu", scale_d=8.0, seed=11,
+        notes="NVFP4 in, NVFP4 out: e2m1 D with a ue4m3 factor per 16 elements of a row, global scale 8"),
     "grouped_16x_bf16": Spec(
         "grouped_16x_bf16", 32768, 4096, 4096, order_a="row", order_b="col", groups=16, act="relu", bias="col",
         seed=10, notes="16 groups of ragged row counts (32768 rows in all), one 4096x4096 B and bias per group"),
