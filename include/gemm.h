@@ -137,8 +137,8 @@ typedef enum { GEMM_BLOCK_SCALE_NONE = 0, GEMM_BLOCK_SCALE_MX = 1, GEMM_BLOCK_SC
  * output's fp32 global scale g = desc.scale_d (> 0 and finite, else
  * GEMM_ERR_INVALID_ARG), each step one fp32 operation rounded to nearest:
  * factor = e4m3(amax / (6 g)) (nearest even, saturating at 448; amax = the
- * block's max |t|), elements e2m1(t / (factor * g)) (nearest even,
- * saturating at +-6), 0 where the factor is 0; a block holding NaN or inf
+ * block's max |t|), elements e2m1(t * r) with r = 1 / (factor * g) (nearest
+ * even, saturating at +-6), 0 where the factor is 0; a block holding NaN or inf
  * gets factor 0x7F and zero elements.  So D * factor * g ~ t, and D with its
  * factors and g is an NVFP4 operand (GEMM_BLOCK_SCALE_NV) for the next GEMM.
  * Same restrictions as GEMM_OUT_SCALE_MX. */

@@ -274,12 +274,12 @@ def mx_quantise_rows(t):
 # SFDVectorSize = 16).  Reading (the page leaves the rule open): blocks of 16
 # consecutive elements of a D row; with the output's fp32 global scale g,
 # factor = e4m3(amax / (6 g)) (ue4m3, nearest even, saturating at 448) and
-# elements = e2m1(t / (factor * g)) (nearest even, saturating at 6), zero
-# where the factor is 0; a block holding NaN or inf gets factor 0x7F and zero
-# elements.  Every step is taken in fp32, the epilogue's precision: t is
-# rounded to fp32 first, and 6 g, the quotient, the factor's value times g and
-# the element quotients are each one fp32 operation, so both sides take the
-# same integer decisions.
+# elements = e2m1(t * r) with r = 1 / (factor * g) (nearest even, saturating
+# at 6), zero where the factor is 0; a block holding NaN or inf gets factor
+# 0x7F and zero elements.  Every step is taken in fp32, the epilogue's
+# precision: t is rounded to fp32 first, and 6 g, the quotient, the factor's
+# value times g, its reciprocal and each element's product are one fp32
+# operation rounded to nearest, so both sides take the same integer decisions.
 
 def encode_e2m1(values):
     """fp64 array -> e2m1 codes (uint8, 0..15), round to nearest even, saturating."""
@@ -311,7 +311,8 @@ def nv_quantise_rows(t, scale_d):
                    dtype=np.float64).reshape(code.shape).astype(f32)
     denom = (dec * g).astype(f32)
     safe = np.where(denom > 0, denom, f32(1))
-    x = np.where((denom > 0)[:, :, None], blk / safe[:, :, None], f32(0)).astype(f32)
+    r = np.where(denom > 0, f32(1) / safe, f32(0)).astype(f32)
+    x = (blk * r[:, :, None]).astype(f32)
     q = encode_e2m1(x.astype(np.float64)).reshape(R, nb * 16)[:, :N]
     q = np.where(np.repeat(bad, 16, axis=1)[:, :N], np.uint8(0), q)
     return code.astype(np.uint8), q.astype(np.uint8)
