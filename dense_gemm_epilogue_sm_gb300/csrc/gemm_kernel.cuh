@@ -939,8 +939,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                         // TMEM lane quadrant this warp may read
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const bool f16_out = p.out_f16 != 0;
-        // Compiled twice: EXT adds GELU and the reductions, so the plain
-        // epilogue carries none of their code.
+        // Compiled twice: EXT adds GELU, the reductions and grouped row
+        // ranges, so the plain epilogue carries none of their code.
         auto epilogue = [&](auto ext_tag) {
             constexpr bool EXT = decltype(ext_tag)::value;
             [[maybe_unused]] uint32_t c_phase[2] = {0u, 0u};
@@ -991,8 +991,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 const int buf = it % C::kAccBufs;
                 const uint32_t acc_par = (uint32_t)(it / C::kAccBufs) & 1u;
+                // (groups are served by the EXT epilogue only, so the plain one
+                // keeps its whole-matrix row range)
                 TilePos tp;
-                tile_pos(p, gw, tile, kTileRows, tp);
+                if constexpr (EXT) {
+                    tile_pos(p, gw, tile, kTileRows, tp);
+                } else {
+                    tile_coords(p, tile, tp.mb, tp.nb, tp.l);
+                    tp.m_base = 0;
+                    tp.m_end = p.M;
+                    tp.cd_l = tp.l;
+                }
                 const int mb = tp.mb, nb = tp.nb, l = tp.l;
                 const int m_end = tp.m_end;        // rows past it belong to no output of this tile
                 const int dl = tp.cd_l;            // batch index of D
@@ -1089,7 +1098,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // NVFP4 output: e2m1 elements and one ue4m3 factor per 16
                             // columns of a row under the global scale g = scale_d, each
                             // step one fp32 operation rounded to nearest:
-                            // factor = e4m3(amax / (6 g)), elements e2m1(t / (factor g))
+                            // factor = e4m3(amax / (6 g)), elements e2m1(t * r) with
+                            // r = 1 / (factor g) once per block
                             const float six_g = __fmul_rn(6.0f, p.scale_d);
 #pragma unroll
                             for (int h = 0; h < C::kEpiCols / 16; ++h) {
@@ -1123,9 +1133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                           : (float)fm * 0.001953125f;     // m * 2^-9
                                     const float denom = __fmul_rn(fval, p.scale_d);
                                     if (denom > 0.f) {
+                                        const float r = __frcp_rn(denom);
                                         float x[16];
 #pragma unroll
-                                        for (int i = 0; i < 16; ++i) x[i] = __fdiv_rn(v[i], denom);
+                                        for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(v[i], r);
                                         out.x = ptx::pack8_e2m1(x);
                                         out.y = ptx::pack8_e2m1(x + 8);
                                     }
@@ -1197,7 +1208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the subtile holding a ragged row end, or a group's last rows
                         // short of the end of D, is stored element by element
                         const bool direct = (p.d_ragged && col0 + C::kEpiCols > p.N) ||
-                                            (row0 + kEpiRows > m_end && m_end < p.M);
+                                            (EXT && row0 + kEpiRows > m_end && m_end < p.M);
                         const int sbi = sub_count % C::kEpiBufs;
                         ++sub_count;
                         uint8_t* sbuf = epi + (ew * C::kEpiBufs + sbi) * kEpiBufBytes;
@@ -1350,7 +1361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     });
             }
         };
-        if (p.act == 2 || p.red_rows || p.red_cols || p.red_amax)
+        if (p.act == 2 || p.red_rows || p.red_cols || p.red_amax || p.groups > 0)
             epilogue(BoolTag<true>{});
         else
             epilogue(BoolTag<false>{});
