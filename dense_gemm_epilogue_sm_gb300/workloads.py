@@ -108,6 +108,9 @@ class Spec:
         if self.block_scale != "none":      # one byte per SV elements of K, per row of A and of B
             sv = SF_VEC[self.block_scale]
             b += self.batch * (self.M + self.N) * ((self.K + sv - 1) // sv)
+        if self.dtype_d in ("e4m3", "e2m1"):  # output factors: one byte per 32 (MX) or 16 (NV) of a row
+            sv = 32 if self.dtype_d == "e4m3" else 16
+            b += self.batch * self.M * ((self.N + sv - 1) // sv)
         return int(b)
 
 
