@@ -129,6 +129,26 @@ def dist_setup():
     return world, rank, local
 
 
+def job_step_ms(total_ms, kernel_ms, steps, flushed, world, device="cpu"):
+    """Per-step time of the whole job: this rank's step time (the timed
+    region over the steps, or the mean launch time when an L2 flush runs
+    between launches), then the maximum over ranks."""
+    import torch
+    import torch.distributed as dist
+
+    local = statistics.mean(kernel_ms) if flushed else total_ms / steps
+    if world > 1:
+        t = torch.tensor([local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        local = float(t.item())
+    return local
+
+
+def job_value(flops_per_rank, world, step_ms):
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's step."""
+    return flops_per_rank * world / (step_ms * 1e-3) / 1e12
+
+
 def oracle_view(spec, inputs):
     """The problem the oracle samples rows of: the workload itself, or for a
     grouped workload its first group (the whole A with B and bias of group
@@ -422,18 +442,14 @@ def run_ours(args):
     launches = op.launches - launches0
     total_ms = total0.elapsed_time(total1)
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    step_ms = job_step_ms(total_ms, kernel_ms, args.steps, flush is not None, world, dev)
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(wall0, wall1)
 
-    # timed region includes the flush writes when a flush is needed; the
-    # per-launch kernel time excludes them
-    step_ms = total_ms / args.steps if flush is None else statistics.mean(kernel_ms)
-    value = flops * world / (step_ms * 1e-3) / 1e12
+    # (the timed region includes the flush writes when a flush is needed;
+    # the per-launch kernel time excludes them)
+    value = job_value(flops, world, step_ms)
     avg_kernel_ms = statistics.mean(kernel_ms)
 
     # end to end through the public API with host buffers: H2D of the inputs,
