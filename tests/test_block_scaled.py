@@ -228,3 +228,29 @@ def test_nvfp4_full_size_sampled_rows():
     bits, op = _run(spec, inputs)
     _check(spec, inputs, bits, rows=H.sample_rows(spec, per_tile=1))
     op.close()
+
+
+# ------------------------------------------------------ work splits ----
+@pytest.mark.parametrize("mode", ["stream_k", "split_tail", "dynamic"])
+@pytest.mark.parametrize("fmt", ["mx", "nv"])
+def test_block_scaled_under_every_work_split_bit_exact(fmt, mode):
+    # 81 pair tiles of 256 x 256 on 76 pairs: the last wave is cut (split
+    # forms) or scheduled on the fly (dynamic); exact sums make every form
+    # equal to the data-parallel result bit for bit
+    dtype = "e4m3" if fmt == "mx" else "e2m1"
+    spec = wl.Spec(f"bs_{fmt}_{mode}", 2304, 2304, 2048, dtype_in=dtype, dtype_d="f32", dist="int4",
+                   block_scale=fmt, seed=150)
+    inputs = wl.make_inputs(spec)
+    modes = {"stream_k": g.SCHED_STREAM_K, "split_tail": g.SCHED_SPLIT_TAIL, "dynamic": g.SCHED_DYNAMIC}
+    op = GemmOp(desc_from_spec(spec, inputs.scale_a, inputs.scale_b))
+    op.set_schedule(modes[mode])
+    if mode != "dynamic":
+        assert op.schedule[2] > 0, "the split cuts no tile: the case tests nothing"
+    bits, _ = _run(spec, inputs, op=op, repeat=2)
+    dp = GemmOp(desc_from_spec(spec, inputs.scale_a, inputs.scale_b))
+    dp.set_schedule(g.SCHED_DATA_PARALLEL)
+    dp_bits, _ = _run(spec, inputs, op=dp)
+    assert np.array_equal(H.logical_d(spec, bits), H.logical_d(spec, dp_bits))
+    _check(spec, inputs, bits, exact=True)
+    op.close()
+    dp.close()
