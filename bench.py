@@ -185,7 +185,8 @@ def oracle_view(spec, inputs):
 
 def oracle_sample(spec, inputs, rows_target_s=12.0):
     """Times the oracle on a bounded random row sample sized for about
-    `rows_target_s` seconds; returns (tflops, rows, secs, threads)."""
+    `rows_target_s` seconds; returns (tflops, number of rows, secs, threads,
+    the rows, the oracle's result for them)."""
     import numpy as np
 
     from oracle import gemm_ref
@@ -201,10 +202,43 @@ def oracle_sample(spec, inputs, rows_target_s=12.0):
     n = int(min(total_rows, max(len(probe), rows_target_s * rows_per_s)))
     rows = np.sort(rng.choice(total_rows, size=n, replace=False))
     t0 = time.perf_counter()
-    run(rows)
+    result = run(rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * len(rows) * spec.N * spec.K
-    return flops / dt / 1e12, len(rows), dt, threads
+    return flops / dt / 1e12, len(rows), dt, threads, rows, result
+
+
+def parity_on_rows(spec, inputs, D, rows, ref_bits):
+    """The timed launches' own output checked on the oracle's sampled rows
+    (l*M + m) with the method's tolerance: per element
+    tau * sqrt(K) * max|A| * max|B| + one output ulp, tau 1e-3 for 16-bit and
+    2e-2 for 8-bit operands.  IEEE output types only; returns a summary."""
+    import numpy as np
+    import torch
+
+    if spec.dtype_d not in ("f32", "f16", "bf16") or spec.block_scale != "none" or getattr(spec, "groups", 0):
+        return None
+    per, ld = spec.matrix_elems("d"), spec.ld("d")
+    l, m = rows // spec.M, rows % spec.M
+    n = np.arange(spec.N)
+    idx = (l * per)[:, None] + ((m * ld)[:, None] + n[None, :] if spec.order_d == "row" else
+                                m[:, None] + (n * ld)[None, :])
+    flat = D.reshape(-1).cpu()
+    got = flat[torch.from_numpy(idx.reshape(-1))].to(torch.float64).numpy().reshape(len(rows), spec.N)
+    bits = torch.from_numpy(np.ascontiguousarray(ref_bits).view(np.int32 if spec.dtype_d == "f32" else np.int16))
+    ref = bits.view({"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[spec.dtype_d])
+    ref = ref.to(torch.float64).numpy()
+    a = inputs.A.to(torch.float32).abs().max().item() * inputs.scale_a
+    b = inputs.B.to(torch.float32).abs().max().item() * inputs.scale_b
+    tau = 2e-2 if spec.dtype_in == "e4m3" else 1e-3
+    mbits = {"f32": 23, "f16": 10, "bf16": 7}[spec.dtype_d]
+    emin = {"f32": -126, "f16": -14, "bf16": -126}[spec.dtype_d]
+    ulp = np.exp2(np.maximum(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** emin))), emin) - mbits)
+    slope = 1.13 if spec.act == "gelu" else 1.0
+    tol = slope * tau * np.sqrt(spec.K) * a * b + ulp
+    worst = float(np.max(np.abs(got - ref) / tol)) if got.size else 0.0
+    return {"rows": int(len(rows)), "elements": int(got.size), "max_err_over_tol": worst,
+            "pass": bool(np.isfinite(got).all() and worst <= 1.0)}
 
 
 def run_reference(args):
@@ -361,8 +395,9 @@ def run_ours(args):
 
     # oracle sample first (on the host cores, before the GPU is busy)
     cpu = None
+    cpu_rows = cpu_ref = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tflops, nrows, secs, threads = oracle_sample(spec, inputs, rows_target_s=args.cpu_seconds)
+        tflops, nrows, secs, threads, cpu_rows, cpu_ref = oracle_sample(spec, inputs, rows_target_s=args.cpu_seconds)
         cpu = {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{nrows} random full rows of {spec.M}x{spec.N}x{spec.K} ({secs:.1f} s, fp64 C loop)"}
 
@@ -440,6 +475,8 @@ def run_ours(args):
     wall1 = time.time()
     op.check()
     launches = op.launches - launches0
+    # the timed launches' own D against the oracle rows sampled above
+    parity = parity_on_rows(spec, inputs, D, cpu_rows, cpu_ref) if cpu_rows is not None else None
     total_ms = total0.elapsed_time(total1)
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     step_ms = job_step_ms(total_ms, kernel_ms, args.steps, flush is not None, world, dev)
@@ -494,6 +531,7 @@ def run_ours(args):
                    "cta_group": info.cta_group, "tiles": info.tiles, "kernel_hash": kernel_hash()},
         "roofline": roofline,
         "cpu_baseline": cpu,
+        "parity": parity,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
