@@ -406,16 +406,17 @@ bool encode_map(CUtensorMap* map, const gl::Layout& lay, int dt, const void* bas
     return r == CUDA_SUCCESS;
 }
 
-// Scale-factor tensor as TMA sees it: rows of 16 bytes, 32 rows (one
-// 512-byte block) per box, `blocks` blocks in all.
+// Scale-factor tensor as TMA sees it: rows of 256 bytes, 2 rows (one
+// 512-byte block) per box, `blocks` blocks in all.  A copy moves a box row
+// at a time, so wide rows keep a block to two requests.
 // Rank 3 (a unit third dimension) like the operand maps, since the kernel
 // issues 3-D tensor copies for both.
 bool encode_sf_map(CUtensorMap* map, const void* base, int64_t blocks) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {16, (cuuint64_t)(blocks * 32), 1};
-    cuuint64_t strides[2] = {16, (cuuint64_t)(blocks * 512)};
-    cuuint32_t box[3] = {16, 32, 1};
+    cuuint64_t dims[3] = {256, (cuuint64_t)(blocks * 2), 1};
+    cuuint64_t strides[2] = {256, (cuuint64_t)(blocks * 512)};
+    cuuint32_t box[3] = {256, 2, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -424,15 +425,15 @@ bool encode_sf_map(CUtensorMap* map, const void* base, int64_t blocks) {
 
 // NVFP4 factors: one ue4m3 per 16 K elements, so a 256-element K stage
 // takes four 512-byte blocks per 128 rows, adjacent in the tensor.  Seen as
-// rows of 16 bytes: dimension 1 walks a 128-row block's K blocks (32 rows
-// each, `kblocks` of them), dimension 2 the 128-row blocks; a box of 128 rows
+// rows of 256 bytes: dimension 1 walks a 128-row block's K blocks (2 rows
+// each, `kblocks` of them), dimension 2 the 128-row blocks; a box of 8 rows
 // is one stage's four blocks, and blocks past the last K block read as zero.
 bool encode_sf_map_nv(CUtensorMap* map, const void* base, int64_t kblocks, int64_t row_blocks) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {16, (cuuint64_t)(kblocks * 32), (cuuint64_t)row_blocks};
-    cuuint64_t strides[2] = {16, (cuuint64_t)(kblocks * 512)};
-    cuuint32_t box[3] = {16, 128, 1};
+    cuuint64_t dims[3] = {256, (cuuint64_t)(kblocks * 2), (cuuint64_t)row_blocks};
+    cuuint64_t strides[2] = {256, (cuuint64_t)(kblocks * 512)};
+    cuuint32_t box[3] = {256, 8, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,

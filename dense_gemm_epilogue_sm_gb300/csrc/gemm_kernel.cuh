@@ -851,26 +851,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 load(sb + c * (kel * 128), &tmB, n0 + c * mn_box, k0, lb);
                         }
                         if constexpr (BS == 2) {
-                            // Four 512-byte blocks per 128 rows and K stage, one box
-                            // at (K block 4 kb, 128-row block) of the batch's tensor
+                            // Four 512-byte blocks per 128 rows and K stage, one box of
+                            // eight 256-byte rows at (K block 4 kb, 128-row block)
                             const uint32_t sf = sb + C::kBBytes;
-                            load(sf, &tmSA, 0, kb * 128, la * p.sf_mblocks + m0 / 128);
+                            load(sf, &tmSA, 0, kb * 8, la * p.sf_mblocks + m0 / 128);
 #pragma unroll
                             for (int j = 0; j < BN / 128; ++j)
-                                load(sf + 2048 * (1 + j), &tmSB, 0, kb * 128, lb * p.sf_nblocks + nb * BN / 128 + j);
+                                load(sf + 2048 * (1 + j), &tmSB, 0, kb * 8, lb * p.sf_nblocks + nb * BN / 128 + j);
                         } else if constexpr (BS == 1) {
                             // One 512-byte scale-factor block per 128 rows and K stage:
                             // block (rows / 128) * num_kb + kb of the batch's tensor, read
-                            // as 32 rows of 16 bytes.  Each CTA takes its own A rows'
+                            // as 2 rows of 256 bytes.  Each CTA takes its own A rows'
                             // block and the block of the tile's whole N range.
                             const uint32_t sf = sb + C::kBBytes;
                             const int blk_a = (la * p.sf_mblocks + m0 / 128) * p.num_kb + kb;
-                            load(sf, &tmSA, 0, blk_a * 32, 0);
+                            load(sf, &tmSA, 0, blk_a * 2, 0);
 #pragma unroll
                             for (int j = 0; j < BN / 128; ++j) {
                                 // (a block past N multiplies zero-filled B columns only)
                                 const int blk_b = (lb * p.sf_nblocks + nb * BN / 128 + j) * p.num_kb + kb;
-                                load(sf + 512 + 512 * j, &tmSB, 0, blk_b * 32, 0);
+                                load(sf + 512 + 512 * j, &tmSB, 0, blk_b * 2, 0);
                             }
                         }
                         const uint32_t bit = 1u << pend_slot(stage);
