@@ -146,15 +146,6 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int3
                  : "memory");
 }
 
-// 1-D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
-// aligned) from global memory into this CTA's shared memory, completing its
-// bytes on `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N committed bulk groups are still reading shared memory.
