@@ -564,8 +564,10 @@ struct MmaCtx {
 // The MMA issuer (one thread of the pair leader).  A tcgen05.mma blocks its
 // issuing thread until the tensor core takes it (the queue is about one
 // instruction deep), so any work between two MMAs is tensor-pipe idle time:
-// the loop asks for the next stage's barrier while the current stage's MMAs
-// issue, builds descriptors by adding offsets to a precomputed base, and
+// the loop asks for the next stage's barrier (non-blocking) once the current
+// stage's MMAs are queued, so the question comes as late as it can and is
+// answered "ready" more often than right after the first MMA (bf16 4096^3
+// +1.9 %); it builds descriptors by adding offsets to a precomputed base and
 // carries the instruction descriptor as an immediate.
 //
 // Every scalar the loop reads is copied into a register first.  The tcgen05
@@ -652,6 +654,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
                     for (int jb = 0; jb < (int)kNB; ++jb)
                         ptx::tmem_cp_32x128b_x4<CG>(sfb + 4u * (kNB * j + jb), sf_desc(sfs + 2048u * (1 + jb) + 512u * j));
                 }
+                // (NVFP4's short stages: asking after the first MMA measures better)
                 ptx::mma_nv<CG, IDESC>(d_tmem, ad, bd, sfa, sfb, first);
                 ready = ptx::mbar_test_wait(full_bar(next), next_phase);
                 ptx::mma_nv<CG, IDESC>(d_tmem, ad + a_step, bd + b_step, sfa + 4u, sfb + 4u * kNB, 1u);
@@ -667,15 +670,15 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
                 for (int jb = 0; jb < BN / 128; ++jb)           // columns 128 jb .. 128 jb + 127 of the tile
                     ptx::tmem_cp_32x128b_x4<CG>(sfb + 4u * jb, sf_desc(sfs + 512u + 512u * jb));
                 ptx::mma_mx<CG, IDESC>(d_tmem, ad, bd, sfa, sfb, first);
-                ready = ptx::mbar_test_wait(full_bar(next), next_phase);
                 ptx::mma_mx<CG, IDESC | (1u << 4) | (1u << 29)>(d_tmem, ad + a_step, bd + b_step, sfa, sfb, 1u);
                 ptx::mma_mx<CG, IDESC | (2u << 4) | (2u << 29)>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, sfa, sfb, 1u);
                 ptx::mma_mx<CG, IDESC | (3u << 4) | (3u << 29)>(d_tmem, ad + 3 * a_step, bd + 3 * b_step, sfa, sfb, 1u);
+                ready = ptx::mbar_test_wait(full_bar(next), next_phase);
             } else {
 #pragma unroll
                 for (int j = 0; j < kStageKBytes / kKStepBytes; ++j) {
                     ptx::mma_imm<CG, F8, IDESC>(d_tmem, ad + j * a_step, bd + j * b_step, j ? 1u : first);
-                    if (j == 0) ready = ptx::mbar_test_wait(full_bar(next), next_phase);
+                    if (j == kStageKBytes / kKStepBytes - 1) ready = ptx::mbar_test_wait(full_bar(next), next_phase);
                 }
             }
             issued = true;
