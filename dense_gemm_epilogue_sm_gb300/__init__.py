@@ -108,6 +108,7 @@ def _load():
         "gemm_run_args": (i32, [vp, ctypes.POINTER(GemmArgs), vp]),
         "gemm_grouped_create": (i32, [ctypes.POINTER(vp), ctypes.POINTER(GemmDesc), i32]),
         "gemm_grouped_run": (i32, [vp, vp, vp, vp, vp, vp, vp, vp]),
+        "gemm_grouped_run_args": (i32, [vp, ctypes.POINTER(GemmArgs), vp, vp]),
         "gemm_check": (i32, [vp]),
         "gemm_destroy": (i32, [vp]),
         "gemm_set_debug": (i32, [vp, i32, u32]),
@@ -132,7 +133,7 @@ def _load():
 
 lib = _load()
 EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_run_ex", "gemm_run_args", "gemm_grouped_create",
-            "gemm_grouped_run", "gemm_check", "gemm_destroy", "gemm_set_debug",
+            "gemm_grouped_run", "gemm_grouped_run_args", "gemm_check", "gemm_destroy", "gemm_set_debug",
             "gemm_set_schedule", "gemm_get_schedule", "gemm_launch_count", "gemm_status_str", "gemm_run_noalloc",
             "gemm_layout_query", "gemm_layout_eval", "gemm_layout_op", "gemm_layout_gather_f32")
 
@@ -233,6 +234,14 @@ def gemm_grouped_run(handle, A, B, C, D, bias, group_rows, stream):
     s = lib.gemm_grouped_run(handle, A, B, C, D, bias, group_rows, stream)
     if s != OK:
         raise GemmError(s, "gemm_grouped_run")
+
+
+def gemm_grouped_run_args(handle, group_rows, stream, **buffers):
+    """Grouped run with every buffer by name (see gemm_run_args)."""
+    a = GemmArgs(**{k: v for k, v in buffers.items() if v is not None})
+    s = lib.gemm_grouped_run_args(handle, ctypes.byref(a), group_rows, stream)
+    if s != OK:
+        raise GemmError(s, "gemm_grouped_run_args")
 
 
 def gemm_check(handle):

@@ -92,8 +92,7 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out, int32_t grou
         if (desc->batch != 1 || desc->stride_a || desc->stride_c || desc->stride_d) return GEMM_ERR_INVALID_ARG;
         if (desc->order_d != GEMM_ROW_MAJOR || (desc->beta != 0.0f && desc->order_c != GEMM_ROW_MAJOR))
             return GEMM_ERR_UNSUPPORTED;
-        if (desc->block_scale != GEMM_BLOCK_SCALE_NONE || desc->out_scale != GEMM_OUT_SCALE_NONE || desc->reduce ||
-            desc->bias == GEMM_BIAS_ROW)
+        if (desc->out_scale != GEMM_OUT_SCALE_NONE || desc->reduce || desc->bias == GEMM_BIAS_ROW)
             return GEMM_ERR_UNSUPPORTED;
         // A K-contiguous: a group's first row is any offset, and a tensor copy
         // may start at any row but only at 16-byte-aligned inner coordinates
@@ -113,7 +112,8 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out, int32_t grou
         const bool a_k = (desc->op_a == GEMM_OP_N) == (desc->order_a == GEMM_ROW_MAJOR);
         const bool b_k = (desc->op_b == GEMM_OP_N) == (desc->order_b == GEMM_COL_MAJOR);
         if (!a_k || !b_k) return GEMM_ERR_UNSUPPORTED;
-        if (desc->lda % 32 || desc->ldb % 32 || (desc->batch > 1 && (desc->stride_a % 32 || desc->stride_b % 32)))
+        if (desc->lda % 32 || desc->ldb % 32 || (desc->batch > 1 && (desc->stride_a % 32 || desc->stride_b % 32)) ||
+            (groups > 1 && desc->stride_b % 32))
             return GEMM_ERR_MISALIGNED;
         view.K /= 2;
         view.lda /= 2;
@@ -705,14 +705,19 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
             h->maps[2] = h->maps[3];
         }
         if (P.kp.block_scaled && d.K > 0) {
-            const int64_t la_n = P.kp.a_batched ? P.kp.L : 1, lb_n = P.kp.b_batched ? P.kp.L : 1;
+            // grouped: A's factors in whole 128-row blocks per group (at most
+            // one partial block per group on top of A's own), B's per group
+            const int64_t groups = P.kp.groups;
+            const int64_t la_n = P.kp.a_batched ? P.kp.L : 1;
+            const int64_t lb_n = P.kp.b_batched ? (groups > 0 ? groups : P.kp.L) : 1;
+            const int64_t a_rowblocks = la_n * P.kp.sf_mblocks + groups;
             if (P.kp.block_scaled == 2) {
                 // K here counts bytes (two elements each): ceil(K/16) factors, four per block
                 const int64_t kblocks = (2 * d.K + 63) / 64;
-                ok = ok && encode_sf_map_nv(&h->maps[4], ksfa, kblocks, la_n * P.kp.sf_mblocks);
+                ok = ok && encode_sf_map_nv(&h->maps[4], ksfa, kblocks, a_rowblocks);
                 ok = ok && encode_sf_map_nv(&h->maps[5], ksfb, kblocks, lb_n * P.kp.sf_nblocks);
             } else {
-                ok = ok && encode_sf_map(&h->maps[4], ksfa, la_n * P.kp.sf_mblocks * (int64_t)P.kp.num_kb);
+                ok = ok && encode_sf_map(&h->maps[4], ksfa, a_rowblocks * (int64_t)P.kp.num_kb);
                 ok = ok && encode_sf_map(&h->maps[5], ksfb, lb_n * P.kp.sf_nblocks * (int64_t)P.kp.num_kb);
             }
         } else {
@@ -802,6 +807,12 @@ gemm_status_t gemm_grouped_run(gemm_handle_t h, const void* A, const void* B, co
                                const float* bias, const int64_t* group_rows, void* stream) {
     if (!group_rows) return GEMM_ERR_INVALID_ARG;
     return run_impl(h, A, B, C, D, bias, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, stream, group_rows);
+}
+
+gemm_status_t gemm_grouped_run_args(gemm_handle_t h, const gemm_args_t* a, const int64_t* group_rows, void* stream) {
+    if (!a || !group_rows) return GEMM_ERR_INVALID_ARG;
+    return run_impl(h, a->A, a->B, a->C, a->D, a->bias, a->row_sum, a->col_sum, a->abs_max, a->sfa, a->sfb, a->sfd,
+                    stream, group_rows);
 }
 
 gemm_status_t gemm_run_args(gemm_handle_t h, const gemm_args_t* a, void* stream) {

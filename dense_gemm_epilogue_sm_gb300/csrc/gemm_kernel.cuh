@@ -173,6 +173,7 @@ struct TilePos {
     int mb, nb, l;
     int m_base, m_end;
     int cd_l;        // batch index of C and D (0 when grouped: one matrix)
+    int sf_base;     // first 128-row scale-factor block of A's rows (grouped: the group's)
 };
 
 // Group offsets as the kernel reads them: each clamped to [0, M], and group
@@ -214,12 +215,14 @@ __device__ __forceinline__ int grouped_tile_count(const KernelParams& p, int til
 
 // A role's walk over the groups: tiles come in increasing order, so the
 // group of the next tile is found by moving forward from the last one.
+// Block-scaled A keeps each group's factors in whole 128-row blocks, one
+// group after another: sf_base counts the blocks of the groups before.
 struct GroupWalk {
-    int g, base, tiles, r0, r1;
+    int g, base, tiles, r0, r1, sf_base;
 };
 
 __device__ __forceinline__ GroupWalk group_walk_make(const KernelParams& p, int tile_rows) {
-    GroupWalk w{0, 0, 0, 0, 0};
+    GroupWalk w{0, 0, 0, 0, 0, 0};
     if (p.groups > 0) {
         w.r0 = clamp_row(p, 0);
         w.r1 = max(w.r0, clamp_row(p, 1));
@@ -234,10 +237,12 @@ __device__ __forceinline__ void tile_pos(const KernelParams& p, GroupWalk& w, in
         t.m_base = 0;
         t.m_end = p.M;
         t.cd_l = t.l;
+        t.sf_base = 0;
         return;
     }
     while (tile >= w.base + w.tiles && w.g + 1 < p.groups) {
         w.base += w.tiles;
+        w.sf_base += (w.r1 - w.r0 + 127) / 128;
         ++w.g;
         w.r0 = w.r1;
         w.r1 = max(w.r1, clamp_row(p, w.g + 1));
@@ -251,6 +256,7 @@ __device__ __forceinline__ void tile_pos(const KernelParams& p, GroupWalk& w, in
     t.m_base = w.r0;
     t.m_end = w.r1;
     t.cd_l = 0;
+    t.sf_base = w.sf_base;
 }
 
 template <bool B>
@@ -818,6 +824,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int mb = tp.mb, nb = tp.nb, l = tp.l;
                 const int la = p.a_batched ? l : 0, lb = p.b_batched ? l : 0;
                 const int m0 = tp.m_base + mb * kTileRows + (int)rank * kTileM;
+                // 128-row factor block of this CTA's A rows (a group's own blocks when grouped)
+                [[maybe_unused]] const int a_sfblk = tp.sf_base + (m0 - tp.m_base) / 128;
                 const int n0 = nb * BN + (int)rank * C::kBRows;
                 bool stop = false;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -857,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // Four 512-byte blocks per 128 rows and K stage, one box of
                             // eight 256-byte rows at (K block 4 kb, 128-row block)
                             const uint32_t sf = sb + C::kBBytes;
-                            load(sf, &tmSA, 0, kb * 8, la * p.sf_mblocks + m0 / 128);
+                            load(sf, &tmSA, 0, kb * 8, la * p.sf_mblocks + a_sfblk);
 #pragma unroll
                             for (int j = 0; j < BN / 128; ++j)
                                 load(sf + 2048 * (1 + j), &tmSB, 0, kb * 8, lb * p.sf_nblocks + nb * BN / 128 + j);
@@ -867,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // as 2 rows of 256 bytes.  Each CTA takes its own A rows'
                             // block and the block of the tile's whole N range.
                             const uint32_t sf = sb + C::kBBytes;
-                            const int blk_a = (la * p.sf_mblocks + m0 / 128) * p.num_kb + kb;
+                            const int blk_a = (la * p.sf_mblocks + a_sfblk) * p.num_kb + kb;
                             load(sf, &tmSA, 0, blk_a * 2, 0);
 #pragma unroll
                             for (int j = 0; j < BN / 128; ++j) {
@@ -1004,6 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tp.m_base = 0;
                     tp.m_end = p.M;
                     tp.cd_l = tp.l;
+                    tp.sf_base = 0;
                 }
                 const int mb = tp.mb, nb = tp.nb, l = tp.l;
                 const int m_end = tp.m_end;        // rows past it belong to no output of this tile

@@ -8,6 +8,7 @@ from . import (ACT_GELU, ACT_NONE, ACT_RELU, BF16, BIAS_COL, BIAS_NONE, BIAS_ROW
                OP_T, REDUCE_ABS_MAX, REDUCE_COL_SUM, REDUCE_ROW_SUM, ROW_MAJOR, BLOCK_SCALE_MX, BLOCK_SCALE_NONE, BLOCK_SCALE_NV,
                OUT_SCALE_MX, OUT_SCALE_NONE, OUT_SCALE_NV,
                gemm_check, gemm_create, gemm_destroy, gemm_get_schedule, gemm_grouped_create, gemm_grouped_run,
+               gemm_grouped_run_args,
                gemm_launch_count, gemm_run, gemm_run_args, gemm_run_ex, gemm_set_schedule, make_desc)
 
 DTYPE_CODE = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1}
@@ -60,11 +61,16 @@ class GemmOp:
         self.groups = groups
         self.handle = gemm_grouped_create(desc, groups) if groups else gemm_create(desc)
 
-    def run_grouped(self, A, B, C, D, group_rows, bias=None, stream=None):
-        """Grouped handle: group_rows is an int64 device tensor of groups + 1 row offsets."""
+    def run_grouped(self, A, B, C, D, group_rows, bias=None, stream=None, sfa=None, sfb=None):
+        """Grouped handle: group_rows is an int64 device tensor of groups + 1 row offsets;
+        sfa / sfb for block-scaled descriptors."""
         s = stream if stream is not None else torch.cuda.current_stream()
-        gemm_grouped_run(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(bias), _ptr(group_rows),
-                         s.cuda_stream)
+        if sfa is not None or sfb is not None:
+            gemm_grouped_run_args(self.handle, _ptr(group_rows), s.cuda_stream, A=_ptr(A), B=_ptr(B), C=_ptr(C),
+                                  D=_ptr(D), bias=_ptr(bias), sfa=_ptr(sfa), sfb=_ptr(sfb))
+        else:
+            gemm_grouped_run(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(bias), _ptr(group_rows),
+                             s.cuda_stream)
 
     def __call__(self, A, B, C, D, bias=None, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream()

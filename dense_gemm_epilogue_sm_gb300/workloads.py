@@ -107,7 +107,7 @@ class Spec:
             b += 4 * (self.N if self.bias == "col" else self.M) * max(1, self.groups)
         if self.block_scale != "none":      # one byte per SV elements of K, per row of A and of B
             sv = SF_VEC[self.block_scale]
-            b += self.batch * (self.M + self.N) * ((self.K + sv - 1) // sv)
+            b += self.batch * (self.M + self.N * max(1, self.groups)) * ((self.K + sv - 1) // sv)
         if self.dtype_d in ("e4m3", "e2m1"):  # output factors: one byte per 32 (MX) or 16 (NV) of a row
             sv = 32 if self.dtype_d == "e4m3" else 16
             b += self.batch * self.M * ((self.N + sv - 1) // sv)
@@ -290,25 +290,54 @@ def _to_storage(spec, which, logical):
     return out
 
 
+def _bs_operand(spec, gen, L, R):
+    """One block-scaled operand of L x R rows of K: (element values (e4m3) or
+    codes (e2m1) (L, R, K), factor codes (L, R, SFK), global scale)."""
+    K = spec.K
+    if spec.block_scale == "mx":
+        sfk = (K + 31) // 32
+        if spec.dist == "int4":
+            # integers in [-4, 4] with factors 2^-1 .. 2^1: every sum exact in fp32
+            q = torch.randint(-4, 5, (L, R, K), generator=gen).to(torch.float32).to(torch.float8_e4m3fn)
+            code = torch.randint(126, 129, (L, R, sfk), generator=gen).to(torch.uint8)
+        else:
+            x = torch.randn(L, R, K, generator=gen, dtype=torch.float32)
+            # a power of two per 32-element block spreads the scale factors
+            shift = torch.randint(-4, 5, (L, R, sfk), generator=gen).to(torch.float32)
+            x = x * torch.exp2(shift.repeat_interleave(32, dim=2)[:, :, :K])
+            q, code = _mx_quantise(x)
+        return q, code, 1.0
+    sfk = (K + 15) // 16
+    if spec.dist == "int4":
+        # any e2m1 code with factors 0.5, 1, 2: every sum exact in fp32
+        q = torch.randint(0, 16, (L, R, K), generator=gen).to(torch.uint8)
+        code = torch.tensor([0x30, 0x38, 0x40], dtype=torch.uint8)[torch.randint(0, 3, (L, R, sfk), generator=gen)]
+        return q, code, 1.0
+    x = torch.randn(L, R, K, generator=gen, dtype=torch.float32)
+    shift = torch.randint(-4, 5, (L, R, sfk), generator=gen).to(torch.float32)
+    x = x * torch.exp2(shift.repeat_interleave(16, dim=2)[:, :, :K])
+    return _nv_quantise(x)
+
+
+# factor code of 1.0, written to the padding of a factor tensor
+SF_ONE = {"mx": 127, "nv": 0x38}
+
+
+def _bs_storage(spec, which, q):
+    """Element values / codes (L, R, K) into the operand's storage."""
+    st = _to_storage(spec, which, q)
+    return _pack_e2m1(st) if spec.block_scale == "nv" else st
+
+
 def _make_mx_inputs(spec, gen):
     L = spec.batch
     ops = {}
     for which, R in (("a", spec.M), ("b", spec.N)):
-        sfk = (spec.K + 31) // 32
-        if spec.dist == "int4":
-            # integers in [-4, 4] with factors 2^-1 .. 2^1: every sum exact in fp32
-            q = torch.randint(-4, 5, (L, R, spec.K), generator=gen).to(torch.float32).to(torch.float8_e4m3fn)
-            code = torch.randint(126, 129, (L, R, sfk), generator=gen).to(torch.uint8)
-        else:
-            x = torch.randn(L, R, spec.K, generator=gen, dtype=torch.float32)
-            # a power of two per 32-element block spreads the scale factors
-            shift = torch.randint(-4, 5, (L, R, sfk), generator=gen).to(torch.float32)
-            x = x * torch.exp2(shift.repeat_interleave(32, dim=2)[:, :, :spec.K])
-            q, code = _mx_quantise(x)
-        off, per = _sf_offsets(L, R, sfk)
-        sf = torch.full((L * per,), 127, dtype=torch.uint8)       # padding factors: 1.0
+        q, code, _ = _bs_operand(spec, gen, L, R)
+        off, per = _sf_offsets(L, R, code.shape[2])
+        sf = torch.full((L * per,), SF_ONE["mx"], dtype=torch.uint8)       # padding factors: 1.0
         sf[off.reshape(-1)] = code.reshape(-1)
-        ops[which] = (_to_storage(spec, which, q), sf)
+        ops[which] = (_bs_storage(spec, which, q), sf)
     return ops
 
 
@@ -316,22 +345,44 @@ def _make_nv_inputs(spec, gen):
     L = spec.batch
     ops = {}
     for which, R in (("a", spec.M), ("b", spec.N)):
-        sfk = (spec.K + 15) // 16
-        if spec.dist == "int4":
-            # any e2m1 code with factors 0.5, 1, 2: every sum exact in fp32
-            q = torch.randint(0, 16, (L, R, spec.K), generator=gen).to(torch.uint8)
-            code = torch.tensor([0x30, 0x38, 0x40], dtype=torch.uint8)[torch.randint(0, 3, (L, R, sfk), generator=gen)]
-            g = 1.0
-        else:
-            x = torch.randn(L, R, spec.K, generator=gen, dtype=torch.float32)
-            shift = torch.randint(-4, 5, (L, R, sfk), generator=gen).to(torch.float32)
-            x = x * torch.exp2(shift.repeat_interleave(16, dim=2)[:, :, :spec.K])
-            q, code, g = _nv_quantise(x)
-        off, per = _sf_offsets(L, R, sfk)
-        sf = torch.full((L * per,), 0x38, dtype=torch.uint8)      # padding factors: 1.0
+        q, code, g = _bs_operand(spec, gen, L, R)
+        off, per = _sf_offsets(L, R, code.shape[2])
+        sf = torch.full((L * per,), SF_ONE["nv"], dtype=torch.uint8)       # padding factors: 1.0
         sf[off.reshape(-1)] = code.reshape(-1)
-        ops[which] = (_pack_e2m1(_to_storage(spec, which, q)), sf, g)
+        ops[which] = (_bs_storage(spec, which, q), sf, g)
     return ops
+
+
+def grouped_sfa_rows(spec, rows):
+    """Row of the factor tensor of A holding each row of A, for a grouped
+    block-scaled workload: every group's rows start a new 128-row block."""
+    out = torch.empty(spec.M, dtype=torch.int64)
+    base = 0
+    for g in range(spec.groups):
+        r0, r1 = int(rows[g]), int(rows[g + 1])
+        out[r0:r1] = base + torch.arange(r1 - r0)
+        base += 128 * ((r1 - r0 + 127) // 128)
+    return out
+
+
+def _make_grouped_bs_inputs(spec, gen, rows):
+    """A (one matrix, factors in per-group 128-row blocks) and B (one matrix
+    and factor tensor per group) of a grouped block-scaled workload."""
+    one = replace(spec, groups=0, group_sizes=(), batch=1)
+    per_group = replace(spec, groups=0, group_sizes=(), batch=spec.groups)
+    qa, ca, ga = _bs_operand(one, gen, 1, spec.M)
+    sfk = ca.shape[2]
+    r_pad = 128 * ((spec.M + 127) // 128 + spec.groups)
+    off, per = _sf_offsets(1, r_pad, sfk)
+    sfa = torch.full((per,), SF_ONE[spec.block_scale], dtype=torch.uint8)
+    covered = int(rows[-1])
+    pr = grouped_sfa_rows(spec, rows)[:covered]
+    sfa[off[0][pr].reshape(-1)] = ca[0][:covered].reshape(-1)
+    qb, cb, gb = _bs_operand(per_group, gen, spec.groups, spec.N)
+    offb, perb = _sf_offsets(spec.groups, spec.N, sfk)
+    sfb = torch.full((spec.groups * perb,), SF_ONE[spec.block_scale], dtype=torch.uint8)
+    sfb[offb.reshape(-1)] = cb.reshape(-1)
+    return _bs_storage(one, "a", qa), _bs_storage(per_group, "b", qb), sfa, sfb, ga, gb
 
 
 def group_rows_of(spec, gen):
@@ -352,15 +403,20 @@ def group_rows_of(spec, gen):
 
 def _make_grouped_inputs(spec, gen):
     rows = group_rows_of(spec, gen)
-    a = _draw(gen, spec.matrix_elems("a"), spec.dist).to(DT[spec.dtype_in])
-    b = _draw(gen, spec.groups * spec.matrix_elems("b"), spec.dist).to(DT[spec.dtype_in])
+    extras = {"group_rows": rows}
+    sa = sb = 1.0
+    if spec.block_scale != "none":
+        a, b, extras["sfa"], extras["sfb"], sa, sb = _make_grouped_bs_inputs(spec, gen, rows)
+    else:
+        a = _draw(gen, spec.matrix_elems("a"), spec.dist).to(DT[spec.dtype_in])
+        b = _draw(gen, spec.groups * spec.matrix_elems("b"), spec.dist).to(DT[spec.dtype_in])
     C = None
     if spec.beta != 0:
         C = _draw(gen, spec.matrix_elems("c"), "normal" if spec.dist != "int4" else "int4").to(DT[spec.dtype_d])
     bias = None
     if spec.bias != "none":
         bias = torch.randn(spec.groups * spec.N, generator=gen, dtype=torch.float32) * spec.bias_sigma
-    return Inputs(spec, a, b, C, bias, 1.0, 1.0, extras={"group_rows": rows})
+    return Inputs(spec, a, b, C, bias, sa, sb, extras=extras)
 
 
 def make_inputs(spec: Spec) -> Inputs:

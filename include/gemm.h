@@ -349,9 +349,17 @@ GEMM_API gemm_status_t gemm_run_args(gemm_handle_t h, const gemm_args_t* args, v
  * (desc.stride_bias apart; 0 = shared):
  *   D[r, :] = act(alpha * A[r, :] op(B_g) + beta * C[r, :] + bias_g)   for r in group g.
  * Descriptor rules: desc.batch = 1 and stride_a = stride_c = stride_d = 0
- * (else GEMM_ERR_INVALID_ARG); D (and C) row-major; no block scaling, MX
- * output, reductions or per-row bias (else GEMM_ERR_UNSUPPORTED); groups in
- * [1, 65535].  The handle runs whole tiles (gemm_set_schedule accepts
+ * (else GEMM_ERR_INVALID_ARG); A K-contiguous, D (and C) row-major; no
+ * block-scaled output, reductions or per-row bias (else
+ * GEMM_ERR_UNSUPPORTED); groups in [1, 65535].
+ * Block-scaled operands (desc.block_scale) run through
+ * gemm_grouped_run_args: SFB holds one basic-block tensor per group (as for a
+ * batch); SFA keeps each group's rows in whole 128-row blocks, the groups'
+ * blocks one after another: row r of group g (r counted from the group's
+ * first row) has its factors in row block B_g + r/128, B_g = the sum over
+ * earlier groups of ceil(rows/128), laid out as one batch of the
+ * basic-block format with R = 128 * (ceil(M/128) + groups) rows; allocate
+ * that many.  The handle runs whole tiles (gemm_set_schedule accepts
  * GEMM_SCHED_AUTO and GEMM_SCHED_DATA_PARALLEL only) and sizes its grid to the
  * GPU, since the tile count is known only on the device.
  * gemm_grouped_run: group_rows is a DEVICE array of groups + 1 int64 row
@@ -366,6 +374,10 @@ GEMM_API gemm_status_t gemm_run_args(gemm_handle_t h, const gemm_args_t* args, v
 GEMM_API gemm_status_t gemm_grouped_create(gemm_handle_t* out, const gemm_desc_t* desc, int32_t groups);
 GEMM_API gemm_status_t gemm_grouped_run(gemm_handle_t h, const void* A, const void* B, const void* C, void* D,
                                         const float* bias, const int64_t* group_rows, void* stream);
+/* gemm_grouped_run with every buffer in one struct (the call for
+ * block-scaled grouped descriptors: sfa / sfb as described above). */
+GEMM_API gemm_status_t gemm_grouped_run_args(gemm_handle_t h, const gemm_args_t* args, const int64_t* group_rows,
+                                             void* stream);
 
 /* Static string for a status code. */
 GEMM_API const char* gemm_status_str(gemm_status_t s);

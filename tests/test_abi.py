@@ -246,8 +246,12 @@ def test_grouped_descriptor_rules():
     assert _grouped_status(_desc(**dict(base, op_a=g.OP_T, order_a=g.COL_MAJOR, lda=256)), 8) == ok   # K-major A
     assert _grouped_status(_desc(**dict(base, reduce=g.REDUCE_ROW_SUM)), 8) == g.ERR_UNSUPPORTED
     assert _grouped_status(_desc(**dict(base, bias=g.BIAS_ROW)), 8) == g.ERR_UNSUPPORTED
-    assert _grouped_status(_desc(**dict(base, dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=g.BLOCK_SCALE_MX)), 8) == \
-        g.ERR_UNSUPPORTED
+    assert _grouped_status(_desc(**dict(base, dtype_a=g.E4M3, dtype_b=g.E4M3, block_scale=g.BLOCK_SCALE_MX)), 8) == ok
+    assert _grouped_status(_desc(**dict(base, dtype_a=g.E2M1, dtype_b=g.E2M1, block_scale=g.BLOCK_SCALE_NV,
+                                        lda=256, ldb=256)), 8) == ok
+    assert _grouped_status(_desc(**dict(base, dtype_a=g.E2M1, dtype_b=g.E2M1, block_scale=g.BLOCK_SCALE_NV,
+                                        lda=256, ldb=256, stride_b=512 * 256 + 16)), 8) == g.ERR_MISALIGNED
+    assert _grouped_status(_desc(**dict(base, dtype_d=g.E4M3, out_scale=g.OUT_SCALE_MX)), 8) == g.ERR_UNSUPPORTED
     assert _grouped_status(_desc(**dict(base, stride_b=512 * 256 + 4)), 8) == g.ERR_MISALIGNED
 
 

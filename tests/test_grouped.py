@@ -205,3 +205,102 @@ def test_grouped_argument_errors():
     assert e.value.status == g.ERR_INVALID_ARG
     plain.close()
     op.close()
+
+
+# ------------------------------------------------- block-scaled groups ----
+U = 2.0 ** -24
+
+
+def _bs_group_problem(spec, inputs, g_, r0, r1):
+    """Group g_ of a grouped block-scaled workload as a problem of its own:
+    its rows of A (and C), its factor blocks of A, B_g, SFB_g and bias_g."""
+    nv = spec.block_scale == "nv"
+    div = 2 if nv else 1                                    # e2m1: two elements per stored byte
+    lda, per_b = spec.ld("a"), spec.matrix_elems("b")
+    sv = 16 if nv else 32
+    kb = ((spec.K + sv - 1) // sv + 3) // 4
+    first = int(wl.grouped_sfa_rows(spec, inputs.extras["group_rows"])[r0]) // 128
+    nblk = (r1 - r0 + 127) // 128
+    sub = dataclasses.replace(spec, M=r1 - r0, groups=0, group_sizes=(), batch=1)
+    per_sfb = ((spec.N + 127) // 128) * kb * 512
+    C = None if inputs.C is None else inputs.C[r0 * spec.ld("c"): r1 * spec.ld("c")].contiguous()
+    bias = None if inputs.bias is None else inputs.bias[g_ * spec.N:(g_ + 1) * spec.N].contiguous()
+    extras = {"sfa": inputs.extras["sfa"][first * kb * 512:(first + nblk) * kb * 512].contiguous(),
+              "sfb": inputs.extras["sfb"][g_ * per_sfb:(g_ + 1) * per_sfb].contiguous()}
+    A = inputs.A[r0 * lda // div: r1 * lda // div].contiguous()
+    B = inputs.B[g_ * per_b // div:(g_ + 1) * per_b // div].contiguous()
+    return sub, wl.Inputs(sub, A, B, C, bias, inputs.scale_a, inputs.scale_b, extras=extras)
+
+
+def _clear_sign(t):
+    if t.dtype == torch.uint8:
+        return t & 0x77
+    return (t.view(torch.uint8) & 0x7F).view(torch.float8_e4m3fn)
+
+
+def _run_bs(spec, inputs):
+    dev = torch.device("cuda", 0)
+    op = GemmOp(desc_from_spec(spec, inputs.scale_a, inputs.scale_b), groups=spec.groups)
+    to = lambda t: None if t is None else t.to(dev)
+    D = H.canary_buffer(spec)
+    op.run_grouped(to(inputs.A), to(inputs.B), to(inputs.C), D, to(inputs.extras["group_rows"]), to(inputs.bias),
+                   sfa=to(inputs.extras["sfa"]), sfb=to(inputs.extras["sfb"]))
+    op.check()
+    torch.cuda.synchronize()
+    info = g.gemm_plan(desc_from_spec(dataclasses.replace(spec, groups=0, group_sizes=())))
+    op.close()
+    return H.bits_of_tensor(D.cpu()), info
+
+
+def _check_bs(spec, inputs, bits, exact):
+    assert H.untouched_outside(spec, bits), "write outside the logical D"
+    d = H.logical_d(spec, bits).reshape(spec.M, spec.N)
+    rows = inputs.extras["group_rows"].tolist()
+    covered = np.zeros(spec.M, dtype=bool)
+    for g_ in range(spec.groups):
+        r0, r1 = rows[g_], rows[g_ + 1]
+        if r1 <= r0:
+            continue
+        covered[r0:r1] = True
+        sub, sub_in = _bs_group_problem(spec, inputs, g_, r0, r1)
+        ref, t = gemm_ref.run_spec_rows(sub, sub_in, want_t=True)
+        if exact:
+            assert np.array_equal(d[r0:r1].astype(np.uint64), ref.astype(np.uint64)), f"group {g_} not bit-exact"
+            continue
+        abs_spec = dataclasses.replace(sub, alpha=1.0, beta=0.0, bias="none", act="none", dtype_d="f32", ldd=0)
+        abs_in = wl.Inputs(abs_spec, _clear_sign(sub_in.A), _clear_sign(sub_in.B), None, None, sub_in.scale_a,
+                           sub_in.scale_b, extras=sub_in.extras)
+        _, tabs = gemm_ref.run_spec_rows(abs_spec, abs_in, want_t=True)
+        got = H.from_bits(d[r0:r1], spec.dtype_d).reshape(r1 - r0, spec.N)
+        want = H.from_bits(ref, spec.dtype_d).reshape(r1 - r0, spec.N)
+        tol = H.SLOPE[spec.act] * (2 * spec.K * U * abs(spec.alpha) * tabs + 4 * U * np.abs(t)) + \
+            H.ulp(want, spec.dtype_d)
+        err = np.abs(got - want)
+        assert np.all(err <= tol), f"group {g_}: {int((err > tol).sum())} elements out of tolerance"
+    assert np.all(d[~covered].astype(np.uint64) == H.CANARY[spec.dtype_d]), "a row outside every group was written"
+
+
+@pytest.mark.parametrize("fmt", ["mx", "nv"])
+@pytest.mark.parametrize("shape", ["pair", "single"])
+def test_grouped_block_scaled_bit_exact(fmt, shape):
+    dt = "e4m3" if fmt == "mx" else "e2m1"
+    if shape == "pair":
+        spec = wl.Spec(f"grp_bs_{fmt}_pair", 5000, 1024, 512, groups=6, group_sizes=(700, 0, 1, 1299, 2000, 900),
+                       dtype_in=dt, dtype_d="f32", dist="int4", block_scale=fmt, seed=160)
+    else:
+        spec = wl.Spec(f"grp_bs_{fmt}_single", 900, 384, 256, groups=3, group_sizes=(100, 250, 550), dtype_in=dt,
+                       dtype_d="f32", dist="int4", block_scale=fmt, seed=161)
+    inputs = wl.make_inputs(spec)
+    bits, info = _run_bs(spec, inputs)
+    assert info.cta_group == (2 if shape == "pair" else 1)
+    _check_bs(spec, inputs, bits, exact=True)
+
+
+@pytest.mark.parametrize("fmt", ["mx", "nv"])
+def test_grouped_block_scaled_matches_oracle(fmt):
+    dt = "e4m3" if fmt == "mx" else "e2m1"
+    spec = wl.Spec(f"grp_bs_{fmt}_fused", 4100, 1100, 640, groups=5, group_sizes=(129, 1000, 0, 2500, 300),
+                   dtype_in=dt, block_scale=fmt, alpha=0.5, beta=1.0, act="relu", bias="col", seed=162)
+    inputs = wl.make_inputs(spec)
+    bits, _ = _run_bs(spec, inputs)
+    _check_bs(spec, inputs, bits, exact=False)
