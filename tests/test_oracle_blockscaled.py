@@ -172,3 +172,30 @@ def test_mx_output_factor_follows_the_shared_exponent_rule():
     assert np.all(np.abs(dq - t[0, :32]) <= 2.0 ** -4 * np.abs(t[0, :32]) + 2.0 ** -16)
     dq1 = np.array([g.decode("e4m3", int(c)) for c in q[0, 32:64]]) * 2.0 ** (int(codes[0, 1]) - 127)
     assert np.all(dq1 == 1792.0)
+
+
+def test_grouped_generator_places_each_groups_factors_in_whole_blocks():
+    # grouped block-scaled A: group g's row r has its factors in row
+    # 128 * (blocks of the groups before) + r of one basic-block tensor,
+    # checked against the oracle's own index function
+    import torch
+    from dense_gemm_epilogue_sm_gb300 import workloads as wl
+    for fmt, dt, sv in (("mx", "e4m3", 32), ("nv", "e2m1", 16)):
+        spec = wl.Spec("grp", 700, 64, 96, groups=4, group_sizes=(130, 0, 1, 500), dtype_in=dt, block_scale=fmt,
+                       dist="int4", seed=9)
+        gen = torch.Generator().manual_seed(spec.seed)
+        rows = wl.group_rows_of(spec, gen)                  # explicit sizes: no draws
+        pr = wl.grouped_sfa_rows(spec, rows).tolist()
+        assert pr[:130] == list(range(130)) and pr[130] == 256 and pr[131:631] == list(range(384, 884))
+        one = dataclasses.replace(spec, groups=0, group_sizes=(), batch=1)
+        _, codes, _ = wl._bs_operand(one, gen, 1, spec.M)     # the generator's first draws: A's factors
+        sfa = wl.make_inputs(spec).extras["sfa"].numpy()
+        sfk = (spec.K + sv - 1) // sv
+        r_pad = 128 * ((spec.M + 127) // 128 + spec.groups)
+        assert sfa.size == (r_pad // 128) * ((sfk + 3) // 4) * 512
+        for r in range(631):                                   # every covered row
+            got = [int(sfa[g.sf_index(0, pr[r], f, r_pad, sfk)]) for f in range(sfk)]
+            assert got == codes[0, r].tolist()
+        # rows between groups are padding: factor 1.0
+        for r in list(range(130, 256, 7)) + list(range(257, 384, 11)):
+            assert all(int(sfa[g.sf_index(0, r, f, r_pad, sfk)]) == wl.SF_ONE[fmt] for f in range(sfk))
