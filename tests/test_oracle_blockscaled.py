@@ -3,6 +3,7 @@ against exact powers of two, the scale-factor index against the byte order
 stated on "Technical Documentation: NVIDIA/cutlass", "Scale Factor Layouts",
 exact rational brute force of D = sum_k (A x SFA)(B x SFB) on small inputs,
 and the closed forms where all scale factors are one or constant."""
+import dataclasses
 import math
 from fractions import Fraction
 
