@@ -28,11 +28,43 @@ KERNEL_SOURCES = ["dense_gemm_epilogue_sm_gb300/csrc/gemm_kernel.cuh", "dense_ge
                   "dense_gemm_epilogue_sm_gb300/csrc/gemm_internal.h"]
 
 
+def _code_only(text):
+    """C++ source without comments, trailing blanks and empty lines: what the
+    compiler sees, so editing a comment does not change the hash."""
+    out, i, n, quote = [], 0, len(text), None
+    while i < n:
+        c = text[i]
+        if quote:
+            out.append(c)
+            if c == "\\" and i + 1 < n:
+                out.append(text[i + 1])
+                i += 2
+                continue
+            if c == quote:
+                quote = None
+            i += 1
+        elif c in "\"'":
+            quote = c
+            out.append(c)
+            i += 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).split("\n") if line.strip())
+
+
 def kernel_hash():
+    """Hash of the kernel's sources as compiled (comments excluded)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
