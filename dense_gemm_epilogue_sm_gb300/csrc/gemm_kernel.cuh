@@ -1,31 +1,38 @@
 // gemm_kernel.cuh - persistent, warp-specialised fused-epilogue GEMM for
 // sm_103a (GB300): TMA -> shared-memory ring -> tcgen05.mma (fp32
-// accumulator in TMEM) -> TMEM loads -> fused alpha/beta/bias/ReLU -> TMA
-// store.
+// accumulator in TMEM) -> TMEM loads -> fused alpha/beta/bias/activation ->
+// TMA (or direct) store.
 //
-// Two variants share this source.  CG = 1: one CTA computes a 128 x BN tile
-// with tcgen05 cta_group::1.  CG = 2: a cluster of two CTAs computes a
-// 256 x BN tile with cta_group::2 MMAs issued by the even CTA (the leader);
-// each CTA loads its own 128 rows of A and BN/2 rows of B, the leader's
-// full[s] barrier counts both CTAs' bytes, commits are multicast to both
-// CTAs, and each CTA's epilogue reads the 128 accumulator rows in its own
-// TMEM and signals the leader's acc_empty barrier.
+// Template parameters: CG = 1: one CTA computes a 128 x BN tile with tcgen05
+// cta_group::1; CG = 2: a cluster of two CTAs computes a 256 x BN tile with
+// cta_group::2 MMAs issued by the even CTA (the leader), each CTA loading its
+// own 128 rows of A and BN/2 rows of B, the leader's full[s] barrier counting
+// both CTAs' bytes, commits multicast to both CTAs, and each CTA's epilogue
+// reading the 128 accumulator rows in its own TMEM and signalling the
+// leader's acc_empty barrier.  BN: 128 or 256 tile columns.  OB: output
+// element bytes (1 = block-scaled e4m3 / e2m1 output with its factors, stored
+// directly).  BS: block-scaled operands (0 none, 1 MXFP8, 2 NVFP4).
 //
 // Structure (the roles of "Technical Documentation: NVIDIA/cutlass",
 // "Blackwell Warp-specialized Persistent Kernel", re-split for this kernel):
-//   warp 0      one lane issues TMA loads of A and B tiles into a STAGES-deep
-//               ring; full[s] counts the bytes, empty[s] is released by the
-//               MMA's commit;
-//   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma into
-//               one of two TMEM accumulators (double buffering lets the
-//               epilogue of tile i overlap the main loop of tile i+1);
+//   warp 0      one lane issues TMA loads of A and B tiles (and their scale
+//               factors) into a STAGES-deep ring; full[s] counts the bytes,
+//               empty[g] is released by the MMA's commit for a group of
+//               stages;
+//   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma into a
+//               TMEM accumulator (two, double buffered, except for 256-wide
+//               block-scaled tiles, whose factor columns leave room for one);
 //   warps 2..5  the epilogue: each warp owns one 32-lane TMEM quadrant
 //               (rows 32q..32q+31 of the 128-row tile), loads the source C
 //               subtile by TMA, applies the fusion in registers, stages D in
 //               swizzled shared memory and stores it by TMA.
-// The persistent loop is the static scheduler of "Blackwell Cluster Launch
-// Control", "Static Persistent Kernel": CTA b takes tiles b, b+grid, ...,
-// in a grouped raster order given as a layout (raster_full / raster_tail).
+// Work: a persistent walk over (tile, K-block range) units shared by all
+// roles: whole tiles in a grouped raster order given as a layout
+// (raster_full / raster_tail), after the static scheduler of "Blackwell
+// Cluster Launch Control", "Static Persistent Kernel"; optionally the last
+// wave cut in K (split tail) or stream-K ranges with an fp32 fix-up; or
+// tiles taken on the fly through cluster launch control; or the tiles of a
+// grouped GEMM, counted from device row offsets.
 //
 // Every mbarrier wait is bounded: on expiry the waiting thread sets the
 // kernel's status word and a shared abort flag, all roles leave their loops,
