@@ -238,8 +238,9 @@ def abs_max(t):
 # floor(log2 amax) - 8, where 8 is the exponent of e4m3's largest power of
 # two, code clamped to [0, 254]; a block with a NaN or infinite element gets
 # code 255 and NaN elements), elements = e4m3(t / 2^(code-127)) rounded to
-# nearest even and saturated at +-448.  The exponent is taken from t rounded
-# to fp32, the precision the epilogue computes t in.
+# nearest even and saturated at +-448.  Everything is taken on the exact
+# (fp64) t: the exponent by frexp, the division by a power of two exactly,
+# and one rounding into e4m3.
 
 def encode_e4m3(values):
     """fp64 array -> e4m3 codes (uint8), round to nearest even, saturating."""
@@ -252,34 +253,41 @@ def encode_e4m3(values):
 def mx_quantise_rows(t):
     """t: (R, N) epilogue values -> (codes (R, ceil(N/32)) uint8, elements
     (R, N) e4m3 codes uint8)."""
-    t32 = np.asarray(t, dtype=np.float64).astype(np.float32).astype(np.float64)
-    R, N = t32.shape
+    t = np.asarray(t, dtype=np.float64)
+    R, N = t.shape
     nb = (N + 31) // 32
     blk = np.zeros((R, nb * 32))
-    blk[:, :N] = t32
+    blk[:, :N] = t
     blk = blk.reshape(R, nb, 32)
-    a = np.abs(blk)
-    bad = ~np.isfinite(a).all(axis=2)
-    amax = np.where(bad, 0.0, a.max(axis=2))
-    _, e = np.frexp(amax)                        # amax = f * 2^e, f in [0.5, 1)
+    with np.errstate(invalid="ignore"):
+        a = np.abs(blk)
+        bad = ~np.isfinite(a).all(axis=2)
+        amax = np.where(bad, 0.0, a.max(axis=2))
+    _, e = np.frexp(amax)                        # amax = f * 2^e, f in [0.5, 1): floor(log2 amax) = e - 1
     code = np.where(amax > 0, np.clip(e - 1 - 8 + 127, 0, 254), 0).astype(np.int64)
-    code = np.where(bad, 255, code)
-    scaled = blk / np.ldexp(1.0, (np.minimum(code, 254) - 127))[:, :, None]
-    q = encode_e4m3(scaled).reshape(R, nb * 32)[:, :N]
-    q = np.where(np.repeat(bad, 32, axis=1)[:, :N], np.uint8(0x7F), q)
-    return code.astype(np.uint8), q.astype(np.uint8)
+    code = np.where(bad, 255, code).astype(np.uint8)
+    return code, mx_quantise_elements(t, code)
+
+
+def mx_quantise_elements(t, codes):
+    """The MX element rule alone, under given ue8m0 codes (R, ceil(N/32)):
+    e4m3(t / 2^(code-127)), nearest even, saturated; NaN (0x7F) where the
+    code is 255.  (R, N) e4m3 codes."""
+    t = np.asarray(t, dtype=np.float64)
+    R, N = t.shape
+    c = np.repeat(codes.astype(np.int64), 32, axis=1)[:, :N]
+    scaled = t / np.ldexp(1.0, np.minimum(c, 254) - 127)      # exact: a power of two
+    q = encode_e4m3(scaled)
+    return np.where(c == 255, np.uint8(0x7F), q).astype(np.uint8)
 
 
 # NVFP4 output ("Blackwell SM100 GEMMs": LinCombBlockScaleFactor with
 # SFDVectorSize = 16).  Reading (the page leaves the rule open): blocks of 16
 # consecutive elements of a D row; with the output's fp32 global scale g,
 # factor = e4m3(amax / (6 g)) (ue4m3, nearest even, saturating at 448) and
-# elements = e2m1(t * r) with r = 1 / (factor * g) (nearest even, saturating
-# at 6), zero where the factor is 0; a block holding NaN or inf gets factor
-# 0x7F and zero elements.  Every step is taken in fp32, the epilogue's
-# precision: t is rounded to fp32 first, and 6 g, the quotient, the factor's
-# value times g, its reciprocal and each element's product are one fp32
-# operation rounded to nearest, so both sides take the same integer decisions.
+# elements = e2m1(t / (factor * g)) (nearest even, saturating at 6), zero
+# where the factor is 0; a block holding NaN or inf gets factor 0x7F and zero
+# elements.  Both roundings are of the exact quotient of the exact t.
 
 def encode_e2m1(values):
     """fp64 array -> e2m1 codes (uint8, 0..15), round to nearest even, saturating."""
@@ -289,30 +297,65 @@ def encode_e2m1(values):
     return out.reshape(np.shape(values))
 
 
+def _grid(dtype, ncodes):
+    """Magnitudes of the non-negative codes 0 .. ncodes-1 (ascending)."""
+    return np.array([decode(dtype, c) for c in range(ncodes)], dtype=np.float64)
+
+
+def rne_quotient(num, den, grid):
+    """Round-to-nearest-even of num / den onto a grid of magnitudes, with
+    saturation: returns the index i of grid[i] nearest to the exact quotient
+    (num >= 0, den > 0, arrays of one shape), the even index of the two on a
+    tie, the last index beyond the last midpoint.  Index parity is the code's
+    last mantissa bit for the grids used here (positive e4m3 and e2m1 codes).
+
+    Decided without dividing: num / den lies above midpoint mid_j exactly when
+    num > mid_j * den.  Every product here is exact in fp64: a midpoint has at
+    most 5 significant bits and den (6 g, or factor * g, g an fp32 value) at
+    most 28, so the comparisons see the exact quotient."""
+    num = np.asarray(num, dtype=np.float64)
+    den = np.asarray(den, dtype=np.float64)
+    mids = (grid[:-1] + grid[1:]) / 2.0
+    prod = den[..., None] * mids
+    n = num[..., None]
+    idx = np.sum(n > prod, axis=-1)              # midpoints strictly below the quotient
+    tie = n == prod                              # quotient exactly on midpoint j: idx == j
+    on_tie = tie.any(axis=-1)
+    odd = (idx % 2) == 1                         # between j (odd) and j + 1 (even): go up
+    return np.where(on_tie & odd, idx + 1, idx)
+
+
 def nv_quantise_rows(t, scale_d):
     """t: (R, N) epilogue values, scale_d: the output's global scale ->
     (factor codes (R, ceil(N/16)) uint8, element codes (R, N) uint8)."""
-    f32 = np.float32
-    t32 = np.asarray(t, dtype=np.float64).astype(f32)
-    R, N = t32.shape
+    t = np.asarray(t, dtype=np.float64)
+    R, N = t.shape
     nb = (N + 15) // 16
-    blk = np.zeros((R, nb * 16), dtype=f32)
-    blk[:, :N] = t32
+    blk = np.zeros((R, nb * 16))
+    blk[:, :N] = t
     blk = blk.reshape(R, nb, 16)
     with np.errstate(invalid="ignore"):
         a = np.abs(blk)
         bad = ~np.isfinite(a).all(axis=2)
-        amax = np.where(bad, f32(0), a.max(axis=2)).astype(f32)
-    g = f32(scale_d)
-    sfv = (amax / (f32(6) * g)).astype(f32)
-    code = encode_e4m3(sfv.astype(np.float64)).astype(np.uint8)
-    code = np.where(bad, np.uint8(0x7F), code)
-    dec = np.array([decode("e4m3", int(c)) if c != 0x7F else 0.0 for c in code.reshape(-1)],
-                   dtype=np.float64).reshape(code.shape).astype(f32)
-    denom = (dec * g).astype(f32)
-    safe = np.where(denom > 0, denom, f32(1))
-    r = np.where(denom > 0, f32(1) / safe, f32(0)).astype(f32)
-    x = (blk * r[:, :, None]).astype(f32)
-    q = encode_e2m1(x.astype(np.float64)).reshape(R, nb * 16)[:, :N]
-    q = np.where(np.repeat(bad, 16, axis=1)[:, :N], np.uint8(0), q)
-    return code.astype(np.uint8), q.astype(np.uint8)
+        amax = np.where(bad, 0.0, a.max(axis=2))
+    g = float(np.float32(scale_d))               # the fp32 global scale
+    e4m3 = _grid("e4m3", 0x7F)                   # 0 .. 448 (code 0x7E)
+    code = rne_quotient(amax, np.full(amax.shape, 6.0 * g), e4m3)
+    code = np.where(bad, 0x7F, code).astype(np.uint8)
+    return code, nv_quantise_elements(t, code, scale_d)
+
+
+def nv_quantise_elements(t, codes, scale_d):
+    """The element rule alone, under given factor codes (R, ceil(N/16)):
+    e2m1(t / (factor * g)) rounded to nearest even and saturated, zero where
+    the factor is 0 or NaN (0x7F).  (R, N) codes, sign in bit 3."""
+    t = np.asarray(t, dtype=np.float64)
+    R, N = t.shape
+    g = float(np.float32(scale_d))
+    fac = np.where(codes == 0x7F, 0.0, _grid("e4m3", 0x80)[np.minimum(codes, 0x7F)])
+    den = np.repeat(fac * g, 16, axis=1)[:, :N]
+    live = den > 0
+    with np.errstate(invalid="ignore"):
+        mag = rne_quotient(np.where(live, np.abs(t), 0.0), np.where(live, den, 1.0), _grid("e2m1", 8))
+    neg = np.signbit(t) & live
+    return np.where(live, mag | np.where(neg, 8, 0), 0).astype(np.uint8)

@@ -182,17 +182,69 @@ def test_nv_output_factor_and_elements_follow_the_rule():
     codes, q = g.nv_quantise_rows(t, 1.0)
     assert codes.shape == (3, 3) and q.shape == (3, 40)
     assert codes[0].tolist() == [0x38, 0x7E, 0x00]
-    assert q[0, :16].tolist() == g.encode_e2m1(np.float32(t[0, :16]).astype(np.float64)).tolist()
+    assert q[0, :16].tolist() == g.encode_e2m1(t[0, :16]).tolist()
     assert np.all(q[0, 16:32] == 7) and np.all(q[0, 32:] == 0)
     assert codes[1, 0] == 0x7F and np.all(q[1, :16] == 0) and codes[1, 1] == 0
     assert codes[2].tolist() == [0x20, 0x20, 0x20] and np.all(q[2] == 7)
+
+
+def _rne_brute(num, den, grid):
+    """Nearest grid value to the exact rational num / den, ties to the even
+    index, saturating: a scan over the whole grid in exact arithmetic."""
+    x = Fraction(num) / Fraction(den)
+    best, best_d = 0, None
+    for i, v in enumerate(grid):
+        d = abs(x - Fraction(v))
+        if best_d is None or d < best_d or (d == best_d and i % 2 == 0):
+            best, best_d = i, d
+    return best
+
+
+def test_rne_quotient_equals_exact_rational_rounding():
+    rng = np.random.default_rng(47)
+    e2m1 = np.array([g.decode("e2m1", c) for c in range(8)])
+    e4m3 = np.array([g.decode("e4m3", c) for c in range(0x7F)])
+    cases = []
+    for _ in range(400):
+        gs = float(np.float32(rng.uniform(0.01, 3.0)))
+        f = e4m3[rng.integers(1, 0x7F)]
+        den = f * gs
+        mid = rng.choice((e2m1[:-1] + e2m1[1:]) / 2)
+        # exact ties, the nearest doubles on either side of them, and random quotients
+        tie = mid * den
+        for num in (tie, np.nextafter(tie, 0), np.nextafter(tie, np.inf), rng.uniform(0, 8) * den):
+            cases.append((num, den, e2m1))
+        den6 = 6.0 * gs
+        mid4 = rng.choice((e4m3[:-1] + e4m3[1:]) / 2)
+        for num in (mid4 * den6, np.nextafter(mid4 * den6, np.inf), rng.uniform(0, 500) * den6):
+            cases.append((num, den6, e4m3))
+    for num, den, grid in cases:
+        got = int(g.rne_quotient(np.array([num]), np.array([den]), grid)[0])
+        assert got == _rne_brute(num, den, grid), (num, den)
+
+
+def test_nv_output_rounds_the_exact_quotient_at_ties():
+    # g = 0.25, factor 144 (0x6E... e4m3 144 = 1.125 * 2^7): factor * g = 36, and t = 9
+    # gives the quotient 0.25 exactly, halfway between 0 and 0.5: the even code 0.
+    # t = 27 gives 0.75 exactly: halfway between 0.5 (code 1) and 1.0 (code 2) -> 2.
+    amax = 144 * 6 * 0.25                           # the block's factor is exactly 144
+    t = np.zeros((1, 16))
+    t[0, :4] = [amax, 9.0, 27.0, -9.0]
+    codes, q = g.nv_quantise_rows(t, 0.25)
+    assert g.decode("e4m3", int(codes[0, 0])) == 144.0
+    assert q[0, 1] == 0 and q[0, 2] == 2 and (q[0, 3] & 7) == 0
+    # the nearest doubles past the ties round away from them
+    t[0, 1] = np.nextafter(9.0, 10.0)
+    t[0, 2] = np.nextafter(27.0, 0.0)
+    _, q = g.nv_quantise_rows(t, 0.25)
+    assert q[0, 1] == 1 and q[0, 2] == 1
 
 
 def test_nv_output_global_scale_is_a_pure_rescaling():
     rng = np.random.default_rng(45)
     t = rng.normal(size=(4, 64)) * 3.0
     c1, q1 = g.nv_quantise_rows(t, 1.0)
-    c2, q2 = g.nv_quantise_rows(t * 2.0 ** 7, 2.0 ** 7)   # powers of two: every fp32 step exact
+    c2, q2 = g.nv_quantise_rows(t * 2.0 ** 7, 2.0 ** 7)   # a power of two scales every quotient exactly
     assert np.array_equal(c1, c2) and np.array_equal(q1, q2)
 
 
