@@ -155,7 +155,8 @@ gemm_status_t validate_and_plan(const gemm_desc_t* desc, Plan* out, int32_t grou
     if (d.out_scale != GEMM_OUT_SCALE_NONE && (d.order_d != GEMM_ROW_MAJOR || d.beta != 0.0f || d.reduce))
         return GEMM_ERR_UNSUPPORTED;
     if (out_nv) {
-        if (!(d.scale_d > 0.0f) || !(d.scale_d < 3.0e38f)) return GEMM_ERR_INVALID_ARG;
+        // a normal fp32 (the kernel's exact rounding tests need g >= 2^-126)
+        if (!(d.scale_d >= 1.17549435e-38f) || !(d.scale_d < 3.0e38f)) return GEMM_ERR_INVALID_ARG;
         if (d.N % 2) return GEMM_ERR_UNSUPPORTED;                  // whole bytes per row
         if (d.ldd % 32 || (d.batch > 1 && d.stride_d % 32)) return GEMM_ERR_MISALIGNED;
     }

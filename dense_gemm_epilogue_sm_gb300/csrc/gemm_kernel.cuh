@@ -558,6 +558,92 @@ __device__ __forceinline__ uint64_t sf_desc(uint32_t addr) {
     return d;
 }
 
+// ------------------------------------------------------- NVFP4 output ---
+// Round-to-nearest-even of exact quotients onto the e4m3 and e2m1 grids,
+// decided by comparisons rather than by a rounded division: x / y lies
+// above a midpoint m of the grid exactly when x > m * y, and with m * y'
+// exact in fp32 (a midpoint has at most 5 significant bits) the sign of
+// fmaf(m y', g, -x) is the sign of the exact m * y' * g - x (the product is
+// not rounded inside the FMA, the one rounding keeps sign and zero).  So the
+// codes are those of the real quotients of the fp32 values, ties to the even
+// code, whatever rounding a division would have added.
+
+// Value of a non-negative e4m3 code (0 .. 0x7E).
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+    const uint32_t fe = c >> 3, fm = c & 7u;
+    return fe ? __uint_as_float(((fe + 120u) << 23) | (fm << 20)) : (float)fm * 0.001953125f;   // m * 2^-9
+}
+
+// ue4m3 factor of an NVFP4 output block: e4m3(amax / (6 g)), nearest even,
+// saturating at 448 (code 0x7E).  amax finite and >= 0, g normal and > 0,
+// inv6g a rounded 1 / (6 g).  The candidate amax * inv6g is within one code
+// of the exact result (its error is a few 2^-24 of the quotient, the grid's
+// spacing at least 2^-3 of it, and past 448 every code saturates); the
+// midpoints on either side settle it.
+__device__ __forceinline__ uint32_t nv_factor_code(float amax, float g, float inv6g) {
+    uint32_t c = ptx::pack4_e4m3(__fmul_rn(amax, inv6g), 0.f, 0.f, 0.f) & 0xFFu;
+    if (c > 0u) {
+        const float lo6 = 3.0f * (e4m3_value(c - 1u) + e4m3_value(c));        // 6 x the lower midpoint, exact
+        const float s = __fmaf_rn(lo6, g, -amax);
+        if (s > 0.f || (s == 0.f && (c & 1u))) return c - 1u;
+    }
+    if (c < 0x7Eu) {
+        const float hi6 = 3.0f * (e4m3_value(c) + e4m3_value(c + 1u));
+        const float s = __fmaf_rn(hi6, g, -amax);
+        if (s < 0.f || (s == 0.f && (c & 1u))) return c + 1u;
+    }
+    return c;
+}
+
+// e2m1 codes of 16 values under factor value f > 0 and global scale g:
+// e2m1(v / (f g)), nearest even, saturating at 6, sign in bit 3; packed two
+// per byte, the lower index in the low nibble.  The magnitude code is the
+// number of midpoints (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) below |v| / (f g),
+// a midpoint that |v| / (f g) equals counting when the code below it is odd
+// (ties to even); three comparisons find it, one per bit, and every midpoint
+// compared at one level has the same parity.
+__device__ __forceinline__ uint2 nv_element_codes(const float (&v)[16], float f, float g) {
+    const float t0 = 0.25f * f, t1 = 0.75f * f, t2 = 1.25f * f, t3 = 1.75f * f;
+    const float t4 = 2.5f * f, t5 = 3.5f * f, t6 = 5.0f * f;     // exact: at most 7 significant bits
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float a = fabsf(v[i]);
+        const bool b2 = __fmaf_rn(t3, g, -a) <= 0.f;                       // at or past 1.75: code >= 4
+        const bool b1 = __fmaf_rn(b2 ? t5 : t1, g, -a) <= 0.f;            // past 3.5 / 0.75 (odd below)
+        const float tl = b2 ? (b1 ? t6 : t4) : (b1 ? t2 : t0);
+        const bool b0 = __fmaf_rn(tl, g, -a) < 0.f;                        // past 5, 2.5, 1.25, 0.25 (even below)
+        const uint32_t mag = a > 0.f ? (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u) : 0u;
+        const uint32_t code = mag | (__float_as_uint(v[i]) >> 28 & 8u);
+        w[i >> 3] |= code << ((i & 7) * 4);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+// The same codes, fast: x = v * r with r a rounded 1 / (f g) is within
+// 4 * 2^-24 of the exact quotient (relative), so rounding x nudged down and
+// up by 2^-20 gives the same e2m1 codes exactly when no rounding midpoint
+// lies within that band, and then they are the codes of the exact quotient
+// too.  A block where any code differs (a quotient at or next to a midpoint)
+// is decided by the comparisons above.  f g below 2^-100 (where r would lose
+// precision or overflow) always takes the comparisons.
+__device__ __forceinline__ uint2 nv_element_codes_fast(const float (&v)[16], float f, float g) {
+    const float fg = __fmul_rn(f, g);
+    if (fg < 7.88860905e-31f) return nv_element_codes(v, f, g);
+    const float r = __frcp_rn(fg);
+    const float r_lo = __fmul_rn(r, 1.0f - 9.5367431640625e-07f), r_hi = __fmul_rn(r, 1.0f + 9.5367431640625e-07f);
+    float lo[16], hi[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        lo[i] = __fmul_rn(v[i], r_lo);
+        hi[i] = __fmul_rn(v[i], r_hi);
+    }
+    const uint2 a = make_uint2(ptx::pack8_e2m1(lo), ptx::pack8_e2m1(lo + 8));
+    const uint2 b = make_uint2(ptx::pack8_e2m1(hi), ptx::pack8_e2m1(hi + 8));
+    if (a.x == b.x && a.y == b.y) return a;
+    return nv_element_codes(v, f, g);
+}
+
 // What the MMA issuer needs from the kernel.
 template <int CG, int BN, int S>
 struct MmaCtx {
@@ -1115,11 +1201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (p.out_f8 == 2) {
                             // NVFP4 output: e2m1 elements and one ue4m3 factor per 16
-                            // columns of a row under the global scale g = scale_d, each
-                            // step one fp32 operation rounded to nearest:
-                            // factor = e4m3(amax / (6 g)), elements e2m1(t * r) with
-                            // r = 1 / (factor g) once per block
-                            const float six_g = __fmul_rn(6.0f, p.scale_d);
+                            // columns of a row under the global scale g = scale_d:
+                            // factor = e4m3(amax / (6 g)), elements e2m1(t / (factor g)),
+                            // both the nearest-even codes of the exact quotients
+                            const float inv6g = __frcp_rn(__fmul_rn(6.0f, p.scale_d));
 #pragma unroll
                             for (int h = 0; h < C::kEpiCols / 16; ++h) {
                                 const int c0 = col0 + h * 16;
@@ -1144,21 +1229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 uint32_t code = 0x7Fu;            // NaN / inf in the block
                                 uint2 out = make_uint2(0u, 0u);
                                 if (amax < 0x7F800000u) {
-                                    const float sfv = __fdiv_rn(__uint_as_float(amax), six_g);
-                                    code = ptx::pack4_e4m3(sfv, 0.f, 0.f, 0.f) & 0xFFu;
-                                    // the factor's value, from its bits (code <= 0x7E, sign 0)
-                                    const uint32_t fe = code >> 3, fm = code & 7u;
-                                    const float fval = fe ? __uint_as_float(((fe + 120u) << 23) | (fm << 20))
-                                                          : (float)fm * 0.001953125f;     // m * 2^-9
-                                    const float denom = __fmul_rn(fval, p.scale_d);
-                                    if (denom > 0.f) {
-                                        const float r = __frcp_rn(denom);
-                                        float x[16];
-#pragma unroll
-                                        for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(v[i], r);
-                                        out.x = ptx::pack8_e2m1(x);
-                                        out.y = ptx::pack8_e2m1(x + 8);
-                                    }
+                                    code = nv_factor_code(__uint_as_float(amax), p.scale_d, inv6g);
+                                    if (code != 0u) out = nv_element_codes_fast(v, e4m3_value(code), p.scale_d);
                                 }
                                 if (row < m_end) {
                                     uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)dl * p.d_bstride +

@@ -134,12 +134,12 @@ typedef enum { GEMM_BLOCK_SCALE_NONE = 0, GEMM_BLOCK_SCALE_MX = 1, GEMM_BLOCK_SC
  * else GEMM_ERR_UNSUPPORTED / GEMM_ERR_MISALIGNED) and every 16 consecutive
  * elements of a D row share one ue4m3 factor, written to gemm_args_t.sfd in
  * the basic-block layout (rows = M, factors per row = ceil(N/16)).  With the
- * output's fp32 global scale g = desc.scale_d (> 0 and finite, else
- * GEMM_ERR_INVALID_ARG), each step one fp32 operation rounded to nearest:
- * factor = e4m3(amax / (6 g)) (nearest even, saturating at 448; amax = the
- * block's max |t|), elements e2m1(t * r) with r = 1 / (factor * g) (nearest
- * even, saturating at +-6), 0 where the factor is 0; a block holding NaN or inf
- * gets factor 0x7F and zero elements.  So D * factor * g ~ t, and D with its
+ * output's fp32 global scale g = desc.scale_d (a normal, finite fp32 > 0,
+ * else GEMM_ERR_INVALID_ARG): factor = e4m3(amax / (6 g)) (nearest even,
+ * saturating at 448; amax = the block's max |t|), elements
+ * e2m1(t / (factor * g)) (nearest even, saturating at +-6), each the
+ * rounding of the exact quotient of the fp32 values; 0 where the factor is
+ * 0; a block holding NaN or inf gets factor 0x7F and zero elements.  So D * factor * g ~ t, and D with its
  * factors and g is an NVFP4 operand (GEMM_BLOCK_SCALE_NV) for the next GEMM.
  * Same restrictions as GEMM_OUT_SCALE_MX. */
 typedef enum { GEMM_OUT_SCALE_NONE = 0, GEMM_OUT_SCALE_MX = 1, GEMM_OUT_SCALE_NV = 2 } gemm_out_scale_t;
