@@ -13,18 +13,21 @@ Definitions followed (section of that page in brackets):
   reduced modulo its extent, so a coordinate past the end continues along it.
   size = product of the shape, cosize = L(size-1) + 1, rank = number of
   top-level modes; the default stride is the compact column-major one.
-* [Coalescing] coalesce flattens, drops extent-1 modes, and merges a mode into
-  its predecessor when predecessor.shape * predecessor.stride equals its
-  stride.  It preserves L(i) for every one-dimensional i.
+* [Coalescing] coalesce flattens, drops extent-1 modes, and joins two
+  neighbouring modes whenever the first's shape * stride equals the second's
+  stride, until no two join.  It preserves L(i) for every 1-D i < size.
 * [Composition: a layout over a layout] R = A o B, R(c) = A(B(c)), with B's
-  shape.  For one mode n:d of B: walk A's coalesced modes, first stepping over
-  d elements, then collecting n; undefined (an error here) unless, at every
-  mode, the extent and the remaining step divide one another and the count
-  still wanted is a multiple of what the mode supplies.  A's last mode is
-  unbounded.  A tuple of layouts as B composes mode by mode.
-* [Complement and division] complement(A, M) lays out the indices of [0, M)
-  that A does not reach, in increasing stride order, so that (A, A*) covers
-  [0, M) exactly once; logical_divide(A, B) = A o (B, complement(B, size A));
+  shape; several modes of B compose separately, side by side.  For one mode
+  n:d the points A(0), A(d), ..., A((n-1) d) are evaluated (A coalesced, its
+  last mode unbounded) and read back as the layout that has them as its 1-D
+  function.  Composition is undefined where the page says so: when the
+  selected elements fall inside a mode of A that one stride cannot express,
+  or when the count wanted cannot be split into whole counts per mode; both
+  are checked as conditions on the prefix products of A's coalesced extents.
+* [Complement and division] complement(A, M) is the layout A* for which
+  (A, A*) covers every index of [0, M) exactly once: the set A reaches is
+  widened by copies shifted by its first gap until it is an interval, then
+  repeated up to M.  logical_divide(A, B) = A o (B, complement(B, size A));
   zipped_divide regroups a mode-wise division as ((tile modes), (rest modes)).
 * [From tiles to threads] local_tile fixes the rest (tile-index) mode of a
   zipped division to a CTA's tile coordinate; local_partition fixes the tile
@@ -125,21 +128,31 @@ class Layout:
         return f"{fmt(self.shape)}:{fmt(self.stride)}"
 
 
-def _index(coord, shape, stride) -> int:
+def _flat_coordinate(coord, shape):
+    """The fully expanded coordinate of `coord` against `shape`, as a list of
+    one value per leaf (left to right).  An integer facing a tuple shape is
+    split colexicographically over that shape's leaves (the leftmost leaf
+    varies fastest); the last leaf keeps the quotient unreduced, so a
+    coordinate past the end continues along it."""
     if _is_tup(coord):
         if not _is_tup(shape) or len(coord) != len(shape):
             raise LayoutError("coordinate does not match the shape's modes")
-        return sum(_index(c, s, d) for c, s, d in zip(coord, shape, stride))
-    if not _is_tup(shape):
-        return coord * stride
-    # integer against a tuple: peel the modes off, fastest first; the last
-    # mode takes whatever is left
-    total, rest = 0, coord
-    for s, d in zip(shape[:-1], stride[:-1]):
-        extent = product(s)
-        total += _index(rest % extent, s, d)
-        rest //= extent
-    return total + _index(rest, shape[-1], stride[-1])
+        out = []
+        for c, s in zip(coord, shape):
+            out.extend(_flat_coordinate(c, s))
+        return out
+    extents = leaves(shape)
+    digits = []
+    for e in extents[:-1]:
+        coord, r = divmod(coord, e)
+        digits.append(r)
+    return digits + [coord]
+
+
+def _index(coord, shape, stride) -> int:
+    """The layout function: the inner product of the expanded coordinate with
+    the stride."""
+    return sum(c * d for c, d in zip(_flat_coordinate(coord, shape), leaves(stride)))
 
 
 def parse(text: str) -> Layout:
@@ -196,64 +209,121 @@ def _from_modes(modes) -> Layout:
 
 
 def coalesce(a: Layout) -> Layout:
-    merged = []
-    for s, d in a.flat():
-        if s == 1:
-            continue
-        if merged and merged[-1][0] * merged[-1][1] == d:
-            merged[-1] = (merged[-1][0] * s, merged[-1][1])
-        else:
-            merged.append((s, d))
-    return _from_modes(merged)
+    """Flattens, drops modes of extent 1, and joins neighbouring modes that
+    meet end to end (extent x stride of the first equals the stride of the
+    second) until no two do.  L(i) is unchanged for every 1-D i."""
+    modes = [(s, d) for s, d in a.flat() if s != 1]
+    joined = True
+    while joined:
+        joined = False
+        for k in range(len(modes) - 1):
+            (s0, d0), (s1, d1) = modes[k], modes[k + 1]
+            if s0 * d0 == d1:
+                modes[k:k + 2] = [(s0 * s1, d0)]
+                joined = True
+                break
+    return _from_modes(modes)
 
 
-def _compose_single(a: Layout, n: int, d: int) -> Layout:
-    """A o (n:d) for one leaf mode of B."""
-    if d == 0:
-        return Layout(n, 0)
-    if n == 1:
-        return Layout(1, 0)        # a single coordinate: extent-1 modes print with stride 0
-    modes = coalesce(a).flat()
-    picked = []
-    want, step = n, d
-    for extent, stride in modes[:-1]:
-        if want == 1:
+def _as_layout(values):
+    """The layout whose 1-D function is the integer sequence `values` (index i
+    -> values[i], values[0] = 0), in its coalesced form, or LayoutError when
+    no layout with that many coordinates has that function.  Each mode in
+    turn takes the longest stretch over which the sequence advances by one
+    fixed stride per copy of everything found so far; the stretch must split
+    the remaining count into whole copies."""
+    n = len(values)
+    modes, block = [], 1
+    while block < n:
+        stride = values[block]
+        extent = 1
+        while block * (extent + 1) <= n and all(
+                values[extent * block + i] == values[i] + extent * stride for i in range(block)):
+            extent += 1
+        if (n // block) % extent:
+            raise LayoutError("the composed points do not split into whole modes")
+        modes.append((extent, stride))
+        block *= extent
+    return _from_modes(modes)
+
+
+def _check_composable(a: Layout, n: int, d: int) -> None:
+    """The two conditions under which A o (n:d) is defined, in terms of the
+    prefix products P_k of A's coalesced extents (P_0 = 1), for every bounded
+    mode k the selected points reach (P_(k-1) < n d):
+    - the step d lands on whole modes: P_k divides d, or d divides P_k
+      (otherwise an element falls inside a mode that one stride cannot
+      express: the page's ∘ 4:4);
+    - whole counts per mode: once d divides P_k, the n points either end
+      inside mode k (n d <= P_k) or use all of it (P_k divides n d)
+      (otherwise the count wanted cannot be split: the page's ∘ 4:2)."""
+    if n == 1 or d == 0:
+        return
+    extents = [s for s, _ in coalesce(a).flat()][:-1]      # the last mode is unbounded
+    prev = 1
+    for e in extents:
+        p = prev * e
+        if prev >= n * d:
             break
-        if extent % step != 0 and step % extent != 0:
-            raise LayoutError(f"stride divisibility fails: extent {extent} vs step {step}")
-        supply = extent // step if extent > step else 1
-        if supply > 1:
-            take = min(supply, want)
-            if want % take != 0:
-                raise LayoutError(f"shape divisibility fails: want {want}, mode gives {take}")
-            picked.append((take, step * stride))
-            want //= take
-        step = -(-step // extent)      # steps left over once past this mode
-    if want != 1:
-        picked.append((want, step * modes[-1][1]))   # the last mode is unbounded
-    return _from_modes(picked)
+        if d % p == 0:
+            prev = p
+            continue
+        if p % d != 0:
+            raise LayoutError(f"stride divisibility fails: prefix {p} vs step {d}")
+        if n * d > p and (n * d) % p != 0:
+            raise LayoutError(f"shape divisibility fails: {n} points of step {d} over prefix {p}")
+        prev = p
 
 
 def composition(a: Layout, b) -> Layout:
+    """R = A o B with R(i) = A(B(i)): computed point by point and read back as
+    a layout, mode by mode of B (a tuple of layouts composes with A's modes
+    one by one, leaving the rest).  A is taken in its coalesced form, as the
+    page's walk starts from it: the same function on [0, size A), and points
+    past the end continue along the coalesced layout's last mode."""
     if isinstance(b, (tuple, list)):           # a tiler: one layout per mode of a
         parts = [composition(a.mode(i), bi) for i, bi in enumerate(b)]
         parts += [a.mode(i) for i in range(len(b), a.rank())]
         return concat(*parts)
     if _is_tup(b.shape):
         return concat(*[composition(a, b.mode(i)) for i in range(b.rank())])
-    return _compose_single(a, b.shape, b.stride)
+    n, d = b.shape, b.stride
+    _check_composable(a, n, d)
+    if n == 1:
+        return Layout(1, 0)        # a single coordinate: extent-1 modes print with stride 0
+    ac = coalesce(a)
+    return _as_layout([ac(i * d) for i in range(n)])
 
 
 def complement(a: Layout, cotarget: int = 1) -> Layout:
-    modes = sorted((d, s) for s, d in a.flat() if s != 1 and d != 0)
-    out, reach = [], 1
-    for d, s in modes:
-        if d % reach != 0:
+    """A* with (A, A*) covering [0, M) exactly once, M >= cotarget: the set
+    of indices A reaches (modes of extent 1 or stride 0 add none) is widened
+    by copies shifted by its first gap, as many as stay disjoint, until it is
+    [0, R); R < cotarget adds a last mode of ceil(cotarget / R) copies at
+    stride R.  LayoutError when A repeats an index or a gap cannot be filled
+    without overlap."""
+    active = [(s, d) for s, d in a.flat() if s != 1 and d != 0]
+    reached = {0}
+    for s, d in active:
+        reached = {x + j * d for x in reached for j in range(s)}
+    if len(reached) != product(tuple(s for s, _ in active)):
+        raise LayoutError("modes overlap; complement undefined")
+    modes = []
+    while True:
+        gap = next(x for x in range(len(reached) + 1) if x not in reached)
+        if gap == len(reached):                 # [0, R) is covered
+            break
+        copies = 1
+        while not any((x + copies * gap) in reached for x in reached):
+            copies += 1
+        if copies == 1:
             raise LayoutError("modes overlap; complement undefined")
-        out.append((d // reach, reach))
-        reach = s * d
-    out.append((-(-cotarget // reach), reach))
-    return coalesce(Layout(tuple(s for s, _ in out), tuple(d for _, d in out)))
+        reached = {x + j * gap for x in reached for j in range(copies)}
+        modes.append((copies, gap))
+    span = len(reached)
+    if span < cotarget:
+        modes.append((-(-cotarget // span), span))
+    return coalesce(_from_modes(modes))
 
 
 def logical_divide(a: Layout, b) -> Layout:
