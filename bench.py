@@ -68,6 +68,62 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
+def workloads_module():
+    """The workload generator, loaded by path: it holds no GEMM code and
+    imports only torch, so the reference arm never runs the package's
+    __init__ (which loads the CUDA library)."""
+    import importlib.util
+
+    name = "dense_gemm_epilogue_sm_gb300_workloads"
+    if name in sys.modules:
+        return sys.modules[name]
+    spec = importlib.util.spec_from_file_location(
+        name, os.path.join(ROOT, "dense_gemm_epilogue_sm_gb300", "workloads.py"))
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[name] = mod
+    spec.loader.exec_module(mod)
+    return mod
+
+
+# Dense tensor-core rate per SM and clock, by operand width: one cta_group::2
+# 256x256x16 bf16 MMA per CTA pair every 128 cycles (8192 FLOP/clk/SM), twice
+# that for 8-bit and four times for 4-bit operands.  ncu on this kernel gives
+# 7988 FLOP per tensor-active cycle per SM for bf16 (cuBLAS: 7819), and about
+# 32k for NVFP4 (profiles/).
+SPEC_FLOP_PER_CLK_SM = {"bf16": 8192, "f16": 8192, "e4m3": 16384, "e2m1": 32768}
+SPEC_SM_MHZ = 2070.0                 # the part's maximum SM clock
+
+
+def spec_peak_tflops(dtype_in, sms, mhz=SPEC_SM_MHZ):
+    """sms x dense FLOP/clk/SM x clock, in TFLOP/s."""
+    return sms * SPEC_FLOP_PER_CLK_SM[dtype_in] * mhz * 1e6 / 1e12
+
+
+def roofline_bound(flops, nbytes, tensor_tflops, hbm_gbs):
+    """'tensor' or 'hbm': whichever of FLOPs / tensor peak and bytes / HBM
+    peak takes longer."""
+    return "hbm" if nbytes / (hbm_gbs * 1e9) > flops / (tensor_tflops * 1e12) else "tensor"
+
+
+def workload_config(spec, flushed):
+    """The workload part of the JSON line's config: the same in both arms."""
+    cfg = {"workload": spec.name, "M": spec.M, "N": spec.N, "K": spec.K, "batch": spec.batch}
+    if getattr(spec, "groups", 0):
+        cfg["groups"] = spec.groups
+    cfg.update({"alpha": spec.alpha, "beta": spec.beta, "act": spec.act, "bias": spec.bias,
+                "in": spec.dtype_in, "out": spec.dtype_d,
+                "l2": "L2 flushed between steps" if flushed else "inputs larger than L2"})
+    return cfg
+
+
+L2_BYTES = 129e6
+
+
+def needs_flush(spec):
+    """Inputs smaller than twice the L2 are flushed from it before every launch."""
+    return spec.algorithmic_bytes() < 2 * L2_BYTES
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -91,8 +147,74 @@ def load_traffic(workload):
     return None
 
 
+class NvmlSampler:
+    """SM clock, power and clock-event reasons read through NVML (ctypes on
+    libnvidia-ml) every `period` seconds on a thread: dense enough that a
+    timed region of a few ms holds samples.  Reads only; changes nothing."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid, period=0.001):
+        import ctypes
+
+        self.samples = []
+        self.period = period
+        self._stop = False
+        self.thread = None
+        self.ok = False
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle)) != 0:
+                return
+            self.nv = nv
+            self.ct = ctypes
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))      # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _read(self):
+        ct, nv, h = self.ct, self.nv, self.handle
+        mhz, mw, reasons = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        while not self._stop:
+            t = time.time()
+            nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz))
+            nv.nvmlDeviceGetPowerUsage(h, ct.byref(mw))
+            nv.nvmlDeviceGetCurrentClocksEventReasons(h, ct.byref(reasons))
+            self.samples.append((t, float(mhz.value), mw.value / 1000.0, int(reasons.value)))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+
+    def stop(self):
+        self._stop = True
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        if not inside:
+            return None
+        bits = 0
+        for x in inside:
+            bits |= x[3]
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(name for b, name in self.REASONS.items() if bits & b),
+                "samples": len(inside), "window": "timed region (NVML, 1 ms)",
+                "power_w_max": max(x[2] for x in inside)}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms (used
+    where NVML cannot be loaded)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -189,9 +311,9 @@ def oracle_view(spec, inputs):
     Returns (spec, inputs, rows to draw from, rows -> result function)."""
     import dataclasses
 
-    from dense_gemm_epilogue_sm_gb300 import workloads as wl
     from oracle import gemm_ref
 
+    wl = workloads_module()
     total = spec.batch * spec.M
     if getattr(spec, "groups", 0):
         sub = dataclasses.replace(spec, groups=0, group_sizes=())
@@ -209,10 +331,52 @@ def oracle_view(spec, inputs):
     if quant is not None:
         spec = dataclasses.replace(spec, dtype_d="f32")
 
-    def run(rows):
-        bits, t = gemm_ref.run_spec_rows(spec, inputs, rows=rows, want_t=quant is not None)
+    def run(rows, nthreads=0):
+        bits, t = gemm_ref.run_spec_rows(spec, inputs, rows=rows, want_t=quant is not None, nthreads=nthreads)
         return quant(t) if quant is not None else bits
     return spec, inputs, total, run
+
+
+def host_cpu():
+    """The host's CPU model and logical core count, as the OS reports them."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"model": model or "unknown", "logical_cores": os.cpu_count()}
+
+
+def single_core_tflops(spec, run, total_rows, seconds=3.0, seed=2):
+    """The oracle on one thread over a small random row sample, sized for
+    about `seconds`; returns (TFLOP/s, rows)."""
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(total_rows, size=1, replace=False))
+    t0 = time.perf_counter()
+    run(rows, nthreads=1)
+    per_row = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(total_rows, max(1, seconds / per_row)))
+    rows = np.sort(rng.choice(total_rows, size=n, replace=False))
+    t0 = time.perf_counter()
+    run(rows, nthreads=1)
+    dt = time.perf_counter() - t0
+    return 2.0 * n * spec.N * spec.K / dt / 1e12, n
 
 
 def oracle_sample(spec, inputs, rows_target_s=12.0):
@@ -237,7 +401,8 @@ def oracle_sample(spec, inputs, rows_target_s=12.0):
     result = run(rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * len(rows) * spec.N * spec.K
-    return flops / dt / 1e12, len(rows), dt, threads, rows, result
+    one, one_rows = single_core_tflops(spec, run, total_rows)
+    return flops / dt / 1e12, len(rows), dt, threads, rows, result, one, one_rows
 
 
 def parity_on_rows(spec, inputs, D, rows, ref_bits):
@@ -278,26 +443,27 @@ def run_reference(args):
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
-    from dense_gemm_epilogue_sm_gb300 import workloads as wl
     from oracle import gemm_ref
     import numpy as np
 
+    wl = workloads_module()
     spec = wl.get(args.workload)
     inputs = wl.make_inputs(spec)
+    config = workload_config(spec, needs_flush(spec))
     threads = gemm_ref.max_threads()
     rng = np.random.default_rng(1)
     grouped = getattr(spec, "groups", 0) > 0
-    wname = spec.name
     spec, inputs, total_rows, run = oracle_view(spec, inputs)
-    # size each step so the whole --steps/--warmup run stays within about two
-    # minutes; a step is at least one full row, and consecutive steps share an
-    # oracle call (about one row per host core) so the cores work in parallel
+    # size each step so the whole --steps/--warmup run stays within about
+    # args.ref_seconds; a step is at least one full row, and consecutive steps
+    # share an oracle call (about one row per host core) so the cores work in
+    # parallel
     probe = np.sort(rng.choice(total_rows, size=min(total_rows, threads), replace=False))
     run(probe[:1])                                           # decodes B once (kept by the oracle)
     t0 = time.perf_counter()
     run(probe)
     per_row = (time.perf_counter() - t0) / len(probe)
-    budget = 100.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     nrows = int(min(total_rows, max(1, budget / max(per_row, 1e-9))))
     per_call = max(1, threads // nrows)                      # steps per oracle call
 
@@ -312,14 +478,16 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     flops = 2.0 * nrows * spec.N * spec.K * args.steps
     value = flops / dt / 1e12
+    one, one_rows = single_core_tflops(spec, run, total_rows)
     sample = f"{nrows} random full rows of the {spec.M}x{spec.N}x{spec.K} workload per step" + \
         (" (rows of group 0)" if grouped else "") + f", {per_call} steps per oracle call"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wname, "M": spec.M, "N": spec.N, "K": spec.K},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "data": "synthetic (seeded torch CPU generator; N(0,1) operands, bias N(0,0.1))", "config": config,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
+                         "single_core": {"value": one, "rows": one_rows}, "host": host_cpu()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -419,8 +587,9 @@ def run_ours(args):
     import torch.distributed as dist
 
     import dense_gemm_epilogue_sm_gb300 as g
-    from dense_gemm_epilogue_sm_gb300 import workloads as wl
     from dense_gemm_epilogue_sm_gb300.torch_ops import GemmOp, desc_from_spec
+
+    wl = workloads_module()
 
     world, rank, local = dist_setup()
     if world > 1:
@@ -435,9 +604,11 @@ def run_ours(args):
     cpu = None
     cpu_rows = cpu_ref = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tflops, nrows, secs, threads, cpu_rows, cpu_ref = oracle_sample(spec, inputs, rows_target_s=args.cpu_seconds)
+        tflops, nrows, secs, threads, cpu_rows, cpu_ref, one, one_rows = oracle_sample(
+            spec, inputs, rows_target_s=args.cpu_seconds)
         cpu = {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{nrows} random full rows of {spec.M}x{spec.N}x{spec.K} ({secs:.1f} s, fp64 C loop)"}
+               "sample": f"{nrows} random full rows of {spec.M}x{spec.N}x{spec.K} ({secs:.1f} s, fp64 C loop)",
+               "single_core": {"value": one, "rows": one_rows}, "host": host_cpu()}
 
     A = inputs.A.to(dev)
     B = inputs.B.to(dev)
@@ -472,10 +643,9 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     flops = spec.flops()
     in_bytes = spec.algorithmic_bytes()
-    l2_bytes = 129e6
     flush = None
-    if in_bytes < 2 * l2_bytes:
-        flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+    if needs_flush(spec):
+        flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
 
     def barrier():
         if world > 1:
@@ -488,8 +658,12 @@ def run_ours(args):
 
     props = torch.cuda.get_device_properties(dev)
     uuid = str(getattr(props, "uuid", "") or "")
-    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local)))
+    uuid = uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else "")
+    sampler = ClockSampler(uuid or str(local))
     sampler.start()
+    nvml = NvmlSampler(uuid) if uuid else None
+    if nvml is not None:
+        nvml.start()
     time.sleep(0.3)
 
     launches0 = op.launches
@@ -520,7 +694,12 @@ def run_ours(args):
     step_ms = job_step_ms(total_ms, kernel_ms, args.steps, flush is not None, world, dev)
     time.sleep(0.2)
     sampler.stop()
-    clocks = sampler.summary(wall0, wall1)
+    clocks = None
+    if nvml is not None:
+        nvml.stop()
+        clocks = nvml.summary(wall0, wall1)
+    if clocks is None:
+        clocks = sampler.summary(wall0, wall1)
 
     # (the timed region includes the flush writes when a flush is needed;
     # the per-launch kernel time excludes them)
@@ -544,29 +723,43 @@ def run_ours(args):
     long_region = total_ms > 1000.0
     pkey = "bf16_tflops_sustained" if long_region else "bf16_tflops"
     peak = float(peaks.get(pkey, FALLBACK_PEAKS[pkey]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     # nominal dense ratios to bf16: fp8 4.5 : 2.25, fp4 13.5 : 2.25
     ratio = {"e4m3": 2.0, "e2m1": 6.0}.get(spec.dtype_in, 1.0)
     peak *= ratio
     achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
+    gbs = in_bytes / (avg_kernel_ms * 1e-3) / 1e9
     traffic = load_traffic(spec.name)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peak_src} {pkey}" + (f" x{ratio:g} ({spec.dtype_in} nominal ratio)" if ratio != 1.0
-                                                       else ""),
-                "algorithmic_bytes": in_bytes,
-                "hbm_frac": (in_bytes / (avg_kernel_ms * 1e-3)) / (float(peaks.get("hbm_gbs", 6800)) * 1e9)}
+    bound = roofline_bound(flops, in_bytes, peak, hbm)
+    sms = props.multi_processor_count
+    spec_peak = spec_peak_tflops(spec.dtype_in, sms)
+    at_clock = spec_peak_tflops(spec.dtype_in, sms, clocks["sm_mhz"]) if clocks.get("sm_mhz") else None
+    if bound == "hbm":
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes": in_bytes,
+                    "tflops": achieved, "tensor_frac": achieved / peak}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic,
+                    "peak_source": f"{peak_src} {pkey}" + (f" x{ratio:g} ({spec.dtype_in} nominal ratio)"
+                                                           if ratio != 1.0 else ""),
+                    "algorithmic_bytes": in_bytes, "hbm_frac": gbs / hbm}
+    # the tensor peak of the part itself: SMs x dense FLOP/clk/SM x 2070 MHz,
+    # and the same at the SM clock sampled during the timed region
+    roofline["spec_peak"] = spec_peak
+    roofline["spec_frac"] = achieved / spec_peak
+    roofline["spec_frac_at_clock"] = achieved / at_clock if at_clock else None
+    roofline["spec_source"] = (f"{sms} SMs x {SPEC_FLOP_PER_CLK_SM[spec.dtype_in]} FLOP/clk/SM "
+                               f"({spec.dtype_in} dense) x {SPEC_SM_MHZ:g} MHz")
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": spec.dtype_in if spec.dtype_in != "e4m3" else "e4m3",
+        "vs_baseline": None, "dtype": spec.dtype_in,
         "data": "synthetic (seeded torch CPU generator; N(0,1) operands, bias N(0,0.1))",
-        "config": {"workload": spec.name, "M": spec.M, "N": spec.N, "K": spec.K, "batch": spec.batch,
-                   **({"groups": groups} if groups else {}),
-                   "alpha": spec.alpha, "beta": spec.beta, "act": spec.act, "bias": spec.bias,
-                   "out": spec.dtype_d, "l2": "inputs larger than L2" if flush is None else "L2 flushed between steps",
-                   "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "stages": info.stages,
-                   "cta_group": info.cta_group, "tiles": info.tiles, "kernel_hash": kernel_hash()},
+        "config": workload_config(spec, flush is not None),
+        "plan": {"tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "stages": info.stages,
+                 "cta_group": info.cta_group, "tiles": info.tiles, "kernel_hash": kernel_hash()},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "parity": parity,
@@ -597,6 +790,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-plain", action="store_true", help="skip the plain-GEMM line beside the fused headline")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--ref-seconds", type=float, default=100.0,
+                    help="reference arm: about how long the whole --steps/--warmup run takes")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

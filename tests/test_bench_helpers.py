@@ -1,11 +1,16 @@
 """Host-side helpers of bench.py (no GPU): the kernel-source hash ignores
 comments only, the parity check of the timed output accepts the oracle's own
 rows and rejects wrong ones in either D order, and the oracle view of
-grouped and block-scaled-output workloads samples the right problem."""
+grouped and block-scaled-output workloads samples the right problem; the
+reference arm runs without the CUDA library, reports the same config as
+the GPU arm, and the roofline bound and the part's tensor peak follow
+their definitions."""
 import os
+import subprocess
 import sys
 
 import numpy as np
+import pytest
 import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -65,3 +70,32 @@ def test_oracle_view_samples_group_zero_and_quantises_block_scaled_d():
     assert total == 64 and f32_spec.dtype_d == "f32"
     codes, q = run(np.array([1, 2]))
     assert codes.shape == (2, 4) and q.shape == (2, 64)
+
+
+def test_reference_arm_loads_no_cuda_library():
+    # the workload generator is loaded by path; the package (whose __init__
+    # loads libgemm_sm103.so) stays out of the reference arm's process
+    code = ("import sys; sys.path.insert(0, %r); import bench; wl = bench.workloads_module(); "
+            "wl.make_inputs(wl.get('tiny_exact_fp16_256')); "
+            "assert 'dense_gemm_epilogue_sm_gb300' not in sys.modules, sorted(sys.modules)" % ROOT)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+
+
+def test_roofline_bound_and_spec_peak():
+    wl = bench.workloads_module()
+    skinny, fused = wl.get("skinny_65536x256x4096"), wl.get("fused_bf16_8192")
+    for spec, want in ((skinny, "hbm"), (fused, "tensor")):
+        assert bench.roofline_bound(spec.flops(), spec.algorithmic_bytes(), 1861.9, 6777.6) == want
+    assert bench.spec_peak_tflops("bf16", 152) == pytest.approx(152 * 8192 * 2.07e9 / 1e12)
+    assert bench.spec_peak_tflops("e4m3", 152) == pytest.approx(2 * bench.spec_peak_tflops("bf16", 152))
+
+
+def test_config_is_the_same_in_both_arms():
+    # both arms build the config from the workload alone (no plan fields)
+    wl = bench.workloads_module()
+    for name in ("fused_bf16_8192", "batched_32x512", "grouped_16x_bf16"):
+        spec = wl.get(name)
+        cfg = bench.workload_config(spec, bench.needs_flush(spec))
+        assert cfg == bench.workload_config(wl.get(name), bench.needs_flush(wl.get(name)))
+        assert not {"tile", "stages", "kernel_hash"} & set(cfg)
