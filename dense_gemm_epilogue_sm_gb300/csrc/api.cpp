@@ -905,7 +905,9 @@ const char* gemm_status_str(gemm_status_t s) {
 namespace gemm_sm103 {
 
 gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void* B, const void* C, void* D,
-                              const float* bias, uint32_t* status, int sm_count, cudaStream_t stream) {
+                              const float* bias, uint32_t* status, int sm_count, cudaStream_t stream,
+                              VariantCache* cache, bool* launched) {
+    *launched = false;
     Plan P;
     const gemm_status_t s = validate_and_plan(desc, &P);
     if (s != GEMM_OK) return s;
@@ -941,9 +943,18 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
     la.tmSA = la.tmA;          // block scaling is refused above
     la.tmSB = la.tmA;
     if (!ok) return GEMM_ERR_CUDA;
-    if (prepare_kernel(P.cta_group, P.tile_n, P.out_bytes, P.kp.block_scaled) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
+    const int slot = VariantCache::slot(P.cta_group, P.tile_n, P.out_bytes);
+    if (!cache->prepared[slot].load(std::memory_order_acquire)) {
+        if (prepare_kernel(P.cta_group, P.tile_n, P.out_bytes, P.kp.block_scaled) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        cache->prepared[slot].store(1, std::memory_order_release);
+    }
+    int clusters = cache->clusters_plus1[slot].load(std::memory_order_acquire) - 1;
+    if (clusters < 0) {
+        clusters = max_active_clusters(P.cta_group, P.tile_n, P.out_bytes, P.kp.block_scaled);
+        cache->clusters_plus1[slot].store(clusters + 1, std::memory_order_release);
     }
     la.p = P.kp;
     la.p.bias = bias;
@@ -953,13 +964,15 @@ gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void
     la.tile_n = P.tile_n;
     la.out_bytes = P.out_bytes;
     la.block_scaled = P.kp.block_scaled;
-    la.grid = grid_for(P, sm_count, max_active_clusters(P.cta_group, P.tile_n, P.out_bytes, P.kp.block_scaled));
+    la.grid = grid_for(P, sm_count, clusters);
     la.stream = stream;
     if (la.grid < 1) return GEMM_OK;
-    if (launch(la) != cudaSuccess) {
+    // every check has passed: clear the status word the previous call left
+    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess || launch(la) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
+    *launched = true;
     return GEMM_OK;
 }
 

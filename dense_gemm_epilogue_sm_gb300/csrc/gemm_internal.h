@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "layout.hpp"
 
 namespace gemm_sm103 {
@@ -147,5 +149,18 @@ size_t smem_bytes_for(int cta_group, int tile_n, int out_bytes, int block_scaled
 cudaError_t prepare_kernel(int cta_group, int tile_n, int out_bytes, int block_scaled);
 int max_active_clusters(int cta_group, int tile_n, int out_bytes, int block_scaled);   // 0 if unknown
 cudaError_t launch(const LaunchArgs& a);
+
+// Launch set-up of the kernel variants (dynamic shared-memory attribute set,
+// clusters that fit at once), kept per device by callers without a handle.
+// One slot per variant without block scaling: CTA group x tile width x
+// output bytes.
+struct VariantCache {
+    static constexpr int kSlots = 12;
+    std::atomic<int> prepared[kSlots] = {};        // 1 once the attribute is set
+    std::atomic<int> clusters_plus1[kSlots] = {};  // 0: not asked yet
+    static int slot(int cta_group, int tile_n, int out_bytes) {
+        return ((cta_group - 1) * 2 + (tile_n == 256)) * 3 + (out_bytes == 1 ? 0 : out_bytes == 2 ? 1 : 2);
+    }
+};
 
 }  // namespace gemm_sm103

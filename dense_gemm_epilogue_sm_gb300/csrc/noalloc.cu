@@ -8,14 +8,20 @@
 // its 4-byte status word, lives in a fixed file-scope device array instead of
 // a buffer allocated by gemm_create, and all host-side state lives on the
 // stack.  The caller still passes A, B, C, D and bias.
+#include <atomic>
 #include <mutex>
 
 #include "../../include/gemm.h"
 #include "gemm_internal.h"
 
 namespace gemm_sm103 {
+// One-shot plan and launch with every host object on the stack (api.cpp), the
+// kernel's status word at `status` (cleared on `stream` right before the
+// launch, once every check has passed); `*launched` tells whether a kernel
+// was queued (empty problems queue none).
 gemm_status_t run_unallocated(const gemm_desc_t* desc, const void* A, const void* B, const void* C, void* D,
-                              const float* bias, uint32_t* status, int sm_count, cudaStream_t stream);
+                              const float* bias, uint32_t* status, int sm_count, cudaStream_t stream,
+                              VariantCache* cache, bool* launched);
 }
 
 namespace {
@@ -28,25 +34,41 @@ constexpr int kWordsPerCall = 1;          // the kernel's status word
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kScratchWords];
 
 // In host code `g_noalloc_scratch` names a host-side stand-in, not device
-// memory: its device address is looked up once per device (with that device
-// current) and cached here.
+// memory: its device address is looked up per device (with that device
+// current) and cached here, with the device's SM count and the kernel
+// variants' launch set-up.  A set-up that fails is tried again on the next
+// call; one that succeeds is kept until the process exits.
 constexpr int kMaxDevices = 64;
 struct DeviceState {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
+    std::mutex mu;
+    std::atomic<bool> ready{false};
     uint32_t* scratch = nullptr;
     int sm_count = 0;
+    gemm_sm103::VariantCache variants;
 };
 DeviceState g_devices[kMaxDevices];
 
-void set_up(DeviceState* st) {
+gemm_status_t set_up(DeviceState* st, int dev) {
+    if (st->ready.load(std::memory_order_acquire)) return GEMM_OK;
+    std::lock_guard<std::mutex> lock(st->mu);
+    if (st->ready.load(std::memory_order_relaxed)) return GEMM_OK;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;
     void* ptr = nullptr;
-    int dev = 0;
-    st->err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (st->err == cudaSuccess) st->err = cudaGetDevice(&dev);
-    if (st->err == cudaSuccess) st->err = cudaDeviceGetAttribute(&st->sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (st->err != cudaSuccess) cudaGetLastError();
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
     st->scratch = static_cast<uint32_t*>(ptr);
+    st->sm_count = sms;
+    st->ready.store(true, std::memory_order_release);
+    return GEMM_OK;
 }
 
 }  // namespace
@@ -63,25 +85,15 @@ extern "C" gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A
         return GEMM_ERR_NO_DEVICE;
     }
     if (dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_NO_DEVICE;
-    }
-    if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;
     DeviceState* st = &g_devices[dev];
-    std::call_once(st->once, set_up, st);       // first call on this device: look up the array's address
-    if (st->err != cudaSuccess || !st->scratch) return GEMM_ERR_CUDA;
+    const gemm_status_t su = set_up(st, dev);     // first call on this device: look up the array's address
+    if (su != GEMM_OK) return su;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: clear the status word.
-    if (cudaMemsetAsync(st->scratch, 0, kWordsPerCall * sizeof(uint32_t), s) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-    }
-    const gemm_status_t r = gemm_sm103::run_unallocated(desc, A, B, C, D, bias, st->scratch, st->sm_count, s);
-    if (r != GEMM_OK || !wait) return r;
+    bool launched = false;
+    const gemm_status_t r = gemm_sm103::run_unallocated(desc, A, B, C, D, bias, st->scratch, st->sm_count, s,
+                                                        &st->variants, &launched);
+    if (r != GEMM_OK || !wait || !launched) return r;
     uint32_t word = 0;
     if (cudaStreamSynchronize(s) != cudaSuccess ||
         cudaMemcpy(&word, st->scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {

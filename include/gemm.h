@@ -303,15 +303,20 @@ GEMM_API uint64_t gemm_launch_count(gemm_handle_t h);
  * other allocating routine is called.
  *
  * The first call on a device looks up that array's device address
- * (cudaGetSymbolAddress, once per device, with the device current); make
- * that first call before any stream capture.  Each call clears the status
- * word on `stream` before launching.  All calls on a device share the array,
- * so calls whose kernels overlap on the GPU race on the status word: issue
- * them on one stream, or wait between them.
+ * (cudaGetSymbolAddress, with the device current) and sets the kernel up;
+ * make that first call before any stream capture.  A set-up that fails
+ * returns its error and is tried again on the next call.  Each call that
+ * passes its checks clears the status word on `stream` right before its
+ * launch (a rejected call queues nothing).  All calls on a device share the
+ * array, so calls whose kernels overlap on the GPU race on the status word:
+ * issue them on one stream, or wait between them.
  *
  * wait = 0: asynchronous; argument and launch errors are returned, an
  * in-kernel timeout is not reported.  wait = 1: the call synchronises
- * `stream` and returns GEMM_ERR_TIMEOUT if a bounded wait ran out.
+ * `stream` and returns GEMM_ERR_TIMEOUT if a bounded wait ran out; it
+ * cannot be used while `stream` is being captured into a graph (the
+ * synchronisation and the read-back would end the capture): only wait = 0
+ * may be used there.
  * Pointers, alignment and errors are as for gemm_run; a descriptor with
  * reductions (which need a handle's workspace) or block scaling (no
  * scale-factor arguments here) returns GEMM_ERR_UNSUPPORTED. */

@@ -5,7 +5,8 @@ framework memory pool that owns the device, latency-critical paths where an
 allocation may synchronise the device).  It keeps the kernel's status word
 in a fixed device array instead of an allocated one.  Two calls in a row,
 through the C ABI, must reproduce what gemm_run computes on the same inputs,
-within the parity tolerance used by the other GPU tests.  This file is
+within the parity tolerance used by the other GPU tests, and so must a call
+that returns at once (wait = 0) once the caller synchronises.  This file is
 collected last so a failure here cannot hide the others.
 """
 import ctypes
@@ -53,10 +54,11 @@ def test_two_calls_match_gemm_run():
         op.check()
         op.close()
 
-        for call in range(2):
+        # two calls that wait, then one that returns at once (the caller synchronises)
+        for call, wait in enumerate((1, 1, 0)):
             out = H.canary_buffer(spec)
             status = g.lib.gemm_run_noalloc(ctypes.byref(desc), _ptr(A), _ptr(B), _ptr(C), _ptr(out), _ptr(bias),
-                                            stream, 1)
+                                            stream, wait)
             assert status == g.OK, g.gemm_status_str(status)
             torch.cuda.synchronize()
             got_bits = H.bits_of_tensor(out.cpu())
@@ -78,3 +80,21 @@ def test_rejects_bad_arguments_without_launching():
     bad.M = -1
     assert g.lib.gemm_run_noalloc(ctypes.byref(bad), None, None, None, None, None, None, 1) == g.ERR_INVALID_ARG
     assert g.lib.gemm_run_noalloc(ctypes.byref(desc), None, None, None, None, None, None, 2) == g.ERR_INVALID_ARG
+
+
+def test_empty_problem_after_a_launch_reports_ok():
+    # an empty problem queues no kernel: waiting must not read the status
+    # word the previous call left
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    stream = torch.cuda.current_stream().cuda_stream
+    spec = SPECS[0]
+    inputs, (A, B, C, bias) = _device_inputs(spec)
+    desc = desc_from_spec(spec, inputs.scale_a, inputs.scale_b)
+    out = H.canary_buffer(spec)
+    assert g.lib.gemm_run_noalloc(ctypes.byref(desc), _ptr(A), _ptr(B), _ptr(C), _ptr(out), _ptr(bias),
+                                  stream, 1) == g.OK
+    empty = desc_from_spec(spec, inputs.scale_a, inputs.scale_b)
+    empty.M = 0
+    assert g.lib.gemm_run_noalloc(ctypes.byref(empty), _ptr(A), _ptr(B), _ptr(C), _ptr(out), _ptr(bias),
+                                  stream, 1) == g.OK
