@@ -24,10 +24,13 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIBRARY_PATH = os.path.join(_HERE, "libgemm_sm103.so")
+# The diagnostic builds (GEMM_DEBUG index checks, GEMM_STAMPS timestamps; see
+# _build.py) are separate libraries, chosen by naming one in
+# GEMM_SM103_LIBRARY; the default is the normal build next to this file.
+LIBRARY_PATH = os.environ.get("GEMM_SM103_LIBRARY") or os.path.join(_HERE, "libgemm_sm103.so")
 
 # gemm_status_t
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_DEVICE = range(7)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_DEVICE, ERR_BOUNDS = range(8)
 # gemm_dtype_t
 F32, F16, BF16, E4M3, E2M1 = 0, 1, 2, 3, 4
 # gemm_order_t
@@ -112,6 +115,8 @@ def _load():
         "gemm_check": (i32, [vp]),
         "gemm_destroy": (i32, [vp]),
         "gemm_set_debug": (i32, [vp, i32, u32]),
+        "gemm_set_stamps": (i32, [vp, vp]),
+        "gemm_build_flags": (i32, []),
         "gemm_launch_count": (ctypes.c_uint64, [vp]),
         "gemm_set_schedule": (i32, [vp, i32]),
         "gemm_get_schedule": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i64),
@@ -134,7 +139,7 @@ def _load():
 lib = _load()
 EXPORTED = ("gemm_plan", "gemm_create", "gemm_run", "gemm_run_ex", "gemm_run_args", "gemm_grouped_create",
             "gemm_grouped_run", "gemm_grouped_run_args", "gemm_check", "gemm_destroy", "gemm_set_debug",
-            "gemm_set_schedule", "gemm_get_schedule", "gemm_launch_count", "gemm_status_str", "gemm_run_noalloc",
+            "gemm_set_stamps", "gemm_build_flags", "gemm_set_schedule", "gemm_get_schedule", "gemm_launch_count", "gemm_status_str", "gemm_run_noalloc",
             "gemm_layout_query", "gemm_layout_eval", "gemm_layout_op", "gemm_layout_gather_f32")
 
 
@@ -258,6 +263,21 @@ def gemm_set_debug(handle, inject_fault, timeout_ms):
     s = lib.gemm_set_debug(handle, inject_fault, timeout_ms)
     if s != OK:
         raise GemmError(s, "gemm_set_debug")
+
+
+def gemm_set_stamps(handle, stamps_ptr):
+    """Diagnostic timestamps (GEMM_STAMPS builds): a device buffer of 8 uint64 per CTA."""
+    s = lib.gemm_set_stamps(handle, stamps_ptr)
+    if s != OK:
+        raise GemmError(s, "gemm_set_stamps")
+
+
+BUILD_DEBUG, BUILD_STAMPS = 1, 2
+
+
+def gemm_build_flags():
+    """Bit 0: index-checked (GEMM_DEBUG) build; bit 1: timestamp (GEMM_STAMPS) build."""
+    return int(lib.gemm_build_flags())
 
 
 def gemm_set_schedule(handle, mode):

@@ -14,6 +14,14 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgemm_sm103.so")
+# Diagnostic builds, each a library of its own (select one at run time with
+# GEMM_SM103_LIBRARY): "debug" checks every store index in the kernel
+# (GEMM_DEBUG), "stamps" records %globaltimer at fixed points (GEMM_STAMPS).
+VARIANTS = {"": [], "debug": ["-DGEMM_DEBUG"], "stamps": ["-DGEMM_STAMPS"]}
+
+
+def library_path(variant=""):
+    return LIB if not variant else os.path.join(HERE, f"libgemm_sm103_{variant}.so")
 SOURCES = ["gemm_ob2.cu", "gemm_ob4.cu", "gemm_ob1.cu", "gemm_sm103.cu", "api.cpp", "layout_api.cu", "noalloc.cu",
            "reduce_finish.cu"]
 HEADERS = ["gemm_internal.h", "gemm_kernel.cuh", "gemm_variants.h", "layout.hpp", "ptx.cuh"]
@@ -35,25 +43,27 @@ def _inputs():
     return files
 
 
-def _stale():
-    if not os.path.exists(LIB):
+def _stale(lib):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
+    lib = library_path(variant)
+    if not force and not _stale(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD if not variant else f"{BUILD}_{variant}"
+    os.makedirs(build_dir, exist_ok=True)
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-                     "-I", os.path.join(os.path.dirname(HERE), "include")]
+                     "-I", os.path.join(os.path.dirname(HERE), "include")] + VARIANTS[variant]
     if verbose:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -65,15 +75,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         for _, log in results:
             print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    variant = next((a.split("=", 1)[1] for a in sys.argv[1:] if a.startswith("--variant=")), "")
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, variant=variant))

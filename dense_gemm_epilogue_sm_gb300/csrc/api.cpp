@@ -836,9 +836,32 @@ gemm_status_t gemm_check(gemm_handle_t h) {
     if (word) {
         cudaMemset(h->status, 0, sizeof(uint32_t));
         if (h->ws || h->red_ws) h->ws_dirty = true;
-        return GEMM_ERR_TIMEOUT;
+        return (word & kStatusTimeout) ? GEMM_ERR_TIMEOUT : GEMM_ERR_BOUNDS;
     }
     return GEMM_OK;
+}
+
+gemm_status_t gemm_set_stamps(gemm_handle_t h, void* stamps) {
+#ifdef GEMM_STAMPS
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    h->plan.kp.stamps = static_cast<unsigned long long*>(stamps);
+    return GEMM_OK;
+#else
+    (void)h;
+    (void)stamps;
+    return GEMM_ERR_UNSUPPORTED;
+#endif
+}
+
+int32_t gemm_build_flags(void) {
+    int32_t f = 0;
+#ifdef GEMM_DEBUG
+    f |= 1;
+#endif
+#ifdef GEMM_STAMPS
+    f |= 2;
+#endif
+    return f;
 }
 
 gemm_status_t gemm_set_schedule(gemm_handle_t h, int32_t mode) {
@@ -891,6 +914,7 @@ const char* gemm_status_str(gemm_status_t s) {
         case GEMM_ERR_CUDA: return "CUDA error";
         case GEMM_ERR_TIMEOUT: return "an in-kernel wait ran out of time";
         case GEMM_ERR_NO_DEVICE: return "no sm_103 GPU available";
+        case GEMM_ERR_BOUNDS: return "an index check of the diagnostic build failed";
         default: return "unknown status";
     }
 }

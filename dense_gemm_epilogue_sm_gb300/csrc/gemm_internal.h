@@ -32,6 +32,9 @@ constexpr uint32_t kStatusRoleMma = 1u << 9;
 constexpr uint32_t kStatusRoleEpi = 1u << 10;
 constexpr uint32_t kStatusRoleDrain = 1u << 11;
 constexpr uint32_t kStatusRoleFixup = 1u << 12;   // a stream-K owner waiting for a partial sum
+// Diagnostic build with index checks (GEMM_DEBUG): a plain store whose index
+// falls outside its buffer is skipped and this bit is recorded.
+constexpr uint32_t kStatusBounds = 2u;
 
 struct KernelParams {
     int32_t M, N, K, L;           // kernel orientation: D is M x N row-major
@@ -117,6 +120,9 @@ struct KernelParams {
     // M-block fastest; each CTA counts the tiles itself (data parallel only).
     int32_t groups;
     const int64_t* group_rows;    // device, groups + 1 entries
+    // Diagnostic build with timestamps (GEMM_STAMPS): 8 %globaltimer values
+    // per CTA (see gemm_kernel.cuh); null otherwise.
+    unsigned long long* stamps;
 };
 
 struct LaunchArgs {

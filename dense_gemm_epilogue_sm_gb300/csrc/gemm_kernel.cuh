@@ -50,6 +50,46 @@
 namespace gemm_sm103 {
 
 
+// Diagnostic timestamps (built with -DGEMM_STAMPS, with a buffer set on the
+// handle): %globaltimer at eight points of each CTA, slot i of CTA b at
+// stamps[8 b + i]:
+//   0 entry, 1 set-up done (barriers, TMEM, tensor maps), 2 first loads
+//   issued, 3 first stage's data in (the MMA thread), 4 first accumulator
+//   committed, 5 the epilogue sees it, 6 the epilogue's last store complete,
+//   7 before TMEM is freed.  Compiled out otherwise.
+//   (6: the last stores have read their staging buffers.)
+#ifdef GEMM_STAMPS
+// The timer is read through a volatile shared-memory round trip, so that the
+// read cannot move across the barriers and waits around the stamp point.
+__device__ __forceinline__ void gemm_stamp(const KernelParams& p, int i) {
+    __shared__ volatile unsigned long long order;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+    order = t;
+    if (p.stamps) p.stamps[(size_t)blockIdx.x * 8 + i] = order;
+}
+#define GEMM_STAMP(p, i) gemm_stamp((p), (i))
+#else
+#define GEMM_STAMP(p, i) \
+    do {                 \
+    } while (0)
+#endif
+
+// Diagnostic index checks (built with -DGEMM_DEBUG): every plain global store
+// and every TMA store is first checked against the extents of its buffer; a
+// failed check records kStatusBounds in the status word (gemm_check then
+// returns GEMM_ERR_BOUNDS) and the access is skipped.  Compiled out (always
+// true) otherwise.
+#ifdef GEMM_DEBUG
+__device__ __forceinline__ bool debug_in_bounds(const KernelParams& p, bool ok) {
+    if (!ok) atomicOr(p.status, kStatusBounds);
+    return ok;
+}
+#define GEMM_IN_BOUNDS(p, cond) debug_in_bounds((p), (cond))
+#else
+#define GEMM_IN_BOUNDS(p, cond) true
+#endif
+
 // TMEM accumulators per CTA: two, so the epilogue of one tile overlaps the
 // main loop of the next (512 columns for BN = 256).
 constexpr int kPairAccBufs = 2;
@@ -732,6 +772,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
                 stop = true;
                 break;
             }
+            if (!issued) GEMM_STAMP(p, 3);
             const int next = stage + 1 == S ? 0 : stage + 1;
             const uint32_t next_phase = stage + 1 == S ? phase ^ 1u : phase;
             const uint64_t soff = (uint64_t)((stage * stage_bytes) >> 4);
@@ -791,6 +832,7 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
                 ptx::mma_commit_mc(accf_bar(buf), 0x3);
             else
                 ptx::mma_commit(accf_bar(buf));
+            if (it == 0) GEMM_STAMP(p, 4);
         } else {                                  // K == 0: nothing accumulated
             ptx::mbar_arrive(accf_bar(buf));
             if constexpr (CG == 2) ptx::mbar_arrive_cluster(accf_bar(buf), 1);
@@ -846,6 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t peer_abort = CG == 2 ? ptx::mapa(ptx::smem_addr(tmem_slot + 1), rank ^ 1u) : 0u;
 
     if (threadIdx.x == 0) {
+        GEMM_STAMP(p, 0);
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
@@ -892,6 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int dp_tiles = p.groups > 0 ? (int)tmem_slot[2] : p.dp_tiles;
+    if (threadIdx.x == 0) GEMM_STAMP(p, 1);
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA loads --
@@ -978,6 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         const uint32_t bit = 1u << pend_slot(stage);
+                        if (!pend) GEMM_STAMP(p, 2);
                         pend |= bit;
                         pend_parity = phase ? (pend_parity | bit) : (pend_parity & ~bit);
                     }
@@ -1112,6 +1157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int dl = tp.cd_l;            // batch index of D
                 ok = __all_sync(0xffffffffu, wait_bar(accf_bar(buf), acc_par, p, abort_flag, kStatusRoleEpi, peer_abort));
                 if (!ok) break;
+                if (it == 0 && ew == 0 && lane == 0) GEMM_STAMP(p, 5);
                 ptx::tc_fence_after();
                 if (kb0 > 0) {
                     // Stream-K: this tile's first K blocks belong to another worker,
@@ -1232,7 +1278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     code = nv_factor_code(__uint_as_float(amax), p.scale_d, inv6g);
                                     if (code != 0u) out = nv_element_codes_fast(v, e4m3_value(code), p.scale_d);
                                 }
-                                if (row < m_end) {
+                                if (row < m_end && GEMM_IN_BOUNDS(p, row >= 0 && row < p.M && c0 >= 0 && c0 < p.N &&
+                                                                         dl >= 0 && dl < p.L)) {
                                     uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)dl * p.d_bstride +
                                                     (int64_t)row * p.ldd;          // bytes: two elements each
                                     if (c0 + 16 <= p.N) {
@@ -1280,7 +1327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 w[k] = code == 255u ? 0x7F7F7F7Fu
                                                     : ptx::pack4_e4m3(v[4 * k] * sc, v[4 * k + 1] * sc, v[4 * k + 2] * sc,
                                                                       v[4 * k + 3] * sc);
-                            if (row < m_end) {
+                            if (row < m_end && GEMM_IN_BOUNDS(p, row >= 0 && row < p.M && c0 >= 0 && c0 < p.N &&
+                                                                     dl >= 0 && dl < p.L)) {
                                 uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)dl * p.d_bstride +
                                                 (int64_t)row * p.ldd;
                                 if (c0 + 32 <= p.N) {
@@ -1395,7 +1443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (p.red_cols) {
                                     int j;
                                     const float cs = chunk_col_sum<VPC>(r, lane, j);
-                                    if ((lane & (32 / VPC - 1)) == 0 && c0 + j < p.N)
+                                    if ((lane & (32 / VPC - 1)) == 0 && c0 + j < p.N &&
+                                        GEMM_IN_BOUNDS(p, l >= 0 && l < p.L && row0 >= 0 && row0 < p.M && c0 + j >= 0))
                                         p.red_col_ws[((int64_t)l * ((p.M + 31) / 32) + row0 / 32) * p.N + c0 + j] = cs;
                                 }
                             }
@@ -1409,7 +1458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             if (!direct) {
                                 *slot = out;
-                            } else if (row < m_end) {
+                            } else if (row < m_end && GEMM_IN_BOUNDS(p, row >= 0 && row < p.M && col0 >= 0 &&
+                                                                          col0 < p.N && dl >= 0 && dl < p.L)) {
                                 const int c0 = col0 + ch * VPC;
                                 const uint32_t w[4] = {out.x, out.y, out.z, out.w};
                                 uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
@@ -1428,7 +1478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!direct) {
                             ptx::fence_async_shared();
                             __syncwarp();
-                            if (lane == 0) {
+                            if (lane == 0 && GEMM_IN_BOUNDS(p, col0 >= 0 && col0 < p.N && row0 >= 0 && row0 < p.M &&
+                                                                   dl >= 0 && dl < p.L)) {
                                 ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, dl);
                                 ptx::bulk_commit();
                             }
@@ -1437,7 +1488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 if (!released) release_acc(buf);
-                if (EXT && p.red_rows && row < m_end) p.red_row_ws[((int64_t)l * p.tiles_n + nb) * p.M + row] = row_acc;
+                if (EXT && p.red_rows && row < m_end &&
+                    GEMM_IN_BOUNDS(p, l >= 0 && l < p.L && nb >= 0 && nb < p.tiles_n && row >= 0 && row < p.M))
+                    p.red_row_ws[((int64_t)l * p.tiles_n + nb) * p.M + row] = row_acc;
                 if (EXT && p.red_amax) {
     #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1)
@@ -1456,12 +1509,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             epilogue(BoolTag<true>{});
         else
             epilogue(BoolTag<false>{});
-        if (lane == 0) ptx::bulk_wait<0>();
+        // the last stores have read their staging buffers (their global writes
+        // complete before the grid does)
+        if (lane == 0) ptx::bulk_wait_read<0>();
+        if (ew == 0 && lane == 0) GEMM_STAMP(p, 6);
         ptx::tc_fence_before();
     }
 
     __syncthreads();
     if constexpr (CG == 2) ptx::cluster_sync();   // no CTA leaves while its peer may still touch its memory
+    if (threadIdx.x == 0) GEMM_STAMP(p, 7);
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc<CG>(tmem_base, C::kTmemCols);

@@ -73,7 +73,8 @@ typedef enum {
     GEMM_ERR_MISALIGNED = 3,
     GEMM_ERR_CUDA = 4,
     GEMM_ERR_TIMEOUT = 5,
-    GEMM_ERR_NO_DEVICE = 6
+    GEMM_ERR_NO_DEVICE = 6,
+    GEMM_ERR_BOUNDS = 7            /* diagnostic build (GEMM_DEBUG) only: an index check failed */
 } gemm_status_t;
 
 /* GEMM_E2M1: 4-bit float (sign, 2 exponent bits with bias 1, 1 mantissa bit;
@@ -236,6 +237,25 @@ GEMM_API gemm_status_t gemm_destroy(gemm_handle_t h);
  * runs out); 0 restores normal operation.  timeout_ms bounds every
  * in-kernel wait (0 keeps the current bound; default 2000 ms). */
 GEMM_API gemm_status_t gemm_set_debug(gemm_handle_t h, int32_t inject_fault, uint32_t timeout_ms);
+
+/* Diagnostic builds.  The library can be built with -DGEMM_DEBUG (every
+ * plain store and TMA store of the kernel checks its index against the
+ * buffer's extents first; a failed check skips the access and gemm_check
+ * returns GEMM_ERR_BOUNDS) and with -DGEMM_STAMPS (the kernel records
+ * %globaltimer at 8 points of each CTA; see gemm_set_stamps).  The default
+ * build has neither.  gemm_build_flags returns bit 0 for GEMM_DEBUG and
+ * bit 1 for GEMM_STAMPS. */
+GEMM_API int32_t gemm_build_flags(void);
+
+/* GEMM_STAMPS builds: `stamps` is a device buffer of 8 uint64 per CTA of the
+ * launch (workers x CTA group of gemm_get_schedule; the dynamic schedule
+ * launches one CTA or pair per tile), in which the next
+ * launches write %globaltimer (ns) at: 0 CTA entry, 1 set-up done, 2 first
+ * operand loads issued, 3 first stage's data arrived at the MMA thread (the
+ * pair's leader), 4 first accumulator committed, 5 the epilogue sees it,
+ * 6 the epilogue's last store complete, 7 before TMEM is freed.  NULL stops
+ * recording.  Other builds: GEMM_ERR_UNSUPPORTED. */
+GEMM_API gemm_status_t gemm_set_stamps(gemm_handle_t h, void* stamps);
 
 /* Work split of the persistent kernel.  The pages name split-K only as a
  * profiler option ("Technical Documentation: NVIDIA/cutlass", "Performance
