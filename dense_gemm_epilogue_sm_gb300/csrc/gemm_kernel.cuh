@@ -204,13 +204,34 @@ static __device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, con
     }
 }
 
+// A flattened raster layout evaluated at c in 32-bit arithmetic (tile counts
+// fit in int32), its modes unrolled so that every shape and stride is read
+// from the parameter bank at a fixed offset: a loop indexed at run time
+// turned each tile's lookup into a chain of dependent parameter loads and
+// 64-bit divisions, about a microsecond at a CTA's first tile.
+__device__ __forceinline__ int raster_eval(const gl::FlatLayout& f, int c) {
+    int idx = 0;
+#pragma unroll
+    for (int i = 0; i < gl::FlatLayout::kMaxModes; ++i) {
+        if (i + 1 >= f.rank) {
+            idx += c * (int)f.stride[i];
+            break;
+        }
+        const int s = (int)f.shape[i];
+        const int q = c / s;
+        idx += (c - q * s) * (int)f.stride[i];
+        c = q;
+    }
+    return idx;
+}
+
 __device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int& mb, int& nb, int& l) {
     l = tile / p.tiles_per_batch;
     const int t = tile - l * p.tiles_per_batch;
-    const int64_t idx = t < p.raster_full_count ? p.raster_full(t)
-                                                : p.raster_tail(t - p.raster_full_count) + p.raster_tail_offset;
-    mb = (int)(idx % p.tiles_m);
-    nb = (int)(idx / p.tiles_m);
+    const int idx = t < p.raster_full_count ? raster_eval(p.raster_full, t)
+                                            : raster_eval(p.raster_tail, t - p.raster_full_count) + p.raster_tail_offset;
+    mb = idx % p.tiles_m;
+    nb = idx / p.tiles_m;
 }
 
 // Where a tile sits: M and N block, batch (group) index, and the tile's row
@@ -1092,6 +1113,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ranges, so the plain epilogue carries none of their code.
         auto epilogue = [&](auto ext_tag) {
             constexpr bool EXT = decltype(ext_tag)::value;
+            // The scalars of the inner loops, held in registers: read through
+            // `p` they would be reloaded from the parameter space after every
+            // store to the staging buffer (a generic pointer the compiler
+            // cannot tell apart from `p`), several dependent loads per chunk.
+            const float e_alpha = p.alpha, e_beta = p.beta, e_scale_d = p.scale_d;
+            const int e_N = p.N, e_M = p.M, e_bias_mode = p.bias_mode, e_act = p.act, e_out_f8 = p.out_f8;
+            const int e_has_c = p.has_c, e_d_ragged = p.d_ragged, e_num_kb = p.num_kb;
+            const int64_t e_ldd = p.ldd, e_d_bstride = p.d_bstride;
             [[maybe_unused]] uint32_t c_phase[2] = {0u, 0u};
             [[maybe_unused]] int sub_count = 0;
             int it = 0;
@@ -1148,7 +1177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     tile_coords(p, tile, tp.mb, tp.nb, tp.l);
                     tp.m_base = 0;
-                    tp.m_end = p.M;
+                    tp.m_end = e_M;
                     tp.cd_l = tp.l;
                     tp.sf_base = 0;
                 }
@@ -1181,8 +1210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // A tile cut short (kb1 < num_kb, stream-K region only): its later
                 // K blocks come from the next workers' partial sums.
-                const bool cut = kb1 < p.num_kb;
-                const int64_t t_end = cut ? (int64_t)(tile - p.dp_tiles + 1) * p.num_kb : 0;
+                const bool cut = kb1 < e_num_kb;
+                const int64_t t_end = cut ? (int64_t)(tile - p.dp_tiles + 1) * e_num_kb : 0;
                 const int64_t r_next = workers - first_tile;        // this worker's range index + 1
                 if (cut) {
                     ok = for_each_part(r_next, t_end, [&](int w) {
@@ -1197,15 +1226,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row0 = tp.m_base + mb * kTileRows + (int)rank * kTileM + q * kEpiRows;
                 const int row = row0 + lane;
                 float row_bias = 0.f;
-                if (p.bias_mode == 2 && row < m_end) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
-                const float* bias_l = p.bias_mode == 1 ? p.bias + (int64_t)l * p.bias_stride : nullptr;
+                if (e_bias_mode == 2 && row < m_end) row_bias = p.bias[(int64_t)l * p.bias_stride + row];
+                const float* bias_l = e_bias_mode == 1 ? p.bias + (int64_t)l * p.bias_stride : nullptr;
                 [[maybe_unused]] const int lc = p.c_batched ? l : 0;
                 // With a single accumulator the MMA waits for the whole
                 // epilogue, so it is released right after its last subtile's
                 // TMEM load, before that subtile's math and stores.  With two
                 // the MMA works on the other one meanwhile and the release
                 // stays at the end of the tile.
-                const int n_end = nb * BN + BN < p.N ? nb * BN + BN : p.N;
+                const int n_end = nb * BN + BN < e_N ? nb * BN + BN : e_N;
                 const int last_sub = (row0 < m_end && n_end > nb * BN) ? (n_end - 1 - nb * BN) / C::kEpiCols : -1;
                 bool released = false;
                 auto early_release = [&](int sub) {
@@ -1219,12 +1248,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll 1
                 for (int sub = 0; sub < C::kSubtiles; ++sub) {
                     const int col0 = nb * BN + sub * C::kEpiCols;
-                    if (row0 >= m_end || col0 >= p.N) continue;     // nothing of this subtile is in range
+                    if (row0 >= m_end || col0 >= e_N) continue;     // nothing of this subtile is in range
                     if constexpr (OB == 1) {
                         // MX output: e4m3 elements and one ue8m0 factor per 32
                         // columns of a row (no C; checked on the host).
                         uint32_t acc[C::kEpiCols];
-                        if (p.num_kb > 0) {
+                        if (e_num_kb > 0) {
                             load_acc(buf, sub, acc);
                         } else {
 #pragma unroll
@@ -1245,29 +1274,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 return true;
                             });
                         }
-                        if (p.out_f8 == 2) {
+                        if (e_out_f8 == 2) {
                             // NVFP4 output: e2m1 elements and one ue4m3 factor per 16
                             // columns of a row under the global scale g = scale_d:
                             // factor = e4m3(amax / (6 g)), elements e2m1(t / (factor g)),
                             // both the nearest-even codes of the exact quotients
-                            const float inv6g = __frcp_rn(__fmul_rn(6.0f, p.scale_d));
+                            const float inv6g = __frcp_rn(__fmul_rn(6.0f, e_scale_d));
 #pragma unroll
                             for (int h = 0; h < C::kEpiCols / 16; ++h) {
                                 const int c0 = col0 + h * 16;
-                                if (c0 >= p.N) break;             // the block lies past the row's end
+                                if (c0 >= e_N) break;             // the block lies past the row's end
                                 float v[16];
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) {
-                                    float x = p.alpha * __uint_as_float(acc[h * 16 + i]);
-                                    if (p.bias_mode == 1)
-                                        x += (c0 + i < p.N) ? __ldg(bias_l + c0 + i) : 0.f;
-                                    else if (p.bias_mode == 2)
+                                    float x = e_alpha * __uint_as_float(acc[h * 16 + i]);
+                                    if (e_bias_mode == 1)
+                                        x += (c0 + i < e_N) ? __ldg(bias_l + c0 + i) : 0.f;
+                                    else if (e_bias_mode == 2)
                                         x += row_bias;
-                                    if (p.act == 1)
+                                    if (e_act == 1)
                                         x = fmaxf(x, 0.f);
-                                    else if (EXT && p.act == 2)
+                                    else if (EXT && e_act == 2)
                                         x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
-                                    v[i] = (c0 + i < p.N) ? x : 0.f;   // columns past N join no block
+                                    v[i] = (c0 + i < e_N) ? x : 0.f;   // columns past N join no block
                                 }
                                 uint32_t amax = 0u;
 #pragma unroll
@@ -1275,17 +1304,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 uint32_t code = 0x7Fu;            // NaN / inf in the block
                                 uint2 out = make_uint2(0u, 0u);
                                 if (amax < 0x7F800000u) {
-                                    code = nv_factor_code(__uint_as_float(amax), p.scale_d, inv6g);
-                                    if (code != 0u) out = nv_element_codes_fast(v, e4m3_value(code), p.scale_d);
+                                    code = nv_factor_code(__uint_as_float(amax), e_scale_d, inv6g);
+                                    if (code != 0u) out = nv_element_codes_fast(v, e4m3_value(code), e_scale_d);
                                 }
-                                if (row < m_end && GEMM_IN_BOUNDS(p, row >= 0 && row < p.M && c0 >= 0 && c0 < p.N &&
+                                if (row < m_end && GEMM_IN_BOUNDS(p, row >= 0 && row < e_M && c0 >= 0 && c0 < e_N &&
                                                                          dl >= 0 && dl < p.L)) {
-                                    uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)dl * p.d_bstride +
-                                                    (int64_t)row * p.ldd;          // bytes: two elements each
-                                    if (c0 + 16 <= p.N) {
+                                    uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)dl * e_d_bstride +
+                                                    (int64_t)row * e_ldd;          // bytes: two elements each
+                                    if (c0 + 16 <= e_N) {
                                         *reinterpret_cast<uint2*>(drow + c0 / 2) = out;
                                     } else {
-                                        for (int i = 0; i < 8 && c0 + 2 * i < p.N; ++i)
+                                        for (int i = 0; i < 8 && c0 + 2 * i < e_N; ++i)
                                             drow[c0 / 2 + i] = (uint8_t)((i < 4 ? out.x : out.y) >> ((i & 3) * 8));
                                     }
                                     const int f = c0 / 16;
@@ -1298,20 +1327,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int h = 0; h < C::kEpiCols / 32; ++h) {
                             const int c0 = col0 + h * 32;
-                            if (c0 >= p.N) break;                 // the block lies past the row's end
+                            if (c0 >= e_N) break;                 // the block lies past the row's end
                             float v[32];
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
-                                float x = p.alpha * __uint_as_float(acc[h * 32 + i]);
-                                if (p.bias_mode == 1)
-                                    x += (c0 + i < p.N) ? __ldg(bias_l + c0 + i) : 0.f;
-                                else if (p.bias_mode == 2)
+                                float x = e_alpha * __uint_as_float(acc[h * 32 + i]);
+                                if (e_bias_mode == 1)
+                                    x += (c0 + i < e_N) ? __ldg(bias_l + c0 + i) : 0.f;
+                                else if (e_bias_mode == 2)
                                     x += row_bias;
-                                if (p.act == 1)
+                                if (e_act == 1)
                                     x = fmaxf(x, 0.f);
-                                else if (EXT && p.act == 2)
+                                else if (EXT && e_act == 2)
                                     x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
-                                v[i] = (c0 + i < p.N) ? x : 0.f;   // columns past N join no block
+                                v[i] = (c0 + i < e_N) ? x : 0.f;   // columns past N join no block
                             }
                             // factor: the OCP MX shared exponent floor(log2 amax) - 8,
                             // read off amax's biased fp32 exponent; 255 for NaN / inf
@@ -1327,15 +1356,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 w[k] = code == 255u ? 0x7F7F7F7Fu
                                                     : ptx::pack4_e4m3(v[4 * k] * sc, v[4 * k + 1] * sc, v[4 * k + 2] * sc,
                                                                       v[4 * k + 3] * sc);
-                            if (row < m_end && GEMM_IN_BOUNDS(p, row >= 0 && row < p.M && c0 >= 0 && c0 < p.N &&
+                            if (row < m_end && GEMM_IN_BOUNDS(p, row >= 0 && row < e_M && c0 >= 0 && c0 < e_N &&
                                                                      dl >= 0 && dl < p.L)) {
-                                uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)dl * p.d_bstride +
-                                                (int64_t)row * p.ldd;
-                                if (c0 + 32 <= p.N) {
+                                uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) + (int64_t)dl * e_d_bstride +
+                                                (int64_t)row * e_ldd;
+                                if (c0 + 32 <= e_N) {
                                     *reinterpret_cast<uint4*>(drow + c0) = make_uint4(w[0], w[1], w[2], w[3]);
                                     *reinterpret_cast<uint4*>(drow + c0 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
                                 } else {
-                                    for (int i = 0; i < 32 && c0 + i < p.N; ++i)
+                                    for (int i = 0; i < 32 && c0 + i < e_N; ++i)
                                         drow[c0 + i] = (uint8_t)(w[i >> 2] >> ((i & 3) * 8));
                                 }
                                 const int f = c0 / 32;
@@ -1346,15 +1375,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         // the subtile holding a ragged row end, or a group's last rows
                         // short of the end of D, is stored element by element
-                        const bool direct = (p.d_ragged && col0 + C::kEpiCols > p.N) ||
-                                            (EXT && row0 + kEpiRows > m_end && m_end < p.M);
+                        const bool direct = (e_d_ragged && col0 + C::kEpiCols > e_N) ||
+                                            (EXT && row0 + kEpiRows > m_end && m_end < e_M);
                         const int sbi = sub_count % C::kEpiBufs;
                         ++sub_count;
                         uint8_t* sbuf = epi + (ew * C::kEpiBufs + sbi) * kEpiBufBytes;
                         const uint32_t sbuf_a = ptx::smem_addr(sbuf);
                         if (lane == 0) ptx::bulk_wait_read<C::kEpiBufs - 1>();   // the store that last used sbuf has read it
                         __syncwarp();
-                        if (p.has_c) {
+                        if (e_has_c) {
                             const uint32_t cb = cfull_bar(ew * 2 + sbi);
                             if (lane == 0) {
                                 ptx::mbar_arrive_expect_tx(cb, kEpiBufBytes);
@@ -1365,7 +1394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!ok) break;
                         }
                         uint32_t acc[C::kEpiCols];
-                        if (p.num_kb > 0) {
+                        if (e_num_kb > 0) {
                             load_acc(buf, sub, acc);
                         } else {
         #pragma unroll
@@ -1394,35 +1423,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint4* slot = reinterpret_cast<uint4*>(row_base + ((ch ^ (lane & 7)) << 4));
                             float v[VPC];
         #pragma unroll
-                            for (int i = 0; i < VPC; ++i) v[i] = p.alpha * __uint_as_float(acc[ch * VPC + i]);
-                            if (p.has_c) {
+                            for (int i = 0; i < VPC; ++i) v[i] = e_alpha * __uint_as_float(acc[ch * VPC + i]);
+                            if (e_has_c) {
                                 const uint4 craw = *slot;
                                 const uint32_t w[4] = {craw.x, craw.y, craw.z, craw.w};
                                 if constexpr (OB == 4) {
         #pragma unroll
-                                    for (int i = 0; i < 4; ++i) v[i] = fmaf(p.beta, __uint_as_float(w[i]), v[i]);
+                                    for (int i = 0; i < 4; ++i) v[i] = fmaf(e_beta, __uint_as_float(w[i]), v[i]);
                                 } else {
         #pragma unroll
                                     for (int i = 0; i < 4; ++i) {
                                         float lo, hi;
                                         unpack2(w[i], f16_out, lo, hi);
-                                        v[2 * i] = fmaf(p.beta, lo, v[2 * i]);
-                                        v[2 * i + 1] = fmaf(p.beta, hi, v[2 * i + 1]);
+                                        v[2 * i] = fmaf(e_beta, lo, v[2 * i]);
+                                        v[2 * i + 1] = fmaf(e_beta, hi, v[2 * i + 1]);
                                     }
                                 }
                             }
-                            if (p.bias_mode == 1) {
+                            if (e_bias_mode == 1) {
                                 const int cb0 = col0 + ch * VPC;
         #pragma unroll
-                                for (int i = 0; i < VPC; ++i) v[i] += (cb0 + i < p.N) ? __ldg(bias_l + cb0 + i) : 0.f;
-                            } else if (p.bias_mode == 2) {
+                                for (int i = 0; i < VPC; ++i) v[i] += (cb0 + i < e_N) ? __ldg(bias_l + cb0 + i) : 0.f;
+                            } else if (e_bias_mode == 2) {
         #pragma unroll
                                 for (int i = 0; i < VPC; ++i) v[i] += row_bias;
                             }
-                            if (p.act == 1) {
+                            if (e_act == 1) {
         #pragma unroll
                                 for (int i = 0; i < VPC; ++i) v[i] = fmaxf(v[i], 0.f);
-                            } else if (EXT && p.act == 2) {
+                            } else if (EXT && e_act == 2) {
         #pragma unroll
                                 for (int i = 0; i < VPC; ++i) v[i] = 0.5f * v[i] * (1.f + erff(v[i] * 0.70710678118654752f));
                             }
@@ -1431,7 +1460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const int c0 = col0 + ch * VPC;
                                 float r[VPC];
         #pragma unroll
-                                for (int i = 0; i < VPC; ++i) r[i] = (row < m_end && c0 + i < p.N) ? v[i] : 0.f;
+                                for (int i = 0; i < VPC; ++i) r[i] = (row < m_end && c0 + i < e_N) ? v[i] : 0.f;
                                 if (p.red_rows) {
         #pragma unroll
                                     for (int i = 0; i < VPC; ++i) row_acc += r[i];
@@ -1443,9 +1472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (p.red_cols) {
                                     int j;
                                     const float cs = chunk_col_sum<VPC>(r, lane, j);
-                                    if ((lane & (32 / VPC - 1)) == 0 && c0 + j < p.N &&
-                                        GEMM_IN_BOUNDS(p, l >= 0 && l < p.L && row0 >= 0 && row0 < p.M && c0 + j >= 0))
-                                        p.red_col_ws[((int64_t)l * ((p.M + 31) / 32) + row0 / 32) * p.N + c0 + j] = cs;
+                                    if ((lane & (32 / VPC - 1)) == 0 && c0 + j < e_N &&
+                                        GEMM_IN_BOUNDS(p, l >= 0 && l < p.L && row0 >= 0 && row0 < e_M && c0 + j >= 0))
+                                        p.red_col_ws[((int64_t)l * ((e_M + 31) / 32) + row0 / 32) * e_N + c0 + j] = cs;
                                 }
                             }
                             uint4 out;
@@ -1458,15 +1487,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             if (!direct) {
                                 *slot = out;
-                            } else if (row < m_end && GEMM_IN_BOUNDS(p, row >= 0 && row < p.M && col0 >= 0 &&
-                                                                          col0 < p.N && dl >= 0 && dl < p.L)) {
+                            } else if (row < m_end && GEMM_IN_BOUNDS(p, row >= 0 && row < e_M && col0 >= 0 &&
+                                                                          col0 < e_N && dl >= 0 && dl < p.L)) {
                                 const int c0 = col0 + ch * VPC;
                                 const uint32_t w[4] = {out.x, out.y, out.z, out.w};
                                 uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
-                                                ((int64_t)dl * p.d_bstride + (int64_t)row * p.ldd) * OB;
+                                                ((int64_t)dl * e_d_bstride + (int64_t)row * e_ldd) * OB;
         #pragma unroll
                                 for (int i = 0; i < VPC; ++i) {
-                                    if (c0 + i >= p.N) break;
+                                    if (c0 + i >= e_N) break;
                                     if constexpr (OB == 4)
                                         *reinterpret_cast<uint32_t*>(drow + (int64_t)(c0 + i) * 4) = w[i];
                                     else
@@ -1478,7 +1507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!direct) {
                             ptx::fence_async_shared();
                             __syncwarp();
-                            if (lane == 0 && GEMM_IN_BOUNDS(p, col0 >= 0 && col0 < p.N && row0 >= 0 && row0 < p.M &&
+                            if (lane == 0 && GEMM_IN_BOUNDS(p, col0 >= 0 && col0 < e_N && row0 >= 0 && row0 < e_M &&
                                                                    dl >= 0 && dl < p.L)) {
                                 ptx::tma_store_3d(&tmD, sbuf_a, col0, row0, dl);
                                 ptx::bulk_commit();
@@ -1489,8 +1518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 if (!released) release_acc(buf);
                 if (EXT && p.red_rows && row < m_end &&
-                    GEMM_IN_BOUNDS(p, l >= 0 && l < p.L && nb >= 0 && nb < p.tiles_n && row >= 0 && row < p.M))
-                    p.red_row_ws[((int64_t)l * p.tiles_n + nb) * p.M + row] = row_acc;
+                    GEMM_IN_BOUNDS(p, l >= 0 && l < p.L && nb >= 0 && nb < p.tiles_n && row >= 0 && row < e_M))
+                    p.red_row_ws[((int64_t)l * p.tiles_n + nb) * e_M + row] = row_acc;
                 if (EXT && p.red_amax) {
     #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1)
