@@ -1117,8 +1117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // `p` they would be reloaded from the parameter space after every
             // store to the staging buffer (a generic pointer the compiler
             // cannot tell apart from `p`), several dependent loads per chunk.
-            const float e_alpha = p.alpha, e_beta = p.beta, e_scale_d = p.scale_d;
-            const int e_N = p.N, e_M = p.M, e_bias_mode = p.bias_mode, e_act = p.act, e_out_f8 = p.out_f8;
+            [[maybe_unused]] const float e_alpha = p.alpha, e_beta = p.beta, e_scale_d = p.scale_d;
+            [[maybe_unused]] const int e_N = p.N, e_M = p.M, e_bias_mode = p.bias_mode, e_act = p.act, e_out_f8 = p.out_f8;
             const int e_has_c = p.has_c, e_d_ragged = p.d_ragged, e_num_kb = p.num_kb;
             const int64_t e_ldd = p.ldd, e_d_bstride = p.d_bstride;
             [[maybe_unused]] uint32_t c_phase[2] = {0u, 0u};
