@@ -191,6 +191,28 @@ static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, cons
     }
 }
 
+// The same bounded wait, polling instead of sleeping: the load thread waits
+// for free stages this way, so a refill starts the moment the MMA releases
+// its stages (measured: +1.2 % fused bf16 8192^3, +2 % bf16 4096^3, +0.7 %
+// on the 65536 x 256 x 4096 workload over waiting in try_wait).  The timer
+// and the abort flag are read every 64 polls.
+static __device__ __noinline__ bool poll_bar(uint32_t bar, uint32_t parity, const KernelParams& p,
+                                      volatile uint32_t* abort_flag, uint32_t role, uint32_t peer_abort) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_test_wait(bar, parity)) return true;
+        if ((n & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                *abort_flag = 1u;
+                if (peer_abort) ptx::st_cluster_u32(peer_abort, 1u);
+                atomicOr(p.status, kStatusTimeout | role);
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait that ignores the abort flag (used to drain in-flight copies
 // and MMAs before the CTA releases its resources).
 static __device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, const KernelParams& p) {
@@ -988,8 +1010,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool stop = false;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     // a group of stages is released together: wait at its first stage
-                    if (stage % C::kGroup == 0 &&
-                        !wait_bar(empty_bar(stage / C::kGroup), phase ^ 1u, p, abort_flag, kStatusRoleLoad, peer_abort)) {
+                    if (stage % C::kGroup == 0 && !ptx::mbar_test_wait(empty_bar(stage / C::kGroup), phase ^ 1u) &&
+                        !poll_bar(empty_bar(stage / C::kGroup), phase ^ 1u, p, abort_flag, kStatusRoleLoad, peer_abort)) {
                         stop = true;
                         break;
                     }
