@@ -20,6 +20,7 @@ constexpr int kTileM = 128;
 constexpr int kStageKBytes = 128;
 constexpr int kKStepBytes = 32;
 constexpr int kThreads = 192;          // warp 0 loads, warp 1 issues MMAs, warps 2-5 run the epilogue
+                                       // (block-scaled kernels add warp 6: scale-factor copies)
 constexpr int kEpiWarps = 4;
 constexpr int kEpiRows = 32;           // rows per epilogue warp (one TMEM lane quadrant)
 constexpr int kEpiBufBytes = kEpiRows * 128;
@@ -32,6 +33,7 @@ constexpr uint32_t kStatusRoleMma = 1u << 9;
 constexpr uint32_t kStatusRoleEpi = 1u << 10;
 constexpr uint32_t kStatusRoleDrain = 1u << 11;
 constexpr uint32_t kStatusRoleFixup = 1u << 12;   // a stream-K owner waiting for a partial sum
+constexpr uint32_t kStatusRoleCopy = 1u << 13;    // the scale-factor copier waiting for a stage
 // Diagnostic build with index checks (GEMM_DEBUG): a plain store whose index
 // falls outside its buffer is skipped and this bit is recorded.
 constexpr uint32_t kStatusBounds = 2u;

@@ -25,7 +25,10 @@
 //   warps 2..5  the epilogue: each warp owns one 32-lane TMEM quadrant
 //               (rows 32q..32q+31 of the 128-row tile), loads the source C
 //               subtile by TMA, applies the fusion in registers, stages D in
-//               swizzled shared memory and stores it by TMA.
+//               swizzled shared memory and stores it by TMA;
+//   warp 6      block-scaled kernels only: one lane copies each stage's
+//               scale factors into TMEM once the stage has landed and
+//               signals factors_ready[s], which the MMA thread waits on.
 // Work: a persistent walk over (tile, K-block range) units shared by all
 // roles: whole tiles in a grouped raster order given as a layout
 // (raster_full / raster_tail), after the static scheduler of "Blackwell
@@ -143,11 +146,36 @@ struct Cfg {
     // frees kGroup stages.
     static constexpr int kGroup = (kStages % 2 == 0 && kStages >= 6) ? 2 : 1;
     static constexpr int kGroups = kStages / kGroup;
-    static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps + 1 + 2 * kClcSlots;
+    // block-scaled kernels: one more warp, which copies each stage's factors
+    // into TMEM and signals the MMA thread on a barrier of its own per stage
+    static constexpr int kBlockThreads = kThreads + (BS ? 32 : 0);
+    static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps + 1 + 2 * kClcSlots + (BS ? kStages : 0);
     static constexpr int kSmemBytes =
         1024 /*alignment slack*/ + kRingBytes + kEpiBytes + kClcSlots * 16 + kNumBars * 8 + 16;
     static_assert(kSmemBytes <= 232448, "227 KB of shared memory per CTA");
 };
+
+// Index of factors_ready[0] in the barrier block (block-scaled kernels): after
+// full[], empty[], the accumulator, C-load and drain barriers and the
+// dynamic-schedule ring.
+__host__ __device__ constexpr int factor_bar_index(int stages) { return 2 * stages + 4 + 2 * kEpiWarps + 1 + 2 * kClcSlots; }
+
+// A stage's scale-factor slot: shared memory holds A's blocks of the stage,
+// then each 128 columns' blocks of B (512 bytes each); TMEM holds A's block j
+// at column 4 j of the slot and B's block j of columns 128 jb .. 128 jb + 127
+// at 4 kBlocks + 4 (kNB j + jb).
+template <int BN, int BS>
+struct SfGeom {
+    static constexpr uint32_t kNB = BN / 128;                       // 128-column blocks of the tile
+    static constexpr uint32_t kBlocks = BS == 2 ? 4u : 1u;          // blocks per 128 rows and stage
+    static constexpr uint32_t kCols = 4u * kBlocks * (1u + kNB);    // TMEM columns of one slot
+    static constexpr uint32_t kBytes = (512u * kBlocks * (1u + kNB) + 1023u) / 1024u * 1024u;
+};
+static_assert(SfGeom<256, 1>::kCols == (uint32_t)Cfg<2, 256, 2, 1>::kSfCols &&
+                  SfGeom<256, 2>::kCols == (uint32_t)Cfg<2, 256, 2, 2>::kSfCols &&
+                  SfGeom<128, 2>::kBytes == (uint32_t)Cfg<1, 128, 2, 2>::kSfBytes &&
+                  SfGeom<256, 1>::kBytes == (uint32_t)Cfg<2, 256, 2, 1>::kSfBytes,
+              "one factor-slot geometry");
 
 
 // ------------------------------------------------------------------------
@@ -814,14 +842,12 @@ struct MmaCtx {
 // (local and kernel-parameter memory behind a reference) would be re-loaded
 // after every MMA, a chain of dependent loads between two MMAs.
 //
-// BS: block-scaled MMAs.  Each stage's scale-factor blocks are copied into
-// TMEM (one slot of columns per stage after the accumulators) ahead of the
-// stage's four MMAs; tcgen05.cp and tcgen05.mma of one thread run in issue
-// order, so a copy never overtakes the MMAs that still read the columns it
-// overwrites one lap later.  MXFP8 (BS = 1): one block each for A and for
-// every 128 columns of B, 4 columns apiece; MMA j (32 elements of K) reads
-// factor byte j of each word.  NVFP4 (BS = 2): four blocks each, and MMA j
-// (64 elements of K) reads the whole words of block j.
+// BS: block-scaled MMAs.  Each stage's scale-factor blocks sit in TMEM (one
+// slot of columns per stage after the accumulators), put there by the copier
+// (factor_copier) before this thread sees the stage as ready.  MXFP8 (BS = 1):
+// one block each for A and for every 128 columns of B, 4 columns apiece; MMA
+// j (32 elements of K) reads factor byte j of each word.  NVFP4 (BS = 2): four
+// blocks each, and MMA j (64 elements of K) reads the whole words of block j.
 template <int CG, int BN, int S, int G, bool F8, uint32_t IDESC, int BS = 0>
 __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     const KernelParams& p = m.p;                 // slow paths (wait_bar) only
@@ -830,7 +856,9 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     const uint32_t tmem_base = m.tmem_base, peer_abort = m.peer_abort;
     volatile uint32_t* const abort_flag = m.abort_flag;
     constexpr int kAccBufs = acc_bufs(CG, BN, BS);
-    auto full_bar = [=](int s) { return bar0 + 8u * s; };
+    // block-scaled: a stage is ready once the copier has put its factors in
+    // TMEM (after its data landed); otherwise once its data landed
+    auto full_bar = [=](int s) { return bar0 + 8u * ((BS ? factor_bar_index(S) : 0) + s); };
     auto empty_bar = [=](int s) { return bar0 + 8u * (S + s); };
     auto accf_bar = [=](int b) { return bar0 + 8u * (2 * S + b); };
     auto acce_bar = [=](int b) { return bar0 + 8u * (2 * S + 2 + b); };
@@ -879,21 +907,10 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
             const uint64_t ad = a_base + soff, bd = b_base + soff;
             const uint32_t first = kb != kb0;
             if constexpr (BS == 2) {
-                // slot columns: A's block j at 4 j, B's block j at 16 + kNB*4 j
-                // (+4 per 128 columns of the tile); shared memory holds A's four
-                // blocks, then each 128 columns' four blocks of B
-                constexpr uint32_t kNB = BN / 128;
-                constexpr uint32_t kSfCol0 = (uint32_t)(kAccBufs * BN);
-                constexpr uint32_t kSfCols = 16u + 16u * kNB, kSfBytes = (2048u + 2048u * kNB + 1023u) / 1024u * 1024u;
-                const uint32_t sfs = ring + (uint32_t)stage * stage_bytes + stage_bytes - kSfBytes;
-                const uint32_t sfa = tmem_base + kSfCol0 + kSfCols * (uint32_t)stage, sfb = sfa + 16u;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    ptx::tmem_cp_32x128b_x4<CG>(sfa + 4u * j, sf_desc(sfs + 512u * j));
-#pragma unroll
-                    for (int jb = 0; jb < (int)kNB; ++jb)
-                        ptx::tmem_cp_32x128b_x4<CG>(sfb + 4u * (kNB * j + jb), sf_desc(sfs + 2048u * (1 + jb) + 512u * j));
-                }
+                using SG = SfGeom<BN, BS>;
+                constexpr uint32_t kNB = SG::kNB;
+                const uint32_t sfa = tmem_base + (uint32_t)(kAccBufs * BN) + SG::kCols * (uint32_t)stage;
+                const uint32_t sfb = sfa + 4u * SG::kBlocks;
                 // (NVFP4's short stages: asking after the first MMA measures better)
                 ptx::mma_nv<CG, IDESC>(d_tmem, ad, bd, sfa, sfb, first);
                 ready = ptx::mbar_test_wait(full_bar(next), next_phase);
@@ -901,14 +918,9 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
                 ptx::mma_nv<CG, IDESC>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, sfa + 8u, sfb + 8u * kNB, 1u);
                 ptx::mma_nv<CG, IDESC>(d_tmem, ad + 3 * a_step, bd + 3 * b_step, sfa + 12u, sfb + 12u * kNB, 1u);
             } else if constexpr (BS == 1) {
-                constexpr uint32_t kSfCol0 = (uint32_t)(kAccBufs * BN);
-                constexpr uint32_t kSfCols = 4u + 4u * (BN / 128), kSfBytes = (512u + 512u * (BN / 128) + 1023u) / 1024u * 1024u;
-                const uint32_t sfs = ring + (uint32_t)stage * stage_bytes + stage_bytes - kSfBytes;
-                const uint32_t sfa = tmem_base + kSfCol0 + kSfCols * (uint32_t)stage, sfb = sfa + 4u;
-                ptx::tmem_cp_32x128b_x4<CG>(sfa, sf_desc(sfs));
-#pragma unroll
-                for (int jb = 0; jb < BN / 128; ++jb)           // columns 128 jb .. 128 jb + 127 of the tile
-                    ptx::tmem_cp_32x128b_x4<CG>(sfb + 4u * jb, sf_desc(sfs + 512u + 512u * jb));
+                using SG = SfGeom<BN, BS>;
+                const uint32_t sfa = tmem_base + (uint32_t)(kAccBufs * BN) + SG::kCols * (uint32_t)stage;
+                const uint32_t sfb = sfa + 4u * SG::kBlocks;
                 ptx::mma_mx<CG, IDESC>(d_tmem, ad, bd, sfa, sfb, first);
                 ptx::mma_mx<CG, IDESC | (1u << 4) | (1u << 29)>(d_tmem, ad + a_step, bd + b_step, sfa, sfb, 1u);
                 ptx::mma_mx<CG, IDESC | (2u << 4) | (2u << 29)>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, sfa, sfb, 1u);
@@ -951,8 +963,65 @@ __device__ __noinline__ void mma_role(const MmaCtx<CG, BN, S>& m) {
     }
 }
 
+// The scale-factor copier of a block-scaled kernel (one thread of the pair
+// leader, warp 6).  It walks the same work units as the MMA thread; for each
+// stage it waits until the stage's data has landed (full[s]), copies the
+// stage's factor blocks into the stage's TMEM slot with tcgen05.cp
+// (cta_group::2: each CTA's blocks into its own TMEM) and commits them to
+// factors_ready[s], the barrier the MMA thread waits on.  Issued from the MMA
+// thread, the copies ran in its issue order between MMAs, about 40 % of an
+// NVFP4 stage's tensor time (twelve copies per stage); from this thread they
+// overlap the MMAs (NVFP4 8192^3 +16 %, MXFP8 unchanged).
+// A slot is rewritten only after full[s] fires for the stage's next fill,
+// which follows the MMA thread's release of that stage, so no copy lands
+// under an MMA still reading the slot.  Before it leaves, the copier waits
+// for its last commit, so no copy is in flight when TMEM is freed.
+template <int CG, int BN, int S, int BS>
+__device__ __noinline__ void factor_copier(const MmaCtx<CG, BN, S>& m) {
+    using G = SfGeom<BN, BS>;
+    const KernelParams& p = m.p;
+    const uint32_t bar0 = m.bar0, ring = m.ring, stage_bytes = m.stage_bytes, peer_abort = m.peer_abort;
+    const uint32_t slot0 = m.tmem_base + (uint32_t)(acc_bufs(CG, BN, BS) * BN);
+    const uint32_t ready0 = bar0 + 8u * factor_bar_index(S);
+    volatile uint32_t* const abort_flag = m.abort_flag;
+    Work wk = work_make(p, m.first_tile, m.tile_step, false, m.resp0, m.clc_full0, m.clc_empty0, 0u, CG, m.dp_tiles);
+    int stage = 0, last = -1;
+    uint32_t phase = 0, last_phase = 0;
+    int tile, kb0, kb1;
+    bool stop = false;
+    while (!stop && work_next(wk, p, tile, kb0, kb1, abort_flag, kStatusRoleCopy, peer_abort, true)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (!ptx::mbar_try_wait(bar0 + 8u * stage, phase) &&
+                !wait_bar(bar0 + 8u * stage, phase, p, abort_flag, kStatusRoleCopy, peer_abort)) {
+                stop = true;
+                break;
+            }
+            const uint32_t sfs = ring + (uint32_t)stage * stage_bytes + stage_bytes - G::kBytes;
+            const uint32_t sfa = slot0 + G::kCols * (uint32_t)stage, sfb = sfa + 4u * G::kBlocks;
+#pragma unroll
+            for (uint32_t j = 0; j < G::kBlocks; ++j) {
+                ptx::tmem_cp_32x128b_x4<CG>(sfa + 4u * j, sf_desc(sfs + 512u * j));
+#pragma unroll
+                for (uint32_t jb = 0; jb < G::kNB; ++jb)
+                    ptx::tmem_cp_32x128b_x4<CG>(sfb + 4u * (G::kNB * j + jb),
+                                                sf_desc(sfs + 512u * G::kBlocks * (1u + jb) + 512u * j));
+            }
+            if constexpr (CG == 2)
+                ptx::mma_commit_cg2(ready0 + 8u * stage);
+            else
+                ptx::mma_commit(ready0 + 8u * stage);
+            last = stage;
+            last_phase = phase;
+            phase = stage + 1 == S ? phase ^ 1u : phase;
+            stage = stage + 1 == S ? 0 : stage + 1;
+        }
+    }
+    if (last >= 0) drain_bar(ready0 + 8u * last, last_phase, p);
+    ptx::tc_fence_before();
+}
+
 template <int CG, int BN, int OB, int BS = 0>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<CG, BN, OB, BS>::kBlockThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -999,14 +1068,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2 * kEpiWarps; ++i) ptx::mbar_init(cfull_bar(i), 1);
         ptx::mbar_init(drain, 1);
+        if constexpr (BS != 0)
+            for (int s = 0; s < S; ++s) ptx::mbar_init(bar0 + 8u * (factor_bar_index(S) + s), 1);
         // A dynamic launch starts clusters that nobody cancelled once others
         // leave; after a recorded error they do no work (no chain of timeouts).
         *abort_flag = p.clc && *reinterpret_cast<volatile uint32_t*>(p.status) != 0u ? 1u : 0u;
         for (int i = 0; i < kClcSlots; ++i) {
             ptx::mbar_init(clc_full0 + 8u * i, 1);
-            // readers of a response: load thread, MMA thread (leader) and the
-            // four epilogue warps of each CTA
-            ptx::mbar_init(clc_empty0 + 8u * i, CG == 2 ? 2 * (1 + kEpiWarps) + 1 : 2 + kEpiWarps);
+            // readers of a response: load thread, MMA thread (leader), the
+            // factor copier (leader, block-scaled) and the four epilogue
+            // warps of each CTA
+            ptx::mbar_init(clc_empty0 + 8u * i, (CG == 2 ? 2 * (1 + kEpiWarps) + 1 : 2 + kEpiWarps) + (BS ? 1 : 0));
         }
         ptx::fence_mbar_init();
     }
@@ -1179,6 +1251,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef GEMM_MMA_CASE
                     default: break;
                 }
+            }
+        }
+    } else if (warp == 2 + kEpiWarps) {
+        // ------------------------------------------ scale-factor copies ----
+        if constexpr (BS != 0) {
+            if (lane == 0 && rank == 0) {
+                MmaCtx<CG, BN, S> m{p,          ptx::smem_addr(ring), C::kABytes, C::kStageBytes, bar0,
+                                    tmem_base,  first_tile,           tile_step,   abort_flag,       peer_abort,
+                                    resp0,      clc_full0,            clc_empty0,  dp_tiles};
+                factor_copier<CG, BN, S, BS>(m);
             }
         }
     } else {
@@ -1676,7 +1758,7 @@ template <int CG, int BN, int OB, int BS>
 static cudaLaunchConfig_t variant_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(Cfg<CG, BN, OB, BS>::kBlockThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg<CG, BN, OB, BS>::kSmemBytes;
     cfg.stream = stream;
     attr->id = cudaLaunchAttributeClusterDimension;
