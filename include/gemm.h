@@ -266,11 +266,17 @@ GEMM_API gemm_status_t gemm_set_stamps(gemm_handle_t h, void* stamps);
  *                             CTA, or a CTA pair), tile w, w + workers, ...
  *   GEMM_SCHED_SPLIT_TAIL     the full waves are computed whole; each of the
  *                             R tiles of the ragged last wave is cut into
- *                             floor(workers / R) equal K ranges (at most one
- *                             per K block), one range per worker.
+ *                             floor(S / R) equal K ranges (at most one per K
+ *                             block), one range per worker, where S is the
+ *                             number of workers the GPU holds at once (SMs
+ *                             per CTA group, or fewer if clusters do not all
+ *                             fit).  A problem of fewer than S tiles is one
+ *                             ragged wave: its launch then has one worker per
+ *                             range.
  *   GEMM_SCHED_STREAM_K       all full waves but the last are computed whole;
  *                             the K blocks of the remaining tiles are cut
- *                             into one equal contiguous range per worker.
+ *                             into one equal contiguous range per worker, S
+ *                             workers.
  *   GEMM_SCHED_DYNAMIC        whole tiles, scheduled by the hardware
  *                             ("Technical Documentation: NVIDIA/cutlass",
  *                             "Blackwell Cluster Launch Control"): the

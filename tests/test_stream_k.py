@@ -28,6 +28,9 @@ SPECS = [
     wl.Spec("sk_pair_e4m3", 2560, 2560, 2048, dtype_in="e4m3", dist="uniform1", seed=43),
     wl.Spec("sk_pair_batched", 512, 1024, 1024, batch=12, beta=1.0, seed=44),
     wl.Spec("sk_single_n128", 20000, 128, 520, bias="col", act="relu", seed=45),
+    # fewer tiles than workers: the split cuts a single, ragged wave
+    wl.Spec("sk_one_wave_pair", 768, 1024, 2048, beta=1.0, bias="row", seed=47),
+    wl.Spec("sk_one_wave_ragged", 1000, 1000, 1000, op_a="T", order_a="col", act="relu", seed=48, pad=2),
 ]
 
 
@@ -73,10 +76,12 @@ def test_split_matches_oracle(spec, mode):
     op.close()
 
 
+@pytest.mark.parametrize("size", [2304, 1024])
 @pytest.mark.parametrize("mode", list(MODES))
-def test_split_integer_sums_equal_data_parallel_bit_for_bit(mode):
+def test_split_integer_sums_equal_data_parallel_bit_for_bit(mode, size):
     # integers in [-4, 4] with K = 1024: every partial and total sum is exact
-    spec = wl.Spec("sk_int_exact", 2304, 2304, 1024, dtype_in="f16", dtype_d="f32", dist="int4", seed=46)
+    # (2304: a full wave and a ragged one; 1024: a single ragged wave)
+    spec = wl.Spec("sk_int_exact", size, size, 1024, dtype_in="f16", dtype_d="f32", dist="int4", seed=46)
     inputs = wl.make_inputs(spec)
     sk_op = _op(spec, inputs, MODES[mode])
     assert _cut_tiles(sk_op, spec)
@@ -132,11 +137,17 @@ def test_auto_schedule_follows_the_stated_rule(name):
     workers, dp, sk, ranges = op.schedule
     info = g.gemm_plan(desc_from_spec(spec))
     tiles, kb = info.tiles, _num_kb(spec)
-    waves, rest = divmod(tiles, workers)
-    pieces = min(workers // rest, kb) if rest else 0
-    use = waves >= 1 and rest != 0 and pieces >= 2 and kb // pieces >= 4
-    want = (waves * workers, rest * kb, rest * pieces) if use else (tiles, 0, 0)
-    assert (dp, sk, ranges) == want
     op.set_schedule(g.SCHED_DATA_PARALLEL)
     assert op.schedule[1:] == (tiles, 0, 0)
+    dp_workers = op.schedule[0]
+    # S, the workers the GPU holds at once: the data-parallel worker count
+    # when there are more tiles; else every SM's CTA (or pair: all fit at once)
+    slots = dp_workers if tiles > dp_workers else \
+        torch.cuda.get_device_properties(0).multi_processor_count // info.cta_group
+    waves, rest = divmod(tiles, slots)
+    pieces = min(slots // rest, kb) if rest else 0
+    use = waves >= 1 and rest != 0 and pieces >= 2 and kb // pieces >= 4
+    want = (waves * slots, rest * kb, rest * pieces) if use else (tiles, 0, 0)
+    assert (dp, sk, ranges) == want
+    assert workers == (max(dp_workers, ranges) if use else dp_workers)
     op.close()
