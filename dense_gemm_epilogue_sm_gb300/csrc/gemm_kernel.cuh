@@ -118,7 +118,8 @@ template <int CG, int BN, int OB, int BS = 0>
 struct Cfg {
     static constexpr int kAccBufs = acc_bufs(CG, BN, BS);
     static constexpr int kBRows = BN / CG;                          // rows of B this CTA loads
-    static constexpr int kStages = BS == 2 ? 5 : BS ? (CG == 2 ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
+    static constexpr int kStages = BS == 2 ? ((CG == 2 && BN == 128) ? 6 : 5)
+                                   : BS ? (CG == 2 ? 6 : 5) : ((CG == 1 && BN == 256) ? 4 : 6);
     static constexpr int kABytes = kTileM * kStageKBytes;           // 16 KiB
     static constexpr int kBBytes = kBRows * kStageKBytes;
     // scale-factor blocks of A's 128 rows and the tile's BN columns, per K

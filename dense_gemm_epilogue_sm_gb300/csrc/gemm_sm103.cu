@@ -7,7 +7,8 @@
 namespace gemm_sm103 {
 
 int stages_for(int cta_group, int tile_n, int block_scaled) {
-    return block_scaled == 2 ? 5 : block_scaled ? (cta_group == 2 ? 6 : 5) : ((cta_group == 1 && tile_n == 256) ? 4 : 6);
+    if (block_scaled == 2) return (cta_group == 2 && tile_n == 128) ? 6 : 5;
+    return block_scaled ? (cta_group == 2 ? 6 : 5) : ((cta_group == 1 && tile_n == 256) ? 4 : 6);
 }
 
 // Kernel variants by (CTA group, tile N, output bytes, block scaling).

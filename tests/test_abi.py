@@ -201,7 +201,10 @@ def test_nvfp4_plans_k_major_e2m1_with_256_element_stages():
     assert s == g.OK and (info.cta_group, info.tile_m, info.tile_n, info.tile_k, info.stages) == (2, 256, 256, 256, 5)
     assert info.a_k_major and info.b_k_major
     s, info = _status(_nv(M=2048, N=1024, ldd=1024))
-    assert s == g.OK and (info.cta_group, info.tile_n, info.tile_k) == (2, 128, 256)
+    assert s == g.OK and (info.cta_group, info.tile_n, info.tile_k, info.stages) == (2, 128, 256, 6)
+    # NVFP4 output: 256 x 128 pairs (two accumulators) wherever 64 of them fill the GPU
+    s, info = _status(_nv(dtype_d=g.E2M1, out_scale=g.OUT_SCALE_NV, ldd=4096))
+    assert s == g.OK and (info.cta_group, info.tile_m, info.tile_n, info.tile_k, info.stages) == (2, 256, 128, 256, 6)
     s, info = _status(_nv(M=512, N=512, K=1000, lda=1024, ldb=1024, ldd=512))
     assert s == g.OK and (info.cta_group, info.tile_n, info.tile_k, info.stages) == (1, 128, 256, 5)
     # column-major D: computed transposed, still K-major on both sides
