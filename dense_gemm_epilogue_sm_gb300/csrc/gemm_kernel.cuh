@@ -688,6 +688,43 @@ __device__ __forceinline__ void stage_subtile(const uint32_t (&acc)[128 / OB], u
     }
 }
 
+// The values t = alpha*acc (+ the column or row bias) (ReLU) of N whole
+// columns j0 .. j0 + N - 1 of a subtile (all inside D), for the block-scaled
+// outputs; the same operations in the same order as their general loop, with
+// no per-element tests.  BIAS 1: lane i holds the bias of subtile columns i
+// and 32 + i, broadcast by shuffle.
+template <int N, int BIAS, bool RELU>
+__device__ __forceinline__ void block_values(const uint32_t* acc, int j0, float alpha, float b_lo, float b_hi,
+                                             float row_bias, float (&v)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        float x = alpha * __uint_as_float(acc[i]);
+        if constexpr (BIAS == 1) {
+            constexpr int kLanes = 32;
+            const int j = j0 + i;
+            x += __shfl_sync(0xffffffffu, j < kLanes ? b_lo : b_hi, j % kLanes);
+        } else if constexpr (BIAS == 2) {
+            x += row_bias;
+        }
+        if constexpr (RELU) x = fmaxf(x, 0.f);
+        v[i] = x;
+    }
+}
+
+// block_values for a bias mode and activation known at run time
+template <int N>
+__device__ __forceinline__ void block_values_for(int bias_mode, bool relu, const uint32_t* acc, int j0, float alpha,
+                                                 float b_lo, float b_hi, float row_bias, float (&v)[N]) {
+    switch (bias_mode * 2 + (relu ? 1 : 0)) {
+        case 0: block_values<N, 0, false>(acc, j0, alpha, b_lo, b_hi, row_bias, v); break;
+        case 1: block_values<N, 0, true>(acc, j0, alpha, b_lo, b_hi, row_bias, v); break;
+        case 2: block_values<N, 1, false>(acc, j0, alpha, b_lo, b_hi, row_bias, v); break;
+        case 3: block_values<N, 1, true>(acc, j0, alpha, b_lo, b_hi, row_bias, v); break;
+        case 4: block_values<N, 2, false>(acc, j0, alpha, b_lo, b_hi, row_bias, v); break;
+        default: block_values<N, 2, true>(acc, j0, alpha, b_lo, b_hi, row_bias, v); break;
+    }
+}
+
 // tcgen05 instruction descriptor (kind::f16 / kind::f8f6f4, dense): D fp32
 // (bits 4-5 = 1), A and B type (bits 7-9, 10-12: f16 0 / bf16 1 for kind::f16,
 // e4m3 0 for kind::f8f6f4), A / B MN-major (bits 15, 16), N >> 3 (bits
@@ -1411,6 +1448,13 @@ __global__ void __launch_bounds__(Cfg<CG, BN, OB, BS>::kBlockThreads, 1)
                 for (int sub = 0; sub < C::kSubtiles; ++sub) {
                     const int col0 = nb * BN + sub * C::kEpiCols;
                     if (row0 >= m_end || col0 >= e_N) continue;     // nothing of this subtile is in range
+                    // the subtile's column bias, fetched once (lane i: columns i and
+                    // 32 + i, 0 past N) for the plain epilogue's compile-time forms
+                    float b_lo = 0.f, b_hi = 0.f;
+                    if (!EXT && e_bias_mode == 1) {
+                        if (col0 + lane < e_N) b_lo = __ldg(bias_l + col0 + lane);
+                        if (C::kEpiCols > 32 && col0 + 32 + lane < e_N) b_hi = __ldg(bias_l + col0 + 32 + lane);
+                    }
                     if constexpr (OB == 1) {
                         // MX output: e4m3 elements and one ue8m0 factor per 32
                         // columns of a row (no C; checked on the host).
@@ -1447,18 +1491,23 @@ __global__ void __launch_bounds__(Cfg<CG, BN, OB, BS>::kBlockThreads, 1)
                                 const int c0 = col0 + h * 16;
                                 if (c0 >= e_N) break;             // the block lies past the row's end
                                 float v[16];
+                                if (!EXT && c0 + 16 <= e_N) {
+                                    block_values_for<16>(e_bias_mode, e_act == 1, acc + h * 16, h * 16, e_alpha, b_lo,
+                                                         b_hi, row_bias, v);
+                                } else {
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    float x = e_alpha * __uint_as_float(acc[h * 16 + i]);
-                                    if (e_bias_mode == 1)
-                                        x += (c0 + i < e_N) ? __ldg(bias_l + c0 + i) : 0.f;
-                                    else if (e_bias_mode == 2)
-                                        x += row_bias;
-                                    if (e_act == 1)
-                                        x = fmaxf(x, 0.f);
-                                    else if (EXT && e_act == 2)
-                                        x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
-                                    v[i] = (c0 + i < e_N) ? x : 0.f;   // columns past N join no block
+                                    for (int i = 0; i < 16; ++i) {
+                                        float x = e_alpha * __uint_as_float(acc[h * 16 + i]);
+                                        if (e_bias_mode == 1)
+                                            x += (c0 + i < e_N) ? __ldg(bias_l + c0 + i) : 0.f;
+                                        else if (e_bias_mode == 2)
+                                            x += row_bias;
+                                        if (e_act == 1)
+                                            x = fmaxf(x, 0.f);
+                                        else if (EXT && e_act == 2)
+                                            x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+                                        v[i] = (c0 + i < e_N) ? x : 0.f;   // columns past N join no block
+                                    }
                                 }
                                 uint32_t amax = 0u;
 #pragma unroll
@@ -1491,18 +1540,23 @@ __global__ void __launch_bounds__(Cfg<CG, BN, OB, BS>::kBlockThreads, 1)
                             const int c0 = col0 + h * 32;
                             if (c0 >= e_N) break;                 // the block lies past the row's end
                             float v[32];
+                            if (!EXT && c0 + 32 <= e_N) {
+                                block_values_for<32>(e_bias_mode, e_act == 1, acc + h * 32, h * 32, e_alpha, b_lo, b_hi,
+                                                     row_bias, v);
+                            } else {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                float x = e_alpha * __uint_as_float(acc[h * 32 + i]);
-                                if (e_bias_mode == 1)
-                                    x += (c0 + i < e_N) ? __ldg(bias_l + c0 + i) : 0.f;
-                                else if (e_bias_mode == 2)
-                                    x += row_bias;
-                                if (e_act == 1)
-                                    x = fmaxf(x, 0.f);
-                                else if (EXT && e_act == 2)
-                                    x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
-                                v[i] = (c0 + i < e_N) ? x : 0.f;   // columns past N join no block
+                                for (int i = 0; i < 32; ++i) {
+                                    float x = e_alpha * __uint_as_float(acc[h * 32 + i]);
+                                    if (e_bias_mode == 1)
+                                        x += (c0 + i < e_N) ? __ldg(bias_l + c0 + i) : 0.f;
+                                    else if (e_bias_mode == 2)
+                                        x += row_bias;
+                                    if (e_act == 1)
+                                        x = fmaxf(x, 0.f);
+                                    else if (EXT && e_act == 2)
+                                        x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+                                    v[i] = (c0 + i < e_N) ? x : 0.f;   // columns past N join no block
+                                }
                             }
                             // factor: the OCP MX shared exponent floor(log2 amax) - 8,
                             // read off amax's biased fp32 exponent; 255 for NaN / inf
@@ -1541,11 +1595,6 @@ __global__ void __launch_bounds__(Cfg<CG, BN, OB, BS>::kBlockThreads, 1)
                                             (EXT && row0 + kEpiRows > m_end && m_end < e_M);
                         // staged tiles of the plain epilogue take stage_subtile
                         const bool quick = !EXT && !direct && e_act != 2;
-                        float b_lo = 0.f, b_hi = 0.f;    // its column bias, fetched early
-                        if (quick && e_bias_mode == 1) {
-                            if (col0 + lane < e_N) b_lo = __ldg(bias_l + col0 + lane);
-                            if (C::kEpiCols > 32 && col0 + 32 + lane < e_N) b_hi = __ldg(bias_l + col0 + 32 + lane);
-                        }
                         const int sbi = sub_count % C::kEpiBufs;
                         ++sub_count;
                         uint8_t* sbuf = epi + (ew * C::kEpiBufs + sbi) * kEpiBufBytes;
