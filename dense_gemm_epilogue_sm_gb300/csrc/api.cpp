@@ -428,17 +428,34 @@ bool encode_sf_map(CUtensorMap* map, const void* base, int64_t blocks) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MXFP8 factors of B for a tile of `per_tile` 128-column blocks: a 4-D view
+// (256-byte row, the block's 2 rows, K block, 128-column block) whose box
+// takes one K block of `per_tile` adjacent column blocks.
+bool encode_sf_map_b4(CUtensorMap* map, const void* base, int64_t kblocks, int64_t nblocks, uint32_t per_tile) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {256, 2, (cuuint64_t)kblocks, (cuuint64_t)nblocks};
+    cuuint64_t strides[3] = {256, 512, (cuuint64_t)(kblocks * 512)};
+    cuuint32_t box[4] = {256, 2, 1, per_tile};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // NVFP4 factors: one ue4m3 per 16 K elements, so a 256-element K stage
 // takes four 512-byte blocks per 128 rows, adjacent in the tensor.  Seen as
 // rows of 256 bytes: dimension 1 walks a 128-row block's K blocks (2 rows
 // each, `kblocks` of them), dimension 2 the 128-row blocks; a box of 8 rows
-// is one stage's four blocks, and blocks past the last K block read as zero.
-bool encode_sf_map_nv(CUtensorMap* map, const void* base, int64_t kblocks, int64_t row_blocks) {
+// is one stage's four blocks (of `per_box` adjacent 128-row blocks: B's box
+// covers a 256-wide tile's two), and blocks past the last K block read as
+// zero.
+bool encode_sf_map_nv(CUtensorMap* map, const void* base, int64_t kblocks, int64_t row_blocks, uint32_t per_box = 1) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {256, (cuuint64_t)(kblocks * 2), (cuuint64_t)row_blocks};
     cuuint64_t strides[2] = {256, (cuuint64_t)(kblocks * 512)};
-    cuuint32_t box[3] = {256, 8, 1};
+    cuuint32_t box[3] = {256, 8, per_box};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -739,10 +756,10 @@ static gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, con
                 // K here counts bytes (two elements each): ceil(K/16) factors, four per block
                 const int64_t kblocks = (2 * d.K + 63) / 64;
                 ok = ok && encode_sf_map_nv(&h->maps[4], ksfa, kblocks, a_rowblocks);
-                ok = ok && encode_sf_map_nv(&h->maps[5], ksfb, kblocks, lb_n * P.kp.sf_nblocks);
+                ok = ok && encode_sf_map_nv(&h->maps[5], ksfb, kblocks, lb_n * P.kp.sf_nblocks, (uint32_t)(tn / 128));
             } else {
                 ok = ok && encode_sf_map(&h->maps[4], ksfa, a_rowblocks * (int64_t)P.kp.num_kb);
-                ok = ok && encode_sf_map(&h->maps[5], ksfb, lb_n * P.kp.sf_nblocks * (int64_t)P.kp.num_kb);
+                ok = ok && encode_sf_map_b4(&h->maps[5], ksfb, P.kp.num_kb, lb_n * P.kp.sf_nblocks, (uint32_t)(tn / 128));
             }
         } else {
             h->maps[4] = h->maps[0];

@@ -117,6 +117,26 @@ __device__ __forceinline__ void tma_load_3d_cg2(uint32_t dst, const void* map, i
         : "memory");
 }
 
+// 4-D tiled loads (a 256-wide tile's MXFP8 B factors in one box), single-CTA
+// and 2-SM forms as above.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, int32_t c0, int32_t c1, int32_t c2,
+                                            int32_t c3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_cg2(uint32_t dst, const void* map, int32_t c0, int32_t c1, int32_t c2,
+                                                int32_t c3, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar_cluster)
+        : "memory");
+}
+
 // Same, with an L2 eviction-priority hint (a createpolicy value).
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* map, int32_t c0, int32_t c1,
                                                  int32_t c2, uint32_t bar, uint64_t policy) {
