@@ -179,8 +179,12 @@ SPECS = [
     wl.Spec("nvo_batched", 256, 384, 320, batch=3, dtype_d="e2m1", seed=143),
     wl.Spec("nvo_from_mx", 1024, 1024, 512, dtype_in="e4m3", block_scale="mx", dtype_d="e2m1", seed=144),
     wl.Spec("nvo_from_nv", 1024, 1024, 512, dtype_in="e2m1", block_scale="nv", dtype_d="e2m1", seed=145),
-    wl.Spec("nvo_from_nv_pair256", 2304, 2304, 1024, dtype_in="e2m1", block_scale="nv", dtype_d="e2m1",
+    # NVFP4 output with block-scaled inputs on CTA pairs: 256 x 128 tiles with
+    # two accumulators (and the ragged last column tile of 2304 / 128 = 18)
+    wl.Spec("nvo_from_nv_pair", 2304, 2304, 1024, dtype_in="e2m1", block_scale="nv", dtype_d="e2m1",
             act="relu", seed=146),
+    wl.Spec("nvo_from_mx_pair", 2304, 2176, 512, dtype_in="e4m3", block_scale="mx", dtype_d="e2m1",
+            bias="col", seed=148),
 ]
 
 
