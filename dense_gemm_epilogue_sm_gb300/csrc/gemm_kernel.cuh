@@ -1455,7 +1455,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, OB, BS>::kBlockThreads, 1)
                     // the subtile's column bias, fetched once (lane i: columns i and
                     // 32 + i, 0 past N) for the plain epilogue's compile-time forms
                     float b_lo = 0.f, b_hi = 0.f;
-                    if (e_bias_mode == 1) {
+                    if (!EXT && e_bias_mode == 1) {
                         if (col0 + lane < e_N) b_lo = __ldg(bias_l + col0 + lane);
                         if (C::kEpiCols > 32 && col0 + 32 + lane < e_N) b_hi = __ldg(bias_l + col0 + 32 + lane);
                     }
@@ -1598,9 +1598,7 @@ __global__ void __launch_bounds__(Cfg<CG, BN, OB, BS>::kBlockThreads, 1)
                         const bool direct = (e_d_ragged && col0 + C::kEpiCols > e_N) ||
                                             (EXT && row0 + kEpiRows > m_end && m_end < e_M);
                         // staged tiles of the plain epilogue take stage_subtile
-                        // (the extended epilogue too, for grouped tiles without GELU or
-                        // reductions)
-                        const bool quick = !direct && e_act != 2 && !reducing;
+                        const bool quick = !EXT && !direct && e_act != 2;
                         const int sbi = sub_count % C::kEpiBufs;
                         ++sub_count;
                         uint8_t* sbuf = epi + (ew * C::kEpiBufs + sbi) * kEpiBufBytes;
